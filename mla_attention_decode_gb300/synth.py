@@ -1,0 +1,142 @@
+"""Seeded synthetic inputs for MLA decode (shared by tests and the benchmark).
+
+This module only *draws and encodes* inputs; it holds none of the decode
+arithmetic (no dequantisation, no attention).  Both the CUDA path and the CPU
+oracle consume the tensors it returns.
+
+Recipe (the pages' benchmark generator is not published, so this stands in for
+it; see the workload table on kernelindex "amd-mixed-mla" submission 593653,
+section "Dispatch", and the shapes named on submission 754939's docstring):
+
+* one ``torch.Generator('cpu')`` seeded with ``seed`` (default 0);
+* q is drawn first, float32 N(0,1) of shape [B, 16, 576], rounded to bf16 (RNE);
+* the latent KV cache is drawn next, float32 N(0,1) of shape [sum(L_b), 576],
+  rounded to bf16 -- rows of sequence b are contiguous (page size 1);
+* kv_indptr = exclusive prefix sum of the lengths, qo_indptr = arange(B+1);
+* fp8: per-tensor scale = amax(|kv|)/448 in fp32 (amax clamped to >= 1e-12),
+  stored value = e4m3fn(clamp(kv / scale, +-448)) (submission 754939,
+  ``quantize_fp8``), computed from the fp32 widening of the bf16 cache;
+* MXFP4: each 576-wide row is cut into 18 blocks of 32; the block's e8m0 byte is
+  clamp(ceil(log2(amax/6)) + 127, 0, 254) (127 for an all-zero block), i.e. the
+  block amax/6 rounded *up* to a power of two so that no element clips; elements
+  are divided by 2^(byte-127) and rounded to e2m1 (nearest, ties to the even
+  code); element 2i goes to the low nibble of byte i, element 2i+1 to the high
+  nibble (the unpack order of submission 754939's stage-1 kernel).
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+NUM_HEADS = 16
+QK_DIM = 576
+V_DIM = 512
+MX_BLOCK = 32
+FP8_MAX = 448.0
+
+KV_DTYPES = ("bf16", "fp8", "mxfp4")
+
+# The five benchmark workloads: (batch, kv_len per sequence, kv dtype).
+WORKLOADS = {
+    "bs4_kv1024_bf16": (4, 1024, "bf16"),
+    "bs32_kv1024_fp8": (32, 1024, "fp8"),
+    "bs4_kv8192_fp8": (4, 8192, "fp8"),
+    "bs64_kv8192_fp8": (64, 8192, "fp8"),
+    "bs32_kv8192_mxfp4": (32, 8192, "mxfp4"),
+}
+WORKLOAD_ORDER = list(WORKLOADS)
+
+
+@dataclasses.dataclass
+class MLAInputs:
+    """One synthetic decode batch (CPU tensors)."""
+    kv_dtype: str
+    q: torch.Tensor                 # bf16 [B, 16, 576]
+    kv_bf16: torch.Tensor           # bf16 [N, 576] (the unquantised draw)
+    kv: torch.Tensor                # bf16 [N,576] | uint8 e4m3 [N,576] | uint8 packed e2m1 [N,288]
+    kv_scale: torch.Tensor | None   # fp32 [1] for fp8, else None
+    block_scales: torch.Tensor | None  # uint8 e8m0 [N, 18] for mxfp4, else None
+    kv_indptr: torch.Tensor         # int32 [B+1]
+    qo_indptr: torch.Tensor         # int32 [B+1]
+
+    @property
+    def batch(self) -> int:
+        return int(self.kv_indptr.numel() - 1)
+
+    @property
+    def total_kv(self) -> int:
+        return int(self.kv_indptr[-1])
+
+    def kv_bytes(self) -> int:
+        """Bytes of KV cache (plus its scales) that one decode call reads."""
+        n = self.total_kv
+        if self.kv_dtype == "bf16":
+            return n * QK_DIM * 2
+        if self.kv_dtype == "fp8":
+            return n * QK_DIM + 4
+        return n * (QK_DIM // 2) + n * (QK_DIM // MX_BLOCK)
+
+
+def quantize_fp8(kv_bf16: torch.Tensor):
+    """Per-tensor e4m3 quantisation -> (uint8 codes [N,576], fp32 scale [1])."""
+    x = kv_bf16.float()
+    amax = x.abs().amax().clamp(min=1e-12)
+    scale = (amax / FP8_MAX).to(torch.float32)
+    q8 = (x / scale).clamp(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
+    return q8.view(torch.uint8).contiguous(), scale.reshape(1).contiguous()
+
+
+def _encode_e2m1(v: np.ndarray) -> np.ndarray:
+    """Round to the nearest e2m1 value (ties to the even code), saturating at 6."""
+    mag = np.abs(v)
+    code = ((mag > 0.25).astype(np.uint8) + (mag >= 0.75) + (mag > 1.25) + (mag >= 1.75)
+            + (mag > 2.5) + (mag >= 3.5) + (mag > 5.0)).astype(np.uint8)
+    return code | (np.signbit(v).astype(np.uint8) << 3)
+
+
+def quantize_mxfp4(kv_bf16: torch.Tensor):
+    """MXFP4 encoding -> (packed e2m1 uint8 [N,288], e8m0 uint8 [N,18])."""
+    x = kv_bf16.float().numpy().astype(np.float64)
+    n = x.shape[0]
+    xb = x.reshape(n, QK_DIM // MX_BLOCK, MX_BLOCK)
+    amax = np.abs(xb).max(axis=2)
+    with np.errstate(divide="ignore"):
+        e = np.where(amax > 0, np.ceil(np.log2(np.where(amax > 0, amax, 1.0) / 6.0)), 0.0)
+    e8 = np.clip(e + 127, 0, 254).astype(np.uint8)
+    scaled = xb / np.ldexp(1.0, e8.astype(np.int32) - 127)[..., None]
+    nib = _encode_e2m1(scaled).reshape(n, QK_DIM)
+    packed = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    return torch.from_numpy(np.ascontiguousarray(packed)), torch.from_numpy(np.ascontiguousarray(e8))
+
+
+def make_inputs(kv_lens, kv_dtype: str = "bf16", seed: int = 0, q_mult: float = 1.0) -> MLAInputs:
+    """Draw one decode batch.  ``kv_lens``: list of per-sequence lengths."""
+    if kv_dtype not in KV_DTYPES:
+        raise ValueError(f"kv_dtype must be one of {KV_DTYPES}")
+    lens = [int(x) for x in kv_lens]
+    if any(x < 0 for x in lens):
+        raise ValueError("negative kv length")
+    b = len(lens)
+    n = int(sum(lens))
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    q = (torch.randn(b, NUM_HEADS, QK_DIM, generator=g, dtype=torch.float32) * q_mult).to(torch.bfloat16)
+    kv_bf16 = torch.randn(n, QK_DIM, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    ind = torch.zeros(b + 1, dtype=torch.int32)
+    if b:
+        ind[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    qo = torch.arange(b + 1, dtype=torch.int32)
+    kv_scale = block_scales = None
+    if kv_dtype == "bf16":
+        kv = kv_bf16
+    elif kv_dtype == "fp8":
+        kv, kv_scale = quantize_fp8(kv_bf16)
+    else:
+        kv, block_scales = quantize_mxfp4(kv_bf16)
+    return MLAInputs(kv_dtype, q.contiguous(), kv_bf16, kv.contiguous(), kv_scale, block_scales, ind, qo)
+
+
+def make_workload(name: str, seed: int = 0) -> MLAInputs:
+    batch, kv_len, dt = WORKLOADS[name]
+    return make_inputs([kv_len] * batch, dt, seed=seed)
