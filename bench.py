@@ -1,0 +1,370 @@
+"""Benchmark: microseconds per MLA decode call on one synthetic workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one mla_decode_fwd call (split kernel + log-sum-exp combine) over one
+batch, inputs resident in HBM, with the L2 flushed (a 256 MiB device write)
+before every timed call; each call is bracketed by CUDA events on its stream.
+Under torchrun (N > 1) every rank decodes its own batch of the same shape
+(independent sequences, no collective on the data path: weak scaling); the
+timed loop is bracketed by a barrier and synchronize, the per-call time is the
+max over ranks.  Rank 0 prints one JSON line.
+
+Extra keys:
+  roofline     the split kernel alone (timed in a second pass through the
+               split/combine entry points, events on the launch stream) against
+               the measured HBM copy bandwidth; algorithmic bytes = KV bytes.
+  cpu_baseline the fp64 C oracle on the host cores (full workload when it takes
+               seconds, else a bounded sample of sequences, scaled).
+  e2e          the same metric through the public call with pinned host q /
+               indptrs copied in and out / lse copied back inside the timed region.
+  clocks       nvidia-smi samples taken during the timed region.
+
+--impl reference times the oracle (the pages' definition evaluated in fp64 on the
+CPU) on the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from mla_attention_decode_gb300 import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "bs32_kv1024_fp8"
+L2_FLUSH_BYTES = 256 << 20
+CODES = {"bf16": 0, "fp8": 1, "mxfp4": 2}
+DTYPE_LABEL = {"bf16": "bf16 x bf16 -> f32", "fp8": "e4m3 x e4m3 -> f32", "mxfp4": "e4m3 x e4m3 -> f32 (e2m1 KV)"}
+KERNEL_SOURCES = ["mla_attention_decode_gb300/csrc/mla_stage1.cuh", "mla_attention_decode_gb300/csrc/mla_ptx.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOAD_ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """dram bytes per split-kernel launch from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def to_device(inp: synth.MLAInputs, dev):
+    scale = inp.kv_scale if inp.kv_dtype == "fp8" else inp.block_scales
+    return dict(q=inp.q.to(dev), kv=inp.kv.to(dev), kv_scale=None if scale is None else scale.to(dev),
+                kv_indptr=inp.kv_indptr.to(dev), qo_indptr=inp.qo_indptr.to(dev))
+
+
+def time_calls(fn, steps, flush, stream):
+    """Per-call device times (us) of `steps` calls, L2 flushed before each."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e3 for a, b in ev]
+
+
+def cpu_baseline(inp: synth.MLAInputs, budget_s: float = 20.0):
+    """Times the oracle as it stands on the host cores; returns (us per full call, cores, sample text)."""
+    import oracle
+    orc = oracle.load()
+    cores = os.cpu_count() or 1
+    lens = (inp.kv_indptr[1:] - inp.kv_indptr[:-1]).tolist()
+    kvs = None if inp.kv_scale is None else inp.kv_scale.numpy()
+    bs = None if inp.block_scales is None else inp.block_scales.numpy()
+    # probe one sequence to size the sample
+    t0 = time.perf_counter()
+    orc.decode(CODES[inp.kv_dtype], inp.q, inp.kv, inp.kv_indptr[:2].numpy(), inp.qo_indptr[:2].numpy(), kvs, bs,
+               num_threads=cores)
+    per_seq = max(time.perf_counter() - t0, 1e-4)
+    nseq = max(1, min(inp.batch, int(budget_s / per_seq)))
+    ind = inp.kv_indptr[:nseq + 1].numpy()
+    t0 = time.perf_counter()
+    orc.decode(CODES[inp.kv_dtype], inp.q, inp.kv, ind, inp.qo_indptr[:nseq + 1].numpy(), kvs, bs, num_threads=cores)
+    dt = time.perf_counter() - t0
+    us_call = dt * 1e6 * (sum(lens) / max(1, sum(lens[:nseq])))
+    sample = (f"{nseq} of {inp.batch} sequences (all 16 heads), fp64 C oracle with OpenMP, "
+              f"scaled by KV rows to the full call")
+    return us_call, cores, sample
+
+
+def run_reference(args, inp, name):
+    rank, world, _ = dist_env()
+    if world > 1 and rank != 0:
+        return
+    import oracle
+    orc = oracle.load()
+    cores = os.cpu_count() or 1
+    kvs = None if inp.kv_scale is None else inp.kv_scale.numpy()
+    bs = None if inp.block_scales is None else inp.block_scales.numpy()
+    lens = (inp.kv_indptr[1:] - inp.kv_indptr[:-1]).tolist()
+    # bound each step to ~2 s of CPU work: a sample of sequences, scaled by rows
+    t0 = time.perf_counter()
+    orc.decode(CODES[inp.kv_dtype], inp.q, inp.kv, inp.kv_indptr[:2].numpy(), inp.qo_indptr[:2].numpy(), kvs, bs,
+               num_threads=cores)
+    per_seq = max(time.perf_counter() - t0, 1e-4)
+    budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    nseq = max(1, min(inp.batch, int(budget / per_seq)))
+    ind = inp.kv_indptr[:nseq + 1].numpy()
+    qo = inp.qo_indptr[:nseq + 1].numpy()
+    scale = sum(lens) / max(1, sum(lens[:nseq]))
+    for _ in range(args.warmup):
+        orc.decode(CODES[inp.kv_dtype], inp.q, inp.kv, ind, qo, kvs, bs, num_threads=cores)
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        orc.decode(CODES[inp.kv_dtype], inp.q, inp.kv, ind, qo, kvs, bs, num_threads=cores)
+        ts.append((time.perf_counter() - t0) * 1e6 * scale)
+    us = statistics.mean(ts)
+    b, L, dt = synth.WORKLOADS[name]
+    line = {
+        "impl": "reference", "metric": "us_per_mla_decode_call", "value": round(us, 2), "unit": "us/call",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "batch": b, "kv_len": L, "kv_dtype": dt},
+        "cpu_baseline": {"value": round(us, 2), "unit": "us/call", "cores": cores, "kind": "oracle",
+                         "sample": f"{nseq} of {inp.batch} sequences per step, scaled by KV rows"},
+        "e2e": {"value": round(us, 2), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    name = args.workload
+    b, L, dt = synth.WORKLOADS[name]
+    inp = synth.make_inputs([L] * b, dt, seed=rank)
+    if args.impl == "reference":
+        run_reference(args, inp, name)
+        return
+
+    from mla_attention_decode_gb300 import binding, build
+    build.build()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    d = to_device(inp, dev)
+    dec = binding.MLADecoder(inp.kv_indptr, dt, device=dev)
+    plan = dec.plan
+    out = torch.empty(b, 16, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(b, 16, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    scale_stride = int(d["kv_scale"].stride(0)) if dt == "mxfp4" else 0
+    launches_per_call = 1 + (1 if plan.splits_max > 1 else 0)
+
+    def call():
+        binding.mla_decode_fwd(d["q"], d["kv"], d["kv_scale"], d["kv_indptr"], d["qo_indptr"], out, lse, plan,
+                               dec.workspace, scale_stride=scale_stride, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    assert dec.poll_error() == 0
+
+    # ---- headline: whole call, device time, L2 flushed before each call
+    barrier()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        per_call = time_calls(call, args.steps, flush, stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    us = statistics.mean(per_call)
+    if pg is not None:
+        t = torch.tensor([us], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        us = float(t.item())
+
+    # ---- the split kernel alone (roofline) and the combine, events on the launch stream
+    ev_split, ev_comb = [], []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        binding.mla_decode_split(d["q"], d["kv"], d["kv_scale"], d["kv_indptr"], d["qo_indptr"], out, lse, plan,
+                                 dec.workspace, scale_stride=scale_stride, stream=stream)
+        e1.record(stream)
+        binding.mla_decode_combine(out, lse, plan, dec.workspace, stream=stream)
+        e2.record(stream)
+        ev_split.append((e0, e1))
+        ev_comb.append((e1, e2))
+    torch.cuda.synchronize()
+    t_split = statistics.mean(a.elapsed_time(c) * 1e3 for a, c in ev_split)
+    t_comb = statistics.mean(a.elapsed_time(c) * 1e3 for a, c in ev_comb)
+    kv_bytes = inp.kv_bytes()
+    peak, peak_kind = measured_peaks()
+    achieved = kv_bytes / (t_split * 1e-6) / 1e9
+
+    # ---- end to end through the public call: pinned host q/indptr in, out/lse out
+    q_h = inp.q.pin_memory()
+    ind_h = inp.kv_indptr.pin_memory()
+    qo_h = inp.qo_indptr.pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_call():
+        d["q"].copy_(q_h, non_blocking=True)
+        d["kv_indptr"].copy_(ind_h, non_blocking=True)
+        d["qo_indptr"].copy_(qo_h, non_blocking=True)
+        call()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_call()
+    barrier()
+    e2e_times = time_calls(e2e_call, args.steps, flush, stream)
+    e2e_us = statistics.mean(e2e_times)
+    h2d = q_h.numel() * q_h.element_size() + ind_h.numel() * 4 + qo_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    assert dec.poll_error() == 0
+    if pg is not None:
+        t = torch.tensor([e2e_us, t_split, t_comb], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_us, t_split, t_comb = (float(x) for x in t.tolist())
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            us_cpu, cores, sample = cpu_baseline(inp)
+            cpu = {"value": round(us_cpu, 1), "unit": "us/call", "cores": cores, "kind": "oracle", "sample": sample}
+        line = {
+            "metric": "us_per_mla_decode_call", "value": round(us, 3), "unit": "us/call", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": DTYPE_LABEL[dt], "data": "synthetic (seeded N(0,1) q and KV, quantised as stated)",
+            "config": {"workload": name, "batch": b, "kv_len": L, "kv_dtype": dt,
+                       "kv_bytes_per_call": kv_bytes, "l2": "flushed before every timed call (256 MiB write)",
+                       "plan": {k: plan.as_dict()[k] for k in ("num_work", "grid", "chunk_tokens", "splits_max")},
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "kv_gbs": round(kv_bytes / (us * 1e-6) / 1e9, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic(name),
+                         "kernel": f"mla_split_kernel<{dt}>", "kernel_us": round(t_split, 3),
+                         "combine_us": round(t_comb, 3), "peak_kind": f"{peak_kind} (HBM copy)"},
+            "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * launches_per_call,
+            "clocks": clk.summary(),
+            "wall_s_timed_loop": round(t_wall, 4),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * mla_decode.h -- C ABI of libmla_decode.so: single-token (q_seq_len = 1)
+ * multi-head latent attention decode on a GB300 (sm_103a).
+ *
+ * The operation (kernelindex "amd-mixed-mla" submission 593653, section
+ * "Slow fallback", _bmm_reference; constants from its "Constants" section):
+ * for every sequence b and query head h < 16,
+ *
+ *   s_t        = (q[qo_indptr[b], h, :576] . dequant(kv[t, :576])) * sm_scale
+ *   out[b,h,:] = sum_t softmax(s)_t * dequant(kv[t, :512])
+ *   lse[b,h]   = ln sum_t exp(s_t)                      (natural log)
+ *
+ * over the KV rows t in [kv_indptr[b], kv_indptr[b+1]) -- one latent KV head
+ * shared by all 16 query heads, QK dim 576 (512 latent + 64 rope), V = the first
+ * 512 columns of the same row, page size 1, sm_scale = 1/sqrt(576) = 1/24.
+ * An empty sequence gives out = 0 and lse = -inf.
+ *
+ * KV storage (submission 593653 "Dispatch" and submission 754939 "Stage 1"):
+ *   MLA_KV_BF16      bf16 [rows, 576]
+ *   MLA_KV_FP8_E4M3  OCP e4m3fn bytes [rows, 576] times one fp32 per-tensor scale
+ *   MLA_KV_MXFP4     packed e2m1 [rows, 288] (element 2i = low nibble of byte i)
+ *                    with one e8m0 byte per 32 elements, [rows, scale_stride],
+ *                    scale_stride >= 18 (only the first 18 bytes are read).
+ *
+ * Calling sequence: mla_decode_plan() on the host for a batch layout (it reads
+ * only the host copy of kv_indptr), mla_decode_workspace_bytes() for the size
+ * of the caller-owned device workspace, then mla_decode_fwd() for each call on
+ * that layout.  The library never allocates device memory, never synchronises
+ * the stream and never exits the process: every entry point returns an
+ * mla_status.  All device buffers are owned by the caller.
+ *
+ * Threading: entry points are reentrant.  Calls that share one workspace must
+ * be ordered on the GPU (same stream, or events); overlapping calls on one
+ * workspace race.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_NUM_HEADS 16
+#define MLA_QK_DIM 576
+#define MLA_V_DIM 512
+#define MLA_MX_BLOCK 32
+#define MLA_MX_SCALES_PER_ROW 18
+#define MLA_MAX_BATCH 65536
+
+typedef enum {
+  MLA_KV_BF16 = 0,
+  MLA_KV_FP8_E4M3 = 1,
+  MLA_KV_MXFP4 = 2
+} mla_kv_dtype;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,          /* null/misaligned pointer, bad size or layout */
+  MLA_ERR_UNSUPPORTED = 2,          /* a shape or dtype this library does not implement */
+  MLA_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < mla_decode_workspace_bytes(plan) */
+  MLA_ERR_CUDA = 4,                 /* a CUDA runtime call or a kernel launch failed */
+  MLA_ERR_DEVICE_INDEX = 5,         /* a kernel found kv_indptr inconsistent with the plan */
+  MLA_ERR_DEVICE_TIMEOUT = 6,       /* a kernel gave up waiting for its own copies */
+  MLA_ERR_NO_DEVICE = 7             /* no CUDA device is visible */
+} mla_status;
+
+/*
+ * The work decomposition of one batch layout (split-K over the KV sequence).
+ * With R = tile_tokens (64 rows for bf16 KV, 128 for e4m3 and e2m1 KV),
+ * sequence b with L_b = kv_indptr[b+1] - kv_indptr[b] rows and
+ * T_b = ceil(L_b / R) row tiles is cut into
+ *   S_b = L_b == 0 ? 1 : min(max_splits, ceil(L_b / chunk_tokens), T_b)
+ * contiguous splits on tile boundaries, split s covering rows
+ *   [kv_indptr[b] + R floor(s T_b / S_b), kv_indptr[b] + min(L_b, R floor((s+1) T_b / S_b))),
+ * so no split is empty when L_b > 0.  Work unit u (0 <= u < num_work) is split
+ * s of sequence b with u = sum_{b' < b} S_b' + s; CTA c of the grid processes
+ * units c, c + grid, c + 2 grid, ...  Fields are filled by mla_decode_plan and
+ * must not be edited.
+ */
+typedef struct {
+  int32_t batch;          /* number of sequences */
+  int32_t kv_dtype;       /* mla_kv_dtype */
+  int32_t total_kv;       /* kv_indptr[batch]: rows of the KV tensor that are read */
+  int32_t chunk_tokens;   /* split length target (tokens) */
+  int32_t max_splits;     /* cap on S_b */
+  int32_t num_work;       /* sum_b S_b = work units = partial slots in the workspace */
+  int32_t grid;           /* CTAs of the split kernel (<= num_sms) */
+  int32_t num_sms;        /* SM count the plan was made for */
+  int32_t splits_max;     /* max_b S_b (1: no combine kernel is launched) */
+  int32_t tile_tokens;    /* R: KV rows per pipeline tile (splits end on tile boundaries) */
+  int32_t units_per_cta;  /* ceil(num_work / grid) */
+  int32_t reserved[5];
+} mla_plan;
+
+/*
+ * mla_decode_plan -- host only; reads kv_indptr_host[0..batch] (int32, the host
+ * copy of the device kv_indptr passed to mla_decode_fwd).  kv_indptr must be
+ * non-decreasing with kv_indptr[0] >= 0.  num_sms <= 0 queries the current
+ * device.  num_splits > 0 forces S_b = min(num_splits, T_b) (at least 1);
+ * num_splits == 0 lets the planner choose a split length that balances the
+ * units over num_sms CTAs.  Returns MLA_OK and fills *plan, or an error code and
+ * leaves *plan untouched.  Never calls CUDA when num_sms > 0.
+ */
+MLA_API int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dtype,
+                    int32_t num_sms, int32_t num_splits, mla_plan* plan);
+
+/* Bytes of device workspace mla_decode_fwd needs for this plan (0 on a null plan).
+ * The workspace holds fp32 partial outputs and lse values of the split units, a
+ * per-sequence split table and an error word; its content between calls is
+ * irrelevant except for the error word (see mla_decode_poll_error). */
+MLA_API size_t mla_decode_workspace_bytes(const mla_plan* plan);
+
+/*
+ * mla_decode_fwd -- enqueue one decode on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream).  Asynchronous: returns after launching.
+ *
+ *   q          device, bf16 [*, 16, 576] row-major; sequence b uses row qo_indptr[b].
+ *              16-byte aligned.
+ *   kv         device, see the storage table above; rows [0, plan->total_kv) are read.
+ *              16-byte aligned.
+ *   kv_scale   device: NULL for bf16; fp32[1] for fp8 (dequant = e4m3 * kv_scale[0]);
+ *              uint8 e8m0 [plan->total_kv, scale_stride] for mxfp4.
+ *   scale_stride  mxfp4: bytes between scale rows, >= 18 and even; otherwise 0.
+ *   kv_indptr  device int32 [batch+1], equal to the host copy the plan was made from.
+ *   qo_indptr  device int32 [batch+1]; only qo_indptr[b] (the query row of b) is read.
+ *   out        device, bf16 [batch, 16, 512] row-major (written).  8-byte aligned.
+ *   lse        device fp32 [batch, 16] (written) or NULL.
+ *   sm_scale   softmax scale (1/24 for this problem).
+ *   workspace  device, >= mla_decode_workspace_bytes(plan) bytes, 256-byte aligned.
+ *
+ * Returns MLA_OK, MLA_ERR_INVALID_ARG / MLA_ERR_WORKSPACE_TOO_SMALL (nothing was
+ * launched) or MLA_ERR_CUDA (a launch failed).  Device-side faults in the index
+ * data are reported by mla_decode_poll_error, not here.
+ */
+MLA_API int mla_decode_fwd(const void* q, const void* kv, const void* kv_scale, int32_t scale_stride,
+                   const int32_t* kv_indptr, const int32_t* qo_indptr, void* out, float* lse,
+                   float sm_scale, const mla_plan* plan, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/*
+ * The two stages of mla_decode_fwd, for callers that schedule them separately
+ * (e.g. to time or overlap them).  mla_decode_split takes exactly the arguments
+ * of mla_decode_fwd and launches only the split kernel: sequences with one
+ * split get their final out/lse, split sequences leave fp32 partials in the
+ * workspace.  mla_decode_combine then merges those partials into out/lse
+ * (log-sum-exp combine; submission 593653's stage-2 kernel _flash_fp8_split_s2)
+ * and launches nothing when plan->splits_max <= 1.  It must follow the split
+ * stage on the same stream with the same plan, workspace, out and lse.
+ */
+MLA_API int mla_decode_split(const void* q, const void* kv, const void* kv_scale, int32_t scale_stride,
+                             const int32_t* kv_indptr, const int32_t* qo_indptr, void* out, float* lse,
+                             float sm_scale, const mla_plan* plan, void* workspace, size_t workspace_bytes,
+                             void* stream);
+MLA_API int mla_decode_combine(void* out, float* lse, const mla_plan* plan, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/*
+ * mla_decode_poll_error -- synchronises `stream`, reads and clears the error
+ * word a kernel leaves in `workspace` (MLA_ERR_DEVICE_INDEX when kv_indptr on
+ * the device disagreed with the plan -- the offending units are skipped;
+ * MLA_ERR_DEVICE_TIMEOUT when a kernel stopped waiting for its own copies).
+ * Returns MLA_OK when the word was clear.  For tests and debugging.
+ */
+MLA_API int mla_decode_poll_error(void* workspace, void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+MLA_API const char* mla_status_string(int status);
+
+/* Library version, "major.minor.patch". */
+MLA_API const char* mla_decode_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H */

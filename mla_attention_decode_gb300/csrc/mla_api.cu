@@ -1,0 +1,418 @@
+// mla_api.cu -- C ABI of libmla_decode.so: split planner, workspace sizing,
+// argument validation and kernel launches (see include/mla_decode.h).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "mla_decode.h"
+#include "mla_internal.h"
+
+namespace {
+
+using mla::kHeads;
+using mla::kMaxUnitsPerCta;
+using mla::kTile;
+using mla::kVDim;
+
+constexpr int32_t kNoCap = 1 << 30;
+
+// KV rows per pipeline tile of each kernel: 64 (bf16, warp-level MMA) or 128
+// (e4m3 and e2m1, one tcgen05 M=128 block).  Splits end on tile boundaries.
+int tile_rows(int kv_dtype) { return kv_dtype == MLA_KV_BF16 ? 64 : 128; }
+
+int rows_bytes(int kv_dtype) {
+  switch (kv_dtype) {
+    case MLA_KV_BF16: return 1152;
+    case MLA_KV_FP8_E4M3: return 576;
+    default: return 288 + 18;
+  }
+}
+
+// Split count of a sequence of `len` rows (the rule stated in mla_decode.h):
+// ceil(len / chunk), capped by `cap` and by the number of 64-row tiles.
+int32_t splits_for(int64_t len, int32_t chunk, int32_t cap, int tile) {
+  if (len <= 0) return 1;
+  int64_t s = (len + chunk - 1) / chunk;
+  const int64_t tiles = (len + tile - 1) / tile;
+  if (s > cap) s = cap;
+  if (s > tiles) s = tiles;
+  return static_cast<int32_t>(s < 1 ? 1 : s);
+}
+
+// Rows of split i of S of a sequence of len rows (splits end on tile boundaries).
+int64_t split_rows(int64_t len, int32_t i, int32_t s, int tile) {
+  if (len <= 0) return 0;
+  const int64_t tiles = (len + tile - 1) / tile;
+  const int64_t a = tile * (i * tiles / s);
+  int64_t b = tile * ((i + 1) * tiles / s);
+  if (b > len) b = len;
+  return b - a;
+}
+
+// Modelled duration (in units of one pipeline tile of this dtype) of a plan:
+// the busiest CTA's tiles plus a fixed cost per unit, plus the combine kernel
+// when any sequence is split (a fixed part and its partial traffic spread over
+// the SMs).  Units are dealt round-robin, as the kernel does.
+double plan_cost(const std::vector<int64_t>& lens, int32_t chunk, int32_t cap, int num_sms, int kv_dtype,
+                 int64_t* work_out) {
+  const double kUnitCost = 0.5, kCombineFixed = 2.0;
+  const int tile = tile_rows(kv_dtype);
+  int64_t work = 0, split_units = 0;
+  for (int64_t L : lens) {
+    const int32_t s = splits_for(L, chunk, cap, tile);
+    work += s;
+    if (s > 1) split_units += s;
+  }
+  *work_out = work;
+  if (work == 0) return 0.0;
+  const int64_t grid = work < num_sms ? work : num_sms;
+  std::vector<double> load(static_cast<size_t>(grid), 0.0);
+  int64_t u = 0;
+  for (int64_t L : lens) {
+    const int32_t s = splits_for(L, chunk, cap, tile);
+    for (int32_t i = 0; i < s; ++i, ++u) {
+      const int64_t rows = split_rows(L, i, s, tile);
+      load[static_cast<size_t>(u % grid)] += (double)((rows + tile - 1) / tile) + kUnitCost;
+    }
+  }
+  double mk = 0.0;
+  for (double v : load) mk = v > mk ? v : mk;
+  if (split_units > 0) {
+    const double tile_bytes = (double)tile * rows_bytes(kv_dtype);
+    const double partial_bytes = (double)kHeads * (kVDim + 1) * 4.0;
+    mk += kCombineFixed + (double)split_units * partial_bytes / ((double)num_sms * tile_bytes);
+  }
+  return mk;
+}
+
+// cuTensorMapEncodeTiled from the driver, fetched through the runtime once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// KV rows viewed as (span bytes, 9 chunks, rows) with the matching swizzle, so a
+// box of `box_rows` rows lands densely in smem with 16-byte units permuted.
+// e4m3 KV rows as a 2-D byte tensor (576, rows); a box is one 64-byte column
+// block of 128 rows, landed with the 64-byte swizzle (the tcgen05 operand layout).
+bool encode_kv_map_tc(CUtensorMap* m, const void* kv, int32_t total_kv) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {576, (cuuint64_t)(total_kv > 0 ? total_kv : 1)};
+  const cuuint64_t strides[1] = {576};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_kv_map(CUtensorMap* m, const void* kv, int kv_dtype, int32_t total_kv, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const uint32_t span = kv_dtype == MLA_KV_BF16 ? 128 : (kv_dtype == MLA_KV_FP8_E4M3 ? 64 : 32);
+  const CUtensorMapSwizzle sw = kv_dtype == MLA_KV_BF16 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : (kv_dtype == MLA_KV_FP8_E4M3 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+  const cuuint64_t dims[3] = {span, 9, (cuuint64_t)(total_kv > 0 ? total_kv : 1)};
+  const cuuint64_t strides[2] = {span, 9ull * span};
+  const cuuint32_t box[3] = {span, 9, box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(kv), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int device_sm_count(int32_t* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_NO_DEVICE;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  *out = n;
+  return MLA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dtype, int32_t num_sms,
+                    int32_t num_splits, mla_plan* plan) {
+  if (!kv_indptr_host || !plan) return MLA_ERR_INVALID_ARG;
+  if (batch < 0 || batch > MLA_MAX_BATCH) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype < MLA_KV_BF16 || kv_dtype > MLA_KV_MXFP4) return MLA_ERR_UNSUPPORTED;
+  if (num_splits < 0) return MLA_ERR_INVALID_ARG;
+  if (kv_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
+  std::vector<int64_t> lens(static_cast<size_t>(batch));
+  int64_t lmax = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int64_t L = (int64_t)kv_indptr_host[b + 1] - kv_indptr_host[b];
+    if (L < 0) return MLA_ERR_INVALID_ARG;
+    lens[static_cast<size_t>(b)] = L;
+    if (L > lmax) lmax = L;
+  }
+  int32_t sms = num_sms;
+  if (sms <= 0) {
+    const int rc = device_sm_count(&sms);
+    if (rc != MLA_OK) return rc;
+  }
+  const int64_t unit_cap = (int64_t)sms * kMaxUnitsPerCta;
+
+  int32_t chunk = 1, cap = kNoCap;
+  int64_t work = 0;
+  if (num_splits > 0) {
+    chunk = 1;
+    cap = num_splits;
+    plan_cost(lens, chunk, cap, sms, kv_dtype, &work);
+    if (work > unit_cap) return MLA_ERR_UNSUPPORTED;
+  } else {
+    const int tile = tile_rows(kv_dtype);
+    // candidates: split counts 1..256 of the longest sequence, as 64-row multiples
+    double best = -1.0;
+    int32_t best_chunk = 0;
+    int32_t prev = -1;
+    const int64_t lref = lmax > 0 ? lmax : 1;
+    for (int s = 1; s <= 256; ++s) {
+      int64_t c = (lref + s - 1) / s;
+      c = (c + tile - 1) / tile * tile;
+      if (c > lref) c = lref;
+      if (c < 1) c = 1;
+      if (c == prev) continue;
+      prev = static_cast<int32_t>(c);
+      int64_t w = 0;
+      const double cost = plan_cost(lens, static_cast<int32_t>(c), kNoCap, sms, kv_dtype, &w);
+      if (w > unit_cap) continue;
+      if (best < 0.0 || cost < best - 1e-9) {
+        best = cost;
+        best_chunk = static_cast<int32_t>(c);
+      }
+      if (c <= tile) break;
+    }
+    if (best < 0.0) return MLA_ERR_UNSUPPORTED;  // too many sequences for the unit table
+    chunk = best_chunk;
+    cap = kNoCap;
+    plan_cost(lens, chunk, cap, sms, kv_dtype, &work);
+  }
+  if (work > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  int32_t smax = 0;
+  for (int64_t L : lens) {
+    const int32_t s = splits_for(L, chunk, cap, tile_rows(kv_dtype));
+    smax = s > smax ? s : smax;
+  }
+  mla_plan p;
+  std::memset(&p, 0, sizeof p);
+  p.batch = batch;
+  p.kv_dtype = kv_dtype;
+  p.total_kv = kv_indptr_host[batch];
+  p.chunk_tokens = chunk;
+  p.max_splits = cap;
+  p.num_work = static_cast<int32_t>(work);
+  p.grid = static_cast<int32_t>(work < sms ? work : sms);
+  p.num_sms = sms;
+  p.splits_max = smax;
+  p.tile_tokens = tile_rows(kv_dtype);
+  p.units_per_cta = p.grid > 0 ? (p.num_work + p.grid - 1) / p.grid : 0;
+  *plan = p;
+  return MLA_OK;
+}
+
+size_t mla_decode_workspace_bytes(const mla_plan* plan) {
+  if (!plan) return 0;
+  return mla::ws_layout(plan->batch, plan->num_work).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validates the arguments of one decode and fills the split-kernel parameters.
+int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_stride, const int32_t* kv_indptr,
+            const int32_t* qo_indptr, void* out, float* lse, float sm_scale, const mla_plan* plan, void* workspace,
+            size_t workspace_bytes, mla::Stage1Params* p, bool* nothing_to_do) {
+  *nothing_to_do = false;
+  if (!plan) return MLA_ERR_INVALID_ARG;
+  if (plan->kv_dtype < MLA_KV_BF16 || plan->kv_dtype > MLA_KV_MXFP4) return MLA_ERR_UNSUPPORTED;
+  if (plan->batch < 0 || plan->num_work < 0 || plan->grid < 0 || plan->chunk_tokens <= 0 || plan->max_splits <= 0)
+    return MLA_ERR_INVALID_ARG;
+  if (plan->batch == 0 || plan->num_work == 0) {
+    *nothing_to_do = true;
+    return MLA_OK;
+  }
+  if (plan->units_per_cta > kMaxUnitsPerCta || plan->grid <= 0) return MLA_ERR_INVALID_ARG;
+  if (!q || !kv || !kv_indptr || !qo_indptr || !out || !workspace) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 8) || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+  if (!aligned(kv_indptr, 4) || !aligned(qo_indptr, 4) || (lse && !aligned(lse, 4))) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
+  if (plan->kv_dtype == MLA_KV_FP8_E4M3 && (!kv_scale || !aligned(kv_scale, 4))) return MLA_ERR_INVALID_ARG;
+  if (plan->kv_dtype == MLA_KV_MXFP4 && (!kv_scale || scale_stride < MLA_MX_SCALES_PER_ROW))
+    return MLA_ERR_INVALID_ARG;
+  const mla::WsLayout w = mla::ws_layout(plan->batch, plan->num_work);
+  if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p->q = static_cast<const uint8_t*>(q);
+  p->kv = static_cast<const uint8_t*>(kv);
+  p->kv_scale = kv_scale;
+  p->scale_stride = plan->kv_dtype == MLA_KV_MXFP4 ? scale_stride : 0;
+  p->kv_indptr = kv_indptr;
+  p->qo_indptr = qo_indptr;
+  p->out = static_cast<uint16_t*>(out);
+  p->lse = lse;
+  p->sm_scale = sm_scale;
+  p->ws_err = reinterpret_cast<int32_t*>(ws + w.err);
+  p->ws_seq = reinterpret_cast<int32_t*>(ws + w.seq);
+  p->ws_lse = reinterpret_cast<float*>(ws + w.lse);
+  p->ws_o = reinterpret_cast<float*>(ws + w.o);
+  p->batch = plan->batch;
+  p->total_kv = plan->total_kv;
+  p->chunk_tokens = plan->chunk_tokens;
+  p->max_splits = plan->max_splits;
+  p->num_work = plan->num_work;
+  p->grid = plan->grid;
+  if (plan->kv_dtype == MLA_KV_FP8_E4M3) {
+    if (!encode_kv_map_tc(&p->tmap_kv64, kv, plan->total_kv)) return MLA_ERR_CUDA;
+    std::memcpy(&p->tmap_kv16, &p->tmap_kv64, sizeof(CUtensorMap));
+  } else if (!encode_kv_map(&p->tmap_kv64, kv, plan->kv_dtype, plan->total_kv, 64) ||
+             !encode_kv_map(&p->tmap_kv16, kv, plan->kv_dtype, plan->total_kv, 16)) {
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+int launch_split_stage(const mla::Stage1Params& p, int kv_dtype, cudaStream_t s) {
+  cudaError_t e;
+  switch (kv_dtype) {
+    case MLA_KV_BF16: e = mla::launch_stage1_bf16(p, s); break;
+    case MLA_KV_FP8_E4M3: e = mla::launch_stage1_fp8(p, s); break;
+    default: e = mla::launch_stage1_mxfp4(p, s); break;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+int launch_combine_stage(const mla::Stage1Params& p, const mla_plan* plan, cudaStream_t s) {
+  if (plan->splits_max <= 1) return MLA_OK;
+  mla::CombineParams c;
+  c.ws_seq = p.ws_seq;
+  c.ws_lse = p.ws_lse;
+  c.ws_o = p.ws_o;
+  c.out = p.out;
+  c.lse = p.lse;
+  c.batch = plan->batch;
+  if (mla::launch_combine(c, s, true) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_fwd(const void* q, const void* kv, const void* kv_scale, int32_t scale_stride,
+                   const int32_t* kv_indptr, const int32_t* qo_indptr, void* out, float* lse, float sm_scale,
+                   const mla_plan* plan, void* workspace, size_t workspace_bytes, void* stream) {
+  mla::Stage1Params p;
+  bool noop = false;
+  int rc = prepare(q, kv, kv_scale, scale_stride, kv_indptr, qo_indptr, out, lse, sm_scale, plan, workspace,
+                   workspace_bytes, &p, &noop);
+  if (rc != MLA_OK || noop) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = launch_split_stage(p, plan->kv_dtype, s);
+  if (rc != MLA_OK) return rc;
+  return launch_combine_stage(p, plan, s);
+}
+
+int mla_decode_split(const void* q, const void* kv, const void* kv_scale, int32_t scale_stride,
+                     const int32_t* kv_indptr, const int32_t* qo_indptr, void* out, float* lse, float sm_scale,
+                     const mla_plan* plan, void* workspace, size_t workspace_bytes, void* stream) {
+  mla::Stage1Params p;
+  bool noop = false;
+  int rc = prepare(q, kv, kv_scale, scale_stride, kv_indptr, qo_indptr, out, lse, sm_scale, plan, workspace,
+                   workspace_bytes, &p, &noop);
+  if (rc != MLA_OK || noop) return rc;
+  return launch_split_stage(p, plan->kv_dtype, static_cast<cudaStream_t>(stream));
+}
+
+int mla_decode_combine(void* out, float* lse, const mla_plan* plan, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  if (!plan) return MLA_ERR_INVALID_ARG;
+  if (plan->batch <= 0 || plan->num_work <= 0 || plan->splits_max <= 1) return MLA_OK;
+  if (!out || !workspace || !aligned(out, 8) || !aligned(workspace, 256) || (lse && !aligned(lse, 4)))
+    return MLA_ERR_INVALID_ARG;
+  const mla::WsLayout w = mla::ws_layout(plan->batch, plan->num_work);
+  if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  mla::Stage1Params p;
+  std::memset(&p, 0, sizeof p);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.ws_seq = reinterpret_cast<int32_t*>(ws + w.seq);
+  p.ws_lse = reinterpret_cast<float*>(ws + w.lse);
+  p.ws_o = reinterpret_cast<float*>(ws + w.o);
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  return launch_combine_stage(p, plan, static_cast<cudaStream_t>(stream));
+}
+
+int mla_decode_poll_error(void* workspace, void* stream) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  int32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  if (word != 0) {
+    if (cudaMemset(workspace, 0, sizeof word) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+  }
+  return word;
+}
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size or layout)";
+    case MLA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than mla_decode_workspace_bytes(plan)";
+    case MLA_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+    case MLA_ERR_DEVICE_INDEX: return "kernel found kv_indptr inconsistent with the plan";
+    case MLA_ERR_DEVICE_TIMEOUT: return "kernel timed out waiting for its own copies";
+    case MLA_ERR_NO_DEVICE: return "no CUDA device visible";
+    default: return "unknown status";
+  }
+}
+
+const char* mla_decode_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,172 @@
+// mla_common.cuh -- pieces shared by the decode kernels: the work-unit list,
+// bounded mbarrier waits, small warp reductions and the two-term e4m3 encoding.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "mla_internal.h"
+#include "mla_ptx.cuh"
+
+namespace mla {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s: a wait this long means a lost copy
+
+struct UnitDesc {
+  int32_t b, start, end, u;  // u: work unit index; bit 31 set when the sequence has one split
+};
+constexpr int32_t kFinalFlag = (int32_t)0x80000000;
+
+// Bounded mbarrier wait.  Returns false (after flagging the error) if the phase
+// did not complete within kWaitTimeoutNs, or immediately if another thread of
+// the CTA already gave up; the caller then carries on without the data so that
+// every warp still reaches the same named barriers and the kernel ends.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           int32_t* ws_err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (*abort_flag) return false;
+    // sleep in the barrier (up to 0.1 ms per try) instead of spinning, so that
+    // waiting warps leave the issue slots to the warps doing work
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1;
+      atomicCAS(ws_err, 0, kErrDeviceTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float quad_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+  return v;
+}
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  return v;
+}
+
+// Two-term e4m3 encoding of four floats: hi = e4m3(x), lo = e4m3(x - hi).
+// Byte i of each word holds element i.
+__device__ __forceinline__ void two_term_e4m3(float x0, float x1, float x2, float x3, uint32_t& hi,
+                                              uint32_t& lo) {
+  const uint32_t h01 = f32x2_to_e4m3x2(x0, x1), h23 = f32x2_to_e4m3x2(x2, x3);
+  const float2 b01 = __half22float2(e4m3x2_to_h2(h01));
+  const float2 b23 = __half22float2(e4m3x2_to_h2(h23));
+  hi = h01 | (h23 << 16);
+  lo = f32x2_to_e4m3x2(x0 - b01.x, x1 - b01.y) | (f32x2_to_e4m3x2(x2 - b23.x, x3 - b23.y) << 16);
+}
+
+__device__ __forceinline__ float4 bf16x4_to_f4(uint2 v) {
+  return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                     __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+}
+
+// ------------------------------------------------------------- unit list
+// Walks kv_indptr (one warp, 32 sequences per step) and writes the units owned
+// by this CTA to smem; CTA 0 also writes the per-sequence split table used by
+// the combine kernel.  Sequence b is cut into S_b splits on TILE-row tile
+// boundaries.  Inconsistent index data raises MLA_ERR_DEVICE_INDEX and the
+// affected sequences are treated as empty.
+template <int TILE>
+__device__ __forceinline__ int splits_of(int len, int chunk, int cap) {
+  if (len <= 0) return 1;
+  const int tiles = (len + TILE - 1) / TILE;
+  int s = (int)(((long long)len + chunk - 1) / chunk);
+  s = min(s, cap);
+  s = min(s, tiles);
+  return max(s, 1);
+}
+
+template <int TILE>
+__device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* units, int* s_nunits, int lane) {
+  int prefix = 0, count = 0;
+  bool bad = false;
+  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    const int b = b0 + lane;
+    int start = 0, end = 0, sb = 0;
+    if (b < p.batch) {
+      start = p.kv_indptr[b];
+      end = p.kv_indptr[b + 1];
+      if (start < 0 || end < start || end > p.total_kv || p.qo_indptr[b] < 0) {
+        bad = true;
+        start = end = 0;
+      }
+      sb = splits_of<TILE>(end - start, p.chunk_tokens, p.max_splits);
+    }
+    int incl = sb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int pb = prefix + incl - sb;
+    if (blockIdx.x == 0 && b < p.batch) {
+      // split table for the combine kernel; never point past the plan's slots
+      const bool fits = pb + sb <= p.num_work;
+      p.ws_seq[2 * b] = fits ? pb : 0;
+      p.ws_seq[2 * b + 1] = fits ? sb : 0;
+    }
+    int n = 0, first = 0;
+    if (b < p.batch) {
+      int off = (int)(((long long)blockIdx.x - pb) % p.grid);
+      if (off < 0) off += p.grid;
+      first = pb + off;
+      if (first < pb + sb) n = (pb + sb - 1 - first) / p.grid + 1;
+    }
+    int nincl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, nincl, o);
+      if (lane >= o) nincl += t;
+    }
+    const int pos = count + nincl - n;
+    const int tiles = (end - start + TILE - 1) / TILE;
+    for (int k = 0; k < n; ++k) {
+      const int u = first + k * p.grid;
+      const int s = u - pb;
+      if (pos + k >= kMaxUnitsPerCta || u >= p.num_work) {
+        bad = true;
+        continue;
+      }
+      UnitDesc d;
+      d.b = b;
+      d.start = start + TILE * (int)((long long)s * tiles / sb);
+      d.end = min(end, start + TILE * (int)((long long)(s + 1) * tiles / sb));
+      d.u = u | (sb == 1 ? kFinalFlag : 0);
+      units[pos + k] = d;
+    }
+    count += __shfl_sync(0xffffffffu, nincl, 31);
+    prefix += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (prefix != p.num_work) bad = true;
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    if (bad) atomicCAS(p.ws_err, 0, kErrDeviceIndex);
+    *s_nunits = min(count, kMaxUnitsPerCta);
+  }
+}
+
+// Cursor over the CTA's KV tiles in consumption order (unit by unit, TILE rows
+// at a time).  Warps that need it keep identical copies.
+struct TileCursor {
+  int k;   // unit index in the CTA's list
+  int t0;  // first row of the tile
+};
+__device__ __forceinline__ void cursor_skip_empty(TileCursor& c, const UnitDesc* units, int nunits) {
+  while (c.k < nunits && units[c.k].start >= units[c.k].end) ++c.k;
+  c.t0 = c.k < nunits ? units[c.k].start : 0;
+}
+template <int TILE>
+__device__ __forceinline__ void cursor_next(TileCursor& c, const UnitDesc* units, int nunits) {
+  c.t0 += TILE;
+  if (c.t0 >= units[c.k].end) {
+    ++c.k;
+    cursor_skip_empty(c, units, nunits);
+  }
+}
+
+}  // namespace mla

@@ -1,0 +1,81 @@
+// mla_internal.h -- parameters shared by the host API and the kernel launchers.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+constexpr int kHeads = 16;
+constexpr int kQkDim = 576;
+constexpr int kVDim = 512;
+constexpr int kTile = 64;              // KV rows per pipeline stage
+constexpr int kConsumerWarps = 8;      // 4 pairs; pair p scores rows [16p, 16p+16) of a tile
+constexpr int kThreads = kConsumerWarps * 32;
+constexpr int kMaxUnitsPerCta = 512;   // work units one CTA may own (unit table in smem)
+
+// Workspace layout (byte offsets from the 256-aligned base).
+struct WsLayout {
+  size_t err;      // int32 error word
+  size_t seq;      // int32 [batch][2] = {first unit, split count}
+  size_t lse;      // fp32 [num_work][16] partial lse (natural log)
+  size_t o;        // fp32 [num_work][16][512] normalised partial outputs
+  size_t total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int batch, int num_work) {
+  WsLayout w;
+  w.err = 0;
+  w.seq = 256;
+  w.lse = align_up(w.seq + sizeof(int32_t) * 2 * static_cast<size_t>(batch), 256);
+  w.o = align_up(w.lse + sizeof(float) * kHeads * static_cast<size_t>(num_work), 256);
+  w.total = align_up(w.o + sizeof(float) * kHeads * kVDim * static_cast<size_t>(num_work), 256);
+  return w;
+}
+
+struct Stage1Params {
+  CUtensorMap tmap_kv64;     // KV rows as (span bytes, 9 chunks, rows), swizzled; 64-row box
+  CUtensorMap tmap_kv16;     // the same with a 16-row box (ragged tails)
+  const uint8_t* q;          // bf16 [*, 16, 576]
+  const uint8_t* kv;         // row bytes depend on the dtype
+  const void* kv_scale;      // fp32[1] (fp8) or e8m0 [rows, scale_stride] (mxfp4)
+  int32_t scale_stride;
+  const int32_t* kv_indptr;
+  const int32_t* qo_indptr;
+  uint16_t* out;             // bf16 [batch, 16, 512]
+  float* lse;                // fp32 [batch, 16] or null
+  float sm_scale;
+  int32_t* ws_err;
+  int32_t* ws_seq;
+  float* ws_lse;
+  float* ws_o;
+  int32_t batch;
+  int32_t total_kv;
+  int32_t chunk_tokens;
+  int32_t max_splits;
+  int32_t num_work;
+  int32_t grid;
+};
+
+struct CombineParams {
+  const int32_t* ws_seq;
+  const float* ws_lse;
+  const float* ws_o;
+  uint16_t* out;
+  float* lse;
+  int32_t batch;
+};
+
+// Device error codes written to the workspace error word (match mla_status).
+constexpr int32_t kErrDeviceIndex = 5;
+constexpr int32_t kErrDeviceTimeout = 6;
+
+cudaError_t launch_stage1_bf16(const Stage1Params& p, cudaStream_t s);
+cudaError_t launch_stage1_fp8(const Stage1Params& p, cudaStream_t s);
+cudaError_t launch_stage1_mxfp4(const Stage1Params& p, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s, bool pdl);
+
+}  // namespace mla

@@ -1,0 +1,77 @@
+"""The C ABI library (no GPU needed): it loads, exports every declared symbol,
+and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mla_attention_decode_gb300 import binding, build
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    assert {"mla_decode_plan", "mla_decode_workspace_bytes", "mla_decode_fwd", "mla_decode_poll_error",
+            "mla_status_string", "mla_decode_version"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in mla_decode.h but not exported"
+
+
+def test_status_strings(lib):
+    from mla_attention_decode_gb300 import binding
+    for code in range(0, 8):
+        assert binding.mla_status_string(code) != "unknown status"
+    assert binding.mla_status_string(99) == "unknown status"
+    assert re.fullmatch(r"\d+\.\d+\.\d+", binding.mla_decode_version())
+
+
+def test_fwd_rejects_bad_arguments_without_cuda(lib):
+    from mla_attention_decode_gb300 import binding
+    plan = binding.mla_decode_plan([0, 10, 20], "fp8", num_sms=152)
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: validation fails first
+    # null plan
+    assert lib.mla_decode_fwd(fake, fake, fake, 0, fake, fake, fake, None, 1 / 24, None, fake, 1 << 30, None) == 1
+    # null q
+    assert lib.mla_decode_fwd(None, fake, fake, 0, fake, fake, fake, None, 1 / 24, ctypes.byref(plan), fake,
+                              1 << 30, None) == 1
+    # misaligned kv
+    assert lib.mla_decode_fwd(fake, P((1 << 20) + 8), fake, 0, fake, fake, fake, None, 1 / 24, ctypes.byref(plan),
+                              fake, 1 << 30, None) == 1
+    # fp8 without its scale
+    assert lib.mla_decode_fwd(fake, fake, None, 0, fake, fake, fake, None, 1 / 24, ctypes.byref(plan), fake,
+                              1 << 30, None) == 1
+    # workspace too small
+    assert lib.mla_decode_fwd(fake, fake, fake, 0, fake, fake, fake, None, 1 / 24, ctypes.byref(plan), fake,
+                              16, None) == 3
+    # non-finite sm_scale
+    assert lib.mla_decode_fwd(fake, fake, fake, 0, fake, fake, fake, None, float("nan"), ctypes.byref(plan), fake,
+                              1 << 30, None) == 1
+    # mxfp4 with a scale stride below 18
+    plan4 = binding.mla_decode_plan([0, 10, 20], "mxfp4", num_sms=152)
+    assert lib.mla_decode_fwd(fake, fake, fake, 17, fake, fake, fake, None, 1 / 24, ctypes.byref(plan4), fake,
+                              1 << 30, None) == 1
+
+
+def test_empty_batch_is_a_noop(lib):
+    from mla_attention_decode_gb300 import binding
+    plan = binding.mla_decode_plan([0], "bf16", num_sms=152)
+    assert plan.batch == 0 and plan.num_work == 0
+    assert lib.mla_decode_fwd(None, None, None, 0, None, None, None, None, 1 / 24, ctypes.byref(plan), None, 0,
+                              None) == 0

@@ -1,0 +1,211 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Tolerances.  The stated bar is |out - oracle| <= 2e-2 + 2e-2 |oracle| on the bf16
+output, and every case checks it.  Each case also holds a tighter internal gate
+derived from the arithmetic of the kernels:
+  * the output is rounded to bf16:            <= 2^-9 |oracle|
+  * the softmax weights enter P.V as bf16 (bf16 KV) or as two e4m3 terms
+    (fp8 KV), a relative error <= 2^-8 per weight, so feature j moves by at
+    most 2^-8 max_t |v[t, j]| over the sequence's rows
+  * fp32 accumulation, two-term (bf16-exact) query: 1e-3 absolute slack
+so |out - oracle| <= 1e-3 + 2^-9 |oracle| + 2^-8 max_t |v[t, j]| per element,
+plus relative Frobenius error <= 1e-2 and |lse - oracle| <= 2e-3.  For long
+sequences (outputs O(0.05)) this is within ~2e-3 absolute, so a wrong but
+plausible kernel cannot pass.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as oracle_pkg
+from mla_attention_decode_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+CODES = {"bf16": 0, "fp8": 1, "mxfp4": 2}
+ABS_SLACK = 1e-3
+REL_FRO = 1e-2
+LSE_ABS = 2e-3
+
+
+def v_absmax(inp, seqs=None):
+    """max_t |v[t, j]| per sequence and feature, from an independent dequantisation."""
+    from oracle_pins import lib_dequant
+    ind = inp.kv_indptr.tolist()
+    out = []
+    for b in (range(inp.batch) if seqs is None else seqs):
+        a, e = ind[b], ind[b + 1]
+        if e <= a:
+            out.append(np.zeros(512))
+            continue
+        sub = synth.MLAInputs(inp.kv_dtype, inp.q, inp.kv_bf16, inp.kv[a:e], inp.kv_scale,
+                              None if inp.block_scales is None else inp.block_scales[a:e],
+                              torch.tensor([0, e - a], dtype=torch.int32), inp.qo_indptr[:2])
+        out.append(np.abs(lib_dequant(sub)[:, :512]).max(axis=0))
+    return np.stack(out)
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle_pkg.load()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from mla_attention_decode_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def gpu_decode(inp, num_splits=0, q=None, qo=None, kv_indptr_dev=None):
+    dev = torch.device("cuda:0")
+    dec = binding.MLADecoder(inp.kv_indptr, inp.kv_dtype, device=dev, num_splits=num_splits)
+    scale = inp.kv_scale if inp.kv_dtype == "fp8" else inp.block_scales
+    qq = inp.q if q is None else q
+    qo_ = inp.qo_indptr if qo is None else qo
+    ind = inp.kv_indptr.to(dev) if kv_indptr_dev is None else kv_indptr_dev
+    out, lse = dec(qq.to(dev), inp.kv.to(dev), ind, qo_.to(dev),
+                   kv_scale=None if scale is None else scale.to(dev))
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy(), lse.double().cpu().numpy(), dec
+
+
+def oracle_decode(orc, inp, q=None, qo=None, seqs=None):
+    ind = inp.kv_indptr
+    qo_ = inp.qo_indptr if qo is None else qo
+    if seqs is not None:  # a sample of sequences, indexing the full KV tensor
+        outs, lses = [], []
+        for b in seqs:
+            o, l = orc.decode(CODES[inp.kv_dtype], inp.q if q is None else q, inp.kv,
+                              np.array([int(ind[b]), int(ind[b + 1])], dtype=np.int32),
+                              np.array([int(qo_[b]), int(qo_[b]) + 1], dtype=np.int32),
+                              kv_scale=None if inp.kv_scale is None else inp.kv_scale.numpy(),
+                              block_scales=None if inp.block_scales is None else inp.block_scales.numpy())
+            outs.append(o[0])
+            lses.append(l[0])
+        return np.stack(outs), np.stack(lses)
+    return orc.decode(CODES[inp.kv_dtype], inp.q if q is None else q, inp.kv, ind, qo_,
+                      kv_scale=None if inp.kv_scale is None else inp.kv_scale.numpy(),
+                      block_scales=None if inp.block_scales is None else inp.block_scales.numpy())
+
+
+def assert_parity(got, ref, lse, ref_lse, what, vmax=None):
+    """vmax: [B, 512] per-sequence max |v| (None: use the output scale only)."""
+    assert got.shape == ref.shape
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    assert np.all(err <= 2e-2 + 2e-2 * np.abs(ref)), f"{what}: outside rtol=atol=2e-2"
+    bound = ABS_SLACK + 2.0 ** -9 * np.abs(ref)
+    if vmax is not None:
+        bound = bound + 2.0 ** -8 * vmax[:, None, :]
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert np.all(err <= bound), (f"{what}: internal gate: err {err[worst]:.3e} > bound {bound[worst]:.3e} at "
+                                  f"{worst} (ref {ref[worst]:.4f}, got {got[worst]:.4f})")
+    nrm = np.linalg.norm(ref)
+    if nrm > 0:
+        assert np.linalg.norm(got - ref) / nrm <= REL_FRO, f"{what}: rel fro {np.linalg.norm(got - ref) / nrm:.3e}"
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(fin, np.isfinite(lse)), f"{what}: lse finiteness differs"
+    assert np.all(np.isneginf(lse[~fin])), f"{what}: empty sequence lse must be -inf"
+    if fin.any():
+        assert np.max(np.abs(lse[fin] - ref_lse[fin])) <= LSE_ABS, f"{what}: lse err"
+
+
+DTYPES = ["bf16", "fp8"]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("num_splits", [0, 1, 3, 7])
+def test_ragged_small(orc, dtype, num_splits):
+    inp = synth.make_inputs([1, 33, 70, 0, 129, 200, 64, 2], dtype, seed=31)
+    got, lse, dec = gpu_decode(inp, num_splits=num_splits)
+    ref, ref_lse = oracle_decode(orc, inp)
+    assert_parity(got, ref, lse, ref_lse, f"ragged {dtype} splits={num_splits}", v_absmax(inp))
+    assert got[3].max() == 0 and got[3].min() == 0, "empty sequence output must be exactly 0"
+    assert dec.poll_error() == 0
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_many_short_sequences(orc, dtype):
+    rng = np.random.default_rng(5)
+    lens = rng.integers(0, 40, size=300).tolist()
+    inp = synth.make_inputs(lens, dtype, seed=37)
+    got, lse, dec = gpu_decode(inp)
+    ref, ref_lse = oracle_decode(orc, inp)
+    assert_parity(got, ref, lse, ref_lse, f"300 short {dtype}", v_absmax(inp))
+    assert dec.poll_error() == 0
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_one_long_sequence(orc, dtype):
+    inp = synth.make_inputs([40001], dtype, seed=41)
+    got, lse, _ = gpu_decode(inp)
+    ref, ref_lse = oracle_decode(orc, inp)
+    assert_parity(got, ref, lse, ref_lse, f"long {dtype}", v_absmax(inp))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_split_matches_unsplit(dtype):
+    inp = synth.make_inputs([3000, 5000, 1], dtype, seed=43)
+    a, la, _ = gpu_decode(inp, num_splits=1)
+    b, lb, _ = gpu_decode(inp, num_splits=0)
+    c, lc, _ = gpu_decode(inp, num_splits=17)
+    assert np.max(np.abs(a - b)) <= 1e-3 and np.max(np.abs(a - c)) <= 1e-3
+    assert np.max(np.abs(la - lb)) <= 1e-3 and np.max(np.abs(la - lc)) <= 1e-3
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_qo_indptr_and_large_logits(orc, dtype):
+    inp = synth.make_inputs([50, 90, 7], dtype, seed=47)
+    # query rows in a permuted order with a spare row
+    q = torch.cat([inp.q[2:3], torch.zeros_like(inp.q[:1]), inp.q[0:1], inp.q[1:2]]) * 8
+    q = q.to(torch.bfloat16)
+    qo = torch.tensor([2, 3, 0, 4], dtype=torch.int32)
+    got, lse, _ = gpu_decode(inp, q=q, qo=qo)
+    ref, ref_lse = oracle_decode(orc, inp, q=q, qo=qo)
+    assert_parity(got, ref, lse, ref_lse, f"qo_indptr x8 logits {dtype}", v_absmax(inp))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_identical_rows_give_the_row(dtype):
+    base = synth.make_inputs([1], dtype, seed=53)
+    L = 777
+    rows = base.kv.repeat(L, 1)
+    inp = synth.MLAInputs(dtype, base.q, base.kv_bf16, rows, base.kv_scale, None,
+                          torch.tensor([0, L], dtype=torch.int32), base.qo_indptr)
+    got, lse, _ = gpu_decode(inp)
+    if dtype == "bf16":
+        r = base.kv[0, :512].double().numpy()
+    else:
+        r = (base.kv.view(torch.float8_e4m3fn)[0, :512].double() * float(base.kv_scale[0])).numpy()
+    assert np.max(np.abs(got[0] - r[None, :])) <= 2e-3 * max(1.0, np.abs(r).max())
+
+
+def test_device_index_error_is_reported():
+    """kv_indptr on the device disagreeing with the plan: flagged, no fault."""
+    inp = synth.make_inputs([100, 100], "fp8", seed=59)
+    bad = inp.kv_indptr.clone()
+    bad[2] = 100000  # beyond the plan's total_kv: the kernel treats it as empty
+    _, _, dec = gpu_decode(inp, kv_indptr_dev=bad.cuda())
+    assert dec.poll_error() == binding.MLA_ERR_DEVICE_INDEX
+    assert dec.poll_error() == 0  # cleared by the first poll
+
+
+@pytest.mark.parametrize("name", ["bs4_kv1024_bf16", "bs32_kv1024_fp8", "bs4_kv8192_fp8"])
+def test_benchmark_workloads_full(orc, name):
+    inp = synth.make_workload(name)
+    got, lse, dec = gpu_decode(inp)
+    ref, ref_lse = oracle_decode(orc, inp)
+    assert_parity(got, ref, lse, ref_lse, name, v_absmax(inp))
+    assert dec.poll_error() == 0
+
+
+def test_benchmark_workload_bs64_kv8192_fp8_sampled(orc):
+    """The largest workload at full size, in the benchmark's launch
+    configuration; the oracle checks a sample of 12 sequences (all 16 heads)."""
+    inp = synth.make_workload("bs64_kv8192_fp8")
+    got, lse, dec = gpu_decode(inp)
+    seqs = [0, 1, 7, 13, 21, 30, 31, 32, 44, 50, 62, 63]
+    ref, ref_lse = oracle_decode(orc, inp, seqs=seqs)
+    assert_parity(got[seqs], ref, lse[seqs], ref_lse, "bs64_kv8192_fp8 sampled", v_absmax(inp, seqs))
+    assert dec.poll_error() == 0

@@ -1,0 +1,100 @@
+"""Host split planner: exact partition of every sequence, no empty split, the
+unit numbering the kernels assume (checked by brute force on the CPU)."""
+import itertools
+import random
+
+import pytest
+
+from mla_attention_decode_gb300 import binding
+
+
+def n_splits(plan, L):
+    if L <= 0:
+        return 1
+    return max(1, min(plan.max_splits, -(-L // plan.chunk_tokens), -(-L // plan.tile_tokens)))
+
+
+def units_of(plan, lens):
+    """The split ranges the plan defines (the rule stated in mla_decode.h)."""
+    out = []
+    start = 0
+    for L in lens:
+        s = n_splits(plan, L)
+        R = plan.tile_tokens
+        t = -(-max(L, 0) // R)
+        for i in range(s):
+            out.append((start + R * (i * t // s), start + min(L, R * ((i + 1) * t // s)) if L > 0 else start))
+        start += max(L, 0)
+    return out
+
+
+def check_plan(lens, dtype="fp8", num_sms=152, num_splits=0):
+    ind = [0] + list(itertools.accumulate(lens))
+    plan = binding.mla_decode_plan(ind, dtype, num_sms=num_sms, num_splits=num_splits)
+    us = units_of(plan, lens)
+    assert plan.num_work == len(us)
+    assert plan.batch == len(lens) and plan.total_kv == ind[-1]
+    assert plan.grid == min(plan.num_work, num_sms)
+    assert plan.units_per_cta == -(-plan.num_work // plan.grid)
+    # contiguous, ordered, exact cover of each sequence; no empty split of a non-empty sequence
+    pos = 0
+    k = 0
+    smax = 0
+    for L, b0 in zip(lens, ind):
+        s = n_splits(plan, L)
+        smax = max(smax, s)
+        assert s >= 1
+        if L > 0:
+            assert s <= -(-L // plan.tile_tokens)
+        cur = b0
+        for i in range(s):
+            a, b = us[k]
+            assert a == cur and b >= a
+            if L > 0:
+                assert b > a, "empty split"
+                assert (a - b0) % plan.tile_tokens == 0, "split does not start on a tile boundary"
+            cur = b
+            k += 1
+        assert cur == b0 + max(L, 0)
+    assert plan.splits_max == smax
+    return plan
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "mxfp4"])
+def test_benchmark_shapes(dtype):
+    for b, L in [(4, 1024), (32, 1024), (4, 8192), (64, 8192), (32, 8192), (256, 1024), (256, 8192)]:
+        plan = check_plan([L] * b, dtype)
+        assert plan.grid <= 152
+        assert plan.tile_tokens == (64 if dtype == "bf16" else 128)
+
+
+def test_forced_splits():
+    for s in (1, 2, 3, 7, 64):
+        plan = check_plan([1, 5, 64, 1000, 0], num_splits=s)
+        assert plan.max_splits == s and plan.chunk_tokens == 1
+
+
+def test_random_ragged_sweep():
+    rng = random.Random(0)
+    for _ in range(300):
+        b = rng.randint(1, 80)
+        lens = [rng.choice([0, 1, 2, rng.randint(1, 300), rng.randint(1, 20000)]) for _ in range(b)]
+        sms = rng.choice([1, 7, 148, 152])
+        check_plan(lens, rng.choice(["bf16", "fp8", "mxfp4"]), num_sms=sms,
+                   num_splits=rng.choice([0, 0, 1, 2, 5]))
+
+
+def test_auto_plan_balances_benchmark_shapes():
+    # every configuration of the benchmark fills the 152 SMs with a balanced split
+    for b, L in [(32, 1024), (4, 8192), (64, 8192), (32, 8192)]:
+        plan = check_plan([L] * b, "fp8")
+        assert plan.grid == 152 or plan.num_work >= 128, plan.as_dict()
+
+
+def test_rejects_bad_layouts():
+    with pytest.raises(binding.MLAError):
+        binding.mla_decode_plan([0, 5, 3], "fp8", num_sms=152)  # decreasing
+    with pytest.raises(binding.MLAError):
+        binding.mla_decode_plan([-1, 5], "fp8", num_sms=152)
+    with pytest.raises(binding.MLAError):
+        binding.mla_decode_plan([0, 5], 7, num_sms=152)
