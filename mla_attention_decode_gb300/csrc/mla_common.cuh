@@ -81,7 +81,7 @@ __device__ __forceinline__ int splits_of(int len, int chunk, int cap) {
   return max(s, 1);
 }
 
-template <int TILE>
+template <int TILE, int MAX_UNITS = kMaxUnitsPerCta>
 __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* units, int* s_nunits, int lane) {
   int prefix = 0, count = 0;
   bool bad = false;
@@ -128,7 +128,7 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
     for (int k = 0; k < n; ++k) {
       const int u = first + k * p.grid;
       const int s = u - pb;
-      if (pos + k >= kMaxUnitsPerCta || u >= p.num_work) {
+      if (pos + k >= MAX_UNITS || u >= p.num_work) {
         bad = true;
         continue;
       }
@@ -146,7 +146,7 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
   bad = __any_sync(0xffffffffu, bad);
   if (lane == 0) {
     if (bad) atomicCAS(p.ws_err, 0, kErrDeviceIndex);
-    *s_nunits = min(count, kMaxUnitsPerCta);
+    *s_nunits = min(count, MAX_UNITS);
   }
 }
 

@@ -13,7 +13,7 @@ constexpr int kVDim = 512;
 constexpr int kTile = 64;              // KV rows per pipeline stage
 constexpr int kConsumerWarps = 8;      // 4 pairs; pair p scores rows [16p, 16p+16) of a tile
 constexpr int kThreads = kConsumerWarps * 32;
-constexpr int kMaxUnitsPerCta = 512;   // work units one CTA may own (unit table in smem)
+constexpr int kMaxUnitsPerCta = 256;   // work units one CTA may own (unit table in smem)
 
 // Workspace layout (byte offsets from the 256-aligned base).
 struct WsLayout {

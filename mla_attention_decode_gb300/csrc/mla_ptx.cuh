@@ -38,6 +38,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking probe of an mbarrier phase (returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // As mbar_try_wait, but the thread may be suspended (not spinning, issuing
 // nothing) for up to `suspend_ns` while the phase is incomplete.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
@@ -186,6 +199,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)(swizzle & 7u) << 61;
   return d;
+}
+// The address-free part of a shared-memory matrix descriptor.  A descriptor is
+// this plus (address >> 4); since the address field never carries into the
+// next one (shared addresses < 256 KB), moving an operand by d bytes is a
+// 64-bit add of d / 16.
+__host__ __device__ constexpr uint64_t desc_template(uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+  return ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)(swizzle & 7u) << 61);
 }
 // Instruction descriptor of kind::f8f6f4 with e4m3 A and B, fp32 accumulator.
 // a_mn / b_mn: operand stored MN-major (1) or K-major (0).

@@ -25,8 +25,9 @@
 // than 8 (log2 units), which keeps P <= 256 inside e4m3 range.  Scores are in
 // log2 units: s = (q . k) * sm_scale * log2(e) * kv_scale.
 //
-// Warp roles: 0 TMA producer (9 column boxes of 64 B x 128 rows per tile into
-// a 2-stage ring); 1 MMA issuer (QK of tile t, then PV of tile t-1) and TMEM
+// Warp roles: 0 TMA producer (9 column boxes of 64 B x 128 rows per tile: the
+// 8 V blocks in pairs into a ring of 10 pair slots, each released by the
+// commit after its P.V block, the rope block into a ring of 2); 1 MMA issuer (QK of tile t, then PV of tile t-1) and TMEM
 // owner; 2-3 query preparation (two-term query per unit, double buffered);
 // 4-7 softmax, O^T rescale and the unit epilogue.  Hand-offs are mbarriers
 // (TMA transaction bytes, tcgen05.commit, thread arrivals).
@@ -40,12 +41,14 @@ namespace mla {
 namespace tcfp8 {
 
 constexpr int kTileRows = 128;
-constexpr int kStages = 2;
 constexpr int kChunkBytes = kTileRows * 64;  // one 64-byte feature column block of a tile
-constexpr int kStageBytes = 9 * kChunkBytes;
+constexpr int kPairBytes = 2 * kChunkBytes;  // two column blocks = features [128 f, 128 f + 128)
+constexpr int kPairSlots = 10;               // ring of V column-block pairs (4 per tile)
+constexpr int kRopeSlots = 2;                // ring of the rope column block (features 512..575)
 constexpr int kQsBytes = 9 * 32 * 64;        // two-term query: 32 rows x 576 B, K-major, 64 B swizzle
 constexpr int kPBytes = kTileRows * 32;      // two-term P^T: 128 rows x 32 B, MN-major, 32 B swizzle
 constexpr int kThreads = 256;
+constexpr int kMaxUnits = 256;               // work units one CTA may own
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0;   // S^T double buffer: columns [0, 32) and [32, 64)
 constexpr uint32_t kColO = 64;  // O^T: 4 feature blocks x 32 columns
@@ -55,31 +58,35 @@ constexpr uint32_t kIdescQK = tc::idesc_e4m3(128, 32, 0, 0);
 constexpr uint32_t kIdescPV = tc::idesc_e4m3(128, 32, 1, 1);
 
 struct Layout {
-  static constexpr int stages = 0;                           // 1024-aligned
-  static constexpr int qs = stages + kStages * kStageBytes;  // [2]
-  static constexpr int pb = qs + 2 * kQsBytes;               // [2]
-  static constexpr int rq = pb + 2 * kPBytes;                // float [2][16] score factor per head
-  static constexpr int red = rq + 2 * 16 * 4;                // float [2][4 warps][16]
+  static constexpr int pairs = 0;                             // 1024-aligned
+  static constexpr int rope = pairs + kPairSlots * kPairBytes;
+  static constexpr int qs = rope + kRopeSlots * kChunkBytes;  // [2]
+  static constexpr int pb = qs + 2 * kQsBytes;                // [2]
+  static constexpr int rq = pb + 2 * kPBytes;                 // float [2][16] score factor per head
+  static constexpr int red = rq + 2 * 16 * 4;                 // float [2][4 warps][16]
   static constexpr int units = red + 2 * 4 * 16 * 4;
-  static constexpr int bars = units + kMaxUnitsPerCta * (int)sizeof(UnitDesc);
-  static constexpr int nbars = 19;
+  static constexpr int bars = units + kMaxUnits * (int)sizeof(UnitDesc);
+  static constexpr int nbars = 40;
   static constexpr int misc = bars + nbars * 8;  // tmem slot, abort flag, unit count
   static constexpr int total = misc + 16;
 };
 
 // mbarrier slots
 enum {
-  kKvFull = 0,    // [2] TMA bytes of a stage
-  kKvEmpty = 2,   // [2] commit after the P.V of the stage's tile
-  kQFull = 4,     // [2] query prepared (2 warps)
-  kQEmpty = 6,    // [2] commit after the unit's last QK
-  kSFull = 8,     // [2] commit after QK
-  kSEmpty = 10,   // [2] softmax read S (4 warps)
-  kPFull = 12,    // [2] P written, O^T rescaled (4 warps)
-  kODone = 14,    // commit after each P.V
-  kOFree = 15,    // unit epilogue read O^T (4 warps)
-  kRFree = 16,    // [2] softmax copied the unit's score factors (4 warps)
-  kFinal = 18,    // commit after the MMA issuer's last operation
+  kPairFull = 0,    // [10] TMA bytes of a V column-block pair
+  kPairEmpty = 10,  // [10] commit after the P.V block that read it
+  kRopeFull = 20,   // [2]  TMA bytes of a rope column block
+  kRopeEmpty = 22,  // [2]  commit after the QK that read it
+  kQFull = 24,      // [2]  query prepared (2 warps)
+  kQEmpty = 26,     // [2]  commit after the unit's last QK
+  kSFull = 28,      // [2]  commit after QK
+  kSEmpty = 30,     // [2]  softmax read S (4 warps)
+  kPFull = 32,      // [2]  P written, O^T rescaled (4 warps)
+  kODone = 34,      // commit after each tile's P.V
+  kOFree = 35,      // unit epilogue read O^T (4 warps)
+  kRFree = 36,      // [2]  softmax copied the unit's score factors (4 warps)
+  kFinal = 38,      // commit after the MMA issuer's last operation
+  kOLast = 39,      // commit after a unit's last P.V (once per unit with tiles)
 };
 
 __device__ __forceinline__ uint32_t sw64_off(int row, int col) {  // byte (row, col) of a 64 B-row, 64 B-swizzled block
@@ -98,28 +105,45 @@ struct Ctx {
 __device__ __forceinline__ int tiles_of(const UnitDesc& d) { return (d.end - d.start + kTileRows - 1) / kTileRows; }
 
 // ------------------------------------------------------------------ producer
+// Column blocks of tile t: pair f (features [128 f, 128 f + 128)) goes to pair
+// slot (4t + f) mod 10, the rope block to rope slot t mod 2; each slot is
+// re-armed as soon as the MMA that read it has completed.
+__device__ __forceinline__ int pair_slot(int t, int f) { return (4 * t + f) % kPairSlots; }
+__device__ __forceinline__ int pair_use(int t, int f) { return (4 * t + f) / kPairSlots; }
+
 __device__ void producer(const Stage1Params& p, const Ctx& x) {
   const uint64_t pol = policy_evict_first();  // KV rows are read once
   int it = 0;
-  int armed[2] = {0, 0};
+  int armed[kPairSlots + kRopeSlots];
+  for (int i = 0; i < kPairSlots + kRopeSlots; ++i) armed[i] = 0;
   for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
     const UnitDesc d = x.units[k];
-    for (int t0 = d.start; t0 < d.end; t0 += kTileRows, ++it) {
-      const int s = it & 1;
-      if (it >= 2) wait_phase(&x.bar[kKvEmpty + s], ((it >> 1) - 1) & 1, x.abort_flag, p.ws_err);
+    for (int t0 = d.start; t0 < d.end && !*x.abort_flag; t0 += kTileRows, ++it) {
+      for (int f = 0; f < 4; ++f) {
+        const int sl = pair_slot(it, f), use = pair_use(it, f);
+        if (use >= 1) wait_phase(&x.bar[kPairEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
+        if (*x.abort_flag) break;
+        uint8_t* dst = x.smem + Layout::pairs + sl * kPairBytes;
+        mbar_arrive_expect_tx(&x.bar[kPairFull + sl], kPairBytes);
+        tma_load_2d(dst, &p.tmap_kv64, 128 * f, t0, &x.bar[kPairFull + sl], pol);
+        tma_load_2d(dst + kChunkBytes, &p.tmap_kv64, 128 * f + 64, t0, &x.bar[kPairFull + sl], pol);
+        ++armed[sl];
+      }
+      const int rs = it % kRopeSlots, ruse = it / kRopeSlots;
+      if (ruse >= 1) wait_phase(&x.bar[kRopeEmpty + rs], (ruse - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
-      uint8_t* st = x.smem + Layout::stages + s * kStageBytes;
-      mbar_arrive_expect_tx(&x.bar[kKvFull + s], kStageBytes);
-      for (int c = 0; c < 9; ++c) tma_load_2d(st + c * kChunkBytes, &p.tmap_kv64, 64 * c, t0, &x.bar[kKvFull + s], pol);
-      ++armed[s];
+      mbar_arrive_expect_tx(&x.bar[kRopeFull + rs], kChunkBytes);
+      tma_load_2d(x.smem + Layout::rope + rs * kChunkBytes, &p.tmap_kv64, 512, t0, &x.bar[kRopeFull + rs], pol);
+      ++armed[kPairSlots + rs];
     }
   }
   if (*x.abort_flag) {
-    // a wait gave up somewhere: never leave with copies in flight (bounded wait per stage)
-    for (int s = 0; s < 2; ++s) {
-      if (armed[s] == 0) continue;
+    // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
+    for (int i = 0; i < kPairSlots + kRopeSlots; ++i) {
+      if (armed[i] == 0) continue;
+      uint64_t* bar = i < kPairSlots ? &x.bar[kPairFull + i] : &x.bar[kRopeFull + i - kPairSlots];
       const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(&x.bar[kKvFull + s], (armed[s] - 1) & 1) && global_timer_ns() - t0 < kWaitTimeoutNs) {
+      while (!mbar_try_wait(bar, (armed[i] - 1) & 1) && global_timer_ns() - t0 < kWaitTimeoutNs) {
       }
     }
   }
@@ -179,66 +203,145 @@ __device__ void prep_query(const Stage1Params& p, const Ctx& x, int j) {
 }
 
 // ------------------------------------------------------------------ MMA issuer
+// One thread issues every tensor-core operation.  Descriptors are built once per
+// tile from templates and moved by constant offsets, so that issuing an MMA
+// costs a few instructions (a single thread is slow at address arithmetic, and
+// the MMAs of this kernel only take ~46 cycles each on the tensor pipe).
+//
+// The QK of tile t and the P.V of tile t' run as two streams in one loop: the
+// P.V of a tile is issued as soon as its P is written (that releases its ring
+// slots), the QK of the next tile as soon as its columns have landed, with at
+// most two tiles between the streams (S and P are double buffered; issuing
+// QK(t) only after P.V(t-2) makes the commit of QK(t) also cover P.V(t-2), so
+// the softmax may overwrite P buffer t mod 2 once S(t) is ready).
 struct PvJob {
-  int it;       // tile index (P buffer / o_done phase)
-  int stage;
+  int it;       // tile index (slots, P buffer, o_done phase)
   int first;    // first tile of its unit
+  int last;     // last tile of its unit
   int ordinal;  // index of its unit among the CTA's units with tiles
 };
 
-__device__ __forceinline__ void issue_pv(const Stage1Params& p, const Ctx& x, const PvJob& j) {
-  wait_phase(&x.bar[kPFull + (j.it & 1)], (j.it >> 1) & 1, x.abort_flag, p.ws_err);
-  if (j.first && j.ordinal > 0) wait_phase(&x.bar[kOFree], (j.ordinal - 1) & 1, x.abort_flag, p.ws_err);
+constexpr uint64_t kTplK64 = tc::desc_template(16, 512, 4);          // K-major, 64 B swizzle
+constexpr uint64_t kTplV = tc::desc_template(kChunkBytes, 512, 4);   // V^T, MN-major, 64 B swizzle
+constexpr uint64_t kTplP = tc::desc_template(1024, 256, 6);          // P^T, MN-major, 32 B swizzle
+
+__device__ __forceinline__ int wrap_slot(int s) { return s >= kPairSlots ? s - kPairSlots : s; }
+
+__device__ __forceinline__ void issue_pv(const Ctx& x, const PvJob& j, uint32_t pairs0, uint32_t pb0) {
   tc::fence_after();
-  const uint32_t st = smem_u32(x.smem + Layout::stages + j.stage * kStageBytes);
-  const uint32_t pb = smem_u32(x.smem + Layout::pb + (j.it & 1) * kPBytes);
+  const uint64_t bp = kTplP + ((pb0 + (uint32_t)(j.it & 1) * kPBytes) >> 4);
+  const int s0 = (4 * j.it) % kPairSlots;
 #pragma unroll
-  for (int fb = 0; fb < 4; ++fb)
+  for (int fb = 0; fb < 4; ++fb) {
+    const int sl = wrap_slot(s0 + fb);
+    // V^T block: features [128 fb, 128 fb + 128) = the slot's two column blocks (LBO)
+    const uint64_t av = kTplV + ((pairs0 + (uint32_t)sl * kPairBytes) >> 4);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      // V^T block: features [128 fb, 128 fb + 128) = chunks 2fb, 2fb+1 (LBO), rows [32q, 32q+32)
-      const uint64_t a = tc::smem_desc(st + 2 * fb * kChunkBytes + q * 32 * 64, kChunkBytes, 512, 4);
-      const uint64_t b = tc::smem_desc(pb + q * 32 * 32, 1024, 256, 6);
-      tc::mma_f8(x.tmem + kColO + 32 * fb, a, b, kIdescPV, (j.first && q == 0) ? 0u : 1u);
-    }
+    for (int q = 0; q < 4; ++q)  // rows [32 q, 32 q + 32): +2048 B of V^T, +1024 B of P^T
+      tc::mma_f8(x.tmem + kColO + 32 * fb, av + q * (2048 >> 4), bp + q * (1024 >> 4), kIdescPV,
+                 (j.first && q == 0) ? 0u : 1u);
+    tc::commit(&x.bar[kPairEmpty + sl]);
+  }
   tc::commit(&x.bar[kODone]);
-  tc::commit(&x.bar[kKvEmpty + j.stage]);
+  if (j.last) tc::commit(&x.bar[kOLast]);
+}
+
+__device__ __forceinline__ void issue_qk(const Ctx& x, int it, int qb, uint32_t pairs0, uint32_t rope0,
+                                         uint32_t qs0) {
+  tc::fence_after();
+  const int s0 = (4 * it) % kPairSlots;
+  uint64_t ap[4];
+#pragma unroll
+  for (int f = 0; f < 4; ++f) ap[f] = kTplK64 + ((pairs0 + (uint32_t)wrap_slot(s0 + f) * kPairBytes) >> 4);
+  const uint64_t ar = kTplK64 + ((rope0 + (uint32_t)(it % kRopeSlots) * kChunkBytes) >> 4);
+  const uint64_t bq = kTplK64 + ((qs0 + (uint32_t)qb * kQsBytes) >> 4);
+  const uint32_t d = x.tmem + kColS + 32 * (it & 1);
+#pragma unroll
+  for (int ks = 0; ks < 18; ++ks) {
+    const int c = ks >> 1, half = ks & 1;
+    const uint64_t a = c < 8 ? ap[c >> 1] + (((c & 1) * kChunkBytes + 32 * half) >> 4) : ar + ((32 * half) >> 4);
+    tc::mma_f8(d, a, bq + ((c * 2048 + 32 * half) >> 4), kIdescQK, ks > 0 ? 1u : 0u);
+  }
+  tc::commit(&x.bar[kSFull + (it & 1)]);
+  tc::commit(&x.bar[kRopeEmpty + it % kRopeSlots]);
 }
 
 __device__ void mma_issuer(const Stage1Params& p, const Ctx& x) {
-  int it = 0, ordinal = 0;
-  PvJob prev{0, 0, 0, 0};
-  bool have_prev = false;
-  for (int k = 0; k < x.nunits; ++k) {
-    const UnitDesc d = x.units[k];
-    const int qb = k & 1;
-    wait_phase(&x.bar[kQFull + qb], (k >> 1) & 1, x.abort_flag, p.ws_err);
-    tc::fence_after();
-    const uint32_t qs = smem_u32(x.smem + Layout::qs + qb * kQsBytes);
-    const int nt = tiles_of(d);
-    for (int t = 0; t < nt; ++t, ++it) {
-      const int s = it & 1;
-      wait_phase(&x.bar[kKvFull + s], (it >> 1) & 1, x.abort_flag, p.ws_err);
-      if (it >= 2) wait_phase(&x.bar[kSEmpty + s], ((it >> 1) - 1) & 1, x.abort_flag, p.ws_err);
-      tc::fence_after();
-      const uint32_t st = smem_u32(x.smem + Layout::stages + s * kStageBytes);
-#pragma unroll
-      for (int ks = 0; ks < 18; ++ks) {
-        const int c = ks >> 1, half = ks & 1;
-        const uint64_t a = tc::smem_desc(st + c * kChunkBytes + 32 * half, 16, 512, 4);
-        const uint64_t b = tc::smem_desc(qs + c * 2048 + 32 * half, 16, 512, 4);
-        tc::mma_f8(x.tmem + kColS + 32 * s, a, b, kIdescQK, ks > 0 ? 1u : 0u);
+  const uint32_t pairs0 = smem_u32(x.smem + Layout::pairs), rope0 = smem_u32(x.smem + Layout::rope);
+  const uint32_t qs0 = smem_u32(x.smem + Layout::qs), pb0 = smem_u32(x.smem + Layout::pb);
+  PvJob pend[2] = {{0, 0, 0, 0}, {0, 0, 0, 0}};  // QK issued, P.V not yet (indexed by tile mod 2)
+  int qk_it = 0, pv_it = 0;                // next tile of each stream
+  int k = 0, t = 0, nt = -1;               // QK stream: unit, tile in unit, tiles of the unit (-1: not begun)
+  int ordinal = 0;
+  bool q_ok = false;
+  uint32_t idle = 0;
+  uint64_t idle_t0 = 0;
+  while (true) {
+    bool progressed = false;
+    // QK stream: step over finished units and, once their query buffer is
+    // filled, empty ones (never block here: pending P.V must still be issued)
+    while (k < x.nunits) {
+      if (nt < 0) {
+        nt = tiles_of(x.units[k]);
+        t = 0;
+        q_ok = false;
       }
-      tc::commit(&x.bar[kSFull + s]);
-      if (t == nt - 1) tc::commit(&x.bar[kQEmpty + qb]);
-      if (have_prev) issue_pv(p, x, prev);
-      prev = PvJob{it, s, t == 0, ordinal};
-      have_prev = true;
+      if (t < nt) break;
+      if (nt == 0) {
+        if (!mbar_test_wait(&x.bar[kQFull + (k & 1)], (k >> 1) & 1)) break;
+        tc::commit(&x.bar[kQEmpty + (k & 1)]);  // nothing to multiply: hand the query buffer back
+        progressed = true;
+      }
+      ++k;
+      nt = -1;
     }
-    if (nt == 0) tc::commit(&x.bar[kQEmpty + qb]);
-    else ++ordinal;
+    const bool qk_done = k >= x.nunits;
+    if (qk_done && pv_it == qk_it) break;
+    if (*x.abort_flag) break;
+    if (pv_it < qk_it) {
+      const PvJob& j = pend[pv_it & 1];
+      if (mbar_test_wait(&x.bar[kPFull + (pv_it & 1)], (pv_it >> 1) & 1) &&
+          (!(j.first && j.ordinal > 0) || mbar_test_wait(&x.bar[kOFree], (j.ordinal - 1) & 1))) {
+        issue_pv(x, j, pairs0, pb0);
+        ++pv_it;
+        progressed = true;
+      }
+    }
+    if (!progressed && !qk_done && t < nt && qk_it <= pv_it + 1) {
+      const int qb = k & 1;
+      if (!q_ok) q_ok = mbar_test_wait(&x.bar[kQFull + qb], (k >> 1) & 1);
+      const int s0 = (4 * qk_it) % kPairSlots, use0 = (4 * qk_it) / kPairSlots;
+      bool ready = q_ok && mbar_test_wait(&x.bar[kRopeFull + qk_it % kRopeSlots], (qk_it / kRopeSlots) & 1) &&
+                   (qk_it < 2 || mbar_test_wait(&x.bar[kSEmpty + (qk_it & 1)], ((qk_it >> 1) - 1) & 1));
+#pragma unroll
+      for (int f = 3; f >= 0 && ready; --f) {
+        const int sl = s0 + f;
+        ready = mbar_test_wait(&x.bar[kPairFull + wrap_slot(sl)], (use0 + (sl >= kPairSlots)) & 1);
+      }
+      if (ready) {
+        issue_qk(x, qk_it, qb, pairs0, rope0, qs0);
+        pend[qk_it & 1] = PvJob{qk_it, t == 0, t == nt - 1, ordinal};
+        ++qk_it;
+        if (++t == nt) {
+          tc::commit(&x.bar[kQEmpty + qb]);
+          ++ordinal;
+        }
+        progressed = true;
+      }
+    }
+    if (progressed) {
+      idle = 0;
+    } else if ((++idle & 255u) == 0) {
+      // bounded: a stream that makes no progress for kWaitTimeoutNs gives up
+      const uint64_t now = global_timer_ns();
+      if (idle == 256u) idle_t0 = now;
+      else if (now - idle_t0 > kWaitTimeoutNs) {
+        *x.abort_flag = 1;
+        atomicCAS(p.ws_err, 0, kErrDeviceTimeout);
+        break;
+      }
+    }
   }
-  if (have_prev) issue_pv(p, x, prev);
 }
 
 // ------------------------------------------------------------------ softmax
@@ -283,7 +386,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
   const float kv_scale = *static_cast<const float*>(p.kv_scale);
   const float* rq = reinterpret_cast<const float*>(x.smem + Layout::rq);
   float* redbuf = reinterpret_cast<float*>(x.smem + Layout::red);
-  int it = 0, red_par = 0;
+  int it = 0, red_par = 0, ordinal = 0;
   for (int k = 0; k < x.nunits; ++k) {
     const UnitDesc d = x.units[k];
     const int qb = k & 1;
@@ -351,7 +454,8 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
         m_ref[h] = mn;
       }
       if (any && t > 0) {
-        // rescale O^T in TMEM once the previous tile's P.V is complete
+        // rescale O^T in TMEM once the previous tile's P.V is complete (exact:
+        // S(it) is committed after P.V(it-2), so the barrier is one phase behind at most)
         wait_phase(&x.bar[kODone], (it - 1) & 1, x.abort_flag, p.ws_err);
         tc::fence_after();
 #pragma unroll 1
@@ -392,12 +496,13 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       if (row >= valid) {
         // rows past the unit's end hold other rows' data: zero their V part so
         // that P = 0 cannot meet a non-finite value
-        uint8_t* st = x.smem + Layout::stages + (it & 1) * kStageBytes;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
+        for (int c = 0; c < 8; ++c) {
+          uint8_t* blk = x.smem + Layout::pairs + pair_slot(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes;
 #pragma unroll
           for (int uu = 0; uu < 4; ++uu)
-            *reinterpret_cast<uint4*>(st + c * kChunkBytes + sw64_off(row, 16 * uu)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(blk + sw64_off(row, 16 * uu)) = make_uint4(0, 0, 0, 0);
+        }
       }
       tc::fence_proxy_async();
       tc::fence_before();
@@ -407,11 +512,14 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
     // unit epilogue: l per head over the 128 rows, O^T -> output
     group_reduce16<false>(l_part, redbuf + red_par * 64, ww, lane);
     red_par ^= 1;
-    wait_phase(&x.bar[kODone], (it - 1) & 1, x.abort_flag, p.ws_err);
+    // the unit's last P.V: its own barrier completes once per unit, so the parity
+    // of the unit's ordinal names it exactly (o_done may be a phase further on)
+    wait_phase(&x.bar[kOLast], ordinal & 1, x.abort_flag, p.ws_err);
+    ++ordinal;
     tc::fence_after();
     float inv[16];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) inv[h] = l_part[h] > 0.f ? kv_scale / l_part[h] : 0.f;
+    for (int h = 0; h < 16; ++h) inv[h] = l_part[h] > 0.f ? kv_scale * __frcp_rn(l_part[h]) : 0.f;
 #pragma unroll 1
     for (int fb = 0; fb < 4; ++fb) {
       uint32_t o[32];
@@ -431,9 +539,10 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
         for (int h = 0; h < 16; ++h) ob[h * kVDim] = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h])) * inv[h];
       }
     }
-    if (row == 0) {
+    // lse of head h is written by row h (every row holds all 16 values)
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
+    for (int h = 0; h < 16; ++h) {
+      if (row == h) {
         const float lse = l_part[h] > 0.f ? (m_ref[h] + log2f(l_part[h])) * kLn2 : -INFINITY;
         if (final_out) {
           if (p.lse) p.lse[d.b * kHeads + h] = lse;
@@ -461,13 +570,19 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_tc_kernel(const __grid_
   int* s_nunits = misc + 2;
 
   if (threadIdx.x == 0) {
-    const uint32_t counts[Layout::nbars] = {1, 1, 1, 1, 2, 2, 1, 1, 1, 1, 4, 4, 4, 4, 1, 4, 4, 4, 1};
+    uint32_t counts[Layout::nbars];
+    for (int i = 0; i < Layout::nbars; ++i) counts[i] = 1;
+    counts[kQFull] = counts[kQFull + 1] = 2;
+    counts[kSEmpty] = counts[kSEmpty + 1] = 4;
+    counts[kPFull] = counts[kPFull + 1] = 4;
+    counts[kOFree] = 4;
+    counts[kRFree] = counts[kRFree + 1] = 4;
     for (int i = 0; i < Layout::nbars; ++i) mbar_init(&x.bar[i], counts[i]);
     *x.abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    scan_units<kTileRows>(p, reinterpret_cast<UnitDesc*>(smem + Layout::units), s_nunits, lane);
+    scan_units<kTileRows, kMaxUnits>(p, reinterpret_cast<UnitDesc*>(smem + Layout::units), s_nunits, lane);
     if (lane == 0) prefetch_tensormap(&p.tmap_kv64);
   }
   if (warp == 1) {
@@ -509,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_tc_kernel(const __grid_
 inline cudaError_t launch_split_tc_fp8(const Stage1Params& p, cudaStream_t stream) {
   using L = tcfp8::Layout;
   static_assert(L::total <= 232448, "shared memory carve-up exceeds the 227 KB per-CTA limit");
-  static_assert(L::qs % 1024 == 0 && L::pb % 1024 == 0, "swizzled operand alignment");
+  static_assert(L::qs % 1024 == 0 && L::pb % 1024 == 0 && L::rope % 1024 == 0, "swizzled operand alignment");
   cudaError_t e =
       cudaFuncSetAttribute(tcfp8::mla_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
   if (e != cudaSuccess) return e;
