@@ -137,6 +137,35 @@ def test_many_short_sequences(orc, dtype):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("lens,num_sms,num_splits", [
+    ([256] * 6, 1, 0),
+    ([1536] * 4, 1, 0),
+    ([384, 512, 640], 1, 0),
+    ([1024, 0, 0, 0, 1024, 1024], 1, 1),
+    ([8192, 8192], 3, 0),
+])
+def test_many_units_per_cta(orc, dtype, lens, num_sms, num_splits):
+    """A grid planned for a few SMs: every CTA runs several multi-tile units
+    back to back (unit boundaries with P.V still in flight, empty units in a
+    row); two launches must agree bit for bit."""
+    inp = synth.make_inputs(lens, dtype, seed=61)
+    dev = torch.device("cuda:0")
+    dec = binding.MLADecoder(inp.kv_indptr, dtype, device=dev, num_sms=num_sms, num_splits=num_splits)
+    assert dec.plan.units_per_cta >= 2
+    scale = inp.kv_scale if dtype == "fp8" else None
+    runs = []
+    for _ in range(2):
+        out, lse = dec(inp.q.to(dev), inp.kv.to(dev), inp.kv_indptr.to(dev), inp.qo_indptr.to(dev),
+                       kv_scale=None if scale is None else scale.to(dev))
+        torch.cuda.synchronize()
+        runs.append((out.double().cpu().numpy(), lse.double().cpu().numpy()))
+    assert np.array_equal(runs[0][0], runs[1][0]) and np.array_equal(runs[0][1], runs[1][1])
+    ref, ref_lse = oracle_decode(orc, inp)
+    assert_parity(runs[0][0], ref, runs[0][1], ref_lse, f"units/CTA {dtype} {lens}", v_absmax(inp))
+    assert dec.poll_error() == 0
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_one_long_sequence(orc, dtype):
     inp = synth.make_inputs([40001], dtype, seed=41)
     got, lse, _ = gpu_decode(inp)
