@@ -38,6 +38,15 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
   }
 }
 
+// Order-preserving map of floats (no NaN) to signed integers, for integer
+// max reductions (redux.sync): non-negative floats keep their bits, negative
+// ones have the magnitude bits flipped.
+__device__ __forceinline__ int float_order_key(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : i ^ 0x7FFFFFFF;
+}
+__device__ __forceinline__ float float_from_order_key(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF); }
+
 __device__ __forceinline__ float quad_max(float v) {
   v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
   v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));

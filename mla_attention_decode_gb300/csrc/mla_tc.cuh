@@ -7,30 +7,34 @@
 // the 16 query heads over a contiguous range of KV rows; final bf16 output and
 // lse for unsplit sequences, fp32 partials and lse for split ones.
 //
-// Per 128-row tile t of a unit (one CTA of 8 warps per SM, persistent):
+// Per 128-row tile t of a unit (one CTA of 9 warps per SM, persistent):
 //   scores  S^T[128 rows x 32] = K_t[128 x 576] . [Q_hi | Q_lo]^T   (tcgen05 kind::f8f6f4,
 //           18 k32 steps; K straight from the TMA stage, K-major, 64 B swizzle;
 //           the query as two e4m3 terms x = hi + lo with a power-of-two scale
 //           per head, 32 "columns" = 16 heads x 2 terms, in TMEM)
 //   softmax one thread per row reads its 32 accumulators, builds the scores,
-//           the per-head tile max (warp shuffles + smem), exponentials and row
-//           sums, and writes P^T[128 rows x 32] = [P_hi | P_lo] (two e4m3 terms)
-//           as the MN-major B operand
+//           exponentials and row sums, and writes P^T[128 rows x 32] =
+//           [P_hi | P_lo] (two e4m3 terms) as the MN-major B operand
 //   P.V     O^T[512 features x 32] += V_t^T[512 x 128] . P^T   (4 blocks of 128
 //           features x 4 k32 steps; V^T read MN-major from the same stage --
 //           V is the first 512 columns of K -- so each KV byte is read from HBM
 //           once per unit), O^T resident in TMEM across the unit's tiles
 // The running max is applied lazily: P = 2^(s - m_ref) with m_ref raised (and
-// O^T, l rescaled in place) only when a head's tile max exceeds m_ref by more
-// than 8 (log2 units), which keeps P <= 256 inside e4m3 range.  Scores are in
-// log2 units: s = (q . k) * sm_scale * log2(e) * kv_scale.
+// O^T, l rescaled in place) only when some score of a head exceeds m_ref by more
+// than 8 (log2 units), which keeps P <= 256 inside e4m3 range.  Deciding that
+// takes one OR over the tile's rows; the tile max itself is reduced only for
+// the heads that rise (always on a unit's first tile).  Scores are in log2
+// units: s = (q . k) * sm_scale * log2(e) * kv_scale.
 //
 // Warp roles: 0 TMA producer (9 column boxes of 64 B x 128 rows per tile: the
-// 8 V blocks in pairs into a ring of 10 pair slots, each released by the
-// commit after its P.V block, the rope block into a ring of 2); 1 MMA issuer (QK of tile t, then PV of tile t-1) and TMEM
-// owner; 2-3 query preparation (two-term query per unit, double buffered);
-// 4-7 softmax, O^T rescale and the unit epilogue.  Hand-offs are mbarriers
-// (TMA transaction bytes, tcgen05.commit, thread arrivals).
+// 8 V blocks in pairs into a ring of 11 pair slots, each released by the
+// commit after its P.V block, the rope block into a ring of 2); 1 QK issuer and
+// TMEM owner; 2 P.V issuer (two issuing threads: one thread cannot issue these
+// small MMAs as fast as the tensor pipe retires them); 3-4 query preparation
+// (two-term query per unit, loaded while the previous unit is in use); 5-8
+// softmax, O^T rescale and the unit epilogue (warp w reads TMEM lanes
+// [32 (w mod 4), +32)).  Hand-offs are mbarriers (TMA transaction bytes,
+// tcgen05.commit, thread arrivals).
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,11 +47,11 @@ namespace tcfp8 {
 constexpr int kTileRows = 128;
 constexpr int kChunkBytes = kTileRows * 64;  // one 64-byte feature column block of a tile
 constexpr int kPairBytes = 2 * kChunkBytes;  // two column blocks = features [128 f, 128 f + 128)
-constexpr int kPairSlots = 10;               // ring of V column-block pairs (4 per tile)
+constexpr int kPairSlots = 11;               // ring of V column-block pairs (4 per tile)
 constexpr int kRopeSlots = 2;                // ring of the rope column block (features 512..575)
 constexpr int kQsBytes = 9 * 32 * 64;        // two-term query: 32 rows x 576 B, K-major, 64 B swizzle
 constexpr int kPBytes = kTileRows * 32;      // two-term P^T: 128 rows x 32 B, MN-major, 32 B swizzle
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;
 constexpr int kMaxUnits = 256;               // work units one CTA may own
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0;   // S^T double buffer: columns [0, 32) and [32, 64)
@@ -60,33 +64,34 @@ constexpr uint32_t kIdescPV = tc::idesc_e4m3(128, 32, 1, 1);
 struct Layout {
   static constexpr int pairs = 0;                             // 1024-aligned
   static constexpr int rope = pairs + kPairSlots * kPairBytes;
-  static constexpr int qs = rope + kRopeSlots * kChunkBytes;  // [2]
-  static constexpr int pb = qs + 2 * kQsBytes;                // [2]
-  static constexpr int rq = pb + 2 * kPBytes;                 // float [2][16] score factor per head
-  static constexpr int red = rq + 2 * 16 * 4;                 // float [2][4 warps][16]
+  static constexpr int qs = rope + kRopeSlots * kChunkBytes;
+  static constexpr int pb = qs + kQsBytes;                    // [2]
+  static constexpr int rq = pb + 2 * kPBytes;                 // float [16] score factor per head
+  static constexpr int red = rq + 16 * 4;                     // float [2][4 warps][16]
   static constexpr int units = red + 2 * 4 * 16 * 4;
   static constexpr int bars = units + kMaxUnits * (int)sizeof(UnitDesc);
-  static constexpr int nbars = 40;
+  static constexpr int nbars = 41;
   static constexpr int misc = bars + nbars * 8;  // tmem slot, abort flag, unit count
   static constexpr int total = misc + 16;
 };
 
 // mbarrier slots
 enum {
-  kPairFull = 0,    // [10] TMA bytes of a V column-block pair
-  kPairEmpty = 10,  // [10] commit after the P.V block that read it
-  kRopeFull = 20,   // [2]  TMA bytes of a rope column block
-  kRopeEmpty = 22,  // [2]  commit after the QK that read it
-  kQFull = 24,      // [2]  query prepared (2 warps)
-  kQEmpty = 26,     // [2]  commit after the unit's last QK
+  kPairFull = 0,    // [11] TMA bytes of a V column-block pair
+  kPairEmpty = 11,  // [11] commit after the P.V block that read it
+  kRopeFull = 22,   // [2]  TMA bytes of a rope column block
+  kRopeEmpty = 24,  // [2]  commit after the QK that read it
+  kQFull = 26,      // query of the next unit prepared (2 warps)
+  kQEmpty = 27,     // commit after the unit's last QK
   kSFull = 28,      // [2]  commit after QK
   kSEmpty = 30,     // [2]  softmax read S (4 warps)
   kPFull = 32,      // [2]  P written, O^T rescaled (4 warps)
   kODone = 34,      // commit after each tile's P.V
   kOFree = 35,      // unit epilogue read O^T (4 warps)
-  kRFree = 36,      // [2]  softmax copied the unit's score factors (4 warps)
-  kFinal = 38,      // commit after the MMA issuer's last operation
-  kOLast = 39,      // commit after a unit's last P.V (once per unit with tiles)
+  kRFree = 36,      // softmax copied the unit's score factors (4 warps)
+  kOLast = 37,      // commit after a unit's last P.V (once per unit with tiles)
+  kFinal = 38,      // commits after both issuers' last operations (count 2)
+  kPFree = 39,      // [2]  commit after the P.V that read P buffer t mod 2
 };
 
 __device__ __forceinline__ uint32_t sw64_off(int row, int col) {  // byte (row, col) of a 64 B-row, 64 B-swizzled block
@@ -106,7 +111,7 @@ __device__ __forceinline__ int tiles_of(const UnitDesc& d) { return (d.end - d.s
 
 // ------------------------------------------------------------------ producer
 // Column blocks of tile t: pair f (features [128 f, 128 f + 128)) goes to pair
-// slot (4t + f) mod 10, the rope block to rope slot t mod 2; each slot is
+// slot (4t + f) mod 11, the rope block to rope slot t mod 2; each slot is
 // re-armed as soon as the MMA that read it has completed.
 __device__ __forceinline__ int pair_slot(int t, int f) { return (4 * t + f) % kPairSlots; }
 __device__ __forceinline__ int pair_use(int t, int f) { return (4 * t + f) / kPairSlots; }
@@ -151,17 +156,16 @@ __device__ void producer(const Stage1Params& p, const Ctx& x) {
 
 // ---------------------------------------------------------- query preparation
 // 64 threads: thread j handles head j/4, features [144 (j%4), 144 (j%4) + 144).
+// One query buffer: unit k's rows are loaded (and their scale found) first,
+// then converted to two e4m3 terms and stored once the last QK of unit k-1 has
+// completed and the softmax has taken unit k-1's score factors.
 __device__ void prep_query(const Stage1Params& p, const Ctx& x, int j) {
   const int h = j >> 2, part = j & 3;
   const float kv_scale = *static_cast<const float*>(p.kv_scale);
   const float base_factor = p.sm_scale * kLog2e * kv_scale;
   float* rq = reinterpret_cast<float*>(x.smem + Layout::rq);
+  uint8_t* qs = x.smem + Layout::qs;
   for (int k = 0; k < x.nunits; ++k) {
-    const int qb = k & 1;
-    if (k >= 2) {
-      wait_phase(&x.bar[kQEmpty + qb], ((k >> 1) - 1) & 1, x.abort_flag, p.ws_err);
-      wait_phase(&x.bar[kRFree + qb], ((k >> 1) - 1) & 1, x.abort_flag, p.ws_err);
-    }
     const int qrow = p.qo_indptr[x.units[k].b];
     const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)qrow * kHeads + h) * kQkDim + 144 * part) * 2);
     uint4 raw[18];
@@ -182,7 +186,10 @@ __device__ void prep_query(const Stage1Params& p, const Ctx& x, int j) {
       sc = exp2f(floorf(log2f(448.f / amax)));
       if (amax * sc > 448.f) sc *= 0.5f;
     }
-    uint8_t* qs = x.smem + Layout::qs + qb * kQsBytes;
+    if (k >= 1) {
+      wait_phase(&x.bar[kQEmpty], (k - 1) & 1, x.abort_flag, p.ws_err);
+      wait_phase(&x.bar[kRFree], (k - 1) & 1, x.abort_flag, p.ws_err);
+    }
 #pragma unroll
     for (int i = 0; i < 18; ++i) {
       const int f0 = 144 * part + 8 * i;  // 8 features, inside one 16-byte unit of a 64-byte chunk
@@ -195,152 +202,102 @@ __device__ void prep_query(const Stage1Params& p, const Ctx& x, int j) {
       *reinterpret_cast<uint2*>(qs + chunk * 2048 + sw64_off(h, col)) = make_uint2(hi0, hi1);
       *reinterpret_cast<uint2*>(qs + chunk * 2048 + sw64_off(16 + h, col)) = make_uint2(lo0, lo1);
     }
-    if (part == 0) rq[qb * 16 + h] = base_factor / sc;
+    if (part == 0) rq[h] = base_factor / sc;
     tc::fence_proxy_async();  // the tensor core reads the query through the async proxy
     __syncwarp();
-    if ((j & 31) == 0) mbar_arrive(&x.bar[kQFull + qb]);
+    if ((j & 31) == 0) mbar_arrive(&x.bar[kQFull]);
   }
 }
 
-// ------------------------------------------------------------------ MMA issuer
-// One thread issues every tensor-core operation.  Descriptors are built once per
-// tile from templates and moved by constant offsets, so that issuing an MMA
-// costs a few instructions (a single thread is slow at address arithmetic, and
-// the MMAs of this kernel only take ~46 cycles each on the tensor pipe).
+// ------------------------------------------------------------------ MMA issuers
+// Two threads issue the tensor-core operations: warp 1 the QK of every tile,
+// warp 2 the P.V of every tile, each in tile order.  Operands are described by
+// descriptors built once per tile from templates and moved by constant
+// offsets (a few instructions per MMA).
 //
-// The QK of tile t and the P.V of tile t' run as two streams in one loop: the
-// P.V of a tile is issued as soon as its P is written (that releases its ring
-// slots), the QK of the next tile as soon as its columns have landed, with at
-// most two tiles between the streams (S and P are double buffered; issuing
-// QK(t) only after P.V(t-2) makes the commit of QK(t) also cover P.V(t-2), so
-// the softmax may overwrite P buffer t mod 2 once S(t) is ready).
-struct PvJob {
-  int it;       // tile index (slots, P buffer, o_done phase)
-  int first;    // first tile of its unit
-  int last;     // last tile of its unit
-  int ordinal;  // index of its unit among the CTA's units with tiles
-};
-
+// Descriptors as (low word, high word): the high word is fixed per operand
+// kind and the low word is the template's low bits plus (address >> 4), so
+// every operand move below is a 32-bit add of a constant.
 constexpr uint64_t kTplK64 = tc::desc_template(16, 512, 4);          // K-major, 64 B swizzle
 constexpr uint64_t kTplV = tc::desc_template(kChunkBytes, 512, 4);   // V^T, MN-major, 64 B swizzle
 constexpr uint64_t kTplP = tc::desc_template(1024, 256, 6);          // P^T, MN-major, 32 B swizzle
+__host__ __device__ constexpr uint32_t lo_word(uint64_t d) { return (uint32_t)d; }
+__host__ __device__ constexpr uint32_t hi_word(uint64_t d) { return (uint32_t)(d >> 32); }
 
 __device__ __forceinline__ int wrap_slot(int s) { return s >= kPairSlots ? s - kPairSlots : s; }
 
-__device__ __forceinline__ void issue_pv(const Ctx& x, const PvJob& j, uint32_t pairs0, uint32_t pb0) {
-  tc::fence_after();
-  const uint64_t bp = kTplP + ((pb0 + (uint32_t)(j.it & 1) * kPBytes) >> 4);
-  const int s0 = (4 * j.it) % kPairSlots;
-#pragma unroll
-  for (int fb = 0; fb < 4; ++fb) {
-    const int sl = wrap_slot(s0 + fb);
-    // V^T block: features [128 fb, 128 fb + 128) = the slot's two column blocks (LBO)
-    const uint64_t av = kTplV + ((pairs0 + (uint32_t)sl * kPairBytes) >> 4);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)  // rows [32 q, 32 q + 32): +2048 B of V^T, +1024 B of P^T
-      tc::mma_f8(x.tmem + kColO + 32 * fb, av + q * (2048 >> 4), bp + q * (1024 >> 4), kIdescPV,
-                 (j.first && q == 0) ? 0u : 1u);
-    tc::commit(&x.bar[kPairEmpty + sl]);
-  }
-  tc::commit(&x.bar[kODone]);
-  if (j.last) tc::commit(&x.bar[kOLast]);
-}
-
-__device__ __forceinline__ void issue_qk(const Ctx& x, int it, int qb, uint32_t pairs0, uint32_t rope0,
-                                         uint32_t qs0) {
-  tc::fence_after();
-  const int s0 = (4 * it) % kPairSlots;
-  uint64_t ap[4];
-#pragma unroll
-  for (int f = 0; f < 4; ++f) ap[f] = kTplK64 + ((pairs0 + (uint32_t)wrap_slot(s0 + f) * kPairBytes) >> 4);
-  const uint64_t ar = kTplK64 + ((rope0 + (uint32_t)(it % kRopeSlots) * kChunkBytes) >> 4);
-  const uint64_t bq = kTplK64 + ((qs0 + (uint32_t)qb * kQsBytes) >> 4);
-  const uint32_t d = x.tmem + kColS + 32 * (it & 1);
-#pragma unroll
-  for (int ks = 0; ks < 18; ++ks) {
-    const int c = ks >> 1, half = ks & 1;
-    const uint64_t a = c < 8 ? ap[c >> 1] + (((c & 1) * kChunkBytes + 32 * half) >> 4) : ar + ((32 * half) >> 4);
-    tc::mma_f8(d, a, bq + ((c * 2048 + 32 * half) >> 4), kIdescQK, ks > 0 ? 1u : 0u);
-  }
-  tc::commit(&x.bar[kSFull + (it & 1)]);
-  tc::commit(&x.bar[kRopeEmpty + it % kRopeSlots]);
-}
-
-__device__ void mma_issuer(const Stage1Params& p, const Ctx& x) {
+// QK of every tile: S^T(t) into TMEM columns [32 (t mod 2), +32).
+__device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
   const uint32_t pairs0 = smem_u32(x.smem + Layout::pairs), rope0 = smem_u32(x.smem + Layout::rope);
-  const uint32_t qs0 = smem_u32(x.smem + Layout::qs), pb0 = smem_u32(x.smem + Layout::pb);
-  PvJob pend[2] = {{0, 0, 0, 0}, {0, 0, 0, 0}};  // QK issued, P.V not yet (indexed by tile mod 2)
-  int qk_it = 0, pv_it = 0;                // next tile of each stream
-  int k = 0, t = 0, nt = -1;               // QK stream: unit, tile in unit, tiles of the unit (-1: not begun)
-  int ordinal = 0;
-  bool q_ok = false;
-  uint32_t idle = 0;
-  uint64_t idle_t0 = 0;
-  while (true) {
-    bool progressed = false;
-    // QK stream: step over finished units and, once their query buffer is
-    // filled, empty ones (never block here: pending P.V must still be issued)
-    while (k < x.nunits) {
-      if (nt < 0) {
-        nt = tiles_of(x.units[k]);
-        t = 0;
-        q_ok = false;
-      }
-      if (t < nt) break;
-      if (nt == 0) {
-        if (!mbar_test_wait(&x.bar[kQFull + (k & 1)], (k >> 1) & 1)) break;
-        tc::commit(&x.bar[kQEmpty + (k & 1)]);  // nothing to multiply: hand the query buffer back
-        progressed = true;
-      }
-      ++k;
-      nt = -1;
-    }
-    const bool qk_done = k >= x.nunits;
-    if (qk_done && pv_it == qk_it) break;
-    if (*x.abort_flag) break;
-    if (pv_it < qk_it) {
-      const PvJob& j = pend[pv_it & 1];
-      if (mbar_test_wait(&x.bar[kPFull + (pv_it & 1)], (pv_it >> 1) & 1) &&
-          (!(j.first && j.ordinal > 0) || mbar_test_wait(&x.bar[kOFree], (j.ordinal - 1) & 1))) {
-        issue_pv(x, j, pairs0, pb0);
-        ++pv_it;
-        progressed = true;
-      }
-    }
-    if (!progressed && !qk_done && t < nt && qk_it <= pv_it + 1) {
-      const int qb = k & 1;
-      if (!q_ok) q_ok = mbar_test_wait(&x.bar[kQFull + qb], (k >> 1) & 1);
-      const int s0 = (4 * qk_it) % kPairSlots, use0 = (4 * qk_it) / kPairSlots;
-      bool ready = q_ok && mbar_test_wait(&x.bar[kRopeFull + qk_it % kRopeSlots], (qk_it / kRopeSlots) & 1) &&
-                   (qk_it < 2 || mbar_test_wait(&x.bar[kSEmpty + (qk_it & 1)], ((qk_it >> 1) - 1) & 1));
+  const uint32_t bq = lo_word(kTplK64) + (smem_u32(x.smem + Layout::qs) >> 4);
+  int it = 0;
+  for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
+    const int nt = tiles_of(x.units[k]);
+    wait_phase(&x.bar[kQFull], k & 1, x.abort_flag, p.ws_err);
+    for (int t = 0; t < nt; ++t, ++it) {
+      const int s0 = (4 * it) % kPairSlots, use0 = (4 * it) / kPairSlots;
 #pragma unroll
-      for (int f = 3; f >= 0 && ready; --f) {
+      for (int f = 0; f < 4; ++f) {
         const int sl = s0 + f;
-        ready = mbar_test_wait(&x.bar[kPairFull + wrap_slot(sl)], (use0 + (sl >= kPairSlots)) & 1);
+        wait_phase(&x.bar[kPairFull + wrap_slot(sl)], (use0 + (sl >= kPairSlots)) & 1, x.abort_flag, p.ws_err);
       }
-      if (ready) {
-        issue_qk(x, qk_it, qb, pairs0, rope0, qs0);
-        pend[qk_it & 1] = PvJob{qk_it, t == 0, t == nt - 1, ordinal};
-        ++qk_it;
-        if (++t == nt) {
-          tc::commit(&x.bar[kQEmpty + qb]);
-          ++ordinal;
-        }
-        progressed = true;
+      wait_phase(&x.bar[kRopeFull + it % kRopeSlots], (it / kRopeSlots) & 1, x.abort_flag, p.ws_err);
+      if (it >= 2) wait_phase(&x.bar[kSEmpty + (it & 1)], ((it >> 1) - 1) & 1, x.abort_flag, p.ws_err);
+      if (*x.abort_flag) break;
+      tc::fence_after();
+      uint32_t ap[4];
+#pragma unroll
+      for (int f = 0; f < 4; ++f)
+        ap[f] = lo_word(kTplK64) + ((pairs0 + (uint32_t)wrap_slot(s0 + f) * kPairBytes) >> 4);
+      const uint32_t ar = lo_word(kTplK64) + ((rope0 + (uint32_t)(it % kRopeSlots) * kChunkBytes) >> 4);
+      const uint32_t d = x.tmem + kColS + 32 * (it & 1);
+#pragma unroll
+      for (int ks = 0; ks < 18; ++ks) {
+        const int c = ks >> 1, half = ks & 1;
+        const uint32_t a =
+            c < 8 ? ap[c >> 1] + (((c & 1) * kChunkBytes + 32 * half) >> 4) : ar + ((32 * half) >> 4);
+        tc::mma_f8_words(d, a, hi_word(kTplK64), bq + ((c * 2048 + 32 * half) >> 4), hi_word(kTplK64), kIdescQK,
+                         ks > 0 ? 1u : 0u);
       }
+      tc::commit(&x.bar[kSFull + (it & 1)]);
+      tc::commit(&x.bar[kRopeEmpty + it % kRopeSlots]);
     }
-    if (progressed) {
-      idle = 0;
-    } else if ((++idle & 255u) == 0) {
-      // bounded: a stream that makes no progress for kWaitTimeoutNs gives up
-      const uint64_t now = global_timer_ns();
-      if (idle == 256u) idle_t0 = now;
-      else if (now - idle_t0 > kWaitTimeoutNs) {
-        *x.abort_flag = 1;
-        atomicCAS(p.ws_err, 0, kErrDeviceTimeout);
-        break;
+    tc::commit(&x.bar[kQEmpty]);  // the query buffer may be refilled
+  }
+}
+
+// P.V of every tile: O^T += V^T(t) . P^T(t); releases the tile's ring slots, its
+// P buffer and, on a unit's last tile, the unit's O^T.
+__device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
+  const uint32_t pairs0 = smem_u32(x.smem + Layout::pairs), pb0 = smem_u32(x.smem + Layout::pb);
+  int it = 0, ordinal = 0;
+  for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
+    const int nt = tiles_of(x.units[k]);
+    if (nt == 0) continue;
+    for (int t = 0; t < nt; ++t, ++it) {
+      wait_phase(&x.bar[kPFull + (it & 1)], (it >> 1) & 1, x.abort_flag, p.ws_err);
+      // a unit's first P.V overwrites O^T: the previous unit's epilogue must have read it
+      if (t == 0 && ordinal > 0) wait_phase(&x.bar[kOFree], (ordinal - 1) & 1, x.abort_flag, p.ws_err);
+      if (*x.abort_flag) break;
+      tc::fence_after();
+      const uint32_t bp = lo_word(kTplP) + ((pb0 + (uint32_t)(it & 1) * kPBytes) >> 4);
+      const int s0 = (4 * it) % kPairSlots;
+#pragma unroll
+      for (int fb = 0; fb < 4; ++fb) {
+        const int sl = wrap_slot(s0 + fb);
+        // V^T block: features [128 fb, 128 fb + 128) = the slot's two column blocks (LBO)
+        const uint32_t av = lo_word(kTplV) + ((pairs0 + (uint32_t)sl * kPairBytes) >> 4);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)  // rows [32 q, 32 q + 32): +2048 B of V^T, +1024 B of P^T
+          tc::mma_f8_words(x.tmem + kColO + 32 * fb, av + q * (2048 >> 4), hi_word(kTplV), bp + q * (1024 >> 4),
+                           hi_word(kTplP), kIdescPV, (t == 0 && q == 0) ? 0u : 1u);
+        tc::commit(&x.bar[kPairEmpty + sl]);
       }
+      tc::commit(&x.bar[kODone]);
+      tc::commit(&x.bar[kPFree + (it & 1)]);
+      if (t == nt - 1) tc::commit(&x.bar[kOLast]);
     }
+    ++ordinal;
   }
 }
 
@@ -389,13 +346,12 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
   int it = 0, red_par = 0, ordinal = 0;
   for (int k = 0; k < x.nunits; ++k) {
     const UnitDesc d = x.units[k];
-    const int qb = k & 1;
-    wait_phase(&x.bar[kQFull + qb], (k >> 1) & 1, x.abort_flag, p.ws_err);
+    wait_phase(&x.bar[kQFull], k & 1, x.abort_flag, p.ws_err);
     float r[16];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) r[h] = rq[qb * 16 + h];
+    for (int h = 0; h < 16; ++h) r[h] = rq[h];
     __syncwarp();
-    if (lane == 0) mbar_arrive(&x.bar[kRFree + qb]);
+    if (lane == 0) mbar_arrive(&x.bar[kRFree]);
     const bool final_out = (d.u & kFinalFlag) != 0;
     const int u = d.u & ~kFinalFlag;
     const int nt = tiles_of(d);
@@ -434,47 +390,66 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&x.bar[kSEmpty + sb]);
-      float sv[16], mx[16];
+      float sv[16];
+      uint32_t need = 0;  // heads with a score above m_ref + 8 in this row
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
         sv[h] = row < valid ? (__uint_as_float(acc[h]) + __uint_as_float(acc[16 + h])) * r[h] : -INFINITY;
-        mx[h] = sv[h];
+        need |= (sv[h] > m_ref[h] + kRescaleLog2 ? 1u : 0u) << h;
       }
-      group_reduce16<true>(mx, redbuf + red_par * 64, ww, lane);
-      red_par ^= 1;
-      // lazy running max: raise m_ref only when a head's tile max exceeds it by > 8
-      bool any = false;
-      float fac[16];
-#pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        const bool up = mx[h] > m_ref[h] + kRescaleLog2;
-        const float mn = up ? mx[h] : m_ref[h];
-        fac[h] = (m_ref[h] == -INFINITY) ? 0.f : fast_exp2(m_ref[h] - mn);
-        any |= up;
-        m_ref[h] = mn;
+      // heads whose reference rises: OR over the warp, then over the 4 warps
+      need = __reduce_or_sync(0xffffffffu, need);
+      {
+        uint32_t* fl = reinterpret_cast<uint32_t*>(redbuf + red_par * 64);
+        if (lane == 0) fl[ww] = need;
+        named_bar_sync(kBarSoftmax, 128);
+        need = fl[0] | fl[1] | fl[2] | fl[3];
+        red_par ^= 1;
       }
-      if (any && t > 0) {
-        // rescale O^T in TMEM once the previous tile's P.V is complete (exact:
-        // S(it) is committed after P.V(it-2), so the barrier is one phase behind at most)
-        wait_phase(&x.bar[kODone], (it - 1) & 1, x.abort_flag, p.ws_err);
-        tc::fence_after();
-#pragma unroll 1
-        for (int fb = 0; fb < 4; ++fb) {
-          uint32_t o[32];
-          tc::ld32(tl + kColO + 32 * fb, o);
-          tc::wait_ld();
+      // P buffer it mod 2 was read by P.V(it-2); waiting for it here also makes
+      // the o_done wait below exact (the barrier is then one phase behind at most)
+      if (it >= 2) wait_phase(&x.bar[kPFree + sb], ((it >> 1) - 1) & 1, x.abort_flag, p.ws_err);
+      if (need) {
+        // tile max of the rising heads: redux over the warp (order-preserving
+        // integer image of the float), then over the 4 warps through smem
+        int* mx = reinterpret_cast<int*>(redbuf + red_par * 64);
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            o[h] = __float_as_uint(__uint_as_float(o[h]) * fac[h]);
-            o[16 + h] = __float_as_uint(__uint_as_float(o[16 + h]) * fac[h]);
+        for (int h = 0; h < 16; ++h)
+          if ((need >> h) & 1u) {
+            const int w = __reduce_max_sync(0xffffffffu, float_order_key(sv[h]));
+            if (lane == 0) mx[ww * 16 + h] = w;
           }
-          tc::st32(tl + kColO + 32 * fb, o);
-        }
-        tc::wait_st();
-      }
-      if (any) {
+        named_bar_sync(kBarSoftmax, 128);
+        float fac[16];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) l_part[h] *= fac[h];
+        for (int h = 0; h < 16; ++h) {
+          fac[h] = 1.f;
+          if ((need >> h) & 1u) {
+            const float mn = float_from_order_key(max(max(mx[h], mx[16 + h]), max(mx[32 + h], mx[48 + h])));
+            fac[h] = (m_ref[h] == -INFINITY) ? 0.f : fast_exp2(m_ref[h] - mn);
+            m_ref[h] = mn;
+            l_part[h] *= fac[h];
+          }
+        }
+        red_par ^= 1;
+        if (t > 0) {
+          // rescale O^T in TMEM once the previous tile's P.V is complete
+          wait_phase(&x.bar[kODone], (it - 1) & 1, x.abort_flag, p.ws_err);
+          tc::fence_after();
+#pragma unroll 1
+          for (int fb = 0; fb < 4; ++fb) {
+            uint32_t o[32];
+            tc::ld32(tl + kColO + 32 * fb, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int h = 0; h < 16; ++h) {
+              o[h] = __float_as_uint(__uint_as_float(o[h]) * fac[h]);
+              o[16 + h] = __float_as_uint(__uint_as_float(o[16 + h]) * fac[h]);
+            }
+            tc::st32(tl + kColO + 32 * fb, o);
+          }
+          tc::wait_st();
+        }
       }
       // probabilities (<= 256), two e4m3 terms, MN-major B operand row = this row
       uint32_t hi[4], lo[4];
@@ -572,11 +547,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_tc_kernel(const __grid_
   if (threadIdx.x == 0) {
     uint32_t counts[Layout::nbars];
     for (int i = 0; i < Layout::nbars; ++i) counts[i] = 1;
-    counts[kQFull] = counts[kQFull + 1] = 2;
+    counts[kQFull] = 2;
+    counts[kFinal] = 2;
     counts[kSEmpty] = counts[kSEmpty + 1] = 4;
     counts[kPFull] = counts[kPFull + 1] = 4;
     counts[kOFree] = 4;
-    counts[kRFree] = counts[kRFree + 1] = 4;
+    counts[kRFree] = 4;
     for (int i = 0; i < Layout::nbars; ++i) mbar_init(&x.bar[i], counts[i]);
     *x.abort_flag = 0;
     fence_mbar_init();
@@ -599,14 +575,16 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_tc_kernel(const __grid_
   if (warp == 0) {
     if (lane == 0) producer(p, x);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer(p, x);
-  } else if (warp < 4) {
-    prep_query(p, x, threadIdx.x - 64);
+    if (lane == 0) qk_issuer(p, x);
+  } else if (warp == 2) {
+    if (lane == 0) pv_issuer(p, x);
+  } else if (warp < 5) {
+    prep_query(p, x, threadIdx.x - 96);
   } else {
-    softmax_epilogue(p, x, warp - 4, lane);
+    softmax_epilogue(p, x, warp & 3, lane);
   }
 
-  if (warp == 1 && lane == 0) {
+  if ((warp == 1 || warp == 2) && lane == 0) {
     // every tensor-core operation of this CTA is complete before TMEM is freed
     tc::commit(&x.bar[kFinal]);
     const uint64_t t0 = global_timer_ns();
