@@ -172,6 +172,38 @@ MLA_API int mla_decode_combine(void* out, float* lse, const mla_plan* plan, void
  */
 MLA_API int mla_decode_poll_error(void* workspace, void* stream);
 
+/*
+ * mla_decode_fwd_static -- mla_decode_fwd for callers that cannot allocate
+ * device memory.  The paper has no counterpart; it exists for code that runs
+ * where it gets no allocator: a plugin or custom-operator interface of a host
+ * runtime that hands it only its inputs and outputs, or a latency-critical loop
+ * where cudaMalloc (which may synchronise the whole device and has unbounded
+ * latency) is not allowed.  Instead of a caller-owned workspace it uses one
+ * device array of MLA_STATIC_WORKSPACE_BYTES inside this library (held by
+ * every GPU that loads the library until the process exits).  It allocates
+ * nothing and calls no allocating routine.
+ *
+ * Arguments are those of mla_decode_fwd without workspace/workspace_bytes, plus
+ *   device_error  device int32[1] or NULL: receives this call's device error word
+ *                 (0, MLA_ERR_DEVICE_INDEX or MLA_ERR_DEVICE_TIMEOUT) in stream order.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Each call clears the array's error word and overwrites the rest,
+ * so nothing carries over between calls -- but every call on a device shares
+ * the one array: calls that may overlap on the GPU (different streams without
+ * ordering, or several host threads) race and give wrong results.
+ *
+ * Returns MLA_ERR_WORKSPACE_TOO_SMALL, launching nothing, when
+ * mla_decode_workspace_bytes(plan) > MLA_STATIC_WORKSPACE_BYTES (a plan with
+ * more split units than fit: plan with fewer SMs or fewer splits, or use
+ * mla_decode_fwd); otherwise the status codes of mla_decode_fwd.
+ */
+#define MLA_STATIC_WORKSPACE_BYTES (16u << 20)
+MLA_API int mla_decode_fwd_static(const void* q, const void* kv, const void* kv_scale, int32_t scale_stride,
+                                  const int32_t* kv_indptr, const int32_t* qo_indptr, void* out, float* lse,
+                                  float sm_scale, const mla_plan* plan, int32_t* device_error, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 MLA_API const char* mla_status_string(int status);
 

@@ -157,6 +157,27 @@ def mla_decode_poll_error(workspace, stream=None) -> int:
     return int(load_library().mla_decode_poll_error(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream)))
 
 
+MLA_STATIC_WORKSPACE_BYTES = 16 << 20
+
+
+def mla_decode_fwd_static(q, kv, kv_scale, kv_indptr, qo_indptr, out, lse, plan: mla_plan, device_error=None,
+                          sm_scale: float = SM_SCALE, scale_stride: int = 0, stream=None) -> None:
+    """mla_decode_fwd without a caller workspace: the library's own device array
+    of MLA_STATIC_WORKSPACE_BYTES is used (for callers that cannot allocate).
+    ``device_error``: optional int32 CUDA tensor of one element that receives
+    the call's device error word.  Calls that overlap on the GPU race."""
+    lib = load_library()
+    fn = lib.mla_decode_fwd_static
+    if fn.argtypes is None:
+        P, i32 = ctypes.c_void_p, ctypes.c_int32
+        fn.argtypes = [P, P, P, i32, P, P, P, P, ctypes.c_float, ctypes.POINTER(mla_plan), P, P]
+        fn.restype = ctypes.c_int
+    rc = fn(_ptr(q), _ptr(kv), _ptr(kv_scale), int(scale_stride), _ptr(kv_indptr), _ptr(qo_indptr), _ptr(out),
+            _ptr(lse), float(sm_scale), ctypes.byref(plan), _ptr(device_error), _stream_handle(stream, q.device))
+    if rc != MLA_OK:
+        raise MLAError(rc, "mla_decode_fwd_static")
+
+
 class MLADecoder:
     """Plan + workspace for one batch layout; call it with device tensors.
 
