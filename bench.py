@@ -45,7 +45,18 @@ DEFAULT_WORKLOAD = "bs32_kv1024_fp8"
 L2_FLUSH_BYTES = 256 << 20
 CODES = {"bf16": 0, "fp8": 1, "mxfp4": 2}
 DTYPE_LABEL = {"bf16": "bf16 x bf16 -> f32", "fp8": "e4m3 x e4m3 -> f32", "mxfp4": "e4m3 x e4m3 -> f32 (e2m1 KV)"}
-KERNEL_SOURCES = ["mla_attention_decode_gb300/csrc/mla_stage1.cuh", "mla_attention_decode_gb300/csrc/mla_ptx.cuh"]
+_CSRC = "mla_attention_decode_gb300/csrc/"
+# sources of the split kernel timed for each KV format (the profiled traffic is
+# only reported while these are unchanged since the capture)
+KERNEL_SOURCES = {
+    "bf16": [_CSRC + f for f in ("mla_stage1.cuh", "mla_common.cuh", "mla_ptx.cuh", "mla_internal.h")],
+    "fp8": [_CSRC + f for f in ("mla_tc.cuh", "mla_common.cuh", "mla_ptx.cuh", "mla_internal.h")],
+    "mxfp4": [_CSRC + f for f in ("mla_tc.cuh", "mla_common.cuh", "mla_ptx.cuh", "mla_internal.h",
+                                  "mla_split_mxfp4.cu")],
+}
+KERNEL_NAMES = {"bf16": "mla_split_kernel (mma.sync, bf16)", "fp8": "mla_split_tc_kernel (tcgen05, e4m3)",
+                "mxfp4": "mla_split_tc_kernel (tcgen05, e2m1 dequantised to e4m3)"}
+CLOCK_SOAK_S = 1.0
 
 
 def parse():
@@ -75,9 +86,9 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(kv_dtype: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kv_dtype]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -92,7 +103,7 @@ def profiled_traffic(workload: str):
     with open(path) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("kernel_sha") != kernel_source_sha():
+    if not e or e.get("kernel_sha") != kernel_source_sha(synth.WORKLOADS[workload][2]):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -274,13 +285,26 @@ def main():
         call()
     assert dec.poll_error() == 0
 
-    # ---- headline: whole call, device time, L2 flushed before each call
+    # ---- headline: whole call, device time, L2 flushed before each call.  The
+    # clock samples cover the timed steps and a soak of the same flushed calls
+    # around them (the timed region alone is shorter than the sampling period).
+    def soak(seconds):
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            for i in range(20):
+                flush.fill_(i)
+                call()
+            torch.cuda.synchronize()
+
     barrier()
     with ClockSampler(local) as clk:
+        soak(CLOCK_SOAK_S / 2)
+        barrier()
         t_wall = time.perf_counter()
         per_call = time_calls(call, args.steps, flush, stream)
         barrier()
         t_wall = time.perf_counter() - t_wall
+        soak(CLOCK_SOAK_S / 2)
     us = statistics.mean(per_call)
     if pg is not None:
         t = torch.tensor([us], device=dev)
@@ -352,12 +376,12 @@ def main():
             "kv_gbs": round(kv_bytes / (us * 1e-6) / 1e9, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": profiled_traffic(name),
-                         "kernel": f"mla_split_kernel<{dt}>", "kernel_us": round(t_split, 3),
+                         "kernel": KERNEL_NAMES[dt], "kernel_us": round(t_split, 3),
                          "combine_us": round(t_comb, 3), "peak_kind": f"{peak_kind} (HBM copy)"},
             "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps * launches_per_call,
-            "clocks": clk.summary(),
+            "clocks": dict(clk.summary(), window="timed steps plus a 1 s soak of the same calls"),
             "wall_s_timed_loop": round(t_wall, 4),
             "cpu_baseline": cpu,
         }
