@@ -15,7 +15,6 @@
 namespace {
 
 using mla::kHeads;
-using mla::kMaxUnitsPerCta;
 using mla::kTile;
 using mla::kVDim;
 
@@ -178,7 +177,7 @@ int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dty
     const int rc = device_sm_count(&sms);
     if (rc != MLA_OK) return rc;
   }
-  const int64_t unit_cap = (int64_t)sms * kMaxUnitsPerCta;
+  const int64_t unit_cap = (int64_t)sms * mla::max_units_per_cta(kv_dtype);
 
   int32_t chunk = 1, cap = kNoCap;
   int64_t work = 0;
@@ -260,7 +259,7 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
     *nothing_to_do = true;
     return MLA_OK;
   }
-  if (plan->units_per_cta > kMaxUnitsPerCta || plan->grid <= 0) return MLA_ERR_INVALID_ARG;
+  if (plan->units_per_cta > mla::max_units_per_cta(plan->kv_dtype) || plan->grid <= 0) return MLA_ERR_INVALID_ARG;
   if (!q || !kv || !kv_indptr || !qo_indptr || !out || !workspace) return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 8) || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   if (!aligned(kv_indptr, 4) || !aligned(qo_indptr, 4) || (lse && !aligned(lse, 4))) return MLA_ERR_INVALID_ARG;
@@ -293,6 +292,10 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   if (plan->kv_dtype == MLA_KV_FP8_E4M3) {
     if (!encode_kv_map_tc(&p->tmap_kv64, kv, plan->total_kv)) return MLA_ERR_CUDA;
     std::memcpy(&p->tmap_kv16, &p->tmap_kv64, sizeof(CUtensorMap));
+  } else if (plan->kv_dtype == MLA_KV_MXFP4) {
+    // packed rows are fetched by 1-D bulk copies: no tensor map
+    std::memset(&p->tmap_kv64, 0, sizeof(CUtensorMap));
+    std::memset(&p->tmap_kv16, 0, sizeof(CUtensorMap));
   } else if (!encode_kv_map(&p->tmap_kv64, kv, plan->kv_dtype, plan->total_kv, 64) ||
              !encode_kv_map(&p->tmap_kv16, kv, plan->kv_dtype, plan->total_kv, 16)) {
     return MLA_ERR_CUDA;

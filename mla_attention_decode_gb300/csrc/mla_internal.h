@@ -14,6 +14,8 @@ constexpr int kTile = 64;              // KV rows per pipeline stage
 constexpr int kConsumerWarps = 8;      // 4 pairs; pair p scores rows [16p, 16p+16) of a tile
 constexpr int kThreads = kConsumerWarps * 32;
 constexpr int kMaxUnitsPerCta = 256;   // work units one CTA may own (unit table in smem)
+constexpr int kMaxUnitsPerCtaMx = 64;  // the same for MXFP4 KV (its staging ring leaves less smem)
+inline int max_units_per_cta(int kv_dtype) { return kv_dtype == 2 ? kMaxUnitsPerCtaMx : kMaxUnitsPerCta; }
 
 // Workspace layout (byte offsets from the 256-aligned base).
 struct WsLayout {

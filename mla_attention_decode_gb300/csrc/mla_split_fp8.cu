@@ -2,5 +2,5 @@
 #include "mla_tc.cuh"
 
 namespace mla {
-cudaError_t launch_stage1_fp8(const Stage1Params& p, cudaStream_t s) { return launch_split_tc_fp8(p, s); }
+cudaError_t launch_stage1_fp8(const Stage1Params& p, cudaStream_t s) { return launch_split_tc<false>(p, s); }
 }  // namespace mla

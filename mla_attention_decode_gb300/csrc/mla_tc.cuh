@@ -1,13 +1,14 @@
-// mla_tc.cuh -- split-K MLA decode for e4m3 KV on the 5th-generation tensor
-// cores (tcgen05, accumulators in tensor memory), sm_103a.
+// mla_tc.cuh -- split-K MLA decode for e4m3 and e2m1 (MXFP4) KV on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory), sm_103a.
 //
 // Same contract as the split kernel in mla_stage1.cuh (kernelindex
 // "amd-mixed-mla" submission 593653, "Slow fallback" for the definition and
-// "_flash_fp8_split_s1" for the split form): per work unit, softmax attention of
-// the 16 query heads over a contiguous range of KV rows; final bf16 output and
-// lse for unsplit sequences, fp32 partials and lse for split ones.
+// "_flash_fp8_split_s1" for the split form; submission 754939 "Stage 1" for the
+// MXFP4 layout): per work unit, softmax attention of the 16 query heads over a
+// contiguous range of KV rows; final bf16 output and lse for unsplit
+// sequences, fp32 partials and lse for split ones.
 //
-// Per 128-row tile t of a unit (one CTA of 9 warps per SM, persistent):
+// Per 128-row tile t of a unit (one persistent CTA per SM: 9 warps for e4m3, 12 for MXFP4):
 //   scores  S^T[128 rows x 32] = K_t[128 x 576] . [Q_hi | Q_lo]^T   (tcgen05 kind::f8f6f4,
 //           18 k32 steps; K straight from the TMA stage, K-major, 64 B swizzle;
 //           the query as two e4m3 terms x = hi + lo with a power-of-two scale
@@ -35,6 +36,18 @@
 // softmax, O^T rescale and the unit epilogue (warp w reads TMEM lanes
 // [32 (w mod 4), +32)).  Hand-offs are mbarriers (TMA transaction bytes,
 // tcgen05.commit, thread arrivals).
+//
+// MXFP4 KV (kMx): rows arrive packed (288 B of e2m1 pairs, element 2i in the low
+// nibble of byte i) by 1-D bulk copies of 64-row halves into a staging ring,
+// and three converter warps (9-11) write them into the same e4m3 ring layout
+// the tensor cores read (8 pair slots: two whole tiles, so that converting
+// tile t only waits for the P.V of tile t-2).  Per row, with G = the largest of its 18 e8m0 bytes,
+// element n * 2^(e-127) becomes the e4m3 value n * 2^(e-G) (exact while the
+// row's block exponents lie within 8 of G; smaller ones round to e4m3's
+// subnormal grid), through an 8-entry magnitude table per shift applied with
+// prmt.  2^(G-127) goes into the row's score factor, and into P for P.V
+// relative to a running per-unit reference Gv (raised lazily like the softmax
+// reference, with O^T rescaled); the output is O^T 2^Gv / l.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -47,12 +60,19 @@ namespace tcfp8 {
 constexpr int kTileRows = 128;
 constexpr int kChunkBytes = kTileRows * 64;  // one 64-byte feature column block of a tile
 constexpr int kPairBytes = 2 * kChunkBytes;  // two column blocks = features [128 f, 128 f + 128)
-constexpr int kPairSlots = 11;               // ring of V column-block pairs (4 per tile)
+template <bool kMx>
+struct Geo {
+  static constexpr int pair_slots = kMx ? 8 : 11;  // ring of V column-block pairs (4 per tile)
+  static constexpr int threads = kMx ? 384 : 288;
+  static constexpr int max_units = kMx ? kMaxUnitsPerCtaMx : kMaxUnitsPerCta;  // work units one CTA may own
+};
 constexpr int kRopeSlots = 2;                // ring of the rope column block (features 512..575)
 constexpr int kQsBytes = 9 * 32 * 64;        // two-term query: 32 rows x 576 B, K-major, 64 B swizzle
 constexpr int kPBytes = kTileRows * 32;      // two-term P^T: 128 rows x 32 B, MN-major, 32 B swizzle
-constexpr int kThreads = 288;
-constexpr int kMaxUnits = 256;               // work units one CTA may own
+constexpr int kHalfRows = 64;                        // MXFP4 staging unit: 64 packed rows
+constexpr int kPackedRowBytes = 288;
+constexpr int kStageBytes = kHalfRows * kPackedRowBytes;  // 18 KB
+constexpr int kStageSlots = 3;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0;   // S^T double buffer: columns [0, 32) and [32, 64)
 constexpr uint32_t kColO = 64;  // O^T: 4 feature blocks x 32 columns
@@ -61,24 +81,30 @@ constexpr uint32_t kBarSoftmax = 1;  // named barrier of the softmax warps (128 
 constexpr uint32_t kIdescQK = tc::idesc_e4m3(128, 32, 0, 0);
 constexpr uint32_t kIdescPV = tc::idesc_e4m3(128, 32, 1, 1);
 
+template <bool kMx>
 struct Layout {
+  static constexpr int kPairSlots = Geo<kMx>::pair_slots;
   static constexpr int pairs = 0;                             // 1024-aligned
   static constexpr int rope = pairs + kPairSlots * kPairBytes;
-  static constexpr int qs = rope + kRopeSlots * kChunkBytes;
+  static constexpr int stage = rope + kRopeSlots * kChunkBytes;      // MXFP4 only: packed rows
+  static constexpr int qs = stage + (kMx ? kStageSlots * kStageBytes : 0);
   static constexpr int pb = qs + kQsBytes;                    // [2]
   static constexpr int rq = pb + 2 * kPBytes;                 // float [16] score factor per head
   static constexpr int red = rq + 16 * 4;                     // float [2][4 warps][16]
-  static constexpr int units = red + 2 * 4 * 16 * 4;
-  static constexpr int bars = units + kMaxUnits * (int)sizeof(UnitDesc);
-  static constexpr int nbars = 41;
+  static constexpr int gred = red + 2 * 4 * 16 * 4;           // int [2][4] tile max of the row exponents
+  static constexpr int grow = gred + 2 * 4 * 4;               // int8 [2][128] row exponent G - 127 (MXFP4)
+  static constexpr int lut = grow + (kMx ? 2 * 128 : 0);      // u8 [16][8] e2m1 magnitude -> e4m3 per shift
+  static constexpr int units = lut + (kMx ? 128 : 0);
+  static constexpr int bars = units + Geo<kMx>::max_units * (int)sizeof(UnitDesc);
+  static constexpr int nbars = 49;
   static constexpr int misc = bars + nbars * 8;  // tmem slot, abort flag, unit count
   static constexpr int total = misc + 16;
 };
 
 // mbarrier slots
 enum {
-  kPairFull = 0,    // [11] TMA bytes of a V column-block pair
-  kPairEmpty = 11,  // [11] commit after the P.V block that read it
+  kPairFull = 0,    // [<=11] TMA bytes of a V column-block pair (e4m3)
+  kPairEmpty = 11,  // [<=11] commit after the P.V block that read it
   kRopeFull = 22,   // [2]  TMA bytes of a rope column block
   kRopeEmpty = 24,  // [2]  commit after the QK that read it
   kQFull = 26,      // query of the next unit prepared (2 warps)
@@ -92,6 +118,9 @@ enum {
   kOLast = 37,      // commit after a unit's last P.V (once per unit with tiles)
   kFinal = 38,      // commits after both issuers' last operations (count 2)
   kPFree = 39,      // [2]  commit after the P.V that read P buffer t mod 2
+  kStageFull = 41,  // [3]  MXFP4: bytes of a staged half tile (or the producer's arrival)
+  kStageEmpty = 44, // [3]  MXFP4: the converter warps read it (3 warps)
+  kConvFull = 47,   // [2]  MXFP4: tile t converted into the ring (3 warps)
 };
 
 __device__ __forceinline__ uint32_t sw64_off(int row, int col) {  // byte (row, col) of a 64 B-row, 64 B-swizzled block
@@ -111,12 +140,19 @@ __device__ __forceinline__ int tiles_of(const UnitDesc& d) { return (d.end - d.s
 
 // ------------------------------------------------------------------ producer
 // Column blocks of tile t: pair f (features [128 f, 128 f + 128)) goes to pair
-// slot (4t + f) mod 11, the rope block to rope slot t mod 2; each slot is
-// re-armed as soon as the MMA that read it has completed.
-__device__ __forceinline__ int pair_slot(int t, int f) { return (4 * t + f) % kPairSlots; }
-__device__ __forceinline__ int pair_use(int t, int f) { return (4 * t + f) / kPairSlots; }
+// slot (4t + f) mod S (S = 11 for e4m3, 7 for MXFP4), the rope block to rope
+// slot t mod 2; each slot is re-filled as soon as the MMA that read it has
+// completed.
+template <bool kMx>
+__device__ __forceinline__ int pair_slot(int t, int f) { return (4 * t + f) % Geo<kMx>::pair_slots; }
+template <bool kMx>
+__device__ __forceinline__ int pair_use(int t, int f) { return (4 * t + f) / Geo<kMx>::pair_slots; }
+template <bool kMx>
+__device__ __forceinline__ int wrap_slot(int s) { return s >= Geo<kMx>::pair_slots ? s - Geo<kMx>::pair_slots : s; }
 
-__device__ void producer(const Stage1Params& p, const Ctx& x) {
+static __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
+  using L = Layout<false>;
+  constexpr int kPairSlots = Geo<false>::pair_slots;
   const uint64_t pol = policy_evict_first();  // KV rows are read once
   int it = 0;
   int armed[kPairSlots + kRopeSlots];
@@ -125,10 +161,10 @@ __device__ void producer(const Stage1Params& p, const Ctx& x) {
     const UnitDesc d = x.units[k];
     for (int t0 = d.start; t0 < d.end && !*x.abort_flag; t0 += kTileRows, ++it) {
       for (int f = 0; f < 4; ++f) {
-        const int sl = pair_slot(it, f), use = pair_use(it, f);
+        const int sl = pair_slot<false>(it, f), use = pair_use<false>(it, f);
         if (use >= 1) wait_phase(&x.bar[kPairEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
         if (*x.abort_flag) break;
-        uint8_t* dst = x.smem + Layout::pairs + sl * kPairBytes;
+        uint8_t* dst = x.smem + L::pairs + sl * kPairBytes;
         mbar_arrive_expect_tx(&x.bar[kPairFull + sl], kPairBytes);
         tma_load_2d(dst, &p.tmap_kv64, 128 * f, t0, &x.bar[kPairFull + sl], pol);
         tma_load_2d(dst + kChunkBytes, &p.tmap_kv64, 128 * f + 64, t0, &x.bar[kPairFull + sl], pol);
@@ -138,7 +174,7 @@ __device__ void producer(const Stage1Params& p, const Ctx& x) {
       if (ruse >= 1) wait_phase(&x.bar[kRopeEmpty + rs], (ruse - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
       mbar_arrive_expect_tx(&x.bar[kRopeFull + rs], kChunkBytes);
-      tma_load_2d(x.smem + Layout::rope + rs * kChunkBytes, &p.tmap_kv64, 512, t0, &x.bar[kRopeFull + rs], pol);
+      tma_load_2d(x.smem + L::rope + rs * kChunkBytes, &p.tmap_kv64, 512, t0, &x.bar[kRopeFull + rs], pol);
       ++armed[kPairSlots + rs];
     }
   }
@@ -154,17 +190,201 @@ __device__ void producer(const Stage1Params& p, const Ctx& x) {
   }
 }
 
+
+// ------------------------------------------------------- MXFP4 producer
+// Half tiles (64 packed rows, 18 KB) into a ring of 3 staging slots by 1-D bulk
+// copies (rows of a unit are contiguous); the rows' scale bytes are prefetched
+// into L2 for the converter warps.  A half with no rows (the second half of a
+// short tile) is signalled by a plain arrival.
+static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
+  using L = Layout<true>;
+  const uint64_t pol = policy_evict_first();  // KV rows are read once
+  const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
+  const size_t ss = (size_t)p.scale_stride;
+  int hh = 0;
+  int uses[kStageSlots] = {0, 0, 0};
+  for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
+    const UnitDesc d = x.units[k];
+    for (int t0 = d.start; t0 < d.end && !*x.abort_flag; t0 += kTileRows) {
+      for (int h = 0; h < 2; ++h, ++hh) {
+        const int sl = hh % kStageSlots, use = hh / kStageSlots;
+        if (use >= 1) wait_phase(&x.bar[kStageEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
+        if (*x.abort_flag) break;
+        const int r0 = t0 + h * kHalfRows;
+        const int rows = max(0, min(kHalfRows, d.end - r0));
+        if (rows > 0) {
+          mbar_arrive_expect_tx(&x.bar[kStageFull + sl], (uint32_t)(rows * kPackedRowBytes));
+          bulk_g2s(x.smem + L::stage + sl * kStageBytes, p.kv + (size_t)r0 * kPackedRowBytes,
+                   (uint32_t)(rows * kPackedRowBytes), &x.bar[kStageFull + sl], pol);
+          const uint8_t* a0 = sc + (size_t)r0 * ss;
+          const size_t nb = (size_t)rows * ss;
+          for (size_t o = 0; o < nb; o += 128) prefetch_l2(a0 + o);
+          prefetch_l2(a0 + nb - 1);
+        } else {
+          mbar_arrive(&x.bar[kStageFull + sl]);
+        }
+        ++uses[sl];
+      }
+    }
+  }
+  if (*x.abort_flag) {
+    // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
+    for (int i = 0; i < kStageSlots; ++i) {
+      if (uses[i] == 0) continue;
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(&x.bar[kStageFull + i], (uses[i] - 1) & 1) && global_timer_ns() - t0 < kWaitTimeoutNs) {
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------- MXFP4 converters
+// Walks the CTA's half tiles in order: unit k, rows [t0 + 64 h, ...) of its
+// tile starting at t0.
+struct HalfCursor {
+  int k = 0, t0 = -1, h = 0;
+  __device__ bool next(const Ctx& x, int& r0, int& rows) {
+    while (k < x.nunits) {
+      const UnitDesc d = x.units[k];
+      if (t0 < 0) t0 = d.start;
+      if (t0 >= d.end) {
+        ++k;
+        t0 = -1;
+        h = 0;
+        continue;
+      }
+      r0 = t0 + h * kHalfRows;
+      rows = max(0, min(kHalfRows, d.end - r0));
+      if (++h == 2) {
+        h = 0;
+        t0 += kTileRows;
+      }
+      return true;
+    }
+    return false;
+  }
+};
+
+// The 18 scale bytes of a row (nothing for a row past the half's end).
+__device__ __forceinline__ void load_row_scales(const uint8_t* sc, size_t ss, int grow_row, bool valid,
+                                                uint32_t (&e)[18]) {
+  const uint8_t* a = sc + (size_t)grow_row * ss;
+#pragma unroll
+  for (int i = 0; i < 18; ++i) e[i] = valid ? (uint32_t)__ldg(a + i) : 127u;
+}
+
+// Eight e2m1 codes (one 32-bit word, element 2i in the low nibble of byte i)
+// to eight e4m3 bytes for the shift whose magnitude table is (lo, hi).
+__device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lut_lo, uint32_t lut_hi) {
+  // prmt selects byte (nibble & 7) of {lut_lo, lut_hi} per element; with bit 3
+  // (the sign) set in the selector the byte becomes 0xFF (the msb of 0x80
+  // replicated) instead of 0x80, which yields the sign bit
+  const uint32_t m0 = prmt(lut_lo, lut_hi, w & 0x7777u);
+  const uint32_t s0 = prmt(0x80808080u, 0x80808080u, w & 0xFFFFu);
+  const uint32_t w1 = w >> 16;
+  const uint32_t m1 = prmt(lut_lo, lut_hi, w1 & 0x7777u);
+  const uint32_t s1 = prmt(0x80808080u, 0x80808080u, w1);
+  return make_uint2(m0 | ((s0 << 1) & 0x80808080u), m1 | ((s1 << 1) & 0x80808080u));
+}
+
+// Converter warp cw (0..2) writes chunks 3 cw .. 3 cw + 2 (features
+// [192 cw, 192 cw + 192)) of rows lane and lane + 32 of every half tile.
+static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw, int lane) {
+  using L = Layout<true>;
+  const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
+  const size_t ss = (size_t)p.scale_stride;
+  const uint2* lut = reinterpret_cast<const uint2*>(x.smem + L::lut);
+  int8_t* grow = reinterpret_cast<int8_t*>(x.smem + L::grow);
+  HalfCursor cur, pre;
+  int r0 = 0, rows = 0, pr0 = 0, prows = 0;
+  uint32_t e_next[2][18];
+  bool have_next = pre.next(x, pr0, prows);
+  if (have_next) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) load_row_scales(sc, ss, pr0 + lane + 32 * j, lane + 32 * j < prows, e_next[j]);
+  }
+  for (int hh = 0; cur.next(x, r0, rows) && !*x.abort_flag; ++hh) {
+    const int it = hh >> 1, h = hh & 1;
+    uint32_t e[2][18];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int i = 0; i < 18; ++i) e[j][i] = e_next[j][i];
+    // the next half's scale bytes are loaded while this one is converted
+    have_next = pre.next(x, pr0, prows);
+    if (have_next) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) load_row_scales(sc, ss, pr0 + lane + 32 * j, lane + 32 * j < prows, e_next[j]);
+    }
+    if (h == 0) {
+      // the tile's ring slots must have been released by the MMAs that read them
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+        const int use = pair_use<true>(it, f);
+        if (use >= 1)
+          wait_phase(&x.bar[kPairEmpty + pair_slot<true>(it, f)], (use - 1) & 1, x.abort_flag, p.ws_err);
+      }
+      const int ruse = it / kRopeSlots;
+      if (ruse >= 1) wait_phase(&x.bar[kRopeEmpty + it % kRopeSlots], (ruse - 1) & 1, x.abort_flag, p.ws_err);
+    }
+    const int sl = hh % kStageSlots;
+    wait_phase(&x.bar[kStageFull + sl], (hh / kStageSlots) & 1, x.abort_flag, p.ws_err);
+    const uint8_t* stage = x.smem + L::stage + sl * kStageBytes;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int lr = lane + 32 * j;       // row within the half
+      const int row = h * kHalfRows + lr;  // row within the tile
+      const bool valid = lr < rows;
+      uint32_t g = 0;
+#pragma unroll
+      for (int i = 0; i < 18; ++i) g = max(g, e[j][i]);
+      g = max(g, 1u);
+      if (cw == 0) grow[(it & 1) * 128 + row] = (int8_t)(valid ? (int)min(g, 254u) - 127 : 0);
+      const uint4* src = reinterpret_cast<const uint4*>(stage + lr * kPackedRowBytes + 96 * cw);
+#pragma unroll
+      for (int bi = 0; bi < 6; ++bi) {  // one 32-element block per 16 packed bytes
+        const int c = 3 * cw + (bi >> 1);
+        uint8_t* base = c < 8 ? x.smem + L::pairs + pair_slot<true>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes
+                              : x.smem + L::rope + (it % kRopeSlots) * kChunkBytes;
+        const int col = 32 * (bi & 1);
+        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+        if (valid) {
+          const uint4 w = src[bi];
+          const uint32_t shift = min(g - e[j][6 * cw + bi], 15u);
+          const uint2 lt = lut[shift];
+          const uint2 a = e2m1x8_to_e4m3(w.x, lt.x, lt.y), b = e2m1x8_to_e4m3(w.y, lt.x, lt.y);
+          const uint2 cc = e2m1x8_to_e4m3(w.z, lt.x, lt.y), dd = e2m1x8_to_e4m3(w.w, lt.x, lt.y);
+          o0 = make_uint4(a.x, a.y, b.x, b.y);
+          o1 = make_uint4(cc.x, cc.y, dd.x, dd.y);
+        }
+        *reinterpret_cast<uint4*>(base + sw64_off(row, col)) = o0;
+        *reinterpret_cast<uint4*>(base + sw64_off(row, col + 16)) = o1;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&x.bar[kStageEmpty + sl]);
+    if (h == 1) {
+      tc::fence_proxy_async();  // the tensor core reads the ring through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&x.bar[kConvFull + (it & 1)]);
+    }
+  }
+}
+
 // ---------------------------------------------------------- query preparation
 // 64 threads: thread j handles head j/4, features [144 (j%4), 144 (j%4) + 144).
 // One query buffer: unit k's rows are loaded (and their scale found) first,
 // then converted to two e4m3 terms and stored once the last QK of unit k-1 has
 // completed and the softmax has taken unit k-1's score factors.
+template <bool kMx>
 __device__ void prep_query(const Stage1Params& p, const Ctx& x, int j) {
+  using L = Layout<kMx>;
   const int h = j >> 2, part = j & 3;
-  const float kv_scale = *static_cast<const float*>(p.kv_scale);
+  // e4m3: the per-tensor scale goes into the score factor; MXFP4 scales are per row
+  const float kv_scale = kMx ? 1.f : *static_cast<const float*>(p.kv_scale);
   const float base_factor = p.sm_scale * kLog2e * kv_scale;
-  float* rq = reinterpret_cast<float*>(x.smem + Layout::rq);
-  uint8_t* qs = x.smem + Layout::qs;
+  float* rq = reinterpret_cast<float*>(x.smem + L::rq);
+  uint8_t* qs = x.smem + L::qs;
   for (int k = 0; k < x.nunits; ++k) {
     const int qrow = p.qo_indptr[x.units[k].b];
     const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)qrow * kHeads + h) * kQkDim + 144 * part) * 2);
@@ -224,31 +444,39 @@ constexpr uint64_t kTplP = tc::desc_template(1024, 256, 6);          // P^T, MN-
 __host__ __device__ constexpr uint32_t lo_word(uint64_t d) { return (uint32_t)d; }
 __host__ __device__ constexpr uint32_t hi_word(uint64_t d) { return (uint32_t)(d >> 32); }
 
-__device__ __forceinline__ int wrap_slot(int s) { return s >= kPairSlots ? s - kPairSlots : s; }
 
 // QK of every tile: S^T(t) into TMEM columns [32 (t mod 2), +32).
+template <bool kMx>
 __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
-  const uint32_t pairs0 = smem_u32(x.smem + Layout::pairs), rope0 = smem_u32(x.smem + Layout::rope);
-  const uint32_t bq = lo_word(kTplK64) + (smem_u32(x.smem + Layout::qs) >> 4);
+  using L = Layout<kMx>;
+  constexpr int kPairSlots = Geo<kMx>::pair_slots;
+  const uint32_t pairs0 = smem_u32(x.smem + L::pairs), rope0 = smem_u32(x.smem + L::rope);
+  const uint32_t bq = lo_word(kTplK64) + (smem_u32(x.smem + L::qs) >> 4);
   int it = 0;
   for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
     const int nt = tiles_of(x.units[k]);
     wait_phase(&x.bar[kQFull], k & 1, x.abort_flag, p.ws_err);
     for (int t = 0; t < nt; ++t, ++it) {
       const int s0 = (4 * it) % kPairSlots, use0 = (4 * it) / kPairSlots;
+      if constexpr (kMx) {
+        // the converter warps filled all of the tile's slots
+        wait_phase(&x.bar[kConvFull + (it & 1)], (it >> 1) & 1, x.abort_flag, p.ws_err);
+      } else {
 #pragma unroll
-      for (int f = 0; f < 4; ++f) {
-        const int sl = s0 + f;
-        wait_phase(&x.bar[kPairFull + wrap_slot(sl)], (use0 + (sl >= kPairSlots)) & 1, x.abort_flag, p.ws_err);
+        for (int f = 0; f < 4; ++f) {
+          const int sl = s0 + f;
+          wait_phase(&x.bar[kPairFull + wrap_slot<kMx>(sl)], (use0 + (sl >= kPairSlots)) & 1, x.abort_flag,
+                     p.ws_err);
+        }
+        wait_phase(&x.bar[kRopeFull + it % kRopeSlots], (it / kRopeSlots) & 1, x.abort_flag, p.ws_err);
       }
-      wait_phase(&x.bar[kRopeFull + it % kRopeSlots], (it / kRopeSlots) & 1, x.abort_flag, p.ws_err);
       if (it >= 2) wait_phase(&x.bar[kSEmpty + (it & 1)], ((it >> 1) - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
       tc::fence_after();
       uint32_t ap[4];
 #pragma unroll
       for (int f = 0; f < 4; ++f)
-        ap[f] = lo_word(kTplK64) + ((pairs0 + (uint32_t)wrap_slot(s0 + f) * kPairBytes) >> 4);
+        ap[f] = lo_word(kTplK64) + ((pairs0 + (uint32_t)wrap_slot<kMx>(s0 + f) * kPairBytes) >> 4);
       const uint32_t ar = lo_word(kTplK64) + ((rope0 + (uint32_t)(it % kRopeSlots) * kChunkBytes) >> 4);
       const uint32_t d = x.tmem + kColS + 32 * (it & 1);
 #pragma unroll
@@ -268,8 +496,11 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
 
 // P.V of every tile: O^T += V^T(t) . P^T(t); releases the tile's ring slots, its
 // P buffer and, on a unit's last tile, the unit's O^T.
+template <bool kMx>
 __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
-  const uint32_t pairs0 = smem_u32(x.smem + Layout::pairs), pb0 = smem_u32(x.smem + Layout::pb);
+  using L = Layout<kMx>;
+  constexpr int kPairSlots = Geo<kMx>::pair_slots;
+  const uint32_t pairs0 = smem_u32(x.smem + L::pairs), pb0 = smem_u32(x.smem + L::pb);
   int it = 0, ordinal = 0;
   for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
     const int nt = tiles_of(x.units[k]);
@@ -284,7 +515,7 @@ __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
       const int s0 = (4 * it) % kPairSlots;
 #pragma unroll
       for (int fb = 0; fb < 4; ++fb) {
-        const int sl = wrap_slot(s0 + fb);
+        const int sl = wrap_slot<kMx>(s0 + fb);
         // V^T block: features [128 fb, 128 fb + 128) = the slot's two column blocks (LBO)
         const uint32_t av = lo_word(kTplV) + ((pairs0 + (uint32_t)sl * kPairBytes) >> 4);
 #pragma unroll
@@ -337,12 +568,20 @@ __device__ __forceinline__ void group_reduce16(float (&v)[16], float* red, int w
   }
 }
 
+// 2^e for an integer e in [-126, 127] (exact).
+__device__ __forceinline__ float exp2_int(int e) { return __int_as_float((e + 127) << 23); }
+
+template <bool kMx>
 __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, int lane) {
+  using L = Layout<kMx>;
+  constexpr int kGvNone = -1000;   // no MXFP4 reference yet
   const int row = 32 * ww + lane;  // tile row == TMEM lane of this thread
   const uint32_t tl = x.tmem + ((uint32_t)(32 * ww) << 16);
-  const float kv_scale = *static_cast<const float*>(p.kv_scale);
-  const float* rq = reinterpret_cast<const float*>(x.smem + Layout::rq);
-  float* redbuf = reinterpret_cast<float*>(x.smem + Layout::red);
+  const float kv_scale = kMx ? 1.f : *static_cast<const float*>(p.kv_scale);
+  const int8_t* grow = reinterpret_cast<const int8_t*>(x.smem + L::grow);
+  int* gred = reinterpret_cast<int*>(x.smem + L::gred);
+  const float* rq = reinterpret_cast<const float*>(x.smem + L::rq);
+  float* redbuf = reinterpret_cast<float*>(x.smem + L::red);
   int it = 0, red_par = 0, ordinal = 0;
   for (int k = 0; k < x.nunits; ++k) {
     const UnitDesc d = x.units[k];
@@ -378,6 +617,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       m_ref[h] = -INFINITY;
       l_part[h] = 0.f;
     }
+    int gv = kGvNone;  // MXFP4: P.V reference exponent of the unit
     for (int t = 0; t < nt; ++t, ++it) {
       const int sb = it & 1;
       const int t0 = d.start + t * kTileRows;
@@ -390,13 +630,20 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&x.bar[kSEmpty + sb]);
+      // MXFP4: the row's exponent G - 127, written by the converter warps before
+      // they released the tile (waited for here too, so that the bytes are visible)
+      if (kMx) wait_phase(&x.bar[kConvFull + sb], (it >> 1) & 1, x.abort_flag, p.ws_err);
+      const int gsh = kMx ? max(-126, (int)grow[sb * 128 + row]) : 0;
+      const float row_fac = kMx ? exp2_int(gsh) : 1.f;
       float sv[16];
-      uint32_t need = 0;  // heads with a score above m_ref + 8 in this row
+      uint32_t need = 0;  // heads with a score above m_ref + 8 in this row (bit 16: G above gv)
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
-        sv[h] = row < valid ? (__uint_as_float(acc[h]) + __uint_as_float(acc[16 + h])) * r[h] : -INFINITY;
+        sv[h] = row < valid ? (__uint_as_float(acc[h]) + __uint_as_float(acc[16 + h])) * (r[h] * row_fac)
+                            : -INFINITY;
         need |= (sv[h] > m_ref[h] + kRescaleLog2 ? 1u : 0u) << h;
       }
+      if (kMx && row < valid && gsh > gv) need |= 1u << 16;
       // heads whose reference rises: OR over the warp, then over the 4 warps
       need = __reduce_or_sync(0xffffffffu, need);
       {
@@ -419,6 +666,10 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
             const int w = __reduce_max_sync(0xffffffffu, float_order_key(sv[h]));
             if (lane == 0) mx[ww * 16 + h] = w;
           }
+        if (kMx && ((need >> 16) & 1u)) {
+          const int w = __reduce_max_sync(0xffffffffu, row < valid ? gsh : kGvNone);
+          if (lane == 0) gred[red_par * 4 + ww] = w;
+        }
         named_bar_sync(kBarSoftmax, 128);
         float fac[16];
 #pragma unroll
@@ -430,6 +681,15 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
             m_ref[h] = mn;
             l_part[h] *= fac[h];
           }
+        }
+        if (kMx && ((need >> 16) & 1u)) {
+          // raise the P.V reference: O^T so far is scaled down by 2^(gv_old - gv_new)
+          const int* g4 = gred + red_par * 4;
+          const int gnew = max(max(g4[0], g4[1]), max(g4[2], g4[3]));
+          const float facg = gv == kGvNone ? 0.f : exp2_int(max(-126, gv - gnew));
+          gv = gnew;
+#pragma unroll
+          for (int h = 0; h < 16; ++h) fac[h] *= facg;
         }
         red_par ^= 1;
         if (t > 0) {
@@ -451,7 +711,9 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
           tc::wait_st();
         }
       }
-      // probabilities (<= 256), two e4m3 terms, MN-major B operand row = this row
+      // probabilities (<= 256), two e4m3 terms, MN-major B operand row = this row;
+      // MXFP4 weights for P.V carry the row's 2^(G-127) relative to 2^gv (<= 1)
+      const float pv_fac = kMx ? exp2_int(max(-126, gsh - gv)) : 1.f;
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
@@ -459,21 +721,22 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int h = 4 * g + e;
-          pv[e] = (m_ref[h] == -INFINITY) ? 0.f : fast_exp2(sv[h] - m_ref[h]);
-          l_part[h] += pv[e];
+          const float pr = (m_ref[h] == -INFINITY) ? 0.f : fast_exp2(sv[h] - m_ref[h]);
+          l_part[h] += pr;
+          pv[e] = pr * pv_fac;
         }
         two_term_e4m3(pv[0], pv[1], pv[2], pv[3], hi[g], lo[g]);
       }
-      uint8_t* pbuf = x.smem + Layout::pb + sb * kPBytes + row * 32;
+      uint8_t* pbuf = x.smem + L::pb + sb * kPBytes + row * 32;
       const int xr = (row >> 2) & 1;  // 32 B swizzle: the 16-byte units of the row swap
       *reinterpret_cast<uint4*>(pbuf + 16 * xr) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(pbuf + 16 * (xr ^ 1)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      if (row >= valid) {
+      if (!kMx && row >= valid) {
         // rows past the unit's end hold other rows' data: zero their V part so
-        // that P = 0 cannot meet a non-finite value
+        // that P = 0 cannot meet a non-finite value (the MXFP4 converters write zeros)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          uint8_t* blk = x.smem + Layout::pairs + pair_slot(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes;
+          uint8_t* blk = x.smem + L::pairs + pair_slot<kMx>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes;
 #pragma unroll
           for (int uu = 0; uu < 4; ++uu)
             *reinterpret_cast<uint4*>(blk + sw64_off(row, 16 * uu)) = make_uint4(0, 0, 0, 0);
@@ -494,7 +757,8 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
     tc::fence_after();
     float inv[16];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) inv[h] = l_part[h] > 0.f ? kv_scale * __frcp_rn(l_part[h]) : 0.f;
+    const float out_scale = kMx ? exp2_int(max(-126, min(127, gv))) : kv_scale;
+    for (int h = 0; h < 16; ++h) inv[h] = l_part[h] > 0.f ? out_scale * __frcp_rn(l_part[h]) : 0.f;
 #pragma unroll 1
     for (int fb = 0; fb < 4; ++fb) {
       uint32_t o[32];
@@ -532,34 +796,44 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mla_split_tc_kernel(const __grid_constant__ Stage1Params p) {
+template <bool kMx>
+__global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(const __grid_constant__ Stage1Params p) {
+  using L = Layout<kMx>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Ctx x;
   x.smem = smem;
-  x.units = reinterpret_cast<const UnitDesc*>(smem + Layout::units);
-  x.bar = reinterpret_cast<uint64_t*>(smem + Layout::bars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Layout::misc);
-  int* misc = reinterpret_cast<int*>(smem + Layout::misc);
+  x.units = reinterpret_cast<const UnitDesc*>(smem + L::units);
+  x.bar = reinterpret_cast<uint64_t*>(smem + L::bars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc);
+  int* misc = reinterpret_cast<int*>(smem + L::misc);
   x.abort_flag = misc + 1;
   int* s_nunits = misc + 2;
 
   if (threadIdx.x == 0) {
-    uint32_t counts[Layout::nbars];
-    for (int i = 0; i < Layout::nbars; ++i) counts[i] = 1;
+    uint32_t counts[L::nbars];
+    for (int i = 0; i < L::nbars; ++i) counts[i] = 1;
     counts[kQFull] = 2;
     counts[kFinal] = 2;
     counts[kSEmpty] = counts[kSEmpty + 1] = 4;
     counts[kPFull] = counts[kPFull + 1] = 4;
     counts[kOFree] = 4;
     counts[kRFree] = 4;
-    for (int i = 0; i < Layout::nbars; ++i) mbar_init(&x.bar[i], counts[i]);
+    for (int i = 0; i < kStageSlots; ++i) counts[kStageEmpty + i] = 3;
+    counts[kConvFull] = counts[kConvFull + 1] = 3;
+    for (int i = 0; i < L::nbars; ++i) mbar_init(&x.bar[i], counts[i]);
     *x.abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    scan_units<kTileRows, kMaxUnits>(p, reinterpret_cast<UnitDesc*>(smem + Layout::units), s_nunits, lane);
-    if (lane == 0) prefetch_tensormap(&p.tmap_kv64);
+    scan_units<kTileRows, Geo<kMx>::max_units>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits, lane);
+    if (lane == 0 && !kMx) prefetch_tensormap(&p.tmap_kv64);
+  }
+  if (kMx && threadIdx.x >= 128 && threadIdx.x < 256) {
+    // e4m3 bytes of the e2m1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} times 2^-shift
+    const int i = threadIdx.x - 128, shift = i >> 3, m = i & 7;
+    const float mag = m < 4 ? 0.5f * (float)m : (float)(2 << ((m - 4) >> 1)) * ((m & 1) ? 1.5f : 1.f);
+    smem[L::lut + i] = (uint8_t)(f32x2_to_e4m3x2(ldexpf(mag, -shift), 0.f) & 0xffu);
   }
   if (warp == 1) {
     tc::alloc(tmem_slot, kTmemCols);
@@ -573,15 +847,22 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_tc_kernel(const __grid_
   x.nunits = *s_nunits;
 
   if (warp == 0) {
-    if (lane == 0) producer(p, x);
+    if (lane == 0) {
+      if constexpr (kMx)
+        producer_mx(p, x);
+      else
+        producer_e4m3(p, x);
+    }
   } else if (warp == 1) {
-    if (lane == 0) qk_issuer(p, x);
+    if (lane == 0) qk_issuer<kMx>(p, x);
   } else if (warp == 2) {
-    if (lane == 0) pv_issuer(p, x);
+    if (lane == 0) pv_issuer<kMx>(p, x);
   } else if (warp < 5) {
-    prep_query(p, x, threadIdx.x - 96);
+    prep_query<kMx>(p, x, threadIdx.x - 96);
+  } else if (warp < 9) {
+    softmax_epilogue<kMx>(p, x, warp & 3, lane);
   } else {
-    softmax_epilogue(p, x, warp & 3, lane);
+    converter_mx(p, x, warp - 9, lane);
   }
 
   if ((warp == 1 || warp == 2) && lane == 0) {
@@ -599,14 +880,16 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_tc_kernel(const __grid_
 
 }  // namespace tcfp8
 
-inline cudaError_t launch_split_tc_fp8(const Stage1Params& p, cudaStream_t stream) {
-  using L = tcfp8::Layout;
+template <bool kMx>
+inline cudaError_t launch_split_tc(const Stage1Params& p, cudaStream_t stream) {
+  using L = tcfp8::Layout<kMx>;
   static_assert(L::total <= 232448, "shared memory carve-up exceeds the 227 KB per-CTA limit");
   static_assert(L::qs % 1024 == 0 && L::pb % 1024 == 0 && L::rope % 1024 == 0, "swizzled operand alignment");
-  cudaError_t e =
-      cudaFuncSetAttribute(tcfp8::mla_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
+  static_assert(L::stage % 16 == 0, "bulk-copy destination alignment");
+  cudaError_t e = cudaFuncSetAttribute(tcfp8::mla_split_tc_kernel<kMx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       L::total);
   if (e != cudaSuccess) return e;
-  tcfp8::mla_split_tc_kernel<<<p.grid, tcfp8::kThreads, L::total, stream>>>(p);
+  tcfp8::mla_split_tc_kernel<kMx><<<p.grid, tcfp8::Geo<kMx>::threads, L::total, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -111,7 +111,7 @@ def assert_parity(got, ref, lse, ref_lse, what, vmax=None):
         assert np.max(np.abs(lse[fin] - ref_lse[fin])) <= LSE_ABS, f"{what}: lse err"
 
 
-DTYPES = ["bf16", "fp8"]
+DTYPES = ["bf16", "fp8", "mxfp4"]
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -152,7 +152,7 @@ def test_many_units_per_cta(orc, dtype, lens, num_sms, num_splits):
     dev = torch.device("cuda:0")
     dec = binding.MLADecoder(inp.kv_indptr, dtype, device=dev, num_sms=num_sms, num_splits=num_splits)
     assert dec.plan.units_per_cta >= 2
-    scale = inp.kv_scale if dtype == "fp8" else None
+    scale = {"bf16": None, "fp8": inp.kv_scale, "mxfp4": inp.block_scales}[dtype]
     runs = []
     for _ in range(2):
         out, lse = dec(inp.q.to(dev), inp.kv.to(dev), inp.kv_indptr.to(dev), inp.qo_indptr.to(dev),
@@ -200,13 +200,12 @@ def test_identical_rows_give_the_row(dtype):
     base = synth.make_inputs([1], dtype, seed=53)
     L = 777
     rows = base.kv.repeat(L, 1)
-    inp = synth.MLAInputs(dtype, base.q, base.kv_bf16, rows, base.kv_scale, None,
+    bs = None if base.block_scales is None else base.block_scales.repeat(L, 1)
+    inp = synth.MLAInputs(dtype, base.q, base.kv_bf16, rows, base.kv_scale, bs,
                           torch.tensor([0, L], dtype=torch.int32), base.qo_indptr)
     got, lse, _ = gpu_decode(inp)
-    if dtype == "bf16":
-        r = base.kv[0, :512].double().numpy()
-    else:
-        r = (base.kv.view(torch.float8_e4m3fn)[0, :512].double() * float(base.kv_scale[0])).numpy()
+    from oracle_pins import lib_dequant
+    r = lib_dequant(base)[0, :512]
     assert np.max(np.abs(got[0] - r[None, :])) <= 2e-3 * max(1.0, np.abs(r).max())
 
 
@@ -226,6 +225,17 @@ def test_benchmark_workloads_full(orc, name):
     got, lse, dec = gpu_decode(inp)
     ref, ref_lse = oracle_decode(orc, inp)
     assert_parity(got, ref, lse, ref_lse, name, v_absmax(inp))
+    assert dec.poll_error() == 0
+
+
+def test_benchmark_workload_bs32_kv8192_mxfp4_sampled(orc):
+    """The MXFP4 workload at full size in the benchmark's launch configuration;
+    the oracle checks a sample of 8 sequences (all 16 heads)."""
+    inp = synth.make_workload("bs32_kv8192_mxfp4")
+    got, lse, dec = gpu_decode(inp)
+    seqs = [0, 1, 9, 15, 16, 22, 30, 31]
+    ref, ref_lse = oracle_decode(orc, inp, seqs=seqs)
+    assert_parity(got[seqs], ref, lse[seqs], ref_lse, "bs32_kv8192_mxfp4 sampled", v_absmax(inp, seqs))
     assert dec.poll_error() == 0
 
 

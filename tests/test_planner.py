@@ -3,6 +3,8 @@ unit numbering the kernels assume (checked by brute force on the CPU)."""
 import itertools
 import random
 
+import numpy as np
+
 import pytest
 
 from mla_attention_decode_gb300 import binding
@@ -80,8 +82,18 @@ def test_random_ragged_sweep():
         b = rng.randint(1, 80)
         lens = [rng.choice([0, 1, 2, rng.randint(1, 300), rng.randint(1, 20000)]) for _ in range(b)]
         sms = rng.choice([1, 7, 148, 152])
-        check_plan(lens, rng.choice(["bf16", "fp8", "mxfp4"]), num_sms=sms,
-                   num_splits=rng.choice([0, 0, 1, 2, 5]))
+        dtype, ns = rng.choice(["bf16", "fp8", "mxfp4"]), rng.choice([0, 0, 1, 2, 5])
+        if dtype == "mxfp4":
+            # an MXFP4 CTA holds at most 64 units: layouts that need more are refused
+            tile = 128
+            need = b if ns == 0 else sum(max(1, min(ns, -(-L // tile))) if L > 0 else 1 for L in lens)
+            if need > 64 * sms:
+                with pytest.raises(binding.MLAError) as e:
+                    binding.mla_decode_plan(np.cumsum([0] + lens).astype(np.int32), dtype, num_sms=sms,
+                                            num_splits=ns)
+                assert e.value.status == binding.MLA_ERR_UNSUPPORTED
+                continue
+        check_plan(lens, dtype, num_sms=sms, num_splits=ns)
 
 
 def test_auto_plan_balances_benchmark_shapes():
