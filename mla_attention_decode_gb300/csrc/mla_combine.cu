@@ -17,41 +17,76 @@
 
 namespace mla {
 
-// One CTA per (sequence, head); 128 threads, 4 output features each.
+// One CTA per (sequence, head, quarter of the 512 features); 128 threads.
+// Every warp finds M over all of the sequence's splits (lanes stride the
+// splits); warp w then accumulates splits w, w + 4, ... for its 128 features
+// (lane: 4 features), four splits' loads in flight at a time, and the four
+// warps' sums meet in shared memory.  The latency is about two L2 round trips
+// whatever the split count.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const __grid_constant__ CombineParams p) {
+  __shared__ float4 part[4][32];
+  __shared__ float wpart[4];
   pdl_wait_primary();
-  const int b = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
+  const int b = blockIdx.x >> 6, h = (blockIdx.x >> 2) & 15, quarter = blockIdx.x & 3;
   const int first = p.ws_seq[2 * b], ns = p.ws_seq[2 * b + 1];
   if (ns <= 1) return;  // written directly by the split kernel
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* lse = p.ws_lse + (size_t)first * kHeads + h;
   float m = -INFINITY;
-  for (int s = 0; s < ns; ++s) m = fmaxf(m, lse[(size_t)s * kHeads]);
-  const int f = 4 * threadIdx.x;
+  for (int s = lane; s < ns; s += 32) m = fmaxf(m, lse[(size_t)s * kHeads]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const int f = 128 * quarter + 4 * lane;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (m != -INFINITY) {
     const float* o = p.ws_o + ((size_t)first * kHeads + h) * kVDim + f;
-    for (int s = 0; s < ns; ++s) {
-      const float l = lse[(size_t)s * kHeads];
-      if (l == -INFINITY) continue;
-      const float w = __expf(l - m);
-      const float4 v = *reinterpret_cast<const float4*>(o + (size_t)s * kHeads * kVDim);
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
-      wsum += w;
+    for (int s0 = warp; s0 < ns; s0 += 16) {
+      float l[4];
+      float4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int s = s0 + 4 * i;
+        l[i] = s < ns ? lse[(size_t)s * kHeads] : -INFINITY;
+        v[i] = s < ns ? *reinterpret_cast<const float4*>(o + (size_t)s * kHeads * kVDim) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (l[i] == -INFINITY) continue;  // an empty split
+        const float w = __expf(l[i] - m);
+        acc.x += w * v[i].x;
+        acc.y += w * v[i].y;
+        acc.z += w * v[i].z;
+        acc.w += w * v[i].w;
+        wsum += w;
+      }
     }
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  uint16_t* out = p.out + ((size_t)b * kHeads + h) * kVDim + f;
-  *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-  if (threadIdx.x == 0 && p.lse) p.lse[b * kHeads + h] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+  part[warp][lane] = acc;
+  if (lane == 0) wpart[warp] = wsum;
+  __syncthreads();
+  if (warp == 0) {
+    float4 t = part[0][lane];
+    float ws = wpart[0];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) {
+      const float4 y = part[w][lane];
+      t.x += y.x;
+      t.y += y.y;
+      t.z += y.z;
+      t.w += y.w;
+      ws += wpart[w];
+    }
+    const float inv = ws > 0.f ? 1.f / ws : 0.f;
+    uint16_t* out = p.out + ((size_t)b * kHeads + h) * kVDim + f;
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16x2(t.x * inv, t.y * inv), pack_bf16x2(t.z * inv, t.w * inv));
+    if (quarter == 0 && lane == 0 && p.lse) p.lse[b * kHeads + h] = ws > 0.f ? m + logf(ws) : -INFINITY;
+  }
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.batch * kHeads);
+  cfg.gridDim = dim3(p.batch * kHeads * 4);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
