@@ -128,8 +128,8 @@ MLA_API size_t mla_decode_workspace_bytes(const mla_plan* plan);
  *   kv         device, see the storage table above; rows [0, plan->total_kv) are read.
  *              16-byte aligned.
  *   kv_scale   device: NULL for bf16; fp32[1] for fp8 (dequant = e4m3 * kv_scale[0]);
- *              uint8 e8m0 [plan->total_kv, scale_stride] for mxfp4.
- *   scale_stride  mxfp4: bytes between scale rows, >= 18 and even; otherwise 0.
+ *              uint8 e8m0 [plan->total_kv, scale_stride] for mxfp4 (16-byte aligned).
+ *   scale_stride  mxfp4: bytes between scale rows, >= 18; otherwise 0.
  *   kv_indptr  device int32 [batch+1], equal to the host copy the plan was made from.
  *   qo_indptr  device int32 [batch+1]; only qo_indptr[b] (the query row of b) is read.
  *   out        device, bf16 [batch, 16, 512] row-major (written).  8-byte aligned.

@@ -265,7 +265,7 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   if (!aligned(kv_indptr, 4) || !aligned(qo_indptr, 4) || (lse && !aligned(lse, 4))) return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
   if (plan->kv_dtype == MLA_KV_FP8_E4M3 && (!kv_scale || !aligned(kv_scale, 4))) return MLA_ERR_INVALID_ARG;
-  if (plan->kv_dtype == MLA_KV_MXFP4 && (!kv_scale || scale_stride < MLA_MX_SCALES_PER_ROW))
+  if (plan->kv_dtype == MLA_KV_MXFP4 && (!kv_scale || !aligned(kv_scale, 16) || scale_stride < MLA_MX_SCALES_PER_ROW))
     return MLA_ERR_INVALID_ARG;
   const mla::WsLayout w = mla::ws_layout(plan->batch, plan->num_work);
   if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE_TOO_SMALL;

@@ -191,53 +191,6 @@ static __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
 }
 
 
-// ------------------------------------------------------- MXFP4 producer
-// Half tiles (64 packed rows, 18 KB) into a ring of 3 staging slots by 1-D bulk
-// copies (rows of a unit are contiguous); the rows' scale bytes are prefetched
-// into L2 for the converter warps.  A half with no rows (the second half of a
-// short tile) is signalled by a plain arrival.
-static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
-  using L = Layout<true>;
-  const uint64_t pol = policy_evict_first();  // KV rows are read once
-  const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
-  const size_t ss = (size_t)p.scale_stride;
-  int hh = 0;
-  int uses[kStageSlots] = {0, 0, 0};
-  for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
-    const UnitDesc d = x.units[k];
-    for (int t0 = d.start; t0 < d.end && !*x.abort_flag; t0 += kTileRows) {
-      for (int h = 0; h < 2; ++h, ++hh) {
-        const int sl = hh % kStageSlots, use = hh / kStageSlots;
-        if (use >= 1) wait_phase(&x.bar[kStageEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
-        if (*x.abort_flag) break;
-        const int r0 = t0 + h * kHalfRows;
-        const int rows = max(0, min(kHalfRows, d.end - r0));
-        if (rows > 0) {
-          mbar_arrive_expect_tx(&x.bar[kStageFull + sl], (uint32_t)(rows * kPackedRowBytes));
-          bulk_g2s(x.smem + L::stage + sl * kStageBytes, p.kv + (size_t)r0 * kPackedRowBytes,
-                   (uint32_t)(rows * kPackedRowBytes), &x.bar[kStageFull + sl], pol);
-          const uint8_t* a0 = sc + (size_t)r0 * ss;
-          const size_t nb = (size_t)rows * ss;
-          for (size_t o = 0; o < nb; o += 128) prefetch_l2(a0 + o);
-          prefetch_l2(a0 + nb - 1);
-        } else {
-          mbar_arrive(&x.bar[kStageFull + sl]);
-        }
-        ++uses[sl];
-      }
-    }
-  }
-  if (*x.abort_flag) {
-    // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
-    for (int i = 0; i < kStageSlots; ++i) {
-      if (uses[i] == 0) continue;
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(&x.bar[kStageFull + i], (uses[i] - 1) & 1) && global_timer_ns() - t0 < kWaitTimeoutNs) {
-      }
-    }
-  }
-}
-
 // ------------------------------------------------------- MXFP4 converters
 // Walks the CTA's half tiles in order: unit k, rows [t0 + 64 h, ...) of its
 // tile starting at t0.
@@ -265,12 +218,82 @@ struct HalfCursor {
   }
 };
 
-// The 18 scale bytes of a row (nothing for a row past the half's end).
+// ------------------------------------------------------- MXFP4 producer
+// Half tiles (64 packed rows, 18 KB) into a ring of 3 staging slots by 1-D bulk
+// copies (rows of a unit are contiguous); the rows' scale bytes are prefetched
+// into L2 for the converter warps.  A half with no rows (the second half of a
+// short tile) is signalled by a plain arrival.
+static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
+  using L = Layout<true>;
+  const uint64_t pol = policy_evict_first();  // KV rows are read once
+  const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
+  const size_t ss = (size_t)p.scale_stride;
+  int hh = 0;
+  int uses[kStageSlots] = {0, 0, 0};
+  // the scale bytes of the half kScalePrefetch ahead go to L2 (the converters
+  // read them a half ahead; this keeps those reads L2 hits)
+  constexpr int kScalePrefetch = 6;
+  HalfCursor pre;
+  // one bulk L2 prefetch per half: the 16-byte-aligned part of its scale rows
+  // that lies inside the tensor (the base is 16-byte aligned)
+  const size_t scale_end = ((size_t)p.total_kv * ss) & ~(size_t)15;
+  auto prefetch_scales = [&](int r0, int rows) {
+    if (rows <= 0) return;
+    const size_t lo = ((size_t)r0 * ss) & ~(size_t)15;
+    size_t hi = ((size_t)(r0 + rows) * ss + 15) & ~(size_t)15;
+    if (hi > scale_end) hi = scale_end;
+    if (hi > lo) bulk_prefetch_l2(sc + lo, (uint32_t)(hi - lo));
+  };
+  for (int i = 0, r0, rows; i < kScalePrefetch && pre.next(x, r0, rows); ++i) prefetch_scales(r0, rows);
+  for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
+    const UnitDesc d = x.units[k];
+    for (int t0 = d.start; t0 < d.end && !*x.abort_flag; t0 += kTileRows) {
+      for (int h = 0; h < 2; ++h, ++hh) {
+        const int sl = hh % kStageSlots, use = hh / kStageSlots;
+        if (use >= 1) wait_phase(&x.bar[kStageEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
+        if (*x.abort_flag) break;
+        const int r0 = t0 + h * kHalfRows;
+        const int rows = max(0, min(kHalfRows, d.end - r0));
+        if (rows > 0) {
+          mbar_arrive_expect_tx(&x.bar[kStageFull + sl], (uint32_t)(rows * kPackedRowBytes));
+          bulk_g2s(x.smem + L::stage + sl * kStageBytes, p.kv + (size_t)r0 * kPackedRowBytes,
+                   (uint32_t)(rows * kPackedRowBytes), &x.bar[kStageFull + sl], pol);
+        } else {
+          mbar_arrive(&x.bar[kStageFull + sl]);
+        }
+        ++uses[sl];
+        int pr0, prows;
+        if (pre.next(x, pr0, prows)) prefetch_scales(pr0, prows);
+      }
+    }
+  }
+  if (*x.abort_flag) {
+    // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
+    for (int i = 0; i < kStageSlots; ++i) {
+      if (uses[i] == 0) continue;
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(&x.bar[kStageFull + i], (uses[i] - 1) & 1) && global_timer_ns() - t0 < kWaitTimeoutNs) {
+      }
+    }
+  }
+}
+
+// The 18 scale bytes of a row as nine pairs (byte 2i in bits 0-7 of e[i], byte
+// 2i+1 in bits 8-15), by 16-bit loads when the row start is even; 127 for a row
+// past the half's end.
 __device__ __forceinline__ void load_row_scales(const uint8_t* sc, size_t ss, int grow_row, bool valid,
-                                                uint32_t (&e)[18]) {
+                                                uint32_t (&e)[9]) {
   const uint8_t* a = sc + (size_t)grow_row * ss;
+  if (!valid) {
 #pragma unroll
-  for (int i = 0; i < 18; ++i) e[i] = valid ? (uint32_t)__ldg(a + i) : 127u;
+    for (int i = 0; i < 9; ++i) e[i] = 0x7f7fu;
+  } else if ((reinterpret_cast<uintptr_t>(a) & 1) == 0) {
+#pragma unroll
+    for (int i = 0; i < 9; ++i) e[i] = __ldg(reinterpret_cast<const unsigned short*>(a) + i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 9; ++i) e[i] = (uint32_t)__ldg(a + 2 * i) | ((uint32_t)__ldg(a + 2 * i + 1) << 8);
+  }
 }
 
 // Eight e2m1 codes (one 32-bit word, element 2i in the low nibble of byte i)
@@ -280,7 +303,7 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lut_lo, uin
   // (the sign) set in the selector the byte becomes 0xFF (the msb of 0x80
   // replicated) instead of 0x80, which yields the sign bit
   const uint32_t m0 = prmt(lut_lo, lut_hi, w & 0x7777u);
-  const uint32_t s0 = prmt(0x80808080u, 0x80808080u, w & 0xFFFFu);
+  const uint32_t s0 = prmt(0x80808080u, 0x80808080u, w);  // prmt reads selector bits 0-15 only
   const uint32_t w1 = w >> 16;
   const uint32_t m1 = prmt(lut_lo, lut_hi, w1 & 0x7777u);
   const uint32_t s1 = prmt(0x80808080u, 0x80808080u, w1);
@@ -297,22 +320,25 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
   int8_t* grow = reinterpret_cast<int8_t*>(x.smem + L::grow);
   HalfCursor cur, pre;
   int r0 = 0, rows = 0, pr0 = 0, prows = 0;
-  uint32_t e_next[2][18];
-  bool have_next = pre.next(x, pr0, prows);
-  if (have_next) {
+  // scale bytes are loaded one half ahead of their use (the producer has
+  // already brought them into L2)
+  uint32_t e_next[2][9];
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int i = 0; i < 9; ++i) e_next[j][i] = 0x7f7fu;
+  if (pre.next(x, pr0, prows)) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) load_row_scales(sc, ss, pr0 + lane + 32 * j, lane + 32 * j < prows, e_next[j]);
   }
   for (int hh = 0; cur.next(x, r0, rows) && !*x.abort_flag; ++hh) {
     const int it = hh >> 1, h = hh & 1;
-    uint32_t e[2][18];
+    uint32_t e[2][9];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
-      for (int i = 0; i < 18; ++i) e[j][i] = e_next[j][i];
-    // the next half's scale bytes are loaded while this one is converted
-    have_next = pre.next(x, pr0, prows);
-    if (have_next) {
+      for (int i = 0; i < 9; ++i) e[j][i] = e_next[j][i];
+    if (pre.next(x, pr0, prows)) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) load_row_scales(sc, ss, pr0 + lane + 32 * j, lane + 32 * j < prows, e_next[j]);
     }
@@ -330,35 +356,47 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
     const int sl = hh % kStageSlots;
     wait_phase(&x.bar[kStageFull + sl], (hh / kStageSlots) & 1, x.abort_flag, p.ws_err);
     const uint8_t* stage = x.smem + L::stage + sl * kStageBytes;
+    // destinations of this warp's three chunks
+    uint8_t* dst[3];
 #pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const int c = 3 * cw + q;
+      dst[q] = c < 8 ? x.smem + L::pairs + pair_slot<true>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes
+                     : x.smem + L::rope + (it % kRopeSlots) * kChunkBytes;
+    }
+#pragma unroll 1  // one row at a time keeps the loop body small (instruction fetch)
     for (int j = 0; j < 2; ++j) {
       const int lr = lane + 32 * j;       // row within the half
       const int row = h * kHalfRows + lr;  // row within the tile
-      const bool valid = lr < rows;
-      uint32_t g = 0;
+      const bool valid = lr < rows;       // rows past the end are written as zeros
+      uint32_t g = 1;
 #pragma unroll
-      for (int i = 0; i < 18; ++i) g = max(g, e[j][i]);
-      g = max(g, 1u);
+      for (int i = 0; i < 9; ++i) g = max(g, max(e[j][i] & 0xffu, e[j][i] >> 8));
       if (cw == 0) grow[(it & 1) * 128 + row] = (int8_t)(valid ? (int)min(g, 254u) - 127 : 0);
-      const uint4* src = reinterpret_cast<const uint4*>(stage + lr * kPackedRowBytes + 96 * cw);
+      // this warp's six block scales, picked with constant indices (a runtime
+      // index would move the scale arrays to local memory)
+      uint32_t mine[3];
 #pragma unroll
-      for (int bi = 0; bi < 6; ++bi) {  // one 32-element block per 16 packed bytes
-        const int c = 3 * cw + (bi >> 1);
-        uint8_t* base = c < 8 ? x.smem + L::pairs + pair_slot<true>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes
-                              : x.smem + L::rope + (it % kRopeSlots) * kChunkBytes;
+      for (int i = 0; i < 3; ++i) mine[i] = cw == 0 ? e[j][i] : (cw == 1 ? e[j][3 + i] : e[j][6 + i]);
+      // all loads first (staging rows past the end hold stale bytes, in bounds)
+      const uint4* src = reinterpret_cast<const uint4*>(stage + lr * kPackedRowBytes + 96 * cw);
+      uint4 w[6];
+      uint2 lt[6];
+#pragma unroll
+      for (int bi = 0; bi < 6; ++bi) {
+        w[bi] = src[bi];
+        const uint32_t eb = (bi & 1) ? (mine[bi >> 1] >> 8) : (mine[bi >> 1] & 0xffu);
+        lt[bi] = lut[min(g - eb, 15u)];
+      }
+#pragma unroll
+      for (int bi = 0; bi < 6; ++bi) {
+        const uint2 a = e2m1x8_to_e4m3(w[bi].x, lt[bi].x, lt[bi].y), b = e2m1x8_to_e4m3(w[bi].y, lt[bi].x, lt[bi].y);
+        const uint2 cc = e2m1x8_to_e4m3(w[bi].z, lt[bi].x, lt[bi].y), dd = e2m1x8_to_e4m3(w[bi].w, lt[bi].x, lt[bi].y);
+        const uint4 o0 = valid ? make_uint4(a.x, a.y, b.x, b.y) : make_uint4(0, 0, 0, 0);
+        const uint4 o1 = valid ? make_uint4(cc.x, cc.y, dd.x, dd.y) : make_uint4(0, 0, 0, 0);
         const int col = 32 * (bi & 1);
-        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-        if (valid) {
-          const uint4 w = src[bi];
-          const uint32_t shift = min(g - e[j][6 * cw + bi], 15u);
-          const uint2 lt = lut[shift];
-          const uint2 a = e2m1x8_to_e4m3(w.x, lt.x, lt.y), b = e2m1x8_to_e4m3(w.y, lt.x, lt.y);
-          const uint2 cc = e2m1x8_to_e4m3(w.z, lt.x, lt.y), dd = e2m1x8_to_e4m3(w.w, lt.x, lt.y);
-          o0 = make_uint4(a.x, a.y, b.x, b.y);
-          o1 = make_uint4(cc.x, cc.y, dd.x, dd.y);
-        }
-        *reinterpret_cast<uint4*>(base + sw64_off(row, col)) = o0;
-        *reinterpret_cast<uint4*>(base + sw64_off(row, col + 16)) = o1;
+        *reinterpret_cast<uint4*>(dst[bi >> 1] + sw64_off(row, col)) = o0;
+        *reinterpret_cast<uint4*>(dst[bi >> 1] + sw64_off(row, col + 16)) = o1;
       }
     }
     __syncwarp();
