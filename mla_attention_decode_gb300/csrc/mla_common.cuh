@@ -14,6 +14,7 @@ constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s: a wait this long mea
 
 struct UnitDesc {
   int32_t b, start, end, u;  // u: work unit index; bit 31 set when the sequence has one split
+  int32_t qrow;              // qo_indptr[b]: the sequence's query row
 };
 constexpr int32_t kFinalFlag = (int32_t)0x80000000;
 
@@ -96,13 +97,15 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
   bool bad = false;
   for (int b0 = 0; b0 < p.batch; b0 += 32) {
     const int b = b0 + lane;
-    int start = 0, end = 0, sb = 0;
+    int start = 0, end = 0, sb = 0, qrow = 0;
     if (b < p.batch) {
       start = p.kv_indptr[b];
       end = p.kv_indptr[b + 1];
-      if (start < 0 || end < start || end > p.total_kv || p.qo_indptr[b] < 0) {
+      qrow = p.qo_indptr[b];
+      if (start < 0 || end < start || end > p.total_kv || qrow < 0) {
         bad = true;
         start = end = 0;
+        qrow = 0;
       }
       sb = splits_of<TILE>(end - start, p.chunk_tokens, p.max_splits);
     }
@@ -146,6 +149,7 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
       d.start = start + TILE * (int)((long long)s * tiles / sb);
       d.end = min(end, start + TILE * (int)((long long)(s + 1) * tiles / sb));
       d.u = u | (sb == 1 ? kFinalFlag : 0);
+      d.qrow = qrow;
       units[pos + k] = d;
     }
     count += __shfl_sync(0xffffffffu, nincl, 31);

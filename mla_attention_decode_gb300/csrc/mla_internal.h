@@ -80,4 +80,23 @@ cudaError_t launch_stage1_fp8(const Stage1Params& p, cudaStream_t s);
 cudaError_t launch_stage1_mxfp4(const Stage1Params& p, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s, bool pdl);
 
+// Launch with programmatic dependent launch allowed: the kernel may start while
+// the previous kernel on the stream finishes, and waits (griddepcontrol.wait)
+// before it reads memory.
+template <class Kernel>
+inline cudaError_t launch_overlapped(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                     const Stage1Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 }  // namespace mla

@@ -136,9 +136,8 @@ __device__ __forceinline__ void issue_tile(const Stage1Params& p, uint8_t* st, u
 }
 
 // One thread: the copy of a unit's query row (16 heads x 1152 B, padded rows).
-__device__ __forceinline__ void issue_q(const Stage1Params& p, uint8_t* qbuf, uint64_t* bar, int b,
+__device__ __forceinline__ void issue_q(const Stage1Params& p, uint8_t* qbuf, uint64_t* bar, int qrow,
                                         int* armed_count, uint64_t pol) {
-  const int qrow = p.qo_indptr[b];
   ++*armed_count;
   mbar_arrive_expect_tx(bar, kHeads * 1152);
   for (int h = 0; h < kHeads; ++h)
@@ -459,7 +458,7 @@ __device__ __forceinline__ void score_loop(const Stage1Params& p, const Ctx& x, 
     named_bar_sync(kBarScore, kScoreWarps * 32);
     // every score warp has read query buffer qb: it takes unit k+2's query
     if (warp == 0 && lane == 0 && k + 2 < x.nunits && !*x.abort_flag)
-      issue_q(p, smem + L::qbuf + qb * kQBufBytes, &x.qfull[qb], x.units[k + 2].b, &x.armed[T::kStages + qb],
+      issue_q(p, smem + L::qbuf + qb * kQBufBytes, &x.qfull[qb], x.units[k + 2].qrow, &x.armed[T::kStages + qb],
               pol_keep);
     const float r_mine = qs_k[hf * 16 + hd], r_part = qs_k[(1 - hf) * 16 + hd];
 
@@ -651,6 +650,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
     fence_mbar_init();
   }
   if (warp == 0) {
+    pdl_wait_primary();  // the previous kernel's writes are visible from here on
     scan_units<kTile>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits, lane);
     __syncwarp();
     if (lane == 0) {
@@ -661,7 +661,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
       const uint64_t pol_keep = policy_evict_last();
       const UnitDesc* units = reinterpret_cast<const UnitDesc*>(smem + L::units);
       for (int k = 0; k < 2 && k < nu; ++k)
-        issue_q(p, smem + L::qbuf + k * kQBufBytes, &x.qfull[k], units[k].b, &x.armed[T::kStages + k], pol_keep);
+        issue_q(p, smem + L::qbuf + k * kQBufBytes, &x.qfull[k], units[k].qrow, &x.armed[T::kStages + k], pol_keep);
       TileCursor cur;
       cur.k = 0;
       cursor_skip_empty(cur, units, nu);
@@ -672,7 +672,9 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
       }
     }
   }
+  __syncwarp();  // lane 0's prologue copies rejoin the warp before the aligned CTA barrier
   __syncthreads();
+  pdl_wait_primary();
   pdl_launch_dependents();
   x.nunits = *s_nunits;
   if (warp < kScoreWarps)
@@ -680,6 +682,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
   else
     pv_loop<KV>(p, x, warp - kScoreWarps, lane);
 
+  __syncwarp();
   __syncthreads();
   if (*x.abort_flag && threadIdx.x == 0) {
     // a wait gave up: never leave with copies in flight (bounded wait per barrier)
@@ -702,7 +705,8 @@ cudaError_t launch_split(const Stage1Params& p, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(mla_split_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
   if (e != cudaSuccess) return e;
-  mla_split_kernel<KV><<<p.grid, kCtaThreads, L::total, stream>>>(p);
+  e = launch_overlapped(mla_split_kernel<KV>, dim3(p.grid), dim3(kCtaThreads), L::total, stream, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

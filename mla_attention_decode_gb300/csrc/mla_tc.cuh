@@ -424,7 +424,7 @@ __device__ void prep_query(const Stage1Params& p, const Ctx& x, int j) {
   float* rq = reinterpret_cast<float*>(x.smem + L::rq);
   uint8_t* qs = x.smem + L::qs;
   for (int k = 0; k < x.nunits; ++k) {
-    const int qrow = p.qo_indptr[x.units[k].b];
+    const int qrow = x.units[k].qrow;
     const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)qrow * kHeads + h) * kQkDim + 144 * part) * 2);
     uint4 raw[18];
 #pragma unroll
@@ -864,6 +864,7 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     fence_mbar_init();
   }
   if (warp == 0) {
+    pdl_wait_primary();  // the previous kernel's writes are visible from here on
     scan_units<kTileRows, Geo<kMx>::max_units>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits, lane);
     if (lane == 0 && !kMx) prefetch_tensormap(&p.tmap_kv64);
   }
@@ -877,9 +878,13 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     tc::alloc(tmem_slot, kTmemCols);
     tc::relinquish();
   }
+  // __syncthreads is an aligned barrier: every warp must reach it converged
+  // (single-lane work above and below rejoins its warp first)
+  __syncwarp();
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
+  pdl_wait_primary();
   pdl_launch_dependents();
   x.tmem = *tmem_slot;
   x.nunits = *s_nunits;
@@ -910,6 +915,7 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     while (!mbar_try_wait(&x.bar[kFinal], 0) && global_timer_ns() - t0 < kWaitTimeoutNs) {
     }
   }
+  __syncwarp();  // the single-lane roles rejoin their warps before the CTA barrier
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -927,7 +933,9 @@ inline cudaError_t launch_split_tc(const Stage1Params& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(tcfp8::mla_split_tc_kernel<kMx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        L::total);
   if (e != cudaSuccess) return e;
-  tcfp8::mla_split_tc_kernel<kMx><<<p.grid, tcfp8::Geo<kMx>::threads, L::total, stream>>>(p);
+  e = launch_overlapped(tcfp8::mla_split_tc_kernel<kMx>, dim3(p.grid), dim3(tcfp8::Geo<kMx>::threads), L::total,
+                        stream, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
