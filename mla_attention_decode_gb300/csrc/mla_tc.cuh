@@ -816,16 +816,20 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
         for (int h = 0; h < 16; ++h) ob[h * kVDim] = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h])) * inv[h];
       }
     }
-    // lse of head h is written by row h (every row holds all 16 values)
+    // lse of head h is written by row h (every row holds all 16 values): pick
+    // this row's head with selects, no divergent branches
+    if (row < kHeads) {
+      float lh = l_part[0], mh = m_ref[0];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) {
-      if (row == h) {
-        const float lse = l_part[h] > 0.f ? (m_ref[h] + log2f(l_part[h])) * kLn2 : -INFINITY;
-        if (final_out) {
-          if (p.lse) p.lse[d.b * kHeads + h] = lse;
-        } else {
-          p.ws_lse[(size_t)u * kHeads + h] = lse;
-        }
+      for (int h = 1; h < 16; ++h) {
+        lh = row == h ? l_part[h] : lh;
+        mh = row == h ? m_ref[h] : mh;
+      }
+      const float lse = lh > 0.f ? (mh + fast_log2(lh)) * kLn2 : -INFINITY;
+      if (final_out) {
+        if (p.lse) p.lse[d.b * kHeads + row] = lse;
+      } else {
+        p.ws_lse[(size_t)u * kHeads + row] = lse;
       }
     }
     tc::fence_before();
