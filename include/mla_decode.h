@@ -83,7 +83,17 @@ typedef enum {
  *   [kv_indptr[b] + R floor(s T_b / S_b), kv_indptr[b] + min(L_b, R floor((s+1) T_b / S_b))),
  * so no split is empty when L_b > 0.  Work unit u (0 <= u < num_work) is split
  * s of sequence b with u = sum_{b' < b} S_b' + s; CTA c of the grid processes
- * units c, c + grid, c + 2 grid, ...  Fields are filled by mla_decode_plan and
+ * units c, c + grid, c + 2 grid, ...  (schedule 0).
+ *
+ * Schedule 1 (contiguous tile ranges) instead lays the sequences' tiles end to
+ * end, each sequence weighing w_b = max(1, T_b) tiles, T = sum_b w_b, and gives
+ * CTA c of G = grid the tiles [floor(c T / G), floor((c+1) T / G)).  A sequence
+ * is split where CTA ranges cut it: with P_b = sum_{b' < b} w_b' and
+ * cta(t) = floor(((t + 1) G - 1) / T), S_b = cta(P_b + w_b - 1) - cta(P_b) + 1,
+ * split s covers the sequence's tiles in CTA cta(P_b) + s's range, and unit
+ * u = sum_{b' < b} S_b' + s.  The planner takes whichever schedule its cost
+ * model (the busiest CTA's tiles and units, plus the combine) prefers; a forced
+ * split count always uses schedule 0.  Fields are filled by mla_decode_plan and
  * must not be edited.
  */
 typedef struct {
@@ -97,8 +107,10 @@ typedef struct {
   int32_t num_sms;        /* SM count the plan was made for */
   int32_t splits_max;     /* max_b S_b (1: no combine kernel is launched) */
   int32_t tile_tokens;    /* R: KV rows per pipeline tile (splits end on tile boundaries) */
-  int32_t units_per_cta;  /* ceil(num_work / grid) */
-  int32_t reserved[5];
+  int32_t units_per_cta;  /* the most units any CTA owns */
+  int32_t schedule;       /* 0: splits dealt round-robin (rule above); 1: contiguous tile ranges */
+  int32_t total_tiles;    /* schedule 1: T = sum_b max(1, T_b) */
+  int32_t reserved[3];
 } mla_plan;
 
 /*

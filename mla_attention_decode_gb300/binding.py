@@ -36,7 +36,7 @@ class mla_plan(ctypes.Structure):
                 ("chunk_tokens", ctypes.c_int32), ("max_splits", ctypes.c_int32), ("num_work", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("num_sms", ctypes.c_int32), ("splits_max", ctypes.c_int32),
                 ("tile_tokens", ctypes.c_int32), ("units_per_cta", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 5)]
+                ("schedule", ctypes.c_int32), ("total_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}

@@ -89,6 +89,56 @@ double plan_cost(const std::vector<int64_t>& lens, int32_t chunk, int32_t cap, i
   return mk;
 }
 
+// Schedule 1 (contiguous tile ranges, see mla_decode.h): CTA c of G owns tiles
+// [c T / G, (c+1) T / G); cta_of(t) is the CTA owning tile t.
+int64_t cta_of(int64_t t, int64_t T, int64_t G) { return ((t + 1) * G - 1) / T; }
+
+struct BalancedPlan {
+  int64_t T = 0, G = 0, work = 0;
+  int32_t smax = 0, max_units = 0;
+  double cost = -1.0;
+};
+
+// The busiest CTA's tiles plus kUnitCost per unit it owns, plus the combine
+// (same model as plan_cost).
+BalancedPlan plan_balanced(const std::vector<int64_t>& lens, int num_sms, int kv_dtype) {
+  const double kUnitCost = 0.5, kCombineFixed = 2.0;
+  const int tile = tile_rows(kv_dtype);
+  BalancedPlan bp;
+  for (int64_t L : lens) bp.T += L > 0 ? (L + tile - 1) / tile : 1;
+  if (bp.T == 0) return bp;
+  bp.G = bp.T < num_sms ? bp.T : num_sms;
+  std::vector<int32_t> units(static_cast<size_t>(bp.G) + 1, 0);  // difference array
+  int64_t P = 0, split_units = 0;
+  for (int64_t L : lens) {
+    const int64_t w = L > 0 ? (L + tile - 1) / tile : 1;
+    const int64_t cf = cta_of(P, bp.T, bp.G), cl = cta_of(P + w - 1, bp.T, bp.G);
+    const int64_t s = cl - cf + 1;
+    bp.work += s;
+    if (s > 1) split_units += s;
+    bp.smax = s > bp.smax ? static_cast<int32_t>(s) : bp.smax;
+    units[static_cast<size_t>(cf)] += 1;
+    units[static_cast<size_t>(cl) + 1] -= 1;
+    P += w;
+  }
+  double mk = 0.0;
+  int32_t run = 0;
+  for (int64_t c = 0; c < bp.G; ++c) {
+    run += units[static_cast<size_t>(c)];
+    const int64_t tiles = (c + 1) * bp.T / bp.G - c * bp.T / bp.G;
+    const double load = (double)tiles + kUnitCost * run;
+    mk = load > mk ? load : mk;
+    bp.max_units = run > bp.max_units ? run : bp.max_units;
+  }
+  if (split_units > 0) {
+    const double tile_bytes = (double)tile * rows_bytes(kv_dtype);
+    const double partial_bytes = (double)kHeads * (kVDim + 1) * 4.0;
+    mk += kCombineFixed + (double)split_units * partial_bytes / ((double)num_sms * tile_bytes);
+  }
+  bp.cost = mk;
+  return bp;
+}
+
 // cuTensorMapEncodeTiled from the driver, fetched through the runtime once.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
@@ -181,6 +231,7 @@ int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dty
 
   int32_t chunk = 1, cap = kNoCap;
   int64_t work = 0;
+  double rr_cost = -1.0;
   if (num_splits > 0) {
     chunk = 1;
     cap = num_splits;
@@ -209,10 +260,33 @@ int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dty
       }
       if (c <= tile) break;
     }
-    if (best < 0.0) return MLA_ERR_UNSUPPORTED;  // too many sequences for the unit table
     chunk = best_chunk;
     cap = kNoCap;
-    plan_cost(lens, chunk, cap, sms, kv_dtype, &work);
+    rr_cost = best;
+    if (best >= 0.0) plan_cost(lens, chunk, cap, sms, kv_dtype, &work);
+    // the contiguous schedule, when it is cheaper (or the only one that fits)
+    const BalancedPlan bp = plan_balanced(lens, sms, kv_dtype);
+    if (bp.cost >= 0.0 && bp.max_units <= mla::max_units_per_cta(kv_dtype) && bp.work <= INT32_MAX &&
+        bp.T <= INT32_MAX && (rr_cost < 0.0 || bp.cost < rr_cost - 1e-9)) {
+      mla_plan p;
+      std::memset(&p, 0, sizeof p);
+      p.batch = batch;
+      p.kv_dtype = kv_dtype;
+      p.total_kv = kv_indptr_host[batch];
+      p.chunk_tokens = tile_rows(kv_dtype);
+      p.max_splits = kNoCap;
+      p.num_work = static_cast<int32_t>(bp.work);
+      p.grid = static_cast<int32_t>(bp.G);
+      p.num_sms = sms;
+      p.splits_max = bp.smax;
+      p.tile_tokens = tile_rows(kv_dtype);
+      p.units_per_cta = bp.max_units;
+      p.schedule = 1;
+      p.total_tiles = static_cast<int32_t>(bp.T);
+      *plan = p;
+      return MLA_OK;
+    }
+    if (best < 0.0) return MLA_ERR_UNSUPPORTED;  // too many sequences for the unit table
   }
   if (work > INT32_MAX) return MLA_ERR_UNSUPPORTED;
   int32_t smax = 0;
@@ -289,6 +363,9 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   p->max_splits = plan->max_splits;
   p->num_work = plan->num_work;
   p->grid = plan->grid;
+  p->schedule = plan->schedule;
+  p->total_tiles = plan->total_tiles;
+  if (plan->schedule != 0 && (plan->schedule != 1 || plan->total_tiles < plan->grid)) return MLA_ERR_INVALID_ARG;
   if (plan->kv_dtype == MLA_KV_FP8_E4M3) {
     if (!encode_kv_map_tc(&p->tmap_kv64, kv, plan->total_kv)) return MLA_ERR_CUDA;
     std::memcpy(&p->tmap_kv16, &p->tmap_kv64, sizeof(CUtensorMap));

@@ -91,8 +91,96 @@ __device__ __forceinline__ int splits_of(int len, int chunk, int cap) {
   return max(s, 1);
 }
 
+// Schedule 1 (contiguous tile ranges): sequence b weighs w_b = max(1, T_b)
+// tiles laid end to end; CTA c owns tiles [c T / G, (c+1) T / G) and takes one
+// unit from every sequence that overlaps its range.
+template <int TILE, int MAX_UNITS>
+__device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, UnitDesc* units, int* s_nunits,
+                                                      int lane) {
+  const long long T = p.total_tiles, G = p.grid, c = blockIdx.x;
+  const long long lo = c * T / G, hi = (c + 1) * T / G;
+  auto cta_of = [&](long long t) { return ((t + 1) * G - 1) / T; };
+  long long tprefix = 0;  // tiles of the sequences before this chunk of 32
+  int uprefix = 0, count = 0;
+  bool bad = false;
+  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    const int b = b0 + lane;
+    int start = 0, end = 0, qrow = 0, w = 0;
+    if (b < p.batch) {
+      start = p.kv_indptr[b];
+      end = p.kv_indptr[b + 1];
+      qrow = p.qo_indptr[b];
+      if (start < 0 || end < start || end > p.total_kv || qrow < 0) {
+        bad = true;
+        start = end = qrow = 0;
+      }
+      w = end > start ? (end - start + TILE - 1) / TILE : 1;
+    }
+    int wincl = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wincl, o);
+      if (lane >= o) wincl += t;
+    }
+    const long long P = tprefix + wincl - w;  // first tile of sequence b
+    int sb = 0, cf = 0;
+    if (b < p.batch) {
+      if (P + w > T) {
+        bad = true;  // the device kv_indptr holds more tiles than the plan
+      } else {
+        cf = (int)cta_of(P);
+        sb = (int)(cta_of(P + w - 1) - cf + 1);
+      }
+    }
+    int sincl = sb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, sincl, o);
+      if (lane >= o) sincl += t;
+    }
+    const int ub = uprefix + sincl - sb;  // first unit of sequence b
+    if (blockIdx.x == 0 && b < p.batch) {
+      // split table for the combine kernel; never point past the plan's slots
+      const bool fits = ub + sb <= p.num_work;
+      p.ws_seq[2 * b] = fits ? ub : 0;
+      p.ws_seq[2 * b + 1] = fits ? sb : 0;
+    }
+    const bool mine = sb > 0 && c >= cf && c < cf + sb;
+    const unsigned m = __ballot_sync(0xffffffffu, mine);
+    if (mine) {
+      const int pos = count + __popc(m & ((1u << lane) - 1));
+      const int u = ub + (int)(c - cf);
+      if (pos >= MAX_UNITS || u >= p.num_work) {
+        bad = true;
+      } else {
+        const long long a = (lo > P ? lo : P) - P, e = (hi < P + w ? hi : P + w) - P;  // the sequence's tiles here
+        UnitDesc d;
+        d.b = b;
+        d.start = end > start ? start + TILE * (int)a : start;
+        d.end = end > start ? min(end, start + TILE * (int)e) : start;
+        d.u = u | (sb == 1 ? kFinalFlag : 0);
+        d.qrow = qrow;
+        units[pos] = d;
+      }
+    }
+    count += __popc(m);
+    tprefix += __shfl_sync(0xffffffffu, wincl, 31);
+    uprefix += __shfl_sync(0xffffffffu, sincl, 31);
+  }
+  if (tprefix != T || uprefix != p.num_work) bad = true;
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    if (bad) atomicCAS(p.ws_err, 0, kErrDeviceIndex);
+    *s_nunits = min(count, MAX_UNITS);
+  }
+}
+
 template <int TILE, int MAX_UNITS = kMaxUnitsPerCta>
 __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* units, int* s_nunits, int lane) {
+  if (p.schedule == 1) {
+    scan_units_contiguous<TILE, MAX_UNITS>(p, units, s_nunits, lane);
+    return;
+  }
   int prefix = 0, count = 0;
   bool bad = false;
   for (int b0 = 0; b0 < p.batch; b0 += 32) {

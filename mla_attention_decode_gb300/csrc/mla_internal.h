@@ -60,6 +60,8 @@ struct Stage1Params {
   int32_t max_splits;
   int32_t num_work;
   int32_t grid;
+  int32_t schedule;     // 0: round-robin splits, 1: contiguous tile ranges
+  int32_t total_tiles;  // schedule 1: sum of the sequences' weights in tiles
 };
 
 struct CombineParams {

@@ -524,7 +524,7 @@ __device__ __forceinline__ void score_loop(const Stage1Params& p, const Ctx& x, 
         const float lt = lsum[hd * 2] + lsum[hd * 2 + 1];
         if (pr == 0 && c == 0) {
           side[16 + hd] = lt;
-          const float lse = lt > 0.f ? (m_run + log2f(lt)) * kLn2 : -INFINITY;
+          const float lse = lt > 0.f ? (m_run + fast_log2(lt)) * kLn2 : -INFINITY;
           if (d.u & kFinalFlag) {
             if (p.lse) p.lse[d.b * kHeads + hd] = lse;
           } else {

@@ -166,6 +166,31 @@ def test_many_units_per_cta(orc, dtype, lens, num_sms, num_splits):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("lens,num_sms", [
+    ([3000, 0, 5000, 1, 0, 0, 9000, 129, 4000, 0, 7777], 7),
+    ([2500, 0, 0, 0, 12000, 300, 7000, 1], 4),
+])
+def test_contiguous_schedule(orc, dtype, lens, num_sms):
+    """Ragged batch with empty sequences under the contiguous-tile schedule:
+    sequences cut at CTA range boundaries, several units per CTA."""
+    inp = synth.make_inputs(lens, dtype, seed=67)
+    dev = torch.device("cuda:0")
+    dec = binding.MLADecoder(inp.kv_indptr, dtype, device=dev, num_sms=num_sms)
+    assert dec.plan.schedule == 1 and dec.plan.splits_max > 1 and dec.plan.units_per_cta > 1
+    scale = {"bf16": None, "fp8": inp.kv_scale, "mxfp4": inp.block_scales}[dtype]
+    out, lse = dec(inp.q.to(dev), inp.kv.to(dev), inp.kv_indptr.to(dev), inp.qo_indptr.to(dev),
+                   kv_scale=None if scale is None else scale.to(dev))
+    torch.cuda.synchronize()
+    got, got_lse = out.double().cpu().numpy(), lse.double().cpu().numpy()
+    ref, ref_lse = oracle_decode(orc, inp)
+    assert_parity(got, ref, got_lse, ref_lse, f"contiguous {dtype} {lens[:3]}", v_absmax(inp))
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert got[b].max() == 0 and got[b].min() == 0
+    assert dec.poll_error() == 0
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_one_long_sequence(orc, dtype):
     inp = synth.make_inputs([40001], dtype, seed=41)
     got, lse, _ = gpu_decode(inp)

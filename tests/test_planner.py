@@ -16,8 +16,32 @@ def n_splits(plan, L):
     return max(1, min(plan.max_splits, -(-L // plan.chunk_tokens), -(-L // plan.tile_tokens)))
 
 
+def cta_of(t, T, G):
+    return ((t + 1) * G - 1) // T
+
+
+def contiguous_units(plan, lens):
+    """Schedule 1 (mla_decode.h): per sequence its splits, each (start, end, cta)."""
+    R, G = plan.tile_tokens, plan.grid
+    w = [max(1, -(-L // R)) for L in lens]
+    T = sum(w)
+    assert plan.total_tiles == T
+    out, P, start = [], 0, 0
+    for L, wb in zip(lens, w):
+        cf, cl = cta_of(P, T, G), cta_of(P + wb - 1, T, G)
+        for c in range(cf, cl + 1):
+            lo, hi = c * T // G, (c + 1) * T // G
+            a, e = max(lo, P) - P, min(hi, P + wb) - P
+            out.append((start + R * a, min(start + L, start + R * e)) if L > 0 else (start, start))
+        P += wb
+        start += max(L, 0)
+    return out
+
+
 def units_of(plan, lens):
     """The split ranges the plan defines (the rule stated in mla_decode.h)."""
+    if plan.schedule == 1:
+        return contiguous_units(plan, lens)
     out = []
     start = 0
     for L in lens:
@@ -30,20 +54,52 @@ def units_of(plan, lens):
     return out
 
 
+def check_contiguous(plan, lens):
+    """Schedule 1: every CTA's tiles are contiguous and within one tile of T / G."""
+    R, G, T = plan.tile_tokens, plan.grid, plan.total_tiles
+    per_cta = [0] * G
+    for c in range(G):
+        n = (c + 1) * T // G - c * T // G
+        assert n in (T // G, -(-T // G))
+    P = 0
+    for L in lens:
+        wb = max(1, -(-L // R))
+        for c in range(cta_of(P, T, G), cta_of(P + wb - 1, T, G) + 1):
+            per_cta[c] += 1
+        P += wb
+    assert max(per_cta) == plan.units_per_cta
+
+
+def n_splits_of(plan, lens):
+    if plan.schedule == 0:
+        return [n_splits(plan, L) for L in lens]
+    R, G, T = plan.tile_tokens, plan.grid, plan.total_tiles
+    out, P = [], 0
+    for L in lens:
+        wb = max(1, -(-L // R))
+        out.append(cta_of(P + wb - 1, T, G) - cta_of(P, T, G) + 1)
+        P += wb
+    return out
+
+
 def check_plan(lens, dtype="fp8", num_sms=152, num_splits=0):
     ind = [0] + list(itertools.accumulate(lens))
     plan = binding.mla_decode_plan(ind, dtype, num_sms=num_sms, num_splits=num_splits)
     us = units_of(plan, lens)
     assert plan.num_work == len(us)
     assert plan.batch == len(lens) and plan.total_kv == ind[-1]
-    assert plan.grid == min(plan.num_work, num_sms)
-    assert plan.units_per_cta == -(-plan.num_work // plan.grid)
+    if plan.schedule == 0:
+        assert plan.grid == min(plan.num_work, num_sms)
+        assert plan.units_per_cta == -(-plan.num_work // plan.grid)
+    else:
+        assert num_splits == 0 and plan.grid == min(plan.total_tiles, num_sms)
+        check_contiguous(plan, lens)
+    splits = n_splits_of(plan, lens)
     # contiguous, ordered, exact cover of each sequence; no empty split of a non-empty sequence
     pos = 0
     k = 0
     smax = 0
-    for L, b0 in zip(lens, ind):
-        s = n_splits(plan, L)
+    for L, b0, s in zip(lens, ind, splits):
         smax = max(smax, s)
         assert s >= 1
         if L > 0:
