@@ -357,6 +357,7 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   p->ws_seq = reinterpret_cast<int32_t*>(ws + w.seq);
   p->ws_lse = reinterpret_cast<float*>(ws + w.lse);
   p->ws_o = reinterpret_cast<float*>(ws + w.o);
+  p->ws_q = ws + w.q;
   p->batch = plan->batch;
   p->total_kv = plan->total_kv;
   p->chunk_tokens = plan->chunk_tokens;
@@ -380,12 +381,20 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   return MLA_OK;
 }
 
+// The split stage: for e4m3 and MXFP4 KV the query preparation, then the split
+// kernel (which overlaps its set-up with the preparation).
 int launch_split_stage(const mla::Stage1Params& p, int kv_dtype, cudaStream_t s) {
   cudaError_t e;
   switch (kv_dtype) {
     case MLA_KV_BF16: e = mla::launch_stage1_bf16(p, s); break;
-    case MLA_KV_FP8_E4M3: e = mla::launch_stage1_fp8(p, s); break;
-    default: e = mla::launch_stage1_mxfp4(p, s); break;
+    case MLA_KV_FP8_E4M3:
+      e = mla::launch_prep_q(p, false, s);
+      if (e == cudaSuccess) e = mla::launch_stage1_fp8(p, s);
+      break;
+    default:
+      e = mla::launch_prep_q(p, true, s);
+      if (e == cudaSuccess) e = mla::launch_stage1_mxfp4(p, s);
+      break;
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

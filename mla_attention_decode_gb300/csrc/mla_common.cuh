@@ -59,6 +59,12 @@ __device__ __forceinline__ float quad_sum(float v) {
   return v;
 }
 
+// Byte (row, col) of a block of 64-byte rows in the tcgen05 64-byte swizzle
+// (16-byte units of a row permuted by bits 1-2 of the row; block 512-byte aligned).
+__device__ __forceinline__ uint32_t sw64_off(int row, int col) {
+  return (uint32_t)(row * 64 + ((((col >> 4) ^ (row >> 1)) & 3) << 4) + (col & 15));
+}
+
 // Two-term e4m3 encoding of four floats: hi = e4m3(x), lo = e4m3(x - hi).
 // Byte i of each word holds element i.
 __device__ __forceinline__ void two_term_e4m3(float x0, float x1, float x2, float x3, uint32_t& hi,

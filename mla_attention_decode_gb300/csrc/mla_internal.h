@@ -23,8 +23,15 @@ struct WsLayout {
   size_t seq;      // int32 [batch][2] = {first unit, split count}
   size_t lse;      // fp32 [num_work][16] partial lse (natural log)
   size_t o;        // fp32 [num_work][16][512] normalised partial outputs
+  size_t q;        // [batch] prepared queries (e4m3 and MXFP4 KV): two-term e4m3 image + 16 fp32 factors
   size_t total;
 };
+
+// A prepared query: the two-term e4m3 query exactly as the tensor cores read
+// it from shared memory (32 rows x 576 B, K-major, 64 B swizzle: 9 blocks of
+// 2048 B), followed by the 16 per-head score factors.
+constexpr size_t kQImageBytes = 9 * 32 * 64;
+constexpr size_t kQPrepBytes = kQImageBytes + 16 * sizeof(float);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -34,7 +41,8 @@ inline WsLayout ws_layout(int batch, int num_work) {
   w.seq = 256;
   w.lse = align_up(w.seq + sizeof(int32_t) * 2 * static_cast<size_t>(batch), 256);
   w.o = align_up(w.lse + sizeof(float) * kHeads * static_cast<size_t>(num_work), 256);
-  w.total = align_up(w.o + sizeof(float) * kHeads * kVDim * static_cast<size_t>(num_work), 256);
+  w.q = align_up(w.o + sizeof(float) * kHeads * kVDim * static_cast<size_t>(num_work), 1024);
+  w.total = align_up(w.q + kQPrepBytes * static_cast<size_t>(batch), 256);
   return w;
 }
 
@@ -54,6 +62,7 @@ struct Stage1Params {
   int32_t* ws_seq;
   float* ws_lse;
   float* ws_o;
+  uint8_t* ws_q;             // prepared queries [batch][kQPrepBytes] (e4m3 / MXFP4 KV)
   int32_t batch;
   int32_t total_kv;
   int32_t chunk_tokens;
@@ -80,6 +89,8 @@ constexpr int32_t kErrDeviceTimeout = 6;
 cudaError_t launch_stage1_bf16(const Stage1Params& p, cudaStream_t s);
 cudaError_t launch_stage1_fp8(const Stage1Params& p, cudaStream_t s);
 cudaError_t launch_stage1_mxfp4(const Stage1Params& p, cudaStream_t s);
+// Two-term e4m3 query of every sequence into the workspace (e4m3 / MXFP4 KV).
+cudaError_t launch_prep_q(const Stage1Params& p, bool mx, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s, bool pdl);
 
 // Launch with programmatic dependent launch allowed: the kernel may start while

@@ -8,7 +8,7 @@
 // contiguous range of KV rows; final bf16 output and lse for unsplit
 // sequences, fp32 partials and lse for split ones.
 //
-// Per 128-row tile t of a unit (one persistent CTA per SM: 9 warps for e4m3, 12 for MXFP4):
+// Per 128-row tile t of a unit (one persistent CTA per SM: 8 warps for e4m3, 11 for MXFP4):
 //   scores  S^T[128 rows x 32] = K_t[128 x 576] . [Q_hi | Q_lo]^T   (tcgen05 kind::f8f6f4,
 //           18 k32 steps; K straight from the TMA stage, K-major, 64 B swizzle;
 //           the query as two e4m3 terms x = hi + lo with a power-of-two scale
@@ -31,15 +31,15 @@
 // 8 V blocks in pairs into a ring of 11 pair slots, each released by the
 // commit after its P.V block, the rope block into a ring of 2); 1 QK issuer and
 // TMEM owner; 2 P.V issuer (two issuing threads: one thread cannot issue these
-// small MMAs as fast as the tensor pipe retires them); 3-4 query preparation
-// (two-term query per unit, loaded while the previous unit is in use); 5-8
+// small MMAs as fast as the tensor pipe retires them); 3 query loader (the
+// query image prepared by mla_prep_q_kernel, two bulk copies per unit); 4-7
 // softmax, O^T rescale and the unit epilogue (warp w reads TMEM lanes
 // [32 (w mod 4), +32)).  Hand-offs are mbarriers (TMA transaction bytes,
 // tcgen05.commit, thread arrivals).
 //
 // MXFP4 KV (kMx): rows arrive packed (288 B of e2m1 pairs, element 2i in the low
 // nibble of byte i) by 1-D bulk copies of 64-row halves into a staging ring,
-// and three converter warps (9-11) write them into the same e4m3 ring layout
+// and three converter warps (8-10) write them into the same e4m3 ring layout
 // the tensor cores read (8 pair slots: two whole tiles, so that converting
 // tile t only waits for the P.V of tile t-2).  Per row, with G = the largest of its 18 e8m0 bytes,
 // element n * 2^(e-127) becomes the e4m3 value n * 2^(e-G) (exact while the
@@ -63,7 +63,7 @@ constexpr int kPairBytes = 2 * kChunkBytes;  // two column blocks = features [12
 template <bool kMx>
 struct Geo {
   static constexpr int pair_slots = kMx ? 8 : 11;  // ring of V column-block pairs (4 per tile)
-  static constexpr int threads = kMx ? 384 : 288;
+  static constexpr int threads = kMx ? 352 : 256;
   static constexpr int max_units = kMx ? kMaxUnitsPerCtaMx : kMaxUnitsPerCta;  // work units one CTA may own
 };
 constexpr int kRopeSlots = 2;                // ring of the rope column block (features 512..575)
@@ -107,7 +107,7 @@ enum {
   kPairEmpty = 11,  // [<=11] commit after the P.V block that read it
   kRopeFull = 22,   // [2]  TMA bytes of a rope column block
   kRopeEmpty = 24,  // [2]  commit after the QK that read it
-  kQFull = 26,      // query of the next unit prepared (2 warps)
+  kQFull = 26,      // query of the next unit copied in (transaction bytes)
   kQEmpty = 27,     // commit after the unit's last QK
   kSFull = 28,      // [2]  commit after QK
   kSEmpty = 30,     // [2]  softmax read S (4 warps)
@@ -123,9 +123,6 @@ enum {
   kConvFull = 47,   // [2]  MXFP4: tile t converted into the ring (3 warps)
 };
 
-__device__ __forceinline__ uint32_t sw64_off(int row, int col) {  // byte (row, col) of a 64 B-row, 64 B-swizzled block
-  return (uint32_t)(row * 64 + ((((col >> 4) ^ (row >> 1)) & 3) << 4) + (col & 15));
-}
 
 struct Ctx {
   uint8_t* smem;
@@ -409,61 +406,36 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
   }
 }
 
-// ---------------------------------------------------------- query preparation
-// 64 threads: thread j handles head j/4, features [144 (j%4), 144 (j%4) + 144).
-// One query buffer: unit k's rows are loaded (and their scale found) first,
-// then converted to two e4m3 terms and stored once the last QK of unit k-1 has
-// completed and the softmax has taken unit k-1's score factors.
+// ---------------------------------------------------------- query loader
+// One thread: the query of unit k, prepared by mla_prep_q_kernel as the exact
+// shared-memory image (two-term e4m3, 64-byte swizzle) plus its 16 score
+// factors, comes in by two bulk copies once the last QK of unit k-1 has
+// completed and the softmax has taken unit k-1's factors.  The prepared
+// queries are the one input written by the preceding grid, so this is the one
+// thread that waits for it.
 template <bool kMx>
-__device__ void prep_query(const Stage1Params& p, const Ctx& x, int j) {
+__device__ void q_loader(const Stage1Params& p, const Ctx& x) {
   using L = Layout<kMx>;
-  const int h = j >> 2, part = j & 3;
-  // e4m3: the per-tensor scale goes into the score factor; MXFP4 scales are per row
-  const float kv_scale = kMx ? 1.f : *static_cast<const float*>(p.kv_scale);
-  const float base_factor = p.sm_scale * kLog2e * kv_scale;
-  float* rq = reinterpret_cast<float*>(x.smem + L::rq);
-  uint8_t* qs = x.smem + L::qs;
-  for (int k = 0; k < x.nunits; ++k) {
-    const int qrow = x.units[k].qrow;
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)qrow * kHeads + h) * kQkDim + 144 * part) * 2);
-    uint4 raw[18];
-#pragma unroll
-    for (int i = 0; i < 18; ++i) raw[i] = __ldg(src + i);
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 18; ++i) {
-      const float4 a = bf16x4_to_f4(make_uint2(raw[i].x, raw[i].y));
-      const float4 b = bf16x4_to_f4(make_uint2(raw[i].z, raw[i].w));
-      amax = fmaxf(amax, fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
-                               fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w)))));
-    }
-    amax = quad_max(amax);
-    // power-of-two scale with amax * scale <= 448 (e4m3 max); 1 for an all-zero head
-    float sc = 1.f;
-    if (amax > 0.f) {
-      sc = exp2f(floorf(log2f(448.f / amax)));
-      if (amax * sc > 448.f) sc *= 0.5f;
-    }
+  const uint64_t pol = policy_evict_last();  // a query serves every split of its sequence
+  pdl_wait_primary();
+  int uses = 0;
+  for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
     if (k >= 1) {
       wait_phase(&x.bar[kQEmpty], (k - 1) & 1, x.abort_flag, p.ws_err);
       wait_phase(&x.bar[kRFree], (k - 1) & 1, x.abort_flag, p.ws_err);
+      if (*x.abort_flag) break;
     }
-#pragma unroll
-    for (int i = 0; i < 18; ++i) {
-      const int f0 = 144 * part + 8 * i;  // 8 features, inside one 16-byte unit of a 64-byte chunk
-      const float4 a = bf16x4_to_f4(make_uint2(raw[i].x, raw[i].y));
-      const float4 b = bf16x4_to_f4(make_uint2(raw[i].z, raw[i].w));
-      uint32_t hi0, lo0, hi1, lo1;
-      two_term_e4m3(a.x * sc, a.y * sc, a.z * sc, a.w * sc, hi0, lo0);
-      two_term_e4m3(b.x * sc, b.y * sc, b.z * sc, b.w * sc, hi1, lo1);
-      const int chunk = f0 >> 6, col = f0 & 63;
-      *reinterpret_cast<uint2*>(qs + chunk * 2048 + sw64_off(h, col)) = make_uint2(hi0, hi1);
-      *reinterpret_cast<uint2*>(qs + chunk * 2048 + sw64_off(16 + h, col)) = make_uint2(lo0, lo1);
+    const uint8_t* src = p.ws_q + (size_t)x.units[k].b * kQPrepBytes;
+    mbar_arrive_expect_tx(&x.bar[kQFull], (uint32_t)kQPrepBytes);
+    bulk_g2s(x.smem + L::qs, src, (uint32_t)kQImageBytes, &x.bar[kQFull], pol);
+    bulk_g2s(x.smem + L::rq, src + kQImageBytes, 16 * sizeof(float), &x.bar[kQFull], pol);
+    ++uses;
+  }
+  if (*x.abort_flag && uses > 0) {
+    // never leave with a copy in flight (bounded)
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(&x.bar[kQFull], (uses - 1) & 1) && global_timer_ns() - t0 < kWaitTimeoutNs) {
     }
-    if (part == 0) rq[h] = base_factor / sc;
-    tc::fence_proxy_async();  // the tensor core reads the query through the async proxy
-    __syncwarp();
-    if ((j & 31) == 0) mbar_arrive(&x.bar[kQFull]);
   }
 }
 
@@ -855,7 +827,7 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
   if (threadIdx.x == 0) {
     uint32_t counts[L::nbars];
     for (int i = 0; i < L::nbars; ++i) counts[i] = 1;
-    counts[kQFull] = 2;
+    counts[kQFull] = 1;
     counts[kFinal] = 2;
     counts[kSEmpty] = counts[kSEmpty + 1] = 4;
     counts[kPFull] = counts[kPFull + 1] = 4;
@@ -868,7 +840,9 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     fence_mbar_init();
   }
   if (warp == 0) {
-    pdl_wait_primary();  // the previous kernel's writes are visible from here on
+    // no grid-dependency wait here: this kernel is launched only once the
+    // query-preparation grid has itself waited for all earlier work, so every
+    // input but the prepared queries is complete (the query loader waits for those)
     scan_units<kTileRows, Geo<kMx>::max_units>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits, lane);
     if (lane == 0 && !kMx) prefetch_tensormap(&p.tmap_kv64);
   }
@@ -888,7 +862,6 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  pdl_wait_primary();
   pdl_launch_dependents();
   x.tmem = *tmem_slot;
   x.nunits = *s_nunits;
@@ -904,12 +877,12 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     if (lane == 0) qk_issuer<kMx>(p, x);
   } else if (warp == 2) {
     if (lane == 0) pv_issuer<kMx>(p, x);
-  } else if (warp < 5) {
-    prep_query<kMx>(p, x, threadIdx.x - 96);
-  } else if (warp < 9) {
+  } else if (warp == 3) {
+    if (lane == 0) q_loader<kMx>(p, x);
+  } else if (warp < 8) {
     softmax_epilogue<kMx>(p, x, warp & 3, lane);
   } else {
-    converter_mx(p, x, warp - 9, lane);
+    converter_mx(p, x, warp - 8, lane);
   }
 
   if ((warp == 1 || warp == 2) && lane == 0) {
