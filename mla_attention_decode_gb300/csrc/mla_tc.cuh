@@ -669,13 +669,16 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       if (need) {
         // tile max of the rising heads: redux over the warp (order-preserving
         // integer image of the float), then over the 4 warps through smem
+        // (all 16 heads, without per-head branches: on a unit's first tile all rise)
         int* mx = reinterpret_cast<int*>(redbuf + red_par * 64);
+        int wmax[16];
 #pragma unroll
-        for (int h = 0; h < 16; ++h)
-          if ((need >> h) & 1u) {
-            const int w = __reduce_max_sync(0xffffffffu, float_order_key(sv[h]));
-            if (lane == 0) mx[ww * 16 + h] = w;
-          }
+        for (int h = 0; h < 16; ++h) wmax[h] = __reduce_max_sync(0xffffffffu, float_order_key(sv[h]));
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < 16; h += 4)
+            *reinterpret_cast<int4*>(mx + ww * 16 + h) = make_int4(wmax[h], wmax[h + 1], wmax[h + 2], wmax[h + 3]);
+        }
         if (kMx && ((need >> 16) & 1u)) {
           const int w = __reduce_max_sync(0xffffffffu, row < valid ? gsh : kGvNone);
           if (lane == 0) gred[red_par * 4 + ww] = w;
