@@ -8,7 +8,7 @@
 // contiguous range of KV rows; final bf16 output and lse for unsplit
 // sequences, fp32 partials and lse for split ones.
 //
-// Per 128-row tile t of a unit (one persistent CTA per SM: 8 warps for e4m3, 11 for MXFP4):
+// Per 128-row tile t of a unit (one persistent CTA per SM: 8 warps for e4m3, 12 for MXFP4):
 //   scores  S^T[128 rows x 32] = K_t[128 x 576] . [Q_hi | Q_lo]^T   (tcgen05 kind::f8f6f4,
 //           18 k32 steps; K straight from the TMA stage, K-major, 64 B swizzle;
 //           the query as two e4m3 terms x = hi + lo with a power-of-two scale
@@ -39,7 +39,7 @@
 //
 // MXFP4 KV (kMx): rows arrive packed (288 B of e2m1 pairs, element 2i in the low
 // nibble of byte i) by 1-D bulk copies of 64-row halves into a staging ring,
-// and three converter warps (8-10) write them into the same e4m3 ring layout
+// and four converter warps (8-11) write them into the same e4m3 ring layout
 // the tensor cores read (8 pair slots: two whole tiles, so that converting
 // tile t only waits for the P.V of tile t-2).  Per row, with G = the largest of its 18 e8m0 bytes,
 // element n * 2^(e-127) becomes the e4m3 value n * 2^(e-G) (exact while the
@@ -63,7 +63,7 @@ constexpr int kPairBytes = 2 * kChunkBytes;  // two column blocks = features [12
 template <bool kMx>
 struct Geo {
   static constexpr int pair_slots = kMx ? 8 : 11;  // ring of V column-block pairs (4 per tile)
-  static constexpr int threads = kMx ? 352 : 256;
+  static constexpr int threads = kMx ? 384 : 256;
   static constexpr int max_units = kMx ? kMaxUnitsPerCtaMx : kMaxUnitsPerCta;  // work units one CTA may own
 };
 constexpr int kRopeSlots = 2;                // ring of the rope column block (features 512..575)
@@ -119,8 +119,8 @@ enum {
   kFinal = 38,      // commits after both issuers' last operations (count 2)
   kPFree = 39,      // [2]  commit after the P.V that read P buffer t mod 2
   kStageFull = 41,  // [3]  MXFP4: bytes of a staged half tile (or the producer's arrival)
-  kStageEmpty = 44, // [3]  MXFP4: the converter warps read it (3 warps)
-  kConvFull = 47,   // [2]  MXFP4: tile t converted into the ring (3 warps)
+  kStageEmpty = 44, // [3]  MXFP4: the converter warps read it (4 warps)
+  kConvFull = 47,   // [2]  MXFP4: tile t converted into the ring (4 warps)
 };
 
 
@@ -307,38 +307,31 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lut_lo, uin
   return make_uint2(m0 | ((s0 << 1) & 0x80808080u), m1 | ((s1 << 1) & 0x80808080u));
 }
 
-// Converter warp cw (0..2) writes chunks 3 cw .. 3 cw + 2 (features
-// [192 cw, 192 cw + 192)) of rows lane and lane + 32 of every half tile.
+// Converter warp cw (0..3) converts rows [16 cw, 16 cw + 16) of every half
+// tile; lane pair (2i, 2i+1) shares row 16 cw + i, lane 2i + hp taking blocks
+// [9 hp, 9 hp + 9) (features [288 hp, 288 hp + 288)).  Four warps, one per SM
+// sub-partition: the conversion is bound by the integer pipe of each.
 static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw, int lane) {
   using L = Layout<true>;
   const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
   const size_t ss = (size_t)p.scale_stride;
   const uint2* lut = reinterpret_cast<const uint2*>(x.smem + L::lut);
   int8_t* grow = reinterpret_cast<int8_t*>(x.smem + L::grow);
+  const int lr = 16 * cw + (lane >> 1), hp = lane & 1;  // row within the half, which half of the row
   HalfCursor cur, pre;
   int r0 = 0, rows = 0, pr0 = 0, prows = 0;
-  // scale bytes are loaded one half ahead of their use (the producer has
-  // already brought them into L2)
-  uint32_t e_next[2][9];
+  // the row's scale bytes are loaded one half ahead of their use (the producer
+  // has already brought them into L2)
+  uint32_t e_next[9];
 #pragma unroll
-  for (int j = 0; j < 2; ++j)
-#pragma unroll
-    for (int i = 0; i < 9; ++i) e_next[j][i] = 0x7f7fu;
-  if (pre.next(x, pr0, prows)) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) load_row_scales(sc, ss, pr0 + lane + 32 * j, lane + 32 * j < prows, e_next[j]);
-  }
+  for (int i = 0; i < 9; ++i) e_next[i] = 0x7f7fu;
+  if (pre.next(x, pr0, prows)) load_row_scales(sc, ss, pr0 + lr, lr < prows, e_next);
   for (int hh = 0; cur.next(x, r0, rows) && !*x.abort_flag; ++hh) {
     const int it = hh >> 1, h = hh & 1;
-    uint32_t e[2][9];
+    uint32_t e[9];
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int i = 0; i < 9; ++i) e[j][i] = e_next[j][i];
-    if (pre.next(x, pr0, prows)) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) load_row_scales(sc, ss, pr0 + lane + 32 * j, lane + 32 * j < prows, e_next[j]);
-    }
+    for (int i = 0; i < 9; ++i) e[i] = e_next[i];
+    if (pre.next(x, pr0, prows)) load_row_scales(sc, ss, pr0 + lr, lr < prows, e_next);
     if (h == 0) {
       // the tile's ring slots must have been released by the MMAs that read them
 #pragma unroll
@@ -353,48 +346,37 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
     const int sl = hh % kStageSlots;
     wait_phase(&x.bar[kStageFull + sl], (hh / kStageSlots) & 1, x.abort_flag, p.ws_err);
     const uint8_t* stage = x.smem + L::stage + sl * kStageBytes;
-    // destinations of this warp's three chunks
-    uint8_t* dst[3];
+    const int row = h * kHalfRows + lr;  // row within the tile
+    const bool valid = lr < rows;       // rows past the end are written as zeros
+    uint32_t g = 1;
 #pragma unroll
-    for (int q = 0; q < 3; ++q) {
-      const int c = 3 * cw + q;
-      dst[q] = c < 8 ? x.smem + L::pairs + pair_slot<true>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes
-                     : x.smem + L::rope + (it % kRopeSlots) * kChunkBytes;
+    for (int i = 0; i < 9; ++i) g = max(g, max(e[i] & 0xffu, e[i] >> 8));
+    if (hp == 0) grow[(it & 1) * 128 + row] = (int8_t)(valid ? (int)min(g, 254u) - 127 : 0);
+    // all loads first (staging rows past the end hold stale bytes, in bounds)
+    const uint4* src = reinterpret_cast<const uint4*>(stage + lr * kPackedRowBytes + 144 * hp);
+    uint4 w[9];
+    uint2 lt[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const int bi = 9 * hp + i;  // block of the row (scale byte bi)
+      w[i] = src[i];
+      // the block's scale byte, picked with constant indices (bi is 9 hp + i)
+      const uint32_t pr = hp ? e[(9 + i) >> 1] : e[i >> 1];
+      const uint32_t eb = ((bi & 1) ? (pr >> 8) : pr) & 0xffu;
+      lt[i] = lut[min(g - eb, 15u)];
     }
-#pragma unroll 1  // one row at a time keeps the loop body small (instruction fetch)
-    for (int j = 0; j < 2; ++j) {
-      const int lr = lane + 32 * j;       // row within the half
-      const int row = h * kHalfRows + lr;  // row within the tile
-      const bool valid = lr < rows;       // rows past the end are written as zeros
-      uint32_t g = 1;
 #pragma unroll
-      for (int i = 0; i < 9; ++i) g = max(g, max(e[j][i] & 0xffu, e[j][i] >> 8));
-      if (cw == 0) grow[(it & 1) * 128 + row] = (int8_t)(valid ? (int)min(g, 254u) - 127 : 0);
-      // this warp's six block scales, picked with constant indices (a runtime
-      // index would move the scale arrays to local memory)
-      uint32_t mine[3];
-#pragma unroll
-      for (int i = 0; i < 3; ++i) mine[i] = cw == 0 ? e[j][i] : (cw == 1 ? e[j][3 + i] : e[j][6 + i]);
-      // all loads first (staging rows past the end hold stale bytes, in bounds)
-      const uint4* src = reinterpret_cast<const uint4*>(stage + lr * kPackedRowBytes + 96 * cw);
-      uint4 w[6];
-      uint2 lt[6];
-#pragma unroll
-      for (int bi = 0; bi < 6; ++bi) {
-        w[bi] = src[bi];
-        const uint32_t eb = (bi & 1) ? (mine[bi >> 1] >> 8) : (mine[bi >> 1] & 0xffu);
-        lt[bi] = lut[min(g - eb, 15u)];
-      }
-#pragma unroll
-      for (int bi = 0; bi < 6; ++bi) {
-        const uint2 a = e2m1x8_to_e4m3(w[bi].x, lt[bi].x, lt[bi].y), b = e2m1x8_to_e4m3(w[bi].y, lt[bi].x, lt[bi].y);
-        const uint2 cc = e2m1x8_to_e4m3(w[bi].z, lt[bi].x, lt[bi].y), dd = e2m1x8_to_e4m3(w[bi].w, lt[bi].x, lt[bi].y);
-        const uint4 o0 = valid ? make_uint4(a.x, a.y, b.x, b.y) : make_uint4(0, 0, 0, 0);
-        const uint4 o1 = valid ? make_uint4(cc.x, cc.y, dd.x, dd.y) : make_uint4(0, 0, 0, 0);
-        const int col = 32 * (bi & 1);
-        *reinterpret_cast<uint4*>(dst[bi >> 1] + sw64_off(row, col)) = o0;
-        *reinterpret_cast<uint4*>(dst[bi >> 1] + sw64_off(row, col + 16)) = o1;
-      }
+    for (int i = 0; i < 9; ++i) {
+      const int bi = 9 * hp + i;
+      const uint2 a = e2m1x8_to_e4m3(w[i].x, lt[i].x, lt[i].y), b2 = e2m1x8_to_e4m3(w[i].y, lt[i].x, lt[i].y);
+      const uint2 cc = e2m1x8_to_e4m3(w[i].z, lt[i].x, lt[i].y), dd = e2m1x8_to_e4m3(w[i].w, lt[i].x, lt[i].y);
+      const uint4 o0 = valid ? make_uint4(a.x, a.y, b2.x, b2.y) : make_uint4(0, 0, 0, 0);
+      const uint4 o1 = valid ? make_uint4(cc.x, cc.y, dd.x, dd.y) : make_uint4(0, 0, 0, 0);
+      const int c = bi >> 1, col = 32 * (bi & 1);
+      uint8_t* base = c < 8 ? x.smem + L::pairs + pair_slot<true>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes
+                            : x.smem + L::rope + (it % kRopeSlots) * kChunkBytes;
+      *reinterpret_cast<uint4*>(base + sw64_off(row, col)) = o0;
+      *reinterpret_cast<uint4*>(base + sw64_off(row, col + 16)) = o1;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&x.bar[kStageEmpty + sl]);
@@ -836,8 +818,8 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     counts[kPFull] = counts[kPFull + 1] = 4;
     counts[kOFree] = 4;
     counts[kRFree] = 4;
-    for (int i = 0; i < kStageSlots; ++i) counts[kStageEmpty + i] = 3;
-    counts[kConvFull] = counts[kConvFull + 1] = 3;
+    for (int i = 0; i < kStageSlots; ++i) counts[kStageEmpty + i] = 4;
+    counts[kConvFull] = counts[kConvFull + 1] = 4;
     for (int i = 0; i < L::nbars; ++i) mbar_init(&x.bar[i], counts[i]);
     *x.abort_flag = 0;
     fence_mbar_init();
