@@ -93,8 +93,8 @@ struct Layout {
   static constexpr int red = rq + 16 * 4;                     // float [2][4 warps][16]
   static constexpr int gred = red + 2 * 4 * 16 * 4;           // int [2][4] tile max of the row exponents
   static constexpr int grow = gred + 2 * 4 * 4;               // int8 [2][128] row exponent G - 127 (MXFP4)
-  static constexpr int lut = grow + (kMx ? 2 * 128 : 0);      // u8 [16][8] e2m1 magnitude -> e4m3 per shift
-  static constexpr int units = lut + (kMx ? 128 : 0);
+  static constexpr int lut = grow + (kMx ? 2 * 128 : 0);      // u8 [32][8] e2m1 magnitude -> e4m3 per shift
+  static constexpr int units = lut + (kMx ? 256 : 0);
   static constexpr int bars = units + Geo<kMx>::max_units * (int)sizeof(UnitDesc);
   static constexpr int nbars = 49;
   static constexpr int misc = bars + nbars * 8;  // tmem slot, abort flag, unit count
@@ -296,26 +296,28 @@ __device__ __forceinline__ void load_row_scales(const uint8_t* sc, size_t ss, in
 // Eight e2m1 codes (one 32-bit word, element 2i in the low nibble of byte i)
 // to eight e4m3 bytes for the shift whose magnitude table is (lo, hi).
 __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lut_lo, uint32_t lut_hi) {
-  // prmt selects byte (nibble & 7) of {lut_lo, lut_hi} per element; with bit 3
-  // (the sign) set in the selector the byte becomes 0xFF (the msb of 0x80
-  // replicated) instead of 0x80, which yields the sign bit
-  const uint32_t m0 = prmt(lut_lo, lut_hi, w & 0x7777u);
-  const uint32_t s0 = prmt(0x80808080u, 0x80808080u, w);  // prmt reads selector bits 0-15 only
-  const uint32_t w1 = w >> 16;
-  const uint32_t m1 = prmt(lut_lo, lut_hi, w1 & 0x7777u);
-  const uint32_t s1 = prmt(0x80808080u, 0x80808080u, w1);
+  // prmt picks byte (nibble & 7) of {lut_lo, lut_hi} for each element; a
+  // selector nibble with bit 3 (the e2m1 sign) set instead replicates the
+  // picked byte's msb, which from 0x80808080 gives 0xff for a negative element
+  // and 0x80 otherwise: bit 6 of that byte, moved up by one, is the e4m3 sign
+  const uint32_t wm = w & 0x77777777u, w1 = w >> 16;
+  const uint32_t m0 = prmt(lut_lo, lut_hi, wm), m1 = prmt(lut_lo, lut_hi, wm >> 16);
+  const uint32_t s0 = prmt(0x80808080u, 0x80808080u, w), s1 = prmt(0x80808080u, 0x80808080u, w1);
   return make_uint2(m0 | ((s0 << 1) & 0x80808080u), m1 | ((s1 << 1) & 0x80808080u));
 }
 
 // Converter warp cw (0..3) converts rows [16 cw, 16 cw + 16) of every half
-// tile; lane pair (2i, 2i+1) shares row 16 cw + i, lane 2i + hp taking blocks
-// [9 hp, 9 hp + 9) (features [288 hp, 288 hp + 288)).  Four warps, one per SM
+// tile; lane pair (2i, 2i+1) shares row 16 cw + i, lane 2i + hp taking the
+// row's blocks 2j + hp (j = 0..8).  Block 2j + hp holds features
+// [64 j + 32 hp, +32), columns [32 hp, 32 hp + 32) of column block j, so the
+// destination block of each is fixed at compile time.  Four warps, one per SM
 // sub-partition: the conversion is bound by the integer pipe of each.
 static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw, int lane) {
   using L = Layout<true>;
   const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
   const size_t ss = (size_t)p.scale_stride;
-  const uint2* lut = reinterpret_cast<const uint2*>(x.smem + L::lut);
+  const uint32_t lut0 = smem_u32(x.smem + L::lut), stage0 = smem_u32(x.smem + L::stage);
+  const uint32_t pairs0 = smem_u32(x.smem + L::pairs), rope0 = smem_u32(x.smem + L::rope);
   int8_t* grow = reinterpret_cast<int8_t*>(x.smem + L::grow);
   const int lr = 16 * cw + (lane >> 1), hp = lane & 1;  // row within the half, which half of the row
   HalfCursor cur, pre;
@@ -345,38 +347,33 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
     }
     const int sl = hh % kStageSlots;
     wait_phase(&x.bar[kStageFull + sl], (hh / kStageSlots) & 1, x.abort_flag, p.ws_err);
-    const uint8_t* stage = x.smem + L::stage + sl * kStageBytes;
     const int row = h * kHalfRows + lr;  // row within the tile
-    const bool valid = lr < rows;       // rows past the end are written as zeros
     uint32_t g = 1;
 #pragma unroll
     for (int i = 0; i < 9; ++i) g = max(g, max(e[i] & 0xffu, e[i] >> 8));
+    const bool valid = lr < rows;
     if (hp == 0) grow[(it & 1) * 128 + row] = (int8_t)(valid ? (int)min(g, 254u) - 127 : 0);
-    // all loads first (staging rows past the end hold stale bytes, in bounds)
-    const uint4* src = reinterpret_cast<const uint4*>(stage + lr * kPackedRowBytes + 144 * hp);
+    // a row past the end takes the all-zero table: its stale staging bytes
+    // (in bounds) become zeros of either sign
+    const uint32_t lutv = lut0 + (valid ? 0u : 128u);
+    const uint32_t src = stage0 + sl * kStageBytes + lr * kPackedRowBytes + 16 * hp;
     uint4 w[9];
     uint2 lt[9];
 #pragma unroll
-    for (int i = 0; i < 9; ++i) {
-      const int bi = 9 * hp + i;  // block of the row (scale byte bi)
-      w[i] = src[i];
-      // the block's scale byte, picked with constant indices (bi is 9 hp + i)
-      const uint32_t pr = hp ? e[(9 + i) >> 1] : e[i >> 1];
-      const uint32_t eb = ((bi & 1) ? (pr >> 8) : pr) & 0xffu;
-      lt[i] = lut[min(g - eb, 15u)];
+    for (int j = 0; j < 9; ++j) {
+      w[j] = lds128(src + 32 * j);
+      const uint32_t eb = (e[j] >> (8 * hp)) & 0xffu;  // scale byte 2j + hp
+      lt[j] = lds64(lutv + 8 * min(g - eb, 15u));
     }
+    const uint32_t off0 = sw64_off(row, 32 * hp), off1 = sw64_off(row, 32 * hp + 16);
 #pragma unroll
-    for (int i = 0; i < 9; ++i) {
-      const int bi = 9 * hp + i;
-      const uint2 a = e2m1x8_to_e4m3(w[i].x, lt[i].x, lt[i].y), b2 = e2m1x8_to_e4m3(w[i].y, lt[i].x, lt[i].y);
-      const uint2 cc = e2m1x8_to_e4m3(w[i].z, lt[i].x, lt[i].y), dd = e2m1x8_to_e4m3(w[i].w, lt[i].x, lt[i].y);
-      const uint4 o0 = valid ? make_uint4(a.x, a.y, b2.x, b2.y) : make_uint4(0, 0, 0, 0);
-      const uint4 o1 = valid ? make_uint4(cc.x, cc.y, dd.x, dd.y) : make_uint4(0, 0, 0, 0);
-      const int c = bi >> 1, col = 32 * (bi & 1);
-      uint8_t* base = c < 8 ? x.smem + L::pairs + pair_slot<true>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes
-                            : x.smem + L::rope + (it % kRopeSlots) * kChunkBytes;
-      *reinterpret_cast<uint4*>(base + sw64_off(row, col)) = o0;
-      *reinterpret_cast<uint4*>(base + sw64_off(row, col + 16)) = o1;
+    for (int j = 0; j < 9; ++j) {
+      const uint2 a = e2m1x8_to_e4m3(w[j].x, lt[j].x, lt[j].y), b = e2m1x8_to_e4m3(w[j].y, lt[j].x, lt[j].y);
+      const uint2 c = e2m1x8_to_e4m3(w[j].z, lt[j].x, lt[j].y), d = e2m1x8_to_e4m3(w[j].w, lt[j].x, lt[j].y);
+      const uint32_t base = j < 8 ? pairs0 + (uint32_t)(pair_slot<true>(it, j >> 1) * kPairBytes + (j & 1) * kChunkBytes)
+                                  : rope0 + (uint32_t)((it % kRopeSlots) * kChunkBytes);
+      sts128(base + off0, a.x, a.y, b.x, b.y);
+      sts128(base + off1, c.x, c.y, d.x, d.y);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&x.bar[kStageEmpty + sl]);
@@ -831,11 +828,12 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     scan_units<kTileRows, Geo<kMx>::max_units>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits, lane);
     if (lane == 0 && !kMx) prefetch_tensormap(&p.tmap_kv64);
   }
-  if (kMx && threadIdx.x >= 128 && threadIdx.x < 256) {
-    // e4m3 bytes of the e2m1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} times 2^-shift
+  if (kMx && threadIdx.x >= 128) {
+    // e4m3 bytes of the e2m1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} times
+    // 2^-shift for shifts 0..15, then 16 all-zero entries (rows past the end)
     const int i = threadIdx.x - 128, shift = i >> 3, m = i & 7;
     const float mag = m < 4 ? 0.5f * (float)m : (float)(2 << ((m - 4) >> 1)) * ((m & 1) ? 1.5f : 1.f);
-    smem[L::lut + i] = (uint8_t)(f32x2_to_e4m3x2(ldexpf(mag, -shift), 0.f) & 0xffu);
+    smem[L::lut + i] = shift < 16 ? (uint8_t)(f32x2_to_e4m3x2(ldexpf(mag, -shift), 0.f) & 0xffu) : (uint8_t)0;
   }
   if (warp == 1) {
     tc::alloc(tmem_slot, kTmemCols);
