@@ -140,3 +140,72 @@ def make_inputs(kv_lens, kv_dtype: str = "bf16", seed: int = 0, q_mult: float = 
 def make_workload(name: str, seed: int = 0) -> MLAInputs:
     batch, kv_len, dt = WORKLOADS[name]
     return make_inputs([kv_len] * batch, dt, seed=seed)
+
+
+@dataclasses.dataclass
+class PagedKV:
+    """A paged copy of a contiguous cache (CPU tensors).
+
+    Sequence b owns the pages ``kv_indices[page_indptr[b]:page_indptr[b+1]]`` in
+    that order; its rows are those pages' rows in order, all ``page_size`` rows
+    of each page but the last, which holds ``last_page_len[b]`` of them (the
+    layout the pages' AITER call takes: ``kv.view(num_pages, page_size, 1, 576)``
+    with ``kv_indptr`` counted in pages, ``kv_indices`` and ``kv_last_page_lens``).
+    """
+    page_size: int
+    num_pages: int
+    kv: torch.Tensor                   # num_pages * page_size rows, same row format as MLAInputs.kv
+    block_scales: torch.Tensor | None  # uint8 e8m0 [num_pages * page_size, 18] for mxfp4
+    page_indptr: torch.Tensor          # int32 [B+1], counted in pages
+    kv_indices: torch.Tensor           # int32 [page_indptr[-1]]
+    last_page_len: torch.Tensor        # int32 [B]
+
+
+# Bytes no decode may use: NaN in every format that has one (bf16 0x7fc0, e4m3
+# 0x7f, e8m0 0xff); e2m1 has no NaN, so for MXFP4 the rows' scales carry it.
+_POISON_BF16 = 0x7FC0
+_POISON_BYTE = {"fp8": 0x7F, "mxfp4": 0x77}
+_POISON_E8M0 = 0xFF
+
+
+def make_paged(inp: MLAInputs, page_size: int, seed: int = 0, spare_pages: int = 3) -> PagedKV:
+    """Scatters the rows of ``inp`` into a paged cache: each sequence's rows go,
+    ``page_size`` at a time, to pages at seeded random positions of the cache.
+    ``spare_pages`` pages that no sequence references, and the unused rows of
+    every last page, are filled with poison (NaN codes), so that a decode that
+    reads anything but the sequences' own rows gives a non-finite result."""
+    if page_size < 1:
+        raise ValueError("page_size must be >= 1")
+    ind = inp.kv_indptr.tolist()
+    b = len(ind) - 1
+    npages = [-(-(ind[i + 1] - ind[i]) // page_size) for i in range(b)]
+    used = int(sum(npages))
+    num_pages = used + int(spare_pages)
+    g = torch.Generator("cpu").manual_seed(int(seed) + 7919)
+    perm = torch.randperm(num_pages, generator=g)[:used].to(torch.int32)  # physical page of logical page j
+    rows = num_pages * page_size
+    if inp.kv_dtype == "bf16":
+        kv = torch.full((rows, QK_DIM), 0, dtype=torch.int16)
+        kv.fill_(_POISON_BF16)
+        kv = kv.view(torch.bfloat16)
+    else:
+        kv = torch.full((rows, inp.kv.shape[1]), _POISON_BYTE[inp.kv_dtype], dtype=torch.uint8)
+    bs = None
+    if inp.kv_dtype == "mxfp4":
+        bs = torch.full((rows, inp.block_scales.shape[1]), _POISON_E8M0, dtype=torch.uint8)
+    page_indptr = torch.zeros(b + 1, dtype=torch.int32)
+    last = torch.zeros(b, dtype=torch.int32)
+    j = 0
+    for i in range(b):
+        start, L = ind[i], ind[i + 1] - ind[i]
+        for k in range(npages[i]):
+            n = min(page_size, L - k * page_size)
+            dst = int(perm[j + k]) * page_size
+            kv[dst:dst + n] = inp.kv[start + k * page_size:start + k * page_size + n]
+            if bs is not None:
+                bs[dst:dst + n] = inp.block_scales[start + k * page_size:start + k * page_size + n]
+        if npages[i]:
+            last[i] = L - (npages[i] - 1) * page_size
+        j += npages[i]
+        page_indptr[i + 1] = j
+    return PagedKV(int(page_size), num_pages, kv.contiguous(), bs, page_indptr, perm.clone(), last)

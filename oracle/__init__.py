@@ -62,6 +62,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         f.restype = None
     lib.oracle_mla_decode.argtypes = [i32, P, P, P, i64, dbl, P, P, i32, dbl, P, P, i32]
     lib.oracle_mla_decode.restype = i32
+    lib.oracle_mla_decode_paged.argtypes = [i32, P, P, P, i64, dbl, P, P, P, i32, i64, P, i32, dbl, P, P, i32]
+    lib.oracle_mla_decode_paged.restype = i32
     lib.oracle_mla_partial.argtypes = [i32, P, P, P, i64, dbl, i64, i64, i64, dbl, P, P]
     lib.oracle_mla_partial.restype = i32
     lib.oracle_mla_combine.argtypes = [i32, P, P, P, P]
@@ -159,6 +161,32 @@ class Oracle:
                                         _ptr(lse), int(num_threads))
         if rc != 0:
             raise ValueError("oracle_mla_decode rejected its arguments")
+        return out, lse
+
+    def decode_paged(self, kv_dtype: int, q, kv, page_indptr, kv_indices, last_page_len, page_size: int,
+                     qo_indptr=None, kv_scale=None, block_scales=None, sm_scale: float = SM_SCALE,
+                     num_threads: int = 0):
+        """Paged cache: kv holds num_pages * page_size rows; sequence b reads the pages
+        kv_indices[page_indptr[b]:page_indptr[b+1]], the last one for last_page_len[b]
+        rows.  Returns (out [B,16,512] float64, lse [B,16] float64)."""
+        q_a = _u16(q)
+        kv_a, sc, bs, stride = self._kv_args(kv_dtype, kv, kv_scale, block_scales)
+        pin = np.ascontiguousarray(np.asarray(page_indptr, dtype=np.int32))
+        idx = np.ascontiguousarray(np.asarray(kv_indices, dtype=np.int32).reshape(-1))
+        last = np.ascontiguousarray(np.asarray(last_page_len, dtype=np.int32).reshape(-1))
+        batch = pin.size - 1
+        num_pages = kv_a.shape[0] // int(page_size)
+        qo = (np.arange(batch + 1, dtype=np.int32) if qo_indptr is None
+              else np.ascontiguousarray(np.asarray(qo_indptr, dtype=np.int32)))
+        out = np.zeros((batch, NUM_HEADS, V_DIM), dtype=np.float64)
+        lse = np.zeros((batch, NUM_HEADS), dtype=np.float64)
+        rc = self.lib.oracle_mla_decode_paged(kv_dtype, _ptr(q_a), _ptr(kv_a), _ptr(bs), stride, sc,
+                                              _ptr(pin), _ptr(idx if idx.size else None),
+                                              _ptr(last if last.size else None), int(page_size),
+                                              int(num_pages), _ptr(qo), batch, float(sm_scale),
+                                              _ptr(out), _ptr(lse), int(num_threads))
+        if rc != 0:
+            raise ValueError("oracle_mla_decode_paged rejected its arguments")
         return out, lse
 
     def partial(self, kv_dtype: int, q, kv, qrow: int, start: int, end: int, kv_scale=None,

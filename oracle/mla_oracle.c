@@ -147,11 +147,13 @@ static void dequant_row(int kv_dtype, const void* kv, const uint8_t* block_scale
   }
 }
 
-/* Attention of one query row over KV rows [start, end), one head.
- * Writes the normalised output (512 values) and the natural-log lse. */
+/* Attention of one query row over KV rows [start, end), one head -- or, when
+ * `rows` is not NULL, over the rows rows[0..end-start) in that order (a paged
+ * cache).  Writes the normalised output (512 values) and the natural-log lse. */
 static void attend_one(int kv_dtype, const double* qv, const void* kv, const uint8_t* block_scales,
                        int64_t scale_stride, double kv_scale, int64_t start, int64_t end,
-                       double sm_scale, double* o, double* lse, double* scores, double* k) {
+                       const int64_t* rows, double sm_scale, double* o, double* lse, double* scores,
+                       double* k) {
   int64_t L = end - start;
   if (L <= 0) {
     for (int j = 0; j < ORACLE_V_DIM; ++j) o[j] = 0.0;
@@ -160,7 +162,7 @@ static void attend_one(int kv_dtype, const double* qv, const void* kv, const uin
   }
   /* pass 1: scores */
   for (int64_t t = 0; t < L; ++t) {
-    dequant_row(kv_dtype, kv, block_scales, scale_stride, kv_scale, start + t, k);
+    dequant_row(kv_dtype, kv, block_scales, scale_stride, kv_scale, rows ? rows[t] : start + t, k);
     double acc = 0.0;
 #if ORACLE_MUTANT == 1
     for (int d = 0; d < 512; ++d) acc += qv[d] * k[d]; /* mistake: rope part dropped */
@@ -189,7 +191,7 @@ static void attend_one(int kv_dtype, const double* qv, const void* kv, const uin
   /* pass 2: weighted sum of V = first 512 columns of the same rows */
   for (int j = 0; j < ORACLE_V_DIM; ++j) o[j] = 0.0;
   for (int64_t t = 0; t < L; ++t) {
-    dequant_row(kv_dtype, kv, block_scales, scale_stride, kv_scale, start + t, k);
+    dequant_row(kv_dtype, kv, block_scales, scale_stride, kv_scale, rows ? rows[t] : start + t, k);
     for (int j = 0; j < ORACLE_V_DIM; ++j) {
 #if ORACLE_MUTANT == 2
       o[j] += scores[t] * k[j + 64]; /* mistake: V taken from the wrong columns */
@@ -254,10 +256,96 @@ int oracle_mla_decode(int kv_dtype, const uint16_t* q, const void* kv, const uin
       int b = (int)(pr / ORACLE_NUM_HEADS), h = (int)(pr % ORACLE_NUM_HEADS);
       widen_q(q, qo_indptr[b], h, qv);
       attend_one(kv_dtype, qv, kv, block_scales, scale_stride, kv_scale, kv_indptr[b],
-                 kv_indptr[b + 1], sm_scale, out + pr * ORACLE_V_DIM, lse + pr, scores, k);
+                 kv_indptr[b + 1], NULL, sm_scale, out + pr * ORACLE_V_DIM, lse + pr, scores, k);
     }
     free(scores);
   }
+  return 0;
+}
+
+/*
+ * Paged cache (kernelindex "amd-mixed-mla" submission 703488's AITER call and
+ * its page_size variants: kv_buffer = kv.view(num_pages, page_size, 1, 576)
+ * with kv_indptr counted in pages, kv_indices and kv_last_page_lens).  Sequence
+ * b owns the pages kv_indices[page_indptr[b] .. page_indptr[b+1]) in that order;
+ * its tokens are those pages' rows in order, all page_size rows of every page
+ * but the last, and last_page_len[b] rows of the last.  Row i of sequence b is
+ * therefore cache row kv_indices[page_indptr[b] + i / P] * P + i % P, and the
+ * attention is the definition above over those rows.  A sequence with no pages
+ * is empty.  Returns 0, or -1 on an invalid argument (including a page index
+ * outside [0, num_pages) or a last-page length outside [1, P]).
+ */
+int oracle_mla_decode_paged(int kv_dtype, const uint16_t* q, const void* kv, const uint8_t* block_scales,
+                            int64_t scale_stride, double kv_scale, const int32_t* page_indptr,
+                            const int32_t* kv_indices, const int32_t* last_page_len, int page_size,
+                            int64_t num_pages, const int32_t* qo_indptr, int batch, double sm_scale,
+                            double* out, double* lse, int num_threads) {
+  if (batch < 0 || !page_indptr || !qo_indptr || !out || !lse || page_size < 1) return -1;
+  if (kv_dtype < 0 || kv_dtype > 2) return -1;
+  if (kv_dtype == ORACLE_KV_MXFP4 && (!block_scales || scale_stride < ORACLE_QK_DIM / ORACLE_MX_BLOCK)) return -1;
+  /* the rows of every sequence, in order */
+  int64_t* first = (int64_t*)malloc(sizeof(int64_t) * (size_t)(batch + 1));
+  first[0] = 0;
+  for (int b = 0; b < batch; ++b) {
+    int64_t np = (int64_t)page_indptr[b + 1] - page_indptr[b];
+    if (np < 0 || (np > 0 && (!kv_indices || !last_page_len))) {
+      free(first);
+      return -1;
+    }
+    int64_t L = 0;
+    if (np > 0) {
+      if (last_page_len[b] < 1 || last_page_len[b] > page_size) {
+        free(first);
+        return -1;
+      }
+#if ORACLE_MUTANT == 11
+      L = np * page_size; /* mistake: the last page read in full */
+#else
+      L = (np - 1) * page_size + last_page_len[b];
+#endif
+    }
+    first[b + 1] = first[b] + L;
+  }
+  int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(first[batch] > 0 ? first[batch] : 1));
+  for (int b = 0; b < batch; ++b) {
+    for (int64_t i = 0; i < first[b + 1] - first[b]; ++i) {
+#if ORACLE_MUTANT == 12
+      int64_t page = (int64_t)page_indptr[b] + i / page_size; /* mistake: page table ignored */
+#else
+      int64_t page = kv_indices[page_indptr[b] + i / page_size];
+#endif
+      if (page < 0 || page >= num_pages) {
+        free(rows);
+        free(first);
+        return -1;
+      }
+      rows[first[b] + i] = page * page_size + i % page_size;
+    }
+  }
+  int64_t Lmax = 0;
+  for (int b = 0; b < batch; ++b)
+    if (first[b + 1] - first[b] > Lmax) Lmax = first[b + 1] - first[b];
+  int64_t pairs = (int64_t)batch * ORACLE_NUM_HEADS;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel
+#endif
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(Lmax > 0 ? Lmax : 1));
+    double qv[ORACLE_QK_DIM], k[ORACLE_QK_DIM];
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+    for (int64_t pr = 0; pr < pairs; ++pr) {
+      int b = (int)(pr / ORACLE_NUM_HEADS), h = (int)(pr % ORACLE_NUM_HEADS);
+      widen_q(q, qo_indptr[b], h, qv);
+      attend_one(kv_dtype, qv, kv, block_scales, scale_stride, kv_scale, 0, first[b + 1] - first[b],
+                 rows + first[b], sm_scale, out + pr * ORACLE_V_DIM, lse + pr, scores, k);
+    }
+    free(scores);
+  }
+  free(rows);
+  free(first);
   return 0;
 }
 
@@ -275,7 +363,7 @@ int oracle_mla_partial(int kv_dtype, const uint16_t* q, const void* kv, const ui
   double qv[ORACLE_QK_DIM], k[ORACLE_QK_DIM];
   for (int h = 0; h < ORACLE_NUM_HEADS; ++h) {
     widen_q(q, qrow, h, qv);
-    attend_one(kv_dtype, qv, kv, block_scales, scale_stride, kv_scale, start, end, sm_scale,
+    attend_one(kv_dtype, qv, kv, block_scales, scale_stride, kv_scale, start, end, NULL, sm_scale,
                o + (int64_t)h * ORACLE_V_DIM, lse + h, scores, k);
   }
   free(scores);

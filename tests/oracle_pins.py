@@ -292,11 +292,30 @@ def pin_qo_indptr(orc):
     _close(lse_b, lse_a, 1e-14, "qo_indptr row selection lse")
 
 
+def pin_paged_cache(orc):
+    """A paged cache (submission 703488's kv.view(num_pages, page_size, 1, 576) with
+    page-counted kv_indptr, kv_indices and kv_last_page_lens) holds the same rows as
+    the contiguous cache it was scattered from, so the paged decode must equal the
+    contiguous decode exactly -- with the pages in a random order, partial last
+    pages, an empty sequence, and poison (NaN) in every row no sequence owns."""
+    for dt in ("bf16", "fp8", "mxfp4"):
+        inp = synth.make_inputs([130, 0, 64, 5, 200], dt, seed=41)
+        ref_out, ref_lse = run(orc, inp)
+        for page_size in (1, 3, 64):
+            pg = synth.make_paged(inp, page_size, seed=page_size)
+            out, lse = orc.decode_paged(KV_CODES[dt], inp.q, pg.kv, pg.page_indptr, pg.kv_indices,
+                                        pg.last_page_len, page_size, inp.qo_indptr,
+                                        kv_scale=None if inp.kv_scale is None else inp.kv_scale.numpy(),
+                                        block_scales=None if pg.block_scales is None else pg.block_scales.numpy())
+            assert np.array_equal(out, ref_out), f"paged {dt} P={page_size}: output differs"
+            assert np.array_equal(lse, ref_lse), f"paged {dt} P={page_size}: lse differs"
+
+
 ALL_PINS = [
     pin_e4m3_all_codes, pin_e2m1_table, pin_e8m0_closed_form, pin_bf16_widen, pin_constants,
     pin_sdpa_bf16, pin_sdpa_fp8, pin_sdpa_mxfp4, pin_identical_rows, pin_single_row,
     pin_zero_query, pin_permutation_and_isolation, pin_large_logits, pin_split_combine,
-    pin_empty_sequence, pin_qo_indptr,
+    pin_empty_sequence, pin_qo_indptr, pin_paged_cache,
 ]
 
 # Planted mistakes compiled into oracle variants (see mla_oracle.c, ORACLE_MUTANT).
@@ -311,4 +330,6 @@ MUTANTS = {
     8: "lse in log2",
     9: "every head reads query head 0",
     10: "e4m3 subnormals decoded as normals",
+    11: "paged cache: the last page read in full",
+    12: "paged cache: the page table ignored",
 }
