@@ -110,7 +110,9 @@ typedef struct {
   int32_t units_per_cta;  /* the most units any CTA owns */
   int32_t schedule;       /* 0: splits dealt round-robin (rule above); 1: contiguous tile ranges */
   int32_t total_tiles;    /* schedule 1: T = sum_b max(1, T_b) */
-  int32_t reserved[3];
+  int32_t page_size;      /* 0: contiguous cache (mla_decode_plan); P >= 64: paged (mla_decode_plan_paged) */
+  int32_t num_pages;      /* paged: pages in the cache tensor; 0 otherwise */
+  int32_t reserved[1];
 } mla_plan;
 
 /*
@@ -183,6 +185,54 @@ MLA_API int mla_decode_combine(void* out, float* lse, const mla_plan* plan, void
  * Returns MLA_OK when the word was clear.  For tests and debugging.
  */
 MLA_API int mla_decode_poll_error(void* workspace, void* stream);
+
+/*
+ * Paged KV cache (kernelindex "amd-mixed-mla" submission 703488: AITER's
+ * mla_decode_fwd over kv_buffer = kv.view(num_pages, page_size, 1, 576) with
+ * kv_indptr counted in pages, kv_indices and kv_last_page_lens).  The cache is
+ * num_pages * page_size rows in the storage format of the dtype (scales: one
+ * row of scale_stride bytes per cache row for MXFP4).  Sequence b owns the
+ * pages kv_indices[kv_page_indptr[b] .. kv_page_indptr[b+1]) in that order;
+ * its tokens are those pages' rows in order: page_size rows of every page but
+ * the last, kv_last_page_len[b] (1..page_size) rows of the last.  A sequence
+ * with no pages is empty (out = 0, lse = -inf).
+ *
+ * page_size must be a power of two >= 64 (one page holds whole 64-row boxes of
+ * the tensor-memory copies; smaller pages with a non-identity table are not
+ * supported: MLA_ERR_UNSUPPORTED).  The plan's splits and rule are those of
+ * mla_decode_plan with start_b = kv_page_indptr[b] * page_size (a position in
+ * the sequences' page-ordered row space) and L_b the token count above;
+ * total_kv is kv_page_indptr[batch] * page_size.  Both that and
+ * num_pages * page_size must fit in int32.
+ *
+ * mla_decode_plan_paged -- host only; kv_page_indptr_host[0..batch] and
+ * kv_last_page_len_host[0..batch-1] are the host copies of the device arrays
+ * passed to mla_decode_fwd_paged.  Returns MLA_OK, MLA_ERR_INVALID_ARG (a bad
+ * layout) or MLA_ERR_UNSUPPORTED (page size, or a layout the unit table cannot
+ * hold).  Never calls CUDA when num_sms > 0.
+ */
+MLA_API int mla_decode_plan_paged(const int32_t* kv_page_indptr_host, const int32_t* kv_last_page_len_host,
+                                  int32_t batch, int32_t page_size, int32_t num_pages, int32_t kv_dtype,
+                                  int32_t num_sms, int32_t num_splits, mla_plan* plan);
+
+/*
+ * mla_decode_fwd_paged -- mla_decode_fwd over a paged cache; the plan must come
+ * from mla_decode_plan_paged.  Arguments as for mla_decode_fwd, except
+ *   kv_pages          device, the cache: num_pages * page_size rows, 16-byte aligned.
+ *   kv_scale          fp8: fp32[1]; mxfp4: uint8 e8m0 [num_pages * page_size, scale_stride].
+ *   kv_page_indptr    device int32 [batch+1], equal to the host copy the plan was made from.
+ *   kv_indices        device int32 [kv_page_indptr[batch]], each in [0, num_pages).
+ *   kv_last_page_len  device int32 [batch].
+ * A page index outside [0, num_pages) or layouts that disagree with the plan are
+ * reported by mla_decode_poll_error (MLA_ERR_DEVICE_INDEX); the affected rows
+ * read page 0 instead.  Only the rows of the sequences' pages are used: other
+ * pages, and the rows of a last page past kv_last_page_len, may hold anything.
+ */
+MLA_API int mla_decode_fwd_paged(const void* q, const void* kv_pages, const void* kv_scale, int32_t scale_stride,
+                                 const int32_t* kv_page_indptr, const int32_t* kv_indices,
+                                 const int32_t* kv_last_page_len, const int32_t* qo_indptr, void* out, float* lse,
+                                 float sm_scale, const mla_plan* plan, void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 /*
  * mla_decode_fwd_static -- mla_decode_fwd for callers that cannot allocate

@@ -36,7 +36,8 @@ class mla_plan(ctypes.Structure):
                 ("chunk_tokens", ctypes.c_int32), ("max_splits", ctypes.c_int32), ("num_work", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("num_sms", ctypes.c_int32), ("splits_max", ctypes.c_int32),
                 ("tile_tokens", ctypes.c_int32), ("units_per_cta", ctypes.c_int32),
-                ("schedule", ctypes.c_int32), ("total_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("schedule", ctypes.c_int32), ("total_tiles", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
@@ -64,6 +65,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.mla_decode_fwd.argtypes = [P, P, P, i32, P, P, P, P, ctypes.c_float, ctypes.POINTER(mla_plan), P,
                                        ctypes.c_size_t, P]
         lib.mla_decode_fwd.restype = ctypes.c_int
+        lib.mla_decode_plan_paged.argtypes = [P, P, i32, i32, i32, i32, i32, i32, ctypes.POINTER(mla_plan)]
+        lib.mla_decode_plan_paged.restype = ctypes.c_int
+        lib.mla_decode_fwd_paged.argtypes = [P, P, P, i32, P, P, P, P, P, P, ctypes.c_float,
+                                             ctypes.POINTER(mla_plan), P, ctypes.c_size_t, P]
+        lib.mla_decode_fwd_paged.restype = ctypes.c_int
         lib.mla_decode_split.argtypes = list(lib.mla_decode_fwd.argtypes)
         lib.mla_decode_split.restype = ctypes.c_int
         lib.mla_decode_combine.argtypes = [P, P, ctypes.POINTER(mla_plan), P, ctypes.c_size_t, P]
@@ -101,6 +107,22 @@ def mla_decode_plan(kv_indptr_host, kv_dtype, num_sms: int = 0, num_splits: int 
     return plan
 
 
+def mla_decode_plan_paged(kv_page_indptr_host, kv_last_page_len_host, page_size: int, num_pages: int, kv_dtype,
+                          num_sms: int = 0, num_splits: int = 0) -> mla_plan:
+    """Host planner for a paged cache (see mla_decode.h): page-counted indptr
+    [batch+1] and last-page lengths [batch] as CPU int32 data."""
+    ind = torch.as_tensor(kv_page_indptr_host, dtype=torch.int32, device="cpu").contiguous()
+    last = torch.as_tensor(kv_last_page_len_host, dtype=torch.int32, device="cpu").contiguous()
+    plan = mla_plan()
+    rc = load_library().mla_decode_plan_paged(ctypes.c_void_p(ind.data_ptr()), ctypes.c_void_p(last.data_ptr()),
+                                              int(ind.numel() - 1), int(page_size), int(num_pages),
+                                              _dtype_code(kv_dtype), int(num_sms), int(num_splits),
+                                              ctypes.byref(plan))
+    if rc != MLA_OK:
+        raise MLAError(rc, "mla_decode_plan_paged")
+    return plan
+
+
 def mla_decode_workspace_bytes(plan: mla_plan) -> int:
     return int(load_library().mla_decode_workspace_bytes(ctypes.byref(plan)))
 
@@ -122,6 +144,20 @@ def mla_decode_fwd(q, kv, kv_scale, kv_indptr, qo_indptr, out, lse, plan: mla_pl
                                        _ptr(workspace), int(workspace.numel() * workspace.element_size()), handle)
     if rc != MLA_OK:
         raise MLAError(rc, "mla_decode_fwd")
+
+
+def mla_decode_fwd_paged(q, kv_pages, kv_scale, kv_page_indptr, kv_indices, kv_last_page_len, qo_indptr, out, lse,
+                         plan: mla_plan, workspace, sm_scale: float = SM_SCALE, scale_stride: int = 0,
+                         stream=None) -> None:
+    """One decode over a paged cache (plan from mla_decode_plan_paged)."""
+    rc = load_library().mla_decode_fwd_paged(_ptr(q), _ptr(kv_pages), _ptr(kv_scale), int(scale_stride),
+                                             _ptr(kv_page_indptr), _ptr(kv_indices), _ptr(kv_last_page_len),
+                                             _ptr(qo_indptr), _ptr(out), _ptr(lse), float(sm_scale),
+                                             ctypes.byref(plan), _ptr(workspace),
+                                             int(workspace.numel() * workspace.element_size()),
+                                             _stream_handle(stream, q.device))
+    if rc != MLA_OK:
+        raise MLAError(rc, "mla_decode_fwd_paged")
 
 
 def _stream_handle(stream, device) -> ctypes.c_void_p:
@@ -200,6 +236,34 @@ class MLADecoder:
         scale_stride = int(kv_scale.stride(0)) if (self.kv_dtype == MLA_KV_MXFP4 and kv_scale is not None) else 0
         mla_decode_fwd(q, kv, kv_scale, kv_indptr, qo_indptr, out, lse, self.plan, self.workspace,
                        sm_scale=sm_scale, scale_stride=scale_stride, stream=stream)
+        return out, lse
+
+    def poll_error(self, stream=None) -> int:
+        return mla_decode_poll_error(self.workspace, stream)
+
+
+class PagedMLADecoder:
+    """Plan + workspace for one paged batch layout (see mla_decode_plan_paged)."""
+
+    def __init__(self, kv_page_indptr_host, kv_last_page_len_host, page_size: int, num_pages: int, kv_dtype,
+                 device="cuda", num_sms: int = 0, num_splits: int = 0):
+        self.kv_dtype = _dtype_code(kv_dtype)
+        self.plan = mla_decode_plan_paged(kv_page_indptr_host, kv_last_page_len_host, page_size, num_pages,
+                                          self.kv_dtype, num_sms, num_splits)
+        nbytes = max(256, mla_decode_workspace_bytes(self.plan))
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, q, kv_pages, kv_page_indptr, kv_indices, kv_last_page_len, qo_indptr, kv_scale=None,
+                 out=None, lse=None, sm_scale: float = SM_SCALE, stream=None):
+        batch = self.plan.batch
+        if out is None:
+            out = torch.empty(batch, 16, 512, dtype=torch.bfloat16, device=q.device)
+        if lse is None:
+            lse = torch.empty(batch, 16, dtype=torch.float32, device=q.device)
+        scale_stride = int(kv_scale.stride(0)) if (self.kv_dtype == MLA_KV_MXFP4 and kv_scale is not None) else 0
+        mla_decode_fwd_paged(q, kv_pages, kv_scale, kv_page_indptr, kv_indices, kv_last_page_len, qo_indptr, out,
+                             lse, self.plan, self.workspace, sm_scale=sm_scale, scale_stride=scale_stride,
+                             stream=stream)
         return out, lse
 
     def poll_error(self, stream=None) -> int:

@@ -158,13 +158,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // KV rows viewed as (span bytes, 9 chunks, rows) with the matching swizzle, so a
 // box of `box_rows` rows lands densely in smem with 16-byte units permuted.
 // e4m3 KV rows as a 2-D byte tensor (576, rows); a box is one 64-byte column
-// block of 128 rows, landed with the 64-byte swizzle (the tcgen05 operand layout).
-bool encode_kv_map_tc(CUtensorMap* m, const void* kv, int32_t total_kv) {
+// block of box_rows rows, landed with the 64-byte swizzle (the tcgen05 operand layout).
+bool encode_kv_map_tc(CUtensorMap* m, const void* kv, int32_t total_kv, uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {576, (cuuint64_t)(total_kv > 0 ? total_kv : 1)};
   const cuuint64_t strides[1] = {576};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -203,25 +203,13 @@ int device_sm_count(int32_t* out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-}  // namespace
-
-extern "C" {
-
-int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dtype, int32_t num_sms,
-                    int32_t num_splits, mla_plan* plan) {
-  if (!kv_indptr_host || !plan) return MLA_ERR_INVALID_ARG;
-  if (batch < 0 || batch > MLA_MAX_BATCH) return MLA_ERR_INVALID_ARG;
-  if (kv_dtype < MLA_KV_BF16 || kv_dtype > MLA_KV_MXFP4) return MLA_ERR_UNSUPPORTED;
-  if (num_splits < 0) return MLA_ERR_INVALID_ARG;
-  if (kv_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
-  std::vector<int64_t> lens(static_cast<size_t>(batch));
+// The plan of a batch of sequences with lengths `lens` whose rows span
+// [0, total_kv) of the row space the kernels walk (see mla_decode.h).
+int plan_lengths(const std::vector<int64_t>& lens, int32_t total_kv, int32_t kv_dtype, int32_t num_sms,
+                 int32_t num_splits, mla_plan* plan) {
+  const int32_t batch = static_cast<int32_t>(lens.size());
   int64_t lmax = 0;
-  for (int32_t b = 0; b < batch; ++b) {
-    const int64_t L = (int64_t)kv_indptr_host[b + 1] - kv_indptr_host[b];
-    if (L < 0) return MLA_ERR_INVALID_ARG;
-    lens[static_cast<size_t>(b)] = L;
-    if (L > lmax) lmax = L;
-  }
+  for (int64_t L : lens) lmax = L > lmax ? L : lmax;
   int32_t sms = num_sms;
   if (sms <= 0) {
     const int rc = device_sm_count(&sms);
@@ -272,7 +260,7 @@ int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dty
       std::memset(&p, 0, sizeof p);
       p.batch = batch;
       p.kv_dtype = kv_dtype;
-      p.total_kv = kv_indptr_host[batch];
+      p.total_kv = total_kv;
       p.chunk_tokens = tile_rows(kv_dtype);
       p.max_splits = kNoCap;
       p.num_work = static_cast<int32_t>(bp.work);
@@ -298,7 +286,7 @@ int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dty
   std::memset(&p, 0, sizeof p);
   p.batch = batch;
   p.kv_dtype = kv_dtype;
-  p.total_kv = kv_indptr_host[batch];
+  p.total_kv = total_kv;
   p.chunk_tokens = chunk;
   p.max_splits = cap;
   p.num_work = static_cast<int32_t>(work);
@@ -307,6 +295,58 @@ int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dty
   p.splits_max = smax;
   p.tile_tokens = tile_rows(kv_dtype);
   p.units_per_cta = p.grid > 0 ? (p.num_work + p.grid - 1) / p.grid : 0;
+  *plan = p;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dtype, int32_t num_sms,
+                    int32_t num_splits, mla_plan* plan) {
+  if (!kv_indptr_host || !plan) return MLA_ERR_INVALID_ARG;
+  if (batch < 0 || batch > MLA_MAX_BATCH) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype < MLA_KV_BF16 || kv_dtype > MLA_KV_MXFP4) return MLA_ERR_UNSUPPORTED;
+  if (num_splits < 0) return MLA_ERR_INVALID_ARG;
+  if (kv_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
+  std::vector<int64_t> lens(static_cast<size_t>(batch));
+  for (int32_t b = 0; b < batch; ++b) {
+    const int64_t L = (int64_t)kv_indptr_host[b + 1] - kv_indptr_host[b];
+    if (L < 0) return MLA_ERR_INVALID_ARG;
+    lens[static_cast<size_t>(b)] = L;
+  }
+  return plan_lengths(lens, kv_indptr_host[batch], kv_dtype, num_sms, num_splits, plan);
+}
+
+int mla_decode_plan_paged(const int32_t* kv_page_indptr_host, const int32_t* kv_last_page_len_host, int32_t batch,
+                          int32_t page_size, int32_t num_pages, int32_t kv_dtype, int32_t num_sms,
+                          int32_t num_splits, mla_plan* plan) {
+  if (!kv_page_indptr_host || !plan || (batch > 0 && !kv_last_page_len_host)) return MLA_ERR_INVALID_ARG;
+  if (batch < 0 || batch > MLA_MAX_BATCH || num_pages < 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype < MLA_KV_BF16 || kv_dtype > MLA_KV_MXFP4) return MLA_ERR_UNSUPPORTED;
+  if (page_size < 64 || page_size > (1 << 20) || (page_size & (page_size - 1)) != 0) return MLA_ERR_UNSUPPORTED;
+  if (kv_page_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
+  if ((int64_t)kv_page_indptr_host[batch] * page_size > INT32_MAX || (int64_t)num_pages * page_size > INT32_MAX)
+    return MLA_ERR_UNSUPPORTED;
+  std::vector<int64_t> lens(static_cast<size_t>(batch));
+  for (int32_t b = 0; b < batch; ++b) {
+    const int64_t np = (int64_t)kv_page_indptr_host[b + 1] - kv_page_indptr_host[b];
+    if (np < 0) return MLA_ERR_INVALID_ARG;
+    int64_t L = 0;
+    if (np > 0) {
+      const int32_t last = kv_last_page_len_host[b];
+      if (last < 1 || last > page_size) return MLA_ERR_INVALID_ARG;
+      L = (np - 1) * page_size + last;
+    }
+    lens[static_cast<size_t>(b)] = L;
+  }
+  const int32_t total = static_cast<int32_t>((int64_t)kv_page_indptr_host[batch] * page_size);
+  mla_plan p;
+  const int rc = plan_lengths(lens, total, kv_dtype, num_sms, num_splits, &p);
+  if (rc != MLA_OK) return rc;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
   *plan = p;
   return MLA_OK;
 }
@@ -320,12 +360,33 @@ size_t mla_decode_workspace_bytes(const mla_plan* plan) {
 
 namespace {
 
+// The page table of a paged cache (null for a contiguous one).
+struct PagedArgs {
+  const int32_t* kv_indices;
+  const int32_t* kv_last_page_len;
+};
+
 // Validates the arguments of one decode and fills the split-kernel parameters.
 int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_stride, const int32_t* kv_indptr,
             const int32_t* qo_indptr, void* out, float* lse, float sm_scale, const mla_plan* plan, void* workspace,
-            size_t workspace_bytes, mla::Stage1Params* p, bool* nothing_to_do) {
+            size_t workspace_bytes, mla::Stage1Params* p, bool* nothing_to_do, const PagedArgs* paged = nullptr) {
   *nothing_to_do = false;
   if (!plan) return MLA_ERR_INVALID_ARG;
+  // a paged plan goes with the paged entry point only, and the reverse
+  if ((plan->page_size != 0) != (paged != nullptr)) return MLA_ERR_INVALID_ARG;
+  int32_t cache_rows = plan->total_kv;
+  int32_t page_shift = 0;
+  if (paged) {
+    const int32_t P = plan->page_size;
+    if (P < 64 || (P & (P - 1)) != 0 || plan->num_pages < 0 || (int64_t)plan->num_pages * P > INT32_MAX)
+      return MLA_ERR_INVALID_ARG;
+    if (plan->total_kv > 0 && plan->num_pages == 0) return MLA_ERR_INVALID_ARG;  // pages with no cache
+    if (plan->total_kv > 0 && (!paged->kv_indices || !paged->kv_last_page_len ||
+                               !aligned(paged->kv_indices, 4) || !aligned(paged->kv_last_page_len, 4)))
+      return MLA_ERR_INVALID_ARG;
+    while ((1 << page_shift) < P) ++page_shift;
+    cache_rows = plan->num_pages * P;
+  }
   if (plan->kv_dtype < MLA_KV_BF16 || plan->kv_dtype > MLA_KV_MXFP4) return MLA_ERR_UNSUPPORTED;
   if (plan->batch < 0 || plan->num_work < 0 || plan->grid < 0 || plan->chunk_tokens <= 0 || plan->max_splits <= 0)
     return MLA_ERR_INVALID_ARG;
@@ -350,6 +411,10 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   p->scale_stride = plan->kv_dtype == MLA_KV_MXFP4 ? scale_stride : 0;
   p->kv_indptr = kv_indptr;
   p->qo_indptr = qo_indptr;
+  p->kv_indices = paged ? paged->kv_indices : nullptr;
+  p->kv_last = paged ? paged->kv_last_page_len : nullptr;
+  p->page_shift = page_shift;
+  p->num_pages = paged ? plan->num_pages : 0;
   p->out = static_cast<uint16_t*>(out);
   p->lse = lse;
   p->sm_scale = sm_scale;
@@ -368,14 +433,19 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   p->total_tiles = plan->total_tiles;
   if (plan->schedule != 0 && (plan->schedule != 1 || plan->total_tiles < plan->grid)) return MLA_ERR_INVALID_ARG;
   if (plan->kv_dtype == MLA_KV_FP8_E4M3) {
-    if (!encode_kv_map_tc(&p->tmap_kv64, kv, plan->total_kv)) return MLA_ERR_CUDA;
-    std::memcpy(&p->tmap_kv16, &p->tmap_kv64, sizeof(CUtensorMap));
+    if (!encode_kv_map_tc(&p->tmap_kv64, kv, cache_rows, 128)) return MLA_ERR_CUDA;
+    if (page_shift == 6) {
+      // 64-row pages: a tile is two 64-row boxes
+      if (!encode_kv_map_tc(&p->tmap_kv16, kv, cache_rows, 64)) return MLA_ERR_CUDA;
+    } else {
+      std::memcpy(&p->tmap_kv16, &p->tmap_kv64, sizeof(CUtensorMap));
+    }
   } else if (plan->kv_dtype == MLA_KV_MXFP4) {
     // packed rows are fetched by 1-D bulk copies: no tensor map
     std::memset(&p->tmap_kv64, 0, sizeof(CUtensorMap));
     std::memset(&p->tmap_kv16, 0, sizeof(CUtensorMap));
-  } else if (!encode_kv_map(&p->tmap_kv64, kv, plan->kv_dtype, plan->total_kv, 64) ||
-             !encode_kv_map(&p->tmap_kv16, kv, plan->kv_dtype, plan->total_kv, 16)) {
+  } else if (!encode_kv_map(&p->tmap_kv64, kv, plan->kv_dtype, cache_rows, 64) ||
+             !encode_kv_map(&p->tmap_kv16, kv, plan->kv_dtype, cache_rows, 16)) {
     return MLA_ERR_CUDA;
   }
   return MLA_OK;
@@ -430,6 +500,22 @@ int mla_decode_fwd(const void* q, const void* kv, const void* kv_scale, int32_t 
   bool noop = false;
   int rc = prepare(q, kv, kv_scale, scale_stride, kv_indptr, qo_indptr, out, lse, sm_scale, plan, workspace,
                    workspace_bytes, &p, &noop);
+  if (rc != MLA_OK || noop) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = launch_split_stage(p, plan->kv_dtype, s);
+  if (rc != MLA_OK) return rc;
+  return launch_combine_stage(p, plan, s);
+}
+
+int mla_decode_fwd_paged(const void* q, const void* kv_pages, const void* kv_scale, int32_t scale_stride,
+                         const int32_t* kv_page_indptr, const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                         const int32_t* qo_indptr, void* out, float* lse, float sm_scale, const mla_plan* plan,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  mla::Stage1Params p;
+  bool noop = false;
+  const PagedArgs paged{kv_indices, kv_last_page_len};
+  int rc = prepare(q, kv_pages, kv_scale, scale_stride, kv_page_indptr, qo_indptr, out, lse, sm_scale, plan,
+                   workspace, workspace_bytes, &p, &noop, &paged);
   if (rc != MLA_OK || noop) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   rc = launch_split_stage(p, plan->kv_dtype, s);

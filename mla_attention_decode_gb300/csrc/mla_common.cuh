@@ -39,6 +39,41 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
   }
 }
 
+// Rows [start, end) of sequence b in the row space the tiles walk: the cache
+// rows themselves, or for a paged cache the page-ordered positions
+// kv_indptr[b] * P + i (i below the sequence's token count: P rows per page,
+// kv_last[b] in the last one).  False for a layout the rules forbid.
+__device__ __forceinline__ bool seq_rows(const Stage1Params& p, int b, int& start, int& end) {
+  const int a = p.kv_indptr[b], z = p.kv_indptr[b + 1];
+  if (p.page_shift == 0) {
+    start = a;
+    end = z;
+    return a >= 0 && z >= a;
+  }
+  if (a < 0 || z < a || z > (p.total_kv >> p.page_shift)) return false;
+  start = a << p.page_shift;
+  end = start;
+  if (z > a) {
+    const int last = p.kv_last[b];
+    if (last < 1 || last > (1 << p.page_shift)) return false;
+    end = start + ((z - a - 1) << p.page_shift) + last;
+  }
+  return true;
+}
+
+// Cache row of row-space position v (a row of some sequence): v itself, or for
+// a paged cache row v % P of page kv_indices[v / P].  A page index outside
+// [0, num_pages) is flagged and page 0 is read instead.
+__device__ __forceinline__ int cache_row(const Stage1Params& p, int v) {
+  if (p.page_shift == 0) return v;
+  int pg = __ldg(p.kv_indices + (v >> p.page_shift));
+  if ((unsigned)pg >= (unsigned)p.num_pages) {
+    atomicCAS(p.ws_err, 0, kErrDeviceIndex);
+    pg = 0;
+  }
+  return (pg << p.page_shift) | (v & ((1 << p.page_shift) - 1));
+}
+
 // Order-preserving map of floats (no NaN) to signed integers, for integer
 // max reductions (redux.sync): non-negative floats keep their bits, negative
 // ones have the magnitude bits flipped.
@@ -113,10 +148,8 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
     const int b = b0 + lane;
     int start = 0, end = 0, qrow = 0, w = 0;
     if (b < p.batch) {
-      start = p.kv_indptr[b];
-      end = p.kv_indptr[b + 1];
       qrow = p.qo_indptr[b];
-      if (start < 0 || end < start || end > p.total_kv || qrow < 0) {
+      if (!seq_rows(p, b, start, end) || end > p.total_kv || qrow < 0) {
         bad = true;
         start = end = qrow = 0;
       }
@@ -193,10 +226,8 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
     const int b = b0 + lane;
     int start = 0, end = 0, sb = 0, qrow = 0;
     if (b < p.batch) {
-      start = p.kv_indptr[b];
-      end = p.kv_indptr[b + 1];
       qrow = p.qo_indptr[b];
-      if (start < 0 || end < start || end > p.total_kv || qrow < 0) {
+      if (!seq_rows(p, b, start, end) || end > p.total_kv || qrow < 0) {
         bad = true;
         start = end = 0;
         qrow = 0;

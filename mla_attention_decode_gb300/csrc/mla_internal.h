@@ -48,13 +48,19 @@ inline WsLayout ws_layout(int batch, int num_work) {
 
 struct Stage1Params {
   CUtensorMap tmap_kv64;     // KV rows as (span bytes, 9 chunks, rows), swizzled; 64-row box
-  CUtensorMap tmap_kv16;     // the same with a 16-row box (ragged tails)
+                             // (e4m3: 64-byte column blocks of 128 rows)
+  CUtensorMap tmap_kv16;     // the same with a 16-row box (ragged tails); e4m3 over a
+                             // 64-row paged cache: 64-byte column blocks of 64 rows
   const uint8_t* q;          // bf16 [*, 16, 576]
   const uint8_t* kv;         // row bytes depend on the dtype
   const void* kv_scale;      // fp32[1] (fp8) or e8m0 [rows, scale_stride] (mxfp4)
   int32_t scale_stride;
-  const int32_t* kv_indptr;
+  const int32_t* kv_indptr;  // rows per sequence; for a paged cache, pages per sequence
   const int32_t* qo_indptr;
+  const int32_t* kv_indices; // paged cache: the page table (else null)
+  const int32_t* kv_last;    // paged cache: rows in each sequence's last page
+  int32_t page_shift;        // paged cache: log2(page size); 0 for a contiguous cache
+  int32_t num_pages;         // paged cache: pages in the cache tensor
   uint16_t* out;             // bf16 [batch, 16, 512]
   float* lse;                // fp32 [batch, 16] or null
   float sm_scale;

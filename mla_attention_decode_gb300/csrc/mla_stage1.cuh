@@ -114,11 +114,12 @@ struct Smem {
 };
 
 // One thread: arms a stage's mbarrier and issues the tensor-map copies of the
-// tile at the cursor (a 64-row box, or 16-row boxes for a short tail).  Rows
-// past the unit's end come from the next rows of the tensor (or are zero past
-// its end); the kernel masks them.
+// tile whose first row is cache row `crow` (a 64-row box, or 16-row boxes for
+// a short tail; a paged cache keeps a tile inside one page).  Rows past the
+// unit's end come from the next rows of the tensor (or are zero past its end);
+// the kernel masks them.
 template <int KV>
-__device__ __forceinline__ void issue_tile(const Stage1Params& p, uint8_t* st, uint64_t* bar, int t0, int rows,
+__device__ __forceinline__ void issue_tile(const Stage1Params& p, uint8_t* st, uint64_t* bar, int crow, int rows,
                                            int* armed_count) {
   using T = KvTraits<KV>;
   const uint64_t pol = policy_evict_first();  // KV rows are read once
@@ -128,10 +129,10 @@ __device__ __forceinline__ void issue_tile(const Stage1Params& p, uint8_t* st, u
   ++*armed_count;
   mbar_arrive_expect_tx(bar, bytes);
   if (big) {
-    tma_load_3d(st, &p.tmap_kv64, 0, 0, t0, bar, pol);
+    tma_load_3d(st, &p.tmap_kv64, 0, 0, crow, bar, pol);
   } else {
     for (int i = 0; i < boxes16; ++i)
-      tma_load_3d(st + i * 16 * T::kRowBytes, &p.tmap_kv16, 0, 0, t0 + 16 * i, bar, pol);
+      tma_load_3d(st + i * 16 * T::kRowBytes, &p.tmap_kv16, 0, 0, crow + 16 * i, bar, pol);
   }
 }
 
@@ -578,6 +579,8 @@ __device__ __forceinline__ void pv_loop(const Stage1Params& p, const Ctx& x, int
     for (int t0 = d.start; t0 < d.end; t0 += kTile, ++it) {
       const int s = it % T::kStages;
       const int pbi = it & 1;
+      // cache row of the refill tile, looked up before this tile's work
+      const int refill_row = (lane == 0 && cur.k < x.nunits) ? cache_row(p, cur.t0) : 0;
       wait_phase(&x.pfull[pbi], (it >> 1) & 1, x.abort_flag, p.ws_err);
       wait_phase(&x.full[s], (it / T::kStages) & 1, x.abort_flag, p.ws_err);
       const uint8_t* st = smem + L::stages + s * L::kStageBytes;
@@ -603,7 +606,7 @@ __device__ __forceinline__ void pv_loop(const Stage1Params& p, const Ctx& x, int
         if (atomicAdd(&tickets[s], 1) == kPvWarps - 1) {
           tickets[s] = 0;
           if (cur.k < x.nunits && !*x.abort_flag)
-            issue_tile<KV>(p, smem + L::stages + s * L::kStageBytes, &x.full[s], cur.t0,
+            issue_tile<KV>(p, smem + L::stages + s * L::kStageBytes, &x.full[s], refill_row,
                            min(kTile, x.units[cur.k].end - cur.t0), &x.armed[s]);
         }
       }
@@ -665,11 +668,22 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
       TileCursor cur;
       cur.k = 0;
       cursor_skip_empty(cur, units, nu);
-      for (int s = 0; s < T::kStages && cur.k < nu; ++s) {
-        issue_tile<KV>(p, smem + L::stages + s * L::kStageBytes, &x.full[s], cur.t0,
-                       min(kTile, units[cur.k].end - cur.t0), &x.armed[s]);
-        cursor_next<kTile>(cur, units, nu);
+      // all the first tiles' cache rows are looked up before any is issued
+      int crow[T::kStages], rows[T::kStages];
+      int nfirst = 0;
+#pragma unroll
+      for (int s = 0; s < T::kStages; ++s) {
+        if (cur.k < nu) {
+          crow[s] = cache_row(p, cur.t0);
+          rows[s] = min(kTile, units[cur.k].end - cur.t0);
+          nfirst = s + 1;
+          cursor_next<kTile>(cur, units, nu);
+        }
       }
+#pragma unroll
+      for (int s = 0; s < T::kStages; ++s)
+        if (s < nfirst)
+          issue_tile<KV>(p, smem + L::stages + s * L::kStageBytes, &x.full[s], crow[s], rows[s], &x.armed[s]);
     }
   }
   __syncwarp();  // lane 0's prologue copies rejoin the warp before the aligned CTA barrier

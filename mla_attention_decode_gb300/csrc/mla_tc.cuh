@@ -147,33 +147,83 @@ __device__ __forceinline__ int pair_use(int t, int f) { return (4 * t + f) / Geo
 template <bool kMx>
 __device__ __forceinline__ int wrap_slot(int s) { return s >= Geo<kMx>::pair_slots ? s - Geo<kMx>::pair_slots : s; }
 
+// The CTA's tiles in order (unit by unit): each tile's first row-space
+// position and its unit's end.
+struct TileWalk {
+  int k = 0, t0 = -1;
+  __device__ bool next(const Ctx& x, int& tile0, int& end) {
+    while (k < x.nunits) {
+      const UnitDesc d = x.units[k];
+      if (t0 < 0) t0 = d.start;
+      if (t0 >= d.end) {
+        ++k;
+        t0 = -1;
+        continue;
+      }
+      tile0 = t0;
+      end = d.end;
+      t0 += kTileRows;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Cache rows of a tile: one 128-row box at r0, or (64-row pages) two 64-row
+// boxes at r0 and r1, the second only when the tile has rows there (r1 < 0).
+struct TileRows {
+  int r0, r1;
+};
+__device__ __forceinline__ TileRows tile_rows(const Stage1Params& p, int t0, int end) {
+  TileRows r;
+  r.r0 = cache_row(p, t0);
+  r.r1 = (p.page_shift == 6 && t0 + 64 < end) ? cache_row(p, t0 + 64) : -1;
+  return r;
+}
+
 static __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
   using L = Layout<false>;
   constexpr int kPairSlots = Geo<false>::pair_slots;
   const uint64_t pol = policy_evict_first();  // KV rows are read once
-  int it = 0;
+  const bool paged64 = p.page_shift == 6;
+  // one 64-byte column block of the tile (and the bytes it brings)
+  auto load_block = [&](uint8_t* dst, int col, const TileRows& r, uint64_t* bar) {
+    if (!paged64) {
+      tma_load_2d(dst, &p.tmap_kv64, col, r.r0, bar, pol);
+    } else {
+      tma_load_2d(dst, &p.tmap_kv16, col, r.r0, bar, pol);
+      if (r.r1 >= 0) tma_load_2d(dst + 64 * 64, &p.tmap_kv16, col, r.r1, bar, pol);
+    }
+  };
   int armed[kPairSlots + kRopeSlots];
   for (int i = 0; i < kPairSlots + kRopeSlots; ++i) armed[i] = 0;
-  for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
-    const UnitDesc d = x.units[k];
-    for (int t0 = d.start; t0 < d.end && !*x.abort_flag; t0 += kTileRows, ++it) {
-      for (int f = 0; f < 4; ++f) {
-        const int sl = pair_slot<false>(it, f), use = pair_use<false>(it, f);
-        if (use >= 1) wait_phase(&x.bar[kPairEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
-        if (*x.abort_flag) break;
-        uint8_t* dst = x.smem + L::pairs + sl * kPairBytes;
-        mbar_arrive_expect_tx(&x.bar[kPairFull + sl], kPairBytes);
-        tma_load_2d(dst, &p.tmap_kv64, 128 * f, t0, &x.bar[kPairFull + sl], pol);
-        tma_load_2d(dst + kChunkBytes, &p.tmap_kv64, 128 * f + 64, t0, &x.bar[kPairFull + sl], pol);
-        ++armed[sl];
-      }
-      const int rs = it % kRopeSlots, ruse = it / kRopeSlots;
-      if (ruse >= 1) wait_phase(&x.bar[kRopeEmpty + rs], (ruse - 1) & 1, x.abort_flag, p.ws_err);
+  // the cache rows of the next tile are looked up one tile ahead (a paged
+  // cache reads the page table; otherwise they are the tile's own rows)
+  TileWalk walk;
+  int nt0 = 0, nend = 0;
+  bool have = walk.next(x, nt0, nend);
+  TileRows nrows = have ? tile_rows(p, nt0, nend) : TileRows{0, -1};
+  for (int it = 0; have && !*x.abort_flag; ++it) {
+    const TileRows rows = nrows;
+    have = walk.next(x, nt0, nend);
+    if (have) nrows = tile_rows(p, nt0, nend);
+    const uint32_t block_bytes = (paged64 && rows.r1 < 0) ? kChunkBytes / 2 : kChunkBytes;
+    for (int f = 0; f < 4; ++f) {
+      const int sl = pair_slot<false>(it, f), use = pair_use<false>(it, f);
+      if (use >= 1) wait_phase(&x.bar[kPairEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
-      mbar_arrive_expect_tx(&x.bar[kRopeFull + rs], kChunkBytes);
-      tma_load_2d(x.smem + L::rope + rs * kChunkBytes, &p.tmap_kv64, 512, t0, &x.bar[kRopeFull + rs], pol);
-      ++armed[kPairSlots + rs];
+      uint8_t* dst = x.smem + L::pairs + sl * kPairBytes;
+      mbar_arrive_expect_tx(&x.bar[kPairFull + sl], 2 * block_bytes);
+      load_block(dst, 128 * f, rows, &x.bar[kPairFull + sl]);
+      load_block(dst + kChunkBytes, 128 * f + 64, rows, &x.bar[kPairFull + sl]);
+      ++armed[sl];
     }
+    const int rs = it % kRopeSlots, ruse = it / kRopeSlots;
+    if (ruse >= 1) wait_phase(&x.bar[kRopeEmpty + rs], (ruse - 1) & 1, x.abort_flag, p.ws_err);
+    if (*x.abort_flag) break;
+    mbar_arrive_expect_tx(&x.bar[kRopeFull + rs], block_bytes);
+    load_block(x.smem + L::rope + rs * kChunkBytes, 512, rows, &x.bar[kRopeFull + rs]);
+    ++armed[kPairSlots + rs];
   }
   if (*x.abort_flag) {
     // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
@@ -225,44 +275,52 @@ static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
   const uint64_t pol = policy_evict_first();  // KV rows are read once
   const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
   const size_t ss = (size_t)p.scale_stride;
-  int hh = 0;
   int uses[kStageSlots] = {0, 0, 0};
   // the scale bytes of the half kScalePrefetch ahead go to L2 (the converters
   // read them a half ahead; this keeps those reads L2 hits)
   constexpr int kScalePrefetch = 6;
-  HalfCursor pre;
   // one bulk L2 prefetch per half: the 16-byte-aligned part of its scale rows
   // that lies inside the tensor (the base is 16-byte aligned)
-  const size_t scale_end = ((size_t)p.total_kv * ss) & ~(size_t)15;
-  auto prefetch_scales = [&](int r0, int rows) {
+  const int cache_rows = p.page_shift ? (p.num_pages << p.page_shift) : p.total_kv;
+  const size_t scale_end = ((size_t)cache_rows * ss) & ~(size_t)15;
+  auto prefetch_scales = [&](int c0, int rows) {
     if (rows <= 0) return;
-    const size_t lo = ((size_t)r0 * ss) & ~(size_t)15;
-    size_t hi = ((size_t)(r0 + rows) * ss + 15) & ~(size_t)15;
+    const size_t lo = ((size_t)c0 * ss) & ~(size_t)15;
+    size_t hi = ((size_t)(c0 + rows) * ss + 15) & ~(size_t)15;
     if (hi > scale_end) hi = scale_end;
     if (hi > lo) bulk_prefetch_l2(sc + lo, (uint32_t)(hi - lo));
   };
-  for (int i = 0, r0, rows; i < kScalePrefetch && pre.next(x, r0, rows); ++i) prefetch_scales(r0, rows);
-  for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
-    const UnitDesc d = x.units[k];
-    for (int t0 = d.start; t0 < d.end && !*x.abort_flag; t0 += kTileRows) {
-      for (int h = 0; h < 2; ++h, ++hh) {
-        const int sl = hh % kStageSlots, use = hh / kStageSlots;
-        if (use >= 1) wait_phase(&x.bar[kStageEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
-        if (*x.abort_flag) break;
-        const int r0 = t0 + h * kHalfRows;
-        const int rows = max(0, min(kHalfRows, d.end - r0));
-        if (rows > 0) {
-          mbar_arrive_expect_tx(&x.bar[kStageFull + sl], (uint32_t)(rows * kPackedRowBytes));
-          bulk_g2s(x.smem + L::stage + sl * kStageBytes, p.kv + (size_t)r0 * kPackedRowBytes,
-                   (uint32_t)(rows * kPackedRowBytes), &x.bar[kStageFull + sl], pol);
-        } else {
-          mbar_arrive(&x.bar[kStageFull + sl]);
-        }
-        ++uses[sl];
-        int pr0, prows;
-        if (pre.next(x, pr0, prows)) prefetch_scales(pr0, prows);
-      }
+  // cache rows are looked up one half before they are used (a paged cache
+  // reads the page table; otherwise a half's cache rows are its own rows)
+  HalfCursor pre;
+  int pf_row = 0, pf_rows = 0;  // the half whose prefetch is issued next
+  auto advance_prefetch = [&]() {
+    prefetch_scales(pf_row, pf_rows);
+    int r0, rows;
+    pf_rows = pre.next(x, r0, rows) ? rows : 0;
+    pf_row = pf_rows > 0 ? cache_row(p, r0) : 0;
+  };
+  for (int i = 0; i <= kScalePrefetch; ++i) advance_prefetch();
+  HalfCursor cur;
+  int nr0 = 0, nrows = 0;
+  bool have = cur.next(x, nr0, nrows);
+  int ncrow = (have && nrows > 0) ? cache_row(p, nr0) : 0;
+  for (int hh = 0; have && !*x.abort_flag; ++hh) {
+    const int rows = nrows, crow = ncrow;
+    have = cur.next(x, nr0, nrows);
+    if (have) ncrow = nrows > 0 ? cache_row(p, nr0) : 0;
+    const int sl = hh % kStageSlots, use = hh / kStageSlots;
+    if (use >= 1) wait_phase(&x.bar[kStageEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
+    if (*x.abort_flag) break;
+    if (rows > 0) {
+      mbar_arrive_expect_tx(&x.bar[kStageFull + sl], (uint32_t)(rows * kPackedRowBytes));
+      bulk_g2s(x.smem + L::stage + sl * kStageBytes, p.kv + (size_t)crow * kPackedRowBytes,
+               (uint32_t)(rows * kPackedRowBytes), &x.bar[kStageFull + sl], pol);
+    } else {
+      mbar_arrive(&x.bar[kStageFull + sl]);
     }
+    ++uses[sl];
+    advance_prefetch();
   }
   if (*x.abort_flag) {
     // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
@@ -323,17 +381,21 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
   HalfCursor cur, pre;
   int r0 = 0, rows = 0, pr0 = 0, prows = 0;
   // the row's scale bytes are loaded one half ahead of their use (the producer
-  // has already brought them into L2)
+  // has already brought them into L2); a half lies inside one page
+  auto load_next_scales = [&](uint32_t (&dst)[9]) {
+    if (pre.next(x, pr0, prows))
+      load_row_scales(sc, ss, (prows > 0 ? cache_row(p, pr0) : 0) + lr, lr < prows, dst);
+  };
   uint32_t e_next[9];
 #pragma unroll
   for (int i = 0; i < 9; ++i) e_next[i] = 0x7f7fu;
-  if (pre.next(x, pr0, prows)) load_row_scales(sc, ss, pr0 + lr, lr < prows, e_next);
+  load_next_scales(e_next);
   for (int hh = 0; cur.next(x, r0, rows) && !*x.abort_flag; ++hh) {
     const int it = hh >> 1, h = hh & 1;
     uint32_t e[9];
 #pragma unroll
     for (int i = 0; i < 9; ++i) e[i] = e_next[i];
-    if (pre.next(x, pr0, prows)) load_row_scales(sc, ss, pr0 + lr, lr < prows, e_next);
+    load_next_scales(e_next);
     if (h == 0) {
       // the tile's ring slots must have been released by the MMAs that read them
 #pragma unroll

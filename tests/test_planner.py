@@ -166,3 +166,37 @@ def test_rejects_bad_layouts():
         binding.mla_decode_plan([-1, 5], "fp8", num_sms=152)
     with pytest.raises(binding.MLAError):
         binding.mla_decode_plan([0, 5], 7, num_sms=152)
+
+
+def test_paged_plan_matches_lengths():
+    """A paged layout plans like the contiguous layout of the same lengths; its
+    row space starts each sequence at page_indptr[b] * page_size."""
+    rng = random.Random(5)
+    for _ in range(60):
+        b = rng.randint(1, 40)
+        P = rng.choice([64, 128, 256, 1024])
+        npages = [rng.choice([0, 1, 2, rng.randint(1, 40)]) for _ in range(b)]
+        last = [rng.randint(1, P) if n else 0 for n in npages]
+        lens = [(n - 1) * P + l if n else 0 for n, l in zip(npages, last)]
+        pind = [0] + list(itertools.accumulate(npages))
+        dtype = rng.choice(["bf16", "fp8", "mxfp4"])
+        sms = rng.choice([7, 152])
+        plan = binding.mla_decode_plan_paged(pind, last, P, pind[-1] + 2, dtype, num_sms=sms)
+        ref = binding.mla_decode_plan(np.cumsum([0] + lens).astype(np.int32), dtype, num_sms=sms)
+        d, r = plan.as_dict(), ref.as_dict()
+        assert d.pop("total_kv") == pind[-1] * P and d.pop("page_size") == P and d.pop("num_pages") == pind[-1] + 2
+        r.pop("total_kv"), r.pop("page_size"), r.pop("num_pages")
+        assert d == r
+
+
+def test_paged_plan_rules():
+    for P in (1, 8, 32, 96):  # not a power of two >= 64
+        with pytest.raises(binding.MLAError) as e:
+            binding.mla_decode_plan_paged([0, 1], [1], P, 1, "fp8", num_sms=152)
+        assert e.value.status == binding.MLA_ERR_UNSUPPORTED
+    for pind, last in (([0, 2], [65]), ([0, 2], [0]), ([1, 0], [1])):  # last page length, order
+        with pytest.raises(binding.MLAError) as e:
+            binding.mla_decode_plan_paged(pind, last, 64, 4, "fp8", num_sms=152)
+        assert e.value.status == binding.MLA_ERR_INVALID_ARG
+    plan = binding.mla_decode_plan_paged([0, 0, 3], [0, 7], 64, 3, "fp8", num_sms=152)
+    assert plan.total_kv == 192 and plan.page_size == 64
