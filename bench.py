@@ -67,6 +67,9 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOAD_ORDER)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="decode the workload's rows from a paged cache with pages of this many rows "
+                         "(pages scattered at random; mla_decode_fwd_paged); 0 = contiguous cache")
     return ap.parse_args()
 
 
@@ -268,18 +271,37 @@ def main():
         torch.cuda.synchronize()
 
     d = to_device(inp, dev)
-    dec = binding.MLADecoder(inp.kv_indptr, dt, device=dev)
+    paged = None
+    if args.page_size:
+        # the same rows in a paged cache: pages at random positions (no spare pages)
+        paged = synth.make_paged(inp, args.page_size, seed=rank, spare_pages=0)
+        d["kv"] = paged.kv.to(dev)
+        if dt == "mxfp4":
+            d["kv_scale"] = paged.block_scales.to(dev)
+        d["page_indptr"] = paged.page_indptr.to(dev)
+        d["kv_indices"] = paged.kv_indices.to(dev)
+        d["last_page_len"] = paged.last_page_len.to(dev)
+        dec = binding.PagedMLADecoder(paged.page_indptr, paged.last_page_len, paged.page_size, paged.num_pages, dt,
+                                      device=dev)
+    else:
+        dec = binding.MLADecoder(inp.kv_indptr, dt, device=dev)
     plan = dec.plan
     out = torch.empty(b, 16, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(b, 16, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     scale_stride = int(d["kv_scale"].stride(0)) if dt == "mxfp4" else 0
-    launches_per_call = 1 + (1 if plan.splits_max > 1 else 0)
+    # query preparation (e4m3 and MXFP4 KV), split kernel, combine when split
+    launches_per_call = (1 if dt == "bf16" else 2) + (1 if plan.splits_max > 1 else 0)
 
     def call():
-        binding.mla_decode_fwd(d["q"], d["kv"], d["kv_scale"], d["kv_indptr"], d["qo_indptr"], out, lse, plan,
-                               dec.workspace, scale_stride=scale_stride, stream=stream)
+        if paged is not None:
+            binding.mla_decode_fwd_paged(d["q"], d["kv"], d["kv_scale"], d["page_indptr"], d["kv_indices"],
+                                         d["last_page_len"], d["qo_indptr"], out, lse, plan, dec.workspace,
+                                         scale_stride=scale_stride, stream=stream)
+        else:
+            binding.mla_decode_fwd(d["q"], d["kv"], d["kv_scale"], d["kv_indptr"], d["qo_indptr"], out, lse, plan,
+                                   dec.workspace, scale_stride=scale_stride, stream=stream)
 
     for _ in range(max(3, args.warmup)):
         call()
@@ -313,7 +335,7 @@ def main():
 
     # ---- the split kernel alone (roofline) and the combine, events on the launch stream
     ev_split, ev_comb = [], []
-    for i in range(args.steps):
+    for i in range(args.steps if paged is None else 0):
         flush.fill_(i & 0xFF)
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         e0.record(stream)
@@ -325,23 +347,32 @@ def main():
         ev_split.append((e0, e1))
         ev_comb.append((e1, e2))
     torch.cuda.synchronize()
-    t_split = statistics.mean(a.elapsed_time(c) * 1e3 for a, c in ev_split)
-    t_comb = statistics.mean(a.elapsed_time(c) * 1e3 for a, c in ev_comb)
+    if paged is None:
+        t_split = statistics.mean(a.elapsed_time(c) * 1e3 for a, c in ev_split)
+        t_comb = statistics.mean(a.elapsed_time(c) * 1e3 for a, c in ev_comb)
+    else:
+        # the paged entry point has no separate stages: the whole call stands in
+        t_split, t_comb = us, 0.0
     kv_bytes = inp.kv_bytes()
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (t_split * 1e-6) / 1e9
 
     # ---- end to end through the public call: pinned host q/indptr in, out/lse out
     q_h = inp.q.pin_memory()
-    ind_h = inp.kv_indptr.pin_memory()
+    ind_h = (inp.kv_indptr if paged is None else paged.page_indptr).pin_memory()
     qo_h = inp.qo_indptr.pin_memory()
+    ind_key = "kv_indptr" if paged is None else "page_indptr"
+    extra_h = [] if paged is None else [(d["kv_indices"], paged.kv_indices.pin_memory()),
+                                        (d["last_page_len"], paged.last_page_len.pin_memory())]
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
 
     def e2e_call():
         d["q"].copy_(q_h, non_blocking=True)
-        d["kv_indptr"].copy_(ind_h, non_blocking=True)
+        d[ind_key].copy_(ind_h, non_blocking=True)
         d["qo_indptr"].copy_(qo_h, non_blocking=True)
+        for dst, src in extra_h:
+            dst.copy_(src, non_blocking=True)
         call()
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
@@ -351,7 +382,8 @@ def main():
     barrier()
     e2e_times = time_calls(e2e_call, args.steps, flush, stream)
     e2e_us = statistics.mean(e2e_times)
-    h2d = q_h.numel() * q_h.element_size() + ind_h.numel() * 4 + qo_h.numel() * 4
+    h2d = q_h.numel() * q_h.element_size() + ind_h.numel() * 4 + qo_h.numel() * 4 + sum(
+        src.numel() * 4 for _, src in extra_h)
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
     assert dec.poll_error() == 0
     if pg is not None:
@@ -369,14 +401,17 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": DTYPE_LABEL[dt], "data": "synthetic (seeded N(0,1) q and KV, quantised as stated)",
-            "config": {"workload": name, "batch": b, "kv_len": L, "kv_dtype": dt,
+            "config": {"workload": name if paged is None else f"{name}_paged{args.page_size}", "batch": b,
+                       "kv_len": L, "kv_dtype": dt, "page_size": args.page_size or 1,
                        "kv_bytes_per_call": kv_bytes, "l2": "flushed before every timed call (256 MiB write)",
                        "plan": {k: plan.as_dict()[k] for k in ("num_work", "grid", "chunk_tokens", "splits_max")},
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "kv_gbs": round(kv_bytes / (us * 1e-6) / 1e9, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic(name),
-                         "kernel": KERNEL_NAMES[dt], "kernel_us": round(t_split, 3),
+                         "frac": round(achieved / peak, 4),
+                         "traffic": profiled_traffic(name) if paged is None else None,
+                         "kernel": KERNEL_NAMES[dt] if paged is None else "whole paged call",
+                         "kernel_us": round(t_split, 3),
                          "combine_us": round(t_comb, 3), "peak_kind": f"{peak_kind} (HBM copy)"},
             "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
