@@ -1,5 +1,6 @@
 // mla_internal.h -- parameters shared by the host API and the kernel launchers.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -98,6 +99,22 @@ cudaError_t launch_stage1_mxfp4(const Stage1Params& p, cudaStream_t s);
 // Two-term e4m3 query of every sequence into the workspace (e4m3 / MXFP4 KV).
 cudaError_t launch_prep_q(const Stage1Params& p, bool mx, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s, bool pdl);
+
+// Sets kernel K's dynamic shared-memory opt-in once per device and process
+// (the attribute belongs to the function in each device's context; setting it
+// on every call costs host time between two dependent launches).
+template <auto K>
+inline cudaError_t smem_opt_in(int bytes) {
+  static std::atomic<uint64_t> done{0};  // bit d: set on device d
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Launch with programmatic dependent launch allowed: the kernel may start while
 // the previous kernel on the stream finishes, and waits (griddepcontrol.wait)

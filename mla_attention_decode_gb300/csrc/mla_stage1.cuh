@@ -716,8 +716,7 @@ cudaError_t launch_split(const Stage1Params& p, cudaStream_t stream) {
   using L = Smem<KV>;
   static_assert(L::total <= 232448, "shared memory carve-up exceeds the 227 KB per-CTA limit");
   static_assert(L::qbuf % 1024 == 0 && L::kStageBytes % 1024 == 0, "TMA swizzle alignment");
-  cudaError_t e =
-      cudaFuncSetAttribute(mla_split_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
+  cudaError_t e = smem_opt_in<mla_split_kernel<KV>>(L::total);
   if (e != cudaSuccess) return e;
   e = launch_overlapped(mla_split_kernel<KV>, dim3(p.grid), dim3(kCtaThreads), L::total, stream, p);
   if (e != cudaSuccess) return e;

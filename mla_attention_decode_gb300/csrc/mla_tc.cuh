@@ -952,8 +952,7 @@ inline cudaError_t launch_split_tc(const Stage1Params& p, cudaStream_t stream) {
   static_assert(L::total <= 232448, "shared memory carve-up exceeds the 227 KB per-CTA limit");
   static_assert(L::qs % 1024 == 0 && L::pb % 1024 == 0 && L::rope % 1024 == 0, "swizzled operand alignment");
   static_assert(L::stage % 16 == 0, "bulk-copy destination alignment");
-  cudaError_t e = cudaFuncSetAttribute(tcfp8::mla_split_tc_kernel<kMx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::total);
+  cudaError_t e = smem_opt_in<tcfp8::mla_split_tc_kernel<kMx>>(L::total);
   if (e != cudaSuccess) return e;
   e = launch_overlapped(tcfp8::mla_split_tc_kernel<kMx>, dim3(p.grid), dim3(tcfp8::Geo<kMx>::threads), L::total,
                         stream, p);
