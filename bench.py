@@ -54,8 +54,10 @@ KERNEL_SOURCES = {
     "mxfp4": [_CSRC + f for f in ("mla_tc.cuh", "mla_common.cuh", "mla_ptx.cuh", "mla_internal.h",
                                   "mla_split_mxfp4.cu")],
 }
-KERNEL_NAMES = {"bf16": "mla_split_kernel (mma.sync, bf16)", "fp8": "mla_split_tc_kernel (tcgen05, e4m3)",
-                "mxfp4": "mla_split_tc_kernel (tcgen05, e2m1 dequantised to e4m3)"}
+KERNEL_NAMES = {"bf16": "mla_split_kernel (mma.sync, bf16)",
+                "fp8": "mla_prep_q_kernel + mla_split_tc_kernel (tcgen05, e4m3), launches overlapped",
+                "mxfp4": "mla_prep_q_kernel + mla_split_tc_kernel (tcgen05, e2m1 dequantised to e4m3), "
+                         "launches overlapped"}
 CLOCK_SOAK_S = 1.0
 
 
