@@ -359,34 +359,44 @@ def main():
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (t_split * 1e-6) / 1e9
 
-    # ---- end to end through the public call: pinned host q/indptr in, out/lse out
-    q_h = inp.q.pin_memory()
-    ind_h = (inp.kv_indptr if paged is None else paged.page_indptr).pin_memory()
-    qo_h = inp.qo_indptr.pin_memory()
-    ind_key = "kv_indptr" if paged is None else "page_indptr"
-    extra_h = [] if paged is None else [(d["kv_indices"], paged.kv_indices.pin_memory()),
-                                        (d["last_page_len"], paged.last_page_len.pin_memory())]
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    # ---- end to end through the public call: the step's inputs (q and the
+    # index arrays) in one pinned host buffer, copied in by one copy; out and
+    # lse in one device buffer, copied back by one copy (binding.PackedBuffers)
+    idx_names = ["kv_indptr"] if paged is None else ["page_indptr", "kv_indices", "last_page_len"]
+    host_src = {"q": inp.q, "qo_indptr": inp.qo_indptr}
+    if paged is None:
+        host_src["kv_indptr"] = inp.kv_indptr
+    else:
+        host_src.update(page_indptr=paged.page_indptr, kv_indices=paged.kv_indices,
+                        last_page_len=paged.last_page_len)
+    ins = binding.PackedBuffers([(k, tuple(v.shape), v.dtype) for k, v in host_src.items()], dev)
+    for k, v in host_src.items():
+        ins.host[k].copy_(v)
+    outs = binding.PackedBuffers([("out", tuple(out.shape), out.dtype), ("lse", tuple(lse.shape), lse.dtype)], dev)
+    e2e_d = dict(d)
+    e2e_d.update({k: ins.dev[k] for k in ["q", "qo_indptr"] + idx_names})
+    out_e, lse_e = outs.dev["out"], outs.dev["lse"]
 
     def e2e_call():
-        d["q"].copy_(q_h, non_blocking=True)
-        d[ind_key].copy_(ind_h, non_blocking=True)
-        d["qo_indptr"].copy_(qo_h, non_blocking=True)
-        for dst, src in extra_h:
-            dst.copy_(src, non_blocking=True)
-        call()
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        ins.to_device(stream)
+        if paged is not None:
+            binding.mla_decode_fwd_paged(e2e_d["q"], e2e_d["kv"], e2e_d["kv_scale"], e2e_d["page_indptr"],
+                                         e2e_d["kv_indices"], e2e_d["last_page_len"], e2e_d["qo_indptr"], out_e,
+                                         lse_e, plan, dec.workspace, scale_stride=scale_stride, stream=stream)
+        else:
+            binding.mla_decode_fwd(e2e_d["q"], e2e_d["kv"], e2e_d["kv_scale"], e2e_d["kv_indptr"],
+                                   e2e_d["qo_indptr"], out_e, lse_e, plan, dec.workspace,
+                                   scale_stride=scale_stride, stream=stream)
+        outs.to_host(stream)
 
     for _ in range(3):
         e2e_call()
     barrier()
     e2e_times = time_calls(e2e_call, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    assert torch.equal(outs.host["out"], out.cpu()), "end-to-end output differs from the device-resident call"
     e2e_us = statistics.mean(e2e_times)
-    h2d = q_h.numel() * q_h.element_size() + ind_h.numel() * 4 + qo_h.numel() * 4 + sum(
-        src.numel() * 4 for _, src in extra_h)
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    h2d, d2h = ins.nbytes, outs.nbytes
     assert dec.poll_error() == 0
     if pg is not None:
         t = torch.tensor([e2e_us, t_split, t_comb], device=dev)

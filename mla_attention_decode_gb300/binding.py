@@ -268,3 +268,48 @@ class PagedMLADecoder:
 
     def poll_error(self, stream=None) -> int:
         return mla_decode_poll_error(self.workspace, stream)
+
+
+class PackedBuffers:
+    """Several tensors laid out in one pinned host buffer and one device buffer
+    (256-byte aligned offsets), so that moving all of them takes one copy each
+    way.  ``specs``: list of (name, shape, dtype).  ``host[name]`` and
+    ``dev[name]`` are views into the two buffers."""
+
+    def __init__(self, specs, device):
+        self.layout = {}
+        off = 0
+        for name, shape, dtype in specs:
+            n = 1
+            for x in shape:
+                n *= int(x)
+            n *= torch.empty((), dtype=dtype).element_size()
+            self.layout[name] = (off, tuple(shape), dtype, n)
+            off = (off + n + 255) // 256 * 256
+        self.nbytes = max(off, 256)
+        self.host_bytes = torch.empty(self.nbytes, dtype=torch.uint8).pin_memory()
+        self.dev_bytes = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self.host = {k: self._view(self.host_bytes, *v) for k, v in self.layout.items()}
+        self.dev = {k: self._view(self.dev_bytes, *v) for k, v in self.layout.items()}
+
+    @staticmethod
+    def _view(buf, off, shape, dtype, n):
+        return buf[off:off + n].view(dtype).view(shape)
+
+    def to_device(self, stream=None):
+        """One host-to-device copy of the whole buffer on ``stream`` (asynchronous)."""
+        with torch.cuda.stream(stream) if stream is not None else _nullcontext():
+            self.dev_bytes.copy_(self.host_bytes, non_blocking=True)
+
+    def to_host(self, stream=None):
+        """One device-to-host copy of the whole buffer on ``stream`` (asynchronous)."""
+        with torch.cuda.stream(stream) if stream is not None else _nullcontext():
+            self.host_bytes.copy_(self.dev_bytes, non_blocking=True)
+
+
+class _nullcontext:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *a):
+        return False
