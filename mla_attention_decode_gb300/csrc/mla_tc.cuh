@@ -63,7 +63,7 @@ constexpr int kPairBytes = 2 * kChunkBytes;  // two column blocks = features [12
 template <bool kMx>
 struct Geo {
   static constexpr int pair_slots = kMx ? 8 : 11;  // ring of V column-block pairs (4 per tile)
-  static constexpr int threads = kMx ? 384 : 256;
+  static constexpr int threads = kMx ? 512 : 256;
   static constexpr int max_units = kMx ? kMaxUnitsPerCtaMx : kMaxUnitsPerCta;  // work units one CTA may own
 };
 constexpr int kRopeSlots = 2;                // ring of the rope column block (features 512..575)
@@ -364,12 +364,14 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lut_lo, uin
   return make_uint2(m0 | ((s0 << 1) & 0x80808080u), m1 | ((s1 << 1) & 0x80808080u));
 }
 
-// Converter warp cw (0..3) converts rows [16 cw, 16 cw + 16) of every half
-// tile; lane pair (2i, 2i+1) shares row 16 cw + i, lane 2i + hp taking the
-// row's blocks 2j + hp (j = 0..8).  Block 2j + hp holds features
-// [64 j + 32 hp, +32), columns [32 hp, 32 hp + 32) of column block j, so the
-// destination block of each is fixed at compile time.  Four warps, one per SM
-// sub-partition: the conversion is bound by the integer pipe of each.
+// Converter warp cw (0..7) converts half cw / 4 of every tile (tile rows
+// [64 (cw / 4), +64)): rows [16 (cw % 4), +16) of that half.  Lane pair
+// (2i, 2i+1) shares row 16 (cw % 4) + i, lane 2i + hp taking the row's blocks
+// 2j + hp (j = 0..8).  Block 2j + hp holds features [64 j + 32 hp, +32),
+// columns [32 hp, 32 hp + 32) of column block j, so the destination block of
+// each is fixed at compile time.  Eight warps, two per SM sub-partition (one
+// per half tile): the conversion is bound by each sub-partition's integer
+// pipe, and a second warp keeps it busy while the first waits.
 static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw, int lane) {
   using L = Layout<true>;
   const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
@@ -377,14 +379,18 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
   const uint32_t lut0 = smem_u32(x.smem + L::lut), stage0 = smem_u32(x.smem + L::stage);
   const uint32_t pairs0 = smem_u32(x.smem + L::pairs), rope0 = smem_u32(x.smem + L::rope);
   int8_t* grow = reinterpret_cast<int8_t*>(x.smem + L::grow);
-  const int lr = 16 * cw + (lane >> 1), hp = lane & 1;  // row within the half, which half of the row
+  const int hsel = cw >> 2;                                    // the half of every tile this warp converts
+  const int lr = 16 * (cw & 3) + (lane >> 1), hp = lane & 1;  // row within the half, which half of the row
   HalfCursor cur, pre;
-  int r0 = 0, rows = 0, pr0 = 0, prows = 0;
-  // the row's scale bytes are loaded one half ahead of their use (the producer
+  int r0 = 0, rows = 0, pr0 = 0, prows = 0, pre_hh = 0;
+  // the row's scale bytes are loaded one tile ahead of their use (the producer
   // has already brought them into L2); a half lies inside one page
   auto load_next_scales = [&](uint32_t (&dst)[9]) {
-    if (pre.next(x, pr0, prows))
+    while (pre.next(x, pr0, prows)) {
+      if ((pre_hh++ & 1) != hsel) continue;  // the other half's rows
       load_row_scales(sc, ss, (prows > 0 ? cache_row(p, pr0) : 0) + lr, lr < prows, dst);
+      return;
+    }
   };
   uint32_t e_next[9];
 #pragma unroll
@@ -392,11 +398,12 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
   load_next_scales(e_next);
   for (int hh = 0; cur.next(x, r0, rows) && !*x.abort_flag; ++hh) {
     const int it = hh >> 1, h = hh & 1;
+    if (h != hsel) continue;
     uint32_t e[9];
 #pragma unroll
     for (int i = 0; i < 9; ++i) e[i] = e_next[i];
     load_next_scales(e_next);
-    if (h == 0) {
+    {
       // the tile's ring slots must have been released by the MMAs that read them
 #pragma unroll
       for (int f = 0; f < 4; ++f) {
@@ -439,11 +446,9 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&x.bar[kStageEmpty + sl]);
-    if (h == 1) {
-      tc::fence_proxy_async();  // the tensor core reads the ring through the async proxy
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&x.bar[kConvFull + (it & 1)]);
-    }
+    tc::fence_proxy_async();  // the tensor core reads the ring through the async proxy
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&x.bar[kConvFull + (it & 1)]);
   }
 }
 
@@ -810,8 +815,8 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
     ++ordinal;
     tc::fence_after();
     float inv[16];
-#pragma unroll
     const float out_scale = kMx ? exp2_int(max(-126, min(127, gv))) : kv_scale;
+#pragma unroll
     for (int h = 0; h < 16; ++h) inv[h] = l_part[h] > 0.f ? out_scale * __frcp_rn(l_part[h]) : 0.f;
 #pragma unroll 1
     for (int fb = 0; fb < 4; ++fb) {
@@ -878,7 +883,7 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     counts[kOFree] = 4;
     counts[kRFree] = 4;
     for (int i = 0; i < kStageSlots; ++i) counts[kStageEmpty + i] = 4;
-    counts[kConvFull] = counts[kConvFull + 1] = 4;
+    counts[kConvFull] = counts[kConvFull + 1] = 8;
     for (int i = 0; i < L::nbars; ++i) mbar_init(&x.bar[i], counts[i]);
     *x.abort_flag = 0;
     fence_mbar_init();
@@ -890,7 +895,7 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     scan_units<kTileRows, Geo<kMx>::max_units>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits, lane);
     if (lane == 0 && !kMx) prefetch_tensormap(&p.tmap_kv64);
   }
-  if (kMx && threadIdx.x >= 128) {
+  if (kMx && threadIdx.x >= 128 && threadIdx.x < 384) {
     // e4m3 bytes of the e2m1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} times
     // 2^-shift for shifts 0..15, then 16 all-zero entries (rows past the end)
     const int i = threadIdx.x - 128, shift = i >> 3, m = i & 7;
