@@ -82,6 +82,16 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(values, pg, device):
+    """Element-wise maximum of per-rank values over the process group (the job
+    takes as long as its slowest rank); the values themselves without one."""
+    if pg is None:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -329,11 +339,7 @@ def main():
         barrier()
         t_wall = time.perf_counter() - t_wall
         soak(CLOCK_SOAK_S / 2)
-    us = statistics.mean(per_call)
-    if pg is not None:
-        t = torch.tensor([us], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        us = float(t.item())
+    us = max_over_ranks([statistics.mean(per_call)], pg, dev)[0]
 
     # ---- the split kernel alone (roofline) and the combine, events on the launch stream
     ev_split, ev_comb = [], []
@@ -398,10 +404,7 @@ def main():
     e2e_us = statistics.mean(e2e_times)
     h2d, d2h = ins.nbytes, outs.nbytes
     assert dec.poll_error() == 0
-    if pg is not None:
-        t = torch.tensor([e2e_us, t_split, t_comb], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_us, t_split, t_comb = (float(x) for x in t.tolist())
+    e2e_us, t_split, t_comb = max_over_ranks([e2e_us, t_split, t_comb], pg, dev)
 
     if rank == 0:
         cpu = None
