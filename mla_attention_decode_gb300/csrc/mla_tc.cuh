@@ -8,7 +8,7 @@
 // contiguous range of KV rows; final bf16 output and lse for unsplit
 // sequences, fp32 partials and lse for split ones.
 //
-// Per 128-row tile t of a unit (one persistent CTA per SM: 8 warps for e4m3, 12 for MXFP4):
+// Per 128-row tile t of a unit (one persistent CTA per SM: 8 warps for e4m3, 16 for MXFP4):
 //   scores  S^T[128 rows x 32] = K_t[128 x 576] . [Q_hi | Q_lo]^T   (tcgen05 kind::f8f6f4,
 //           18 k32 steps; K straight from the TMA stage, K-major, 64 B swizzle;
 //           the query as two e4m3 terms x = hi + lo with a power-of-two scale
@@ -39,7 +39,7 @@
 //
 // MXFP4 KV (kMx): rows arrive packed (288 B of e2m1 pairs, element 2i in the low
 // nibble of byte i) by 1-D bulk copies of 64-row halves into a staging ring,
-// and four converter warps (8-11) write them into the same e4m3 ring layout
+// and eight converter warps (8-15, four per half tile) write them into the same e4m3 ring layout
 // the tensor cores read (8 pair slots: two whole tiles, so that converting
 // tile t only waits for the P.V of tile t-2).  Per row, with G = the largest of its 18 e8m0 bytes,
 // element n * 2^(e-127) becomes the e4m3 value n * 2^(e-G) (exact while the
@@ -119,8 +119,8 @@ enum {
   kFinal = 38,      // commits after both issuers' last operations (count 2)
   kPFree = 39,      // [2]  commit after the P.V that read P buffer t mod 2
   kStageFull = 41,  // [3]  MXFP4: bytes of a staged half tile (or the producer's arrival)
-  kStageEmpty = 44, // [3]  MXFP4: the converter warps read it (4 warps)
-  kConvFull = 47,   // [2]  MXFP4: tile t converted into the ring (4 warps)
+  kStageEmpty = 44, // [3]  MXFP4: the converter warps of that half read it (4 warps)
+  kConvFull = 47,   // [2]  MXFP4: tile t converted into the ring (8 warps)
 };
 
 
