@@ -18,69 +18,81 @@
 namespace mla {
 
 // One CTA per (sequence, head, quarter of the 512 features); 128 threads.
-// Every warp finds M over all of the sequence's splits (lanes stride the
-// splits); warp w then accumulates splits w, w + 4, ... for its 128 features
-// (lane: 4 features), four splits' loads in flight at a time, and the four
-// warps' sums meet in shared memory.  The latency is about two L2 round trips
-// whatever the split count.
+// Warp w takes splits w, w + 4, ... for its 128 features (lane: 4 features),
+// loading each split's lse and partial together, four splits in flight at a
+// time, and keeps a running log-sum-exp against its own maximum; the four
+// warps' sums meet in shared memory, rescaled to the common maximum.  After
+// the split table, the latency is one L2 round trip whatever the split count.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const __grid_constant__ CombineParams p) {
   __shared__ float4 part[4][32];
-  __shared__ float wpart[4];
+  __shared__ float wpart[4], mpart[4];
   pdl_wait_primary();
   const int b = blockIdx.x >> 6, h = (blockIdx.x >> 2) & 15, quarter = blockIdx.x & 3;
   const int first = p.ws_seq[2 * b], ns = p.ws_seq[2 * b + 1];
   if (ns <= 1) return;  // written directly by the split kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* lse = p.ws_lse + (size_t)first * kHeads + h;
-  float m = -INFINITY;
-  for (int s = lane; s < ns; s += 32) m = fmaxf(m, lse[(size_t)s * kHeads]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const int f = 128 * quarter + 4 * lane;
+  const float* o = p.ws_o + ((size_t)first * kHeads + h) * kVDim + f;
+  float m = -INFINITY;  // this warp's running maximum of the split lse values
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-  if (m != -INFINITY) {
-    const float* o = p.ws_o + ((size_t)first * kHeads + h) * kVDim + f;
-    for (int s0 = warp; s0 < ns; s0 += 16) {
-      float l[4];
-      float4 v[4];
+  for (int s0 = warp; s0 < ns; s0 += 16) {
+    float l[4];
+    float4 v[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int s = s0 + 4 * i;
-        l[i] = s < ns ? lse[(size_t)s * kHeads] : -INFINITY;
-        v[i] = s < ns ? *reinterpret_cast<const float4*>(o + (size_t)s * kHeads * kVDim) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+    for (int i = 0; i < 4; ++i) {
+      const int s = s0 + 4 * i;
+      l[i] = s < ns ? lse[(size_t)s * kHeads] : -INFINITY;
+      v[i] = s < ns ? *reinterpret_cast<const float4*>(o + (size_t)s * kHeads * kVDim) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float mb = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+    if (mb > m) {
+      // the maximum rises: what was summed so far is rescaled to it
+      const float c = m == -INFINITY ? 0.f : __expf(m - mb);
+      acc.x *= c;
+      acc.y *= c;
+      acc.z *= c;
+      acc.w *= c;
+      wsum *= c;
+      m = mb;
+    }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (l[i] == -INFINITY) continue;  // an empty split
-        const float w = __expf(l[i] - m);
-        acc.x += w * v[i].x;
-        acc.y += w * v[i].y;
-        acc.z += w * v[i].z;
-        acc.w += w * v[i].w;
-        wsum += w;
-      }
+    for (int i = 0; i < 4; ++i) {
+      if (l[i] == -INFINITY) continue;  // an empty split
+      const float w = __expf(l[i] - m);
+      acc.x += w * v[i].x;
+      acc.y += w * v[i].y;
+      acc.z += w * v[i].z;
+      acc.w += w * v[i].w;
+      wsum += w;
     }
   }
   part[warp][lane] = acc;
-  if (lane == 0) wpart[warp] = wsum;
+  if (lane == 0) {
+    wpart[warp] = wsum;
+    mpart[warp] = m;
+  }
   __syncthreads();
   if (warp == 0) {
-    float4 t = part[0][lane];
-    float ws = wpart[0];
+    const float M = fmaxf(fmaxf(mpart[0], mpart[1]), fmaxf(mpart[2], mpart[3]));
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    float ws = 0.f;
 #pragma unroll
-    for (int w = 1; w < 4; ++w) {
+    for (int w = 0; w < 4; ++w) {
+      if (mpart[w] == -INFINITY) continue;  // no non-empty split in this warp
+      const float c = __expf(mpart[w] - M);
       const float4 y = part[w][lane];
-      t.x += y.x;
-      t.y += y.y;
-      t.z += y.z;
-      t.w += y.w;
-      ws += wpart[w];
+      t.x += c * y.x;
+      t.y += c * y.y;
+      t.z += c * y.z;
+      t.w += c * y.w;
+      ws += c * wpart[w];
     }
     const float inv = ws > 0.f ? 1.f / ws : 0.f;
     uint16_t* out = p.out + ((size_t)b * kHeads + h) * kVDim + f;
     *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16x2(t.x * inv, t.y * inv), pack_bf16x2(t.z * inv, t.w * inv));
-    if (quarter == 0 && lane == 0 && p.lse) p.lse[b * kHeads + h] = ws > 0.f ? m + logf(ws) : -INFINITY;
+    if (quarter == 0 && lane == 0 && p.lse) p.lse[b * kHeads + h] = ws > 0.f ? M + logf(ws) : -INFINITY;
   }
 }
 
