@@ -86,12 +86,14 @@ typedef enum {
  * units c, c + grid, c + 2 grid, ...  (schedule 0).
  *
  * Schedule 1 (contiguous tile ranges) instead lays the sequences' tiles end to
- * end, each sequence weighing w_b = max(1, T_b) tiles, T = sum_b w_b, and gives
- * CTA c of G = grid the tiles [floor(c T / G), floor((c+1) T / G)).  A sequence
- * is split where CTA ranges cut it: with P_b = sum_{b' < b} w_b' and
- * cta(t) = floor(((t + 1) G - 1) / T), S_b = cta(P_b + w_b - 1) - cta(P_b) + 1,
- * split s covers the sequence's tiles in CTA cta(P_b) + s's range, and unit
- * u = sum_{b' < b} S_b' + s.  The planner takes whichever schedule its cost
+ * end, each sequence weighing w_b = max(1, T_b) tiles, T = sum_b w_b, with
+ * U = unit_cost empty positions between consecutive sequences (the weight of
+ * a unit boundary), C = T + U (batch - 1) positions in all, and gives CTA c of
+ * G = grid the positions [floor(c C / G), floor((c+1) C / G)).  Sequence b's
+ * tiles sit at positions X_b + i, X_b = P_b + U b with P_b = sum_{b' < b} w_b';
+ * it is split where CTA ranges cut it: with cta(x) = floor(((x + 1) G - 1) / C),
+ * S_b = cta(X_b + w_b - 1) - cta(X_b) + 1, split s covers the sequence's tiles
+ * in CTA cta(X_b) + s's range, and unit u = sum_{b' < b} S_b' + s.  The planner takes whichever schedule its cost
  * model (the busiest CTA's tiles and units, plus the combine) prefers; a forced
  * split count always uses schedule 0.  Fields are filled by mla_decode_plan and
  * must not be edited.
@@ -112,7 +114,7 @@ typedef struct {
   int32_t total_tiles;    /* schedule 1: T = sum_b max(1, T_b) */
   int32_t page_size;      /* 0: contiguous cache (mla_decode_plan); P >= 64: paged (mla_decode_plan_paged) */
   int32_t num_pages;      /* paged: pages in the cache tensor; 0 otherwise */
-  int32_t reserved[1];
+  int32_t unit_cost;      /* schedule 1: U, empty tile positions between consecutive sequences */
 } mla_plan;
 
 /*

@@ -37,10 +37,10 @@ class mla_plan(ctypes.Structure):
                 ("grid", ctypes.c_int32), ("num_sms", ctypes.c_int32), ("splits_max", ctypes.c_int32),
                 ("tile_tokens", ctypes.c_int32), ("units_per_cta", ctypes.c_int32),
                 ("schedule", ctypes.c_int32), ("total_tiles", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("num_pages", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
+                ("num_pages", ctypes.c_int32), ("unit_cost", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
-        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+        return {k: getattr(self, k) for k, _ in self._fields_}
 
 
 _lock = threading.Lock()

@@ -89,15 +89,23 @@ double plan_cost(const std::vector<int64_t>& lens, int32_t chunk, int32_t cap, i
   return mk;
 }
 
-// Schedule 1 (contiguous tile ranges, see mla_decode.h): CTA c of G owns tiles
-// [c T / G, (c+1) T / G); cta_of(t) is the CTA owning tile t.
-int64_t cta_of(int64_t t, int64_t T, int64_t G) { return ((t + 1) * G - 1) / T; }
+// Schedule 1 (contiguous tile ranges, see mla_decode.h): the sequences' tiles
+// laid end to end with unit_cost empty positions between consecutive
+// sequences; CTA c of G owns positions [c C / G, (c+1) C / G) of the C in
+// all, and cta_of(x) is the CTA owning position x.
+int64_t cta_of(int64_t x, int64_t C, int64_t G) { return ((x + 1) * G - 1) / C; }
 
 struct BalancedPlan {
-  int64_t T = 0, G = 0, work = 0;
-  int32_t smax = 0, max_units = 0;
+  int64_t T = 0, C = 0, G = 0, work = 0;
+  int32_t smax = 0, max_units = 0, unit_cost = 0;
   double cost = -1.0;
 };
+
+// A unit boundary inside a CTA (the epilogue of one unit, the next unit's
+// query and the refill of the ring) costs about two tiles of pipeline time;
+// schedule 1 gives each boundary that weight when the CTAs have at least
+// four tiles each (below that the weight would leave CTAs without tiles).
+constexpr int32_t kScheduleUnitCost = 2;
 
 // The busiest CTA's tiles plus kUnitCost per unit it owns, plus the combine
 // (same model as plan_cost).
@@ -108,27 +116,33 @@ BalancedPlan plan_balanced(const std::vector<int64_t>& lens, int num_sms, int kv
   for (int64_t L : lens) bp.T += L > 0 ? (L + tile - 1) / tile : 1;
   if (bp.T == 0) return bp;
   bp.G = bp.T < num_sms ? bp.T : num_sms;
-  std::vector<int32_t> units(static_cast<size_t>(bp.G) + 1, 0);  // difference array
+  const int64_t B = static_cast<int64_t>(lens.size());
+  bp.unit_cost = bp.T >= (kScheduleUnitCost + 2) * bp.G ? kScheduleUnitCost : 0;
+  bp.C = bp.T + bp.unit_cost * (B - 1);
+  std::vector<int64_t> tiles(static_cast<size_t>(bp.G), 0);
+  std::vector<int32_t> units(static_cast<size_t>(bp.G), 0);
   int64_t P = 0, split_units = 0;
-  for (int64_t L : lens) {
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t L = lens[static_cast<size_t>(b)];
     const int64_t w = L > 0 ? (L + tile - 1) / tile : 1;
-    const int64_t cf = cta_of(P, bp.T, bp.G), cl = cta_of(P + w - 1, bp.T, bp.G);
+    const int64_t x = P + bp.unit_cost * b;  // position of the sequence's first tile
+    const int64_t cf = cta_of(x, bp.C, bp.G), cl = cta_of(x + w - 1, bp.C, bp.G);
     const int64_t s = cl - cf + 1;
     bp.work += s;
     if (s > 1) split_units += s;
     bp.smax = s > bp.smax ? static_cast<int32_t>(s) : bp.smax;
-    units[static_cast<size_t>(cf)] += 1;
-    units[static_cast<size_t>(cl) + 1] -= 1;
+    for (int64_t c = cf; c <= cl; ++c) {
+      const int64_t lo = c * bp.C / bp.G, hi = (c + 1) * bp.C / bp.G;
+      tiles[static_cast<size_t>(c)] += (hi < x + w ? hi : x + w) - (lo > x ? lo : x);
+      units[static_cast<size_t>(c)] += 1;
+    }
     P += w;
   }
   double mk = 0.0;
-  int32_t run = 0;
   for (int64_t c = 0; c < bp.G; ++c) {
-    run += units[static_cast<size_t>(c)];
-    const int64_t tiles = (c + 1) * bp.T / bp.G - c * bp.T / bp.G;
-    const double load = (double)tiles + kUnitCost * run;
+    const double load = (double)tiles[static_cast<size_t>(c)] + kUnitCost * units[static_cast<size_t>(c)];
     mk = load > mk ? load : mk;
-    bp.max_units = run > bp.max_units ? run : bp.max_units;
+    bp.max_units = units[static_cast<size_t>(c)] > bp.max_units ? units[static_cast<size_t>(c)] : bp.max_units;
   }
   if (split_units > 0) {
     const double tile_bytes = (double)tile * rows_bytes(kv_dtype);
@@ -255,7 +269,7 @@ int plan_lengths(const std::vector<int64_t>& lens, int32_t total_kv, int32_t kv_
     // the contiguous schedule, when it is cheaper (or the only one that fits)
     const BalancedPlan bp = plan_balanced(lens, sms, kv_dtype);
     if (bp.cost >= 0.0 && bp.max_units <= mla::max_units_per_cta(kv_dtype) && bp.work <= INT32_MAX &&
-        bp.T <= INT32_MAX && (rr_cost < 0.0 || bp.cost < rr_cost - 1e-9)) {
+        bp.C <= INT32_MAX && (rr_cost < 0.0 || bp.cost < rr_cost - 1e-9)) {
       mla_plan p;
       std::memset(&p, 0, sizeof p);
       p.batch = batch;
@@ -271,6 +285,7 @@ int plan_lengths(const std::vector<int64_t>& lens, int32_t total_kv, int32_t kv_
       p.units_per_cta = bp.max_units;
       p.schedule = 1;
       p.total_tiles = static_cast<int32_t>(bp.T);
+      p.unit_cost = bp.unit_cost;
       *plan = p;
       return MLA_OK;
     }
@@ -431,7 +446,11 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   p->grid = plan->grid;
   p->schedule = plan->schedule;
   p->total_tiles = plan->total_tiles;
+  p->unit_cost = plan->unit_cost;
   if (plan->schedule != 0 && (plan->schedule != 1 || plan->total_tiles < plan->grid)) return MLA_ERR_INVALID_ARG;
+  if (plan->unit_cost < 0 || (plan->schedule == 1 && (int64_t)plan->total_tiles +
+                              (int64_t)plan->unit_cost * (plan->batch > 0 ? plan->batch - 1 : 0) > INT32_MAX))
+    return MLA_ERR_INVALID_ARG;
   if (plan->kv_dtype == MLA_KV_FP8_E4M3) {
     if (!encode_kv_map_tc(&p->tmap_kv64, kv, cache_rows, 128)) return MLA_ERR_CUDA;
     if (page_shift == 6) {

@@ -133,14 +133,16 @@ __device__ __forceinline__ int splits_of(int len, int chunk, int cap) {
 }
 
 // Schedule 1 (contiguous tile ranges): sequence b weighs w_b = max(1, T_b)
-// tiles laid end to end; CTA c owns tiles [c T / G, (c+1) T / G) and takes one
-// unit from every sequence that overlaps its range.
+// tiles, laid end to end with unit_cost empty positions between consecutive
+// sequences (C positions in all); CTA c owns positions [c C / G, (c+1) C / G)
+// and takes one unit from every sequence whose tiles overlap its range.
 template <int TILE, int MAX_UNITS>
 __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, UnitDesc* units, int* s_nunits,
                                                       int lane) {
-  const long long T = p.total_tiles, G = p.grid, c = blockIdx.x;
-  const long long lo = c * T / G, hi = (c + 1) * T / G;
-  auto cta_of = [&](long long t) { return ((t + 1) * G - 1) / T; };
+  const long long T = p.total_tiles, G = p.grid, c = blockIdx.x, U = p.unit_cost;
+  const long long C = T + U * (p.batch > 0 ? p.batch - 1 : 0);
+  const long long lo = c * C / G, hi = (c + 1) * C / G;
+  auto cta_of = [&](long long x) { return ((x + 1) * G - 1) / C; };
   long long tprefix = 0;  // tiles of the sequences before this chunk of 32
   int uprefix = 0, count = 0;
   bool bad = false;
@@ -161,14 +163,15 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
       const int t = __shfl_up_sync(0xffffffffu, wincl, o);
       if (lane >= o) wincl += t;
     }
-    const long long P = tprefix + wincl - w;  // first tile of sequence b
+    const long long P = tprefix + wincl - w;  // tiles before sequence b
+    const long long X = P + U * b;            // position of its first tile
     int sb = 0, cf = 0;
     if (b < p.batch) {
       if (P + w > T) {
         bad = true;  // the device kv_indptr holds more tiles than the plan
       } else {
-        cf = (int)cta_of(P);
-        sb = (int)(cta_of(P + w - 1) - cf + 1);
+        cf = (int)cta_of(X);
+        sb = (int)(cta_of(X + w - 1) - cf + 1);
       }
     }
     int sincl = sb;
@@ -192,7 +195,7 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
       if (pos >= MAX_UNITS || u >= p.num_work) {
         bad = true;
       } else {
-        const long long a = (lo > P ? lo : P) - P, e = (hi < P + w ? hi : P + w) - P;  // the sequence's tiles here
+        const long long a = (lo > X ? lo : X) - X, e = (hi < X + w ? hi : X + w) - X;  // the sequence's tiles here
         UnitDesc d;
         d.b = b;
         d.start = end > start ? start + TILE * (int)a : start;

@@ -16,24 +16,31 @@ def n_splits(plan, L):
     return max(1, min(plan.max_splits, -(-L // plan.chunk_tokens), -(-L // plan.tile_tokens)))
 
 
-def cta_of(t, T, G):
-    return ((t + 1) * G - 1) // T
+def cta_of(x, C, G):
+    return ((x + 1) * G - 1) // C
 
 
-def contiguous_units(plan, lens):
-    """Schedule 1 (mla_decode.h): per sequence its splits, each (start, end, cta)."""
-    R, G = plan.tile_tokens, plan.grid
+def positions(plan, lens):
+    """Schedule 1 (mla_decode.h): tiles per sequence, first-tile positions, C."""
+    R, U = plan.tile_tokens, plan.unit_cost
     w = [max(1, -(-L // R)) for L in lens]
     T = sum(w)
     assert plan.total_tiles == T
-    out, P, start = [], 0, 0
-    for L, wb in zip(lens, w):
-        cf, cl = cta_of(P, T, G), cta_of(P + wb - 1, T, G)
+    X = [sum(w[:b]) + U * b for b in range(len(w))]
+    return w, X, T + U * max(0, len(w) - 1)
+
+
+def contiguous_units(plan, lens):
+    """Schedule 1 (mla_decode.h): per sequence its splits, each (start, end)."""
+    R, G = plan.tile_tokens, plan.grid
+    w, X, C = positions(plan, lens)
+    out, start = [], 0
+    for L, wb, x in zip(lens, w, X):
+        cf, cl = cta_of(x, C, G), cta_of(x + wb - 1, C, G)
         for c in range(cf, cl + 1):
-            lo, hi = c * T // G, (c + 1) * T // G
-            a, e = max(lo, P) - P, min(hi, P + wb) - P
+            lo, hi = c * C // G, (c + 1) * C // G
+            a, e = max(lo, x) - x, min(hi, x + wb) - x
             out.append((start + R * a, min(start + L, start + R * e)) if L > 0 else (start, start))
-        P += wb
         start += max(L, 0)
     return out
 
@@ -55,31 +62,29 @@ def units_of(plan, lens):
 
 
 def check_contiguous(plan, lens):
-    """Schedule 1: every CTA's tiles are contiguous and within one tile of T / G."""
-    R, G, T = plan.tile_tokens, plan.grid, plan.total_tiles
-    per_cta = [0] * G
+    """Schedule 1: every CTA's range is within one position of C / G, no CTA is
+    left without tiles, and the unit count per CTA matches the plan."""
+    G = plan.grid
+    w, X, C = positions(plan, lens)
     for c in range(G):
-        n = (c + 1) * T // G - c * T // G
-        assert n in (T // G, -(-T // G))
-    P = 0
-    for L in lens:
-        wb = max(1, -(-L // R))
-        for c in range(cta_of(P, T, G), cta_of(P + wb - 1, T, G) + 1):
+        n = (c + 1) * C // G - c * C // G
+        assert n in (C // G, -(-C // G))
+    per_cta, tiles = [0] * G, [0] * G
+    for wb, x in zip(w, X):
+        for c in range(cta_of(x, C, G), cta_of(x + wb - 1, C, G) + 1):
             per_cta[c] += 1
-        P += wb
+            tiles[c] += min((c + 1) * C // G, x + wb) - max(c * C // G, x)
     assert max(per_cta) == plan.units_per_cta
+    assert min(tiles) >= 1, "a CTA without tiles"
+    assert sum(tiles) == sum(w)
 
 
 def n_splits_of(plan, lens):
     if plan.schedule == 0:
         return [n_splits(plan, L) for L in lens]
-    R, G, T = plan.tile_tokens, plan.grid, plan.total_tiles
-    out, P = [], 0
-    for L in lens:
-        wb = max(1, -(-L // R))
-        out.append(cta_of(P + wb - 1, T, G) - cta_of(P, T, G) + 1)
-        P += wb
-    return out
+    G = plan.grid
+    w, X, C = positions(plan, lens)
+    return [cta_of(x + wb - 1, C, G) - cta_of(x, C, G) + 1 for wb, x in zip(w, X)]
 
 
 def check_plan(lens, dtype="fp8", num_sms=152, num_splits=0):
