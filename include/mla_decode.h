@@ -139,6 +139,11 @@ MLA_API size_t mla_decode_workspace_bytes(const mla_plan* plan);
  * mla_decode_fwd -- enqueue one decode on `stream` (a cudaStream_t; NULL = the
  * legacy default stream).  Asynchronous: returns after launching.
  *
+ * "device" below means memory the GPU can address: device memory, or pinned
+ * (page-locked, CUDA-registered) host memory, which the kernels then read or
+ * write across the host link.  The KV cache, its scales and the workspace
+ * must be device memory, and so must q for bf16 KV (fetched by bulk copies).
+ *
  *   q          device, bf16 [*, 16, 576] row-major; sequence b uses row qo_indptr[b].
  *              16-byte aligned.
  *   kv         device, see the storage table above; rows [0, plan->total_kv) are read.

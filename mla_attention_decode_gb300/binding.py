@@ -137,7 +137,7 @@ def mla_decode_fwd(q, kv, kv_scale, kv_indptr, qo_indptr, out, lse, plan: mla_pl
     tensors are CUDA tensors; ``workspace`` is a uint8 tensor of at least
     ``mla_decode_workspace_bytes(plan)`` bytes."""
     if stream is None:
-        stream = torch.cuda.current_stream(q.device)
+        stream = torch.cuda.current_stream(kv.device)  # q may be pinned host memory
     handle = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
     rc = load_library().mla_decode_fwd(_ptr(q), _ptr(kv), _ptr(kv_scale), int(scale_stride), _ptr(kv_indptr),
                                        _ptr(qo_indptr), _ptr(out), _ptr(lse), float(sm_scale), ctypes.byref(plan),
@@ -155,7 +155,7 @@ def mla_decode_fwd_paged(q, kv_pages, kv_scale, kv_page_indptr, kv_indices, kv_l
                                              _ptr(qo_indptr), _ptr(out), _ptr(lse), float(sm_scale),
                                              ctypes.byref(plan), _ptr(workspace),
                                              int(workspace.numel() * workspace.element_size()),
-                                             _stream_handle(stream, q.device))
+                                             _stream_handle(stream, kv_pages.device))
     if rc != MLA_OK:
         raise MLAError(rc, "mla_decode_fwd_paged")
 
@@ -173,7 +173,7 @@ def mla_decode_split(q, kv, kv_scale, kv_indptr, qo_indptr, out, lse, plan: mla_
                                          _ptr(qo_indptr), _ptr(out), _ptr(lse), float(sm_scale),
                                          ctypes.byref(plan), _ptr(workspace),
                                          int(workspace.numel() * workspace.element_size()),
-                                         _stream_handle(stream, q.device))
+                                         _stream_handle(stream, kv.device))
     if rc != MLA_OK:
         raise MLAError(rc, "mla_decode_split")
 
@@ -209,7 +209,7 @@ def mla_decode_fwd_static(q, kv, kv_scale, kv_indptr, qo_indptr, out, lse, plan:
         fn.argtypes = [P, P, P, i32, P, P, P, P, ctypes.c_float, ctypes.POINTER(mla_plan), P, P]
         fn.restype = ctypes.c_int
     rc = fn(_ptr(q), _ptr(kv), _ptr(kv_scale), int(scale_stride), _ptr(kv_indptr), _ptr(qo_indptr), _ptr(out),
-            _ptr(lse), float(sm_scale), ctypes.byref(plan), _ptr(device_error), _stream_handle(stream, q.device))
+            _ptr(lse), float(sm_scale), ctypes.byref(plan), _ptr(device_error), _stream_handle(stream, kv.device))
     if rc != MLA_OK:
         raise MLAError(rc, "mla_decode_fwd_static")
 
@@ -230,9 +230,9 @@ class MLADecoder:
                  sm_scale: float = SM_SCALE, stream=None):
         batch = self.plan.batch
         if out is None:
-            out = torch.empty(batch, 16, 512, dtype=torch.bfloat16, device=q.device)
+            out = torch.empty(batch, 16, 512, dtype=torch.bfloat16, device=self.workspace.device)
         if lse is None:
-            lse = torch.empty(batch, 16, dtype=torch.float32, device=q.device)
+            lse = torch.empty(batch, 16, dtype=torch.float32, device=self.workspace.device)
         scale_stride = int(kv_scale.stride(0)) if (self.kv_dtype == MLA_KV_MXFP4 and kv_scale is not None) else 0
         mla_decode_fwd(q, kv, kv_scale, kv_indptr, qo_indptr, out, lse, self.plan, self.workspace,
                        sm_scale=sm_scale, scale_stride=scale_stride, stream=stream)
@@ -257,9 +257,9 @@ class PagedMLADecoder:
                  out=None, lse=None, sm_scale: float = SM_SCALE, stream=None):
         batch = self.plan.batch
         if out is None:
-            out = torch.empty(batch, 16, 512, dtype=torch.bfloat16, device=q.device)
+            out = torch.empty(batch, 16, 512, dtype=torch.bfloat16, device=self.workspace.device)
         if lse is None:
-            lse = torch.empty(batch, 16, dtype=torch.float32, device=q.device)
+            lse = torch.empty(batch, 16, dtype=torch.float32, device=self.workspace.device)
         scale_stride = int(kv_scale.stride(0)) if (self.kv_dtype == MLA_KV_MXFP4 and kv_scale is not None) else 0
         mla_decode_fwd_paged(q, kv_pages, kv_scale, kv_page_indptr, kv_indices, kv_last_page_len, qo_indptr, out,
                              lse, self.plan, self.workspace, sm_scale=sm_scale, scale_stride=scale_stride,
