@@ -111,8 +111,12 @@ def quantize_mxfp4(kv_bf16: torch.Tensor):
     return torch.from_numpy(np.ascontiguousarray(packed)), torch.from_numpy(np.ascontiguousarray(e8))
 
 
-def make_inputs(kv_lens, kv_dtype: str = "bf16", seed: int = 0, q_mult: float = 1.0) -> MLAInputs:
-    """Draw one decode batch.  ``kv_lens``: list of per-sequence lengths."""
+def make_inputs(kv_lens, kv_dtype: str = "bf16", seed: int = 0, q_mult: float = 1.0,
+                block_spread: int = 0) -> MLAInputs:
+    """Draw one decode batch.  ``kv_lens``: list of per-sequence lengths.
+    ``block_spread`` > 0 scales the 32-element blocks 3j+1 and 3j+2 of every KV
+    row by 2^-block_spread and 2^-2 block_spread before quantisation (rows
+    whose block scales differ widely)."""
     if kv_dtype not in KV_DTYPES:
         raise ValueError(f"kv_dtype must be one of {KV_DTYPES}")
     lens = [int(x) for x in kv_lens]
@@ -122,7 +126,13 @@ def make_inputs(kv_lens, kv_dtype: str = "bf16", seed: int = 0, q_mult: float = 
     n = int(sum(lens))
     g = torch.Generator("cpu").manual_seed(int(seed))
     q = (torch.randn(b, NUM_HEADS, QK_DIM, generator=g, dtype=torch.float32) * q_mult).to(torch.bfloat16)
-    kv_bf16 = torch.randn(n, QK_DIM, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    kv_f = torch.randn(n, QK_DIM, generator=g, dtype=torch.float32)
+    if block_spread:
+        gain = torch.ones(QK_DIM // MX_BLOCK, dtype=torch.float32)
+        gain[1::3] = 2.0 ** -block_spread
+        gain[2::3] = 2.0 ** (-2 * block_spread)
+        kv_f = kv_f * gain.repeat_interleave(MX_BLOCK)
+    kv_bf16 = kv_f.to(torch.bfloat16)
     ind = torch.zeros(b + 1, dtype=torch.int32)
     if b:
         ind[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)

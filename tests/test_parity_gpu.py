@@ -275,3 +275,14 @@ def test_benchmark_workload_bs64_kv8192_fp8_sampled(orc):
     ref, ref_lse = oracle_decode(orc, inp, seqs=seqs)
     assert_parity(got[seqs], ref, lse[seqs], ref_lse, "bs64_kv8192_fp8 sampled", v_absmax(inp, seqs))
     assert dec.poll_error() == 0
+
+
+@pytest.mark.parametrize("spread", [6, 12])
+def test_mxfp4_wide_block_exponents(orc, spread):
+    """MXFP4 rows whose block scales lie up to 2 x spread below the row's
+    largest: the kernel's e4m3 copy is exact within 8 of the largest exponent
+    and rounds smaller blocks to e4m3's subnormal grid, which the bound covers."""
+    inp = synth.make_inputs([700, 1, 2500, 130], "mxfp4", seed=spread, block_spread=spread)
+    got, lse, _ = gpu_decode(inp)
+    ref, ref_lse = oracle_decode(orc, inp)
+    assert_parity(got, ref, lse, ref_lse, f"mxfp4 block spread {spread}", v_absmax(inp))
