@@ -64,6 +64,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_mla_decode.restype = i32
     lib.oracle_mla_decode_paged.argtypes = [i32, P, P, P, i64, dbl, P, P, P, i32, i64, P, i32, dbl, P, P, i32]
     lib.oracle_mla_decode_paged.restype = i32
+    lib.oracle_mla_decode_multi.argtypes = [i32, P, P, P, i64, dbl, P, P, i32, i32, dbl, P, P, i32]
+    lib.oracle_mla_decode_multi.restype = i32
     lib.oracle_mla_partial.argtypes = [i32, P, P, P, i64, dbl, i64, i64, i64, dbl, P, P]
     lib.oracle_mla_partial.restype = i32
     lib.oracle_mla_combine.argtypes = [i32, P, P, P, P]
@@ -187,6 +189,26 @@ class Oracle:
                                               _ptr(out), _ptr(lse), int(num_threads))
         if rc != 0:
             raise ValueError("oracle_mla_decode_paged rejected its arguments")
+        return out, lse
+
+    def decode_multi(self, kv_dtype: int, q, kv, kv_indptr, q_len: int, qo_indptr=None, kv_scale=None,
+                     block_scales=None, sm_scale: float = SM_SCALE, num_threads: int = 0):
+        """q_len query tokens per sequence: token i of sequence b (query row
+        qo_indptr[b] + i) attends causally to the first L_b - (q_len - 1 - i) rows.
+        Returns (out [B*q_len,16,512], lse [B*q_len,16]) in (b, i) order."""
+        q_a = _u16(q)
+        kv_a, sc, bs, stride = self._kv_args(kv_dtype, kv, kv_scale, block_scales)
+        ind = np.ascontiguousarray(np.asarray(kv_indptr, dtype=np.int32))
+        batch = ind.size - 1
+        qo = (np.arange(batch + 1, dtype=np.int32) * int(q_len) if qo_indptr is None
+              else np.ascontiguousarray(np.asarray(qo_indptr, dtype=np.int32)))
+        out = np.zeros((batch * q_len, NUM_HEADS, V_DIM), dtype=np.float64)
+        lse = np.zeros((batch * q_len, NUM_HEADS), dtype=np.float64)
+        rc = self.lib.oracle_mla_decode_multi(kv_dtype, _ptr(q_a), _ptr(kv_a), _ptr(bs), stride, sc, _ptr(ind),
+                                              _ptr(qo), batch, int(q_len), float(sm_scale), _ptr(out), _ptr(lse),
+                                              int(num_threads))
+        if rc != 0:
+            raise ValueError("oracle_mla_decode_multi rejected its arguments")
         return out, lse
 
     def partial(self, kv_dtype: int, q, kv, qrow: int, start: int, end: int, kv_scale=None,

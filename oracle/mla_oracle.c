@@ -350,6 +350,53 @@ int oracle_mla_decode_paged(int kv_dtype, const uint16_t* q, const void* kv, con
 }
 
 /*
+ * Several query tokens per sequence (q_len > 1: the decode of q_len draft or
+ * verification tokens at once).  The pages decode one token per sequence;
+ * this is the plain causal reading for more: sequence b's tokens are query
+ * rows qo_indptr[b] + i (i < q_len) and the last q_len of its L_b cached rows
+ * are those tokens' own entries, so token i attends to the first
+ * L_b - (q_len - 1 - i) rows [kv_indptr[b], kv_indptr[b+1] - (q_len - 1 - i))
+ * (none when that is not positive: out = 0, lse = -inf).  Outputs are in
+ * (b, i) order: out [batch * q_len, 16, 512], lse [batch * q_len, 16].
+ */
+int oracle_mla_decode_multi(int kv_dtype, const uint16_t* q, const void* kv, const uint8_t* block_scales,
+                            int64_t scale_stride, double kv_scale, const int32_t* kv_indptr,
+                            const int32_t* qo_indptr, int batch, int q_len, double sm_scale, double* out,
+                            double* lse, int num_threads) {
+  if (batch < 0 || q_len < 1 || !kv_indptr || !qo_indptr || !out || !lse) return -1;
+  if (kv_dtype < 0 || kv_dtype > 2) return -1;
+  if (kv_dtype == ORACLE_KV_MXFP4 && (!block_scales || scale_stride < ORACLE_QK_DIM / ORACLE_MX_BLOCK)) return -1;
+  int64_t Lmax = max_len(kv_indptr, batch);
+  int64_t pairs = (int64_t)batch * q_len * ORACLE_NUM_HEADS;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel
+#endif
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(Lmax > 0 ? Lmax : 1));
+    double qv[ORACLE_QK_DIM], k[ORACLE_QK_DIM];
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+    for (int64_t pr = 0; pr < pairs; ++pr) {
+      const int64_t t = pr / ORACLE_NUM_HEADS;  /* (b, i) in order */
+      const int b = (int)(t / q_len), i = (int)(t % q_len), h = (int)(pr % ORACLE_NUM_HEADS);
+#if ORACLE_MUTANT == 13
+      int64_t end = (int64_t)kv_indptr[b + 1] - (q_len - i); /* mistake: the token's own row left out */
+#else
+      int64_t end = (int64_t)kv_indptr[b + 1] - (q_len - 1 - i);
+#endif
+      if (end < kv_indptr[b]) end = kv_indptr[b];
+      widen_q(q, (int64_t)qo_indptr[b] + i, h, qv);
+      attend_one(kv_dtype, qv, kv, block_scales, scale_stride, kv_scale, kv_indptr[b], end, NULL, sm_scale,
+                 out + pr * ORACLE_V_DIM, lse + pr, scores, k);
+    }
+    free(scores);
+  }
+  return 0;
+}
+
+/*
  * One split: the normalised partial attention of query row qrow over KV rows
  * [start, end), all 16 heads.  o: [16, 512]; lse: [16].  An empty range gives
  * o = 0 and lse = -inf.

@@ -311,11 +311,42 @@ def pin_paged_cache(orc):
             assert np.array_equal(lse, ref_lse), f"paged {dt} P={page_size}: lse differs"
 
 
+def pin_multi_token_causal(orc):
+    """q_len query tokens per sequence, the causal reading: token i sees the
+    first L - (q_len - 1 - i) rows.  Checked against torch float64
+    scaled_dot_product_attention with an explicit causal mask (a library
+    routine), and q_len = 1 against the single-token decode."""
+    for dt in ("bf16", "fp8", "mxfp4"):
+        q_len = 3
+        base = synth.make_inputs([5, 40, 3], dt, seed=17)
+        qg = torch.Generator("cpu").manual_seed(5)
+        q = torch.randn(3 * q_len, 16, 576, generator=qg).to(torch.bfloat16)
+        out, lse = orc.decode_multi(KV_CODES[dt], q, base.kv, base.kv_indptr, q_len,
+                                    kv_scale=None if base.kv_scale is None else base.kv_scale.numpy(),
+                                    block_scales=None if base.block_scales is None else base.block_scales.numpy())
+        k_all = torch.from_numpy(lib_dequant(base))
+        ind = base.kv_indptr.tolist()
+        for b in range(3):
+            k = k_all[ind[b]:ind[b + 1]]
+            L = k.shape[0]
+            qb = q[b * q_len:(b + 1) * q_len].to(torch.float64).transpose(0, 1)  # [16, q_len, 576]
+            mask = torch.arange(L)[None, :] <= (L - q_len + torch.arange(q_len))[:, None]
+            ref = F.scaled_dot_product_attention(qb, k[None], k[None, :, :512], attn_mask=mask[None],
+                                                 scale=1.0 / 24.0).transpose(0, 1)
+            _close(out[b * q_len:(b + 1) * q_len], ref.numpy(), 1e-11, f"multi-token {dt} b={b}")
+        one, lse1 = orc.decode_multi(KV_CODES[dt], base.q, base.kv, base.kv_indptr, 1,
+                                     kv_scale=None if base.kv_scale is None else base.kv_scale.numpy(),
+                                     block_scales=None if base.block_scales is None else base.block_scales.numpy())
+        ref1, rlse1 = run(orc, base)
+        _close(one, ref1, 1e-14, f"multi-token q_len=1 {dt}")
+        _close(lse1, rlse1, 1e-14, f"multi-token q_len=1 lse {dt}")
+
+
 ALL_PINS = [
     pin_e4m3_all_codes, pin_e2m1_table, pin_e8m0_closed_form, pin_bf16_widen, pin_constants,
     pin_sdpa_bf16, pin_sdpa_fp8, pin_sdpa_mxfp4, pin_identical_rows, pin_single_row,
     pin_zero_query, pin_permutation_and_isolation, pin_large_logits, pin_split_combine,
-    pin_empty_sequence, pin_qo_indptr, pin_paged_cache,
+    pin_empty_sequence, pin_qo_indptr, pin_paged_cache, pin_multi_token_causal,
 ]
 
 # Planted mistakes compiled into oracle variants (see mla_oracle.c, ORACLE_MUTANT).
@@ -332,4 +363,5 @@ MUTANTS = {
     10: "e4m3 subnormals decoded as normals",
     11: "paged cache: the last page read in full",
     12: "paged cache: the page table ignored",
+    13: "multi-token: a token's own row left out",
 }
