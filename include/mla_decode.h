@@ -115,6 +115,8 @@ typedef struct {
   int32_t page_size;      /* 0: contiguous cache (mla_decode_plan); P >= 64: paged (mla_decode_plan_paged) */
   int32_t num_pages;      /* paged: pages in the cache tensor; 0 otherwise */
   int32_t unit_cost;      /* schedule 1: U, empty tile positions between consecutive sequences */
+  int32_t q_len;          /* query tokens per sequence (0 or 1: one; see mla_decode_plan_multi) */
+  int32_t reserved[3];
 } mla_plan;
 
 /*
@@ -192,6 +194,27 @@ MLA_API int mla_decode_combine(void* out, float* lse, const mla_plan* plan, void
  * Returns MLA_OK when the word was clear.  For tests and debugging.
  */
 MLA_API int mla_decode_poll_error(void* workspace, void* stream);
+
+/*
+ * Several query tokens per sequence (q_len > 1), e.g. draft tokens checked in
+ * one step.  The pages decode one token per sequence; this is the causal
+ * reading for more: sequence b's tokens are query rows qo_indptr[b] + i
+ * (i < q_len), the last q_len of its L_b cached rows are those tokens' own
+ * entries, and token i attends to the first L_b - (q_len - 1 - i) rows
+ * [kv_indptr[b], kv_indptr[b+1] - (q_len - 1 - i)) (none when that is not
+ * positive: out = 0, lse = -inf).  The decode treats each token as a sequence
+ * of its own over its visible rows, so the cache rows of a sequence are read
+ * once per token.
+ *
+ * mla_decode_plan_multi -- as mla_decode_plan for num_seqs sequences of
+ * q_len (1..16) tokens each; the plan's batch is num_seqs * q_len (one output
+ * row per token) and its rule applies to the tokens' row ranges in (b, i)
+ * order.  mla_decode_fwd with such a plan reads q rows qo_indptr[b] + i and
+ * writes out [num_seqs * q_len, 16, 512] and lse [num_seqs * q_len, 16] in
+ * (b, i) order.  Returns the status codes of mla_decode_plan.
+ */
+MLA_API int mla_decode_plan_multi(const int32_t* kv_indptr_host, int32_t num_seqs, int32_t q_len, int32_t kv_dtype,
+                                  int32_t num_sms, int32_t num_splits, mla_plan* plan);
 
 /*
  * Paged KV cache (kernelindex "amd-mixed-mla" submission 703488: AITER's

@@ -37,10 +37,11 @@ class mla_plan(ctypes.Structure):
                 ("grid", ctypes.c_int32), ("num_sms", ctypes.c_int32), ("splits_max", ctypes.c_int32),
                 ("tile_tokens", ctypes.c_int32), ("units_per_cta", ctypes.c_int32),
                 ("schedule", ctypes.c_int32), ("total_tiles", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("num_pages", ctypes.c_int32), ("unit_cost", ctypes.c_int32)]
+                ("num_pages", ctypes.c_int32), ("unit_cost", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 3)]
 
     def as_dict(self) -> dict:
-        return {k: getattr(self, k) for k, _ in self._fields_}
+        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
 
 
 _lock = threading.Lock()
@@ -65,6 +66,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.mla_decode_fwd.argtypes = [P, P, P, i32, P, P, P, P, ctypes.c_float, ctypes.POINTER(mla_plan), P,
                                        ctypes.c_size_t, P]
         lib.mla_decode_fwd.restype = ctypes.c_int
+        lib.mla_decode_plan_multi.argtypes = [P, i32, i32, i32, i32, i32, ctypes.POINTER(mla_plan)]
+        lib.mla_decode_plan_multi.restype = ctypes.c_int
         lib.mla_decode_plan_paged.argtypes = [P, P, i32, i32, i32, i32, i32, i32, ctypes.POINTER(mla_plan)]
         lib.mla_decode_plan_paged.restype = ctypes.c_int
         lib.mla_decode_fwd_paged.argtypes = [P, P, P, i32, P, P, P, P, P, P, ctypes.c_float,
@@ -104,6 +107,18 @@ def mla_decode_plan(kv_indptr_host, kv_dtype, num_sms: int = 0, num_splits: int 
                                         _dtype_code(kv_dtype), int(num_sms), int(num_splits), ctypes.byref(plan))
     if rc != MLA_OK:
         raise MLAError(rc, "mla_decode_plan")
+    return plan
+
+
+def mla_decode_plan_multi(kv_indptr_host, q_len: int, kv_dtype, num_sms: int = 0, num_splits: int = 0) -> mla_plan:
+    """Host planner for q_len query tokens per sequence (see mla_decode.h)."""
+    ind = torch.as_tensor(kv_indptr_host, dtype=torch.int32, device="cpu").contiguous()
+    plan = mla_plan()
+    rc = load_library().mla_decode_plan_multi(ctypes.c_void_p(ind.data_ptr()), int(ind.numel() - 1), int(q_len),
+                                              _dtype_code(kv_dtype), int(num_sms), int(num_splits),
+                                              ctypes.byref(plan))
+    if rc != MLA_OK:
+        raise MLAError(rc, "mla_decode_plan_multi")
     return plan
 
 
@@ -220,9 +235,13 @@ class MLADecoder:
     The workspace is allocated once here (torch device memory) and zeroed; the
     library itself never allocates."""
 
-    def __init__(self, kv_indptr_host, kv_dtype, device="cuda", num_sms: int = 0, num_splits: int = 0):
+    def __init__(self, kv_indptr_host, kv_dtype, device="cuda", num_sms: int = 0, num_splits: int = 0,
+                 q_len: int = 1):
         self.kv_dtype = _dtype_code(kv_dtype)
-        self.plan = mla_decode_plan(kv_indptr_host, self.kv_dtype, num_sms, num_splits)
+        if q_len > 1:
+            self.plan = mla_decode_plan_multi(kv_indptr_host, q_len, self.kv_dtype, num_sms, num_splits)
+        else:
+            self.plan = mla_decode_plan(kv_indptr_host, self.kv_dtype, num_sms, num_splits)
         nbytes = max(256, mla_decode_workspace_bytes(self.plan))
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=device)
 

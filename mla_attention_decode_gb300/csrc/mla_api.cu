@@ -334,6 +334,31 @@ int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dty
   return plan_lengths(lens, kv_indptr_host[batch], kv_dtype, num_sms, num_splits, plan);
 }
 
+int mla_decode_plan_multi(const int32_t* kv_indptr_host, int32_t num_seqs, int32_t q_len, int32_t kv_dtype,
+                          int32_t num_sms, int32_t num_splits, mla_plan* plan) {
+  if (!kv_indptr_host || !plan) return MLA_ERR_INVALID_ARG;
+  if (q_len < 1 || q_len > 16) return MLA_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || (int64_t)num_seqs * q_len > MLA_MAX_BATCH) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype < MLA_KV_BF16 || kv_dtype > MLA_KV_MXFP4) return MLA_ERR_UNSUPPORTED;
+  if (num_splits < 0) return MLA_ERR_INVALID_ARG;
+  if (kv_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
+  std::vector<int64_t> lens(static_cast<size_t>(num_seqs) * q_len);
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    const int64_t L = (int64_t)kv_indptr_host[b + 1] - kv_indptr_host[b];
+    if (L < 0) return MLA_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < q_len; ++i) {
+      const int64_t Li = L - (q_len - 1 - i);  // the rows up to token i's own entry
+      lens[static_cast<size_t>(b) * q_len + i] = Li > 0 ? Li : 0;
+    }
+  }
+  mla_plan p;
+  const int rc = plan_lengths(lens, kv_indptr_host[num_seqs], kv_dtype, num_sms, num_splits, &p);
+  if (rc != MLA_OK) return rc;
+  p.q_len = q_len;
+  *plan = p;
+  return MLA_OK;
+}
+
 int mla_decode_plan_paged(const int32_t* kv_page_indptr_host, const int32_t* kv_last_page_len_host, int32_t batch,
                           int32_t page_size, int32_t num_pages, int32_t kv_dtype, int32_t num_sms,
                           int32_t num_splits, mla_plan* plan) {
@@ -447,6 +472,8 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   p->schedule = plan->schedule;
   p->total_tiles = plan->total_tiles;
   p->unit_cost = plan->unit_cost;
+  p->q_len = plan->q_len > 1 ? plan->q_len : 1;
+  if (plan->q_len > 16 || (p->q_len > 1 && (paged || plan->batch % p->q_len != 0))) return MLA_ERR_INVALID_ARG;
   if (plan->schedule != 0 && (plan->schedule != 1 || plan->total_tiles < plan->grid)) return MLA_ERR_INVALID_ARG;
   if (plan->unit_cost < 0 || (plan->schedule == 1 && (int64_t)plan->total_tiles +
                               (int64_t)plan->unit_cost * (plan->batch > 0 ? plan->batch - 1 : 0) > INT32_MAX))

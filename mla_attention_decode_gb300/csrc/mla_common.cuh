@@ -44,6 +44,14 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
 // kv_indptr[b] * P + i (i below the sequence's token count: P rows per page,
 // kv_last[b] in the last one).  False for a layout the rules forbid.
 __device__ __forceinline__ bool seq_rows(const Stage1Params& p, int b, int& start, int& end) {
+  if (p.q_len > 1) {
+    // token b % q_len of sequence b / q_len: the rows up to its own entry
+    const int s = b / p.q_len, i = b - s * p.q_len;
+    const int a = p.kv_indptr[s], z = p.kv_indptr[s + 1];
+    start = a;
+    end = max(a, z - (p.q_len - 1 - i));
+    return a >= 0 && z >= a;
+  }
   const int a = p.kv_indptr[b], z = p.kv_indptr[b + 1];
   if (p.page_shift == 0) {
     start = a;
@@ -59,6 +67,16 @@ __device__ __forceinline__ bool seq_rows(const Stage1Params& p, int b, int& star
     end = start + ((z - a - 1) << p.page_shift) + last;
   }
   return true;
+}
+
+// Query row of output row b (a sequence, or with several tokens per sequence
+// token b % q_len of sequence b / q_len).
+__device__ __forceinline__ int query_row(const Stage1Params& p, int b) {
+  if (p.q_len > 1) {
+    const int s = b / p.q_len;
+    return p.qo_indptr[s] + (b - s * p.q_len);
+  }
+  return p.qo_indptr[b];
 }
 
 // Cache row of row-space position v (a row of some sequence): v itself, or for
@@ -150,7 +168,7 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
     const int b = b0 + lane;
     int start = 0, end = 0, qrow = 0, w = 0;
     if (b < p.batch) {
-      qrow = p.qo_indptr[b];
+      qrow = query_row(p, b);
       if (!seq_rows(p, b, start, end) || end > p.total_kv || qrow < 0) {
         bad = true;
         start = end = qrow = 0;
@@ -229,7 +247,7 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
     const int b = b0 + lane;
     int start = 0, end = 0, sb = 0, qrow = 0;
     if (b < p.batch) {
-      qrow = p.qo_indptr[b];
+      qrow = query_row(p, b);
       if (!seq_rows(p, b, start, end) || end > p.total_kv || qrow < 0) {
         bad = true;
         start = end = 0;

@@ -79,6 +79,7 @@ struct Stage1Params {
   int32_t schedule;     // 0: round-robin splits, 1: contiguous tile ranges
   int32_t total_tiles;  // schedule 1: sum of the sequences' weights in tiles
   int32_t unit_cost;    // schedule 1: empty positions between consecutive sequences
+  int32_t q_len;        // query tokens per sequence; batch counts tokens
 };
 
 struct CombineParams {

@@ -26,10 +26,10 @@ __global__ void __launch_bounds__(64) mla_prep_q_kernel(const __grid_constant__ 
   pdl_wait_primary();      // q and qo_indptr written by earlier work are visible
   pdl_launch_dependents();  // the split kernel may begin its set-up
   const int b = blockIdx.x, j = threadIdx.x;
-  const int qrow = p.qo_indptr[b];
+  const int qrow = query_row(p, b);
   // bring the sequence's kv_indptr entries into L2 for the split kernel's unit
   // scan (the comparison only keeps the load; offsets are never negative)
-  if (j == 0 && __ldg(p.kv_indptr + b) < 0) p.ws_err[1] = 1;
+  if (j == 0 && __ldg(p.kv_indptr + (p.q_len > 1 ? b / p.q_len : b)) < 0) p.ws_err[1] = 1;
   if (qrow < 0) return;  // the split kernel reports the bad index
   const int h = j >> 2, part = j & 3;
   const float kv_scale = kMx ? 1.f : *static_cast<const float*>(p.kv_scale);

@@ -286,3 +286,33 @@ def test_mxfp4_wide_block_exponents(orc, spread):
     got, lse, _ = gpu_decode(inp)
     ref, ref_lse = oracle_decode(orc, inp)
     assert_parity(got, ref, lse, ref_lse, f"mxfp4 block spread {spread}", v_absmax(inp))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("q_len,lens,num_splits", [
+    (2, [1000, 1, 0, 64, 2500], 0),
+    (3, [3000, 2, 129, 700], 0),
+    (4, [260, 5000], 3),
+])
+def test_multi_token(orc, dtype, q_len, lens, num_splits):
+    """q_len query tokens per sequence, each attending to the cache rows up to
+    its own entry (the causal reading); tokens with no visible row give 0 and
+    -inf."""
+    inp = synth.make_inputs(lens, dtype, seed=q_len + 100)
+    g = torch.Generator("cpu").manual_seed(q_len)
+    q = torch.randn(len(lens) * q_len, 16, 576, generator=g).to(torch.bfloat16)
+    qo = torch.arange(len(lens) + 1, dtype=torch.int32) * q_len
+    dev = torch.device("cuda:0")
+    dec = binding.MLADecoder(inp.kv_indptr, dtype, device=dev, num_splits=num_splits, q_len=q_len)
+    assert dec.plan.batch == len(lens) * q_len
+    scale = {"bf16": None, "fp8": inp.kv_scale, "mxfp4": inp.block_scales}[dtype]
+    out, lse = dec(q.to(dev), inp.kv.to(dev), inp.kv_indptr.to(dev), qo.to(dev),
+                   kv_scale=None if scale is None else scale.to(dev))
+    torch.cuda.synchronize()
+    assert dec.poll_error() == 0
+    ref, ref_lse = orc.decode_multi(CODES[dtype], q, inp.kv, inp.kv_indptr, q_len, qo,
+                                    kv_scale=None if inp.kv_scale is None else inp.kv_scale.numpy(),
+                                    block_scales=None if inp.block_scales is None else inp.block_scales.numpy())
+    vmax = np.repeat(v_absmax(inp), q_len, axis=0)
+    assert_parity(out.double().cpu().numpy(), ref, lse.double().cpu().numpy(), ref_lse,
+                  f"multi-token {dtype} q_len={q_len}", vmax)

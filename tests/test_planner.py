@@ -205,3 +205,31 @@ def test_paged_plan_rules():
         assert e.value.status == binding.MLA_ERR_INVALID_ARG
     plan = binding.mla_decode_plan_paged([0, 0, 3], [0, 7], 64, 3, "fp8", num_sms=152)
     assert plan.total_kv == 192 and plan.page_size == 64
+
+
+def test_multi_token_plan_matches_token_lengths():
+    """q_len tokens per sequence plan like the batch of the tokens' visible
+    lengths L_b - (q_len - 1 - i), one output row per token."""
+    rng = random.Random(11)
+    for _ in range(60):
+        b = rng.randint(1, 30)
+        q_len = rng.choice([2, 3, 4, 8])
+        lens = [rng.choice([0, 1, 2, rng.randint(1, 300), rng.randint(1, 9000)]) for _ in range(b)]
+        dtype = rng.choice(["bf16", "fp8", "mxfp4"])
+        sms = rng.choice([7, 152])
+        ind = np.cumsum([0] + lens).astype(np.int32)
+        plan = binding.mla_decode_plan_multi(ind, q_len, dtype, num_sms=sms)
+        tok = [max(0, L - (q_len - 1 - i)) for L in lens for i in range(q_len)]
+        ref = binding.mla_decode_plan(np.cumsum([0] + tok).astype(np.int32), dtype, num_sms=sms)
+        d, r = plan.as_dict(), ref.as_dict()
+        assert d.pop("q_len") == q_len and r.pop("q_len") == 0
+        assert d.pop("total_kv") == ind[-1]
+        r.pop("total_kv")
+        assert d == r and plan.batch == b * q_len
+
+
+def test_multi_token_plan_rules():
+    for q_len in (0, 17):
+        with pytest.raises(binding.MLAError) as e:
+            binding.mla_decode_plan_multi([0, 10], q_len, "fp8", num_sms=152)
+        assert e.value.status == binding.MLA_ERR_UNSUPPORTED
