@@ -69,6 +69,9 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOAD_ORDER)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="query tokens per sequence (mla_decode_plan_multi; each token attends to the rows up "
+                         "to its own entry)")
     ap.add_argument("--page-size", type=int, default=0,
                     help="decode the workload's rows from a paged cache with pages of this many rows "
                          "(pages scattered at random; mla_decode_fwd_paged); 0 = contiguous cache")
@@ -282,6 +285,11 @@ def main():
             pg.barrier()
         torch.cuda.synchronize()
 
+    if args.q_len > 1:
+        # q_len tokens per sequence: query rows b * q_len + i
+        g = torch.Generator("cpu").manual_seed(1000 + rank)
+        inp.q = torch.randn(b * args.q_len, 16, 576, generator=g).to(torch.bfloat16)
+        inp.qo_indptr = torch.arange(b + 1, dtype=torch.int32) * args.q_len
     d = to_device(inp, dev)
     paged = None
     if args.page_size:
@@ -296,10 +304,11 @@ def main():
         dec = binding.PagedMLADecoder(paged.page_indptr, paged.last_page_len, paged.page_size, paged.num_pages, dt,
                                       device=dev)
     else:
-        dec = binding.MLADecoder(inp.kv_indptr, dt, device=dev)
+        dec = binding.MLADecoder(inp.kv_indptr, dt, device=dev, q_len=args.q_len)
+    assert paged is None or args.q_len == 1, "--page-size and --q-len are not combined"
     plan = dec.plan
-    out = torch.empty(b, 16, 512, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(b, 16, dtype=torch.float32, device=dev)
+    out = torch.empty(plan.batch, 16, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(plan.batch, 16, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     scale_stride = int(d["kv_scale"].stride(0)) if dt == "mxfp4" else 0
@@ -427,7 +436,7 @@ def main():
 
     if rank == 0:
         cpu = None
-        if not args.no_cpu_baseline and world == 1:
+        if not args.no_cpu_baseline and world == 1 and args.q_len == 1:
             us_cpu, cores, sample = cpu_baseline(inp)
             cpu = {"value": round(us_cpu, 1), "unit": "us/call", "cores": cores, "kind": "oracle", "sample": sample}
         line = {
@@ -435,8 +444,9 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": DTYPE_LABEL[dt], "data": "synthetic (seeded N(0,1) q and KV, quantised as stated)",
-            "config": {"workload": name if paged is None else f"{name}_paged{args.page_size}", "batch": b,
-                       "kv_len": L, "kv_dtype": dt, "page_size": args.page_size or 1,
+            "config": {"workload": name + (f"_paged{args.page_size}" if paged is not None else "") +
+                                   (f"_q{args.q_len}" if args.q_len > 1 else ""), "batch": b,
+                       "kv_len": L, "kv_dtype": dt, "page_size": args.page_size or 1, "q_len": args.q_len,
                        "kv_bytes_per_call": kv_bytes, "l2": "flushed before every timed call (256 MiB write)",
                        "plan": {k: plan.as_dict()[k] for k in ("num_work", "grid", "chunk_tokens", "splits_max")},
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
