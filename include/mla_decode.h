@@ -1,6 +1,6 @@
 /*
- * mla_decode.h -- C ABI of libmla_decode.so: single-token (q_seq_len = 1)
- * multi-head latent attention decode on a GB300 (sm_103a).
+ * mla_decode.h -- C ABI of libmla_decode.so: multi-head latent attention
+ * decode (one query token per sequence, or a few) on a GB300 (sm_103a).
  *
  * The operation (kernelindex "amd-mixed-mla" submission 593653, section
  * "Slow fallback", _bmm_reference; constants from its "Constants" section):
@@ -13,7 +13,9 @@
  * over the KV rows t in [kv_indptr[b], kv_indptr[b+1]) -- one latent KV head
  * shared by all 16 query heads, QK dim 576 (512 latent + 64 rope), V = the first
  * 512 columns of the same row, page size 1, sm_scale = 1/sqrt(576) = 1/24.
- * An empty sequence gives out = 0 and lse = -inf.
+ * An empty sequence gives out = 0 and lse = -inf.  Extensions below: a paged
+ * cache (mla_decode_plan_paged / mla_decode_fwd_paged) and several query
+ * tokens per sequence (mla_decode_plan_multi).
  *
  * KV storage (submission 593653 "Dispatch" and submission 754939 "Stage 1"):
  *   MLA_KV_BF16      bf16 [rows, 576]
@@ -22,8 +24,9 @@
  *                    with one e8m0 byte per 32 elements, [rows, scale_stride],
  *                    scale_stride >= 18 (only the first 18 bytes are read).
  *
- * Calling sequence: mla_decode_plan() on the host for a batch layout (it reads
- * only the host copy of kv_indptr), mla_decode_workspace_bytes() for the size
+ * Calling sequence: mla_decode_plan() (or mla_decode_plan_multi /
+ * mla_decode_plan_paged) on the host for a batch layout (it reads only the
+ * host copy of the index arrays), mla_decode_workspace_bytes() for the size
  * of the caller-owned device workspace, then mla_decode_fwd() for each call on
  * that layout.  The library never allocates device memory, never synchronises
  * the stream and never exits the process: every entry point returns an
@@ -99,7 +102,7 @@ typedef enum {
  * must not be edited.
  */
 typedef struct {
-  int32_t batch;          /* number of sequences */
+  int32_t batch;          /* output rows: sequences (times q_len for mla_decode_plan_multi) */
   int32_t kv_dtype;       /* mla_kv_dtype */
   int32_t total_kv;       /* kv_indptr[batch]: rows of the KV tensor that are read */
   int32_t chunk_tokens;   /* split length target (tokens) */
