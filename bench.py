@@ -448,7 +448,8 @@ def main():
                                    (f"_q{args.q_len}" if args.q_len > 1 else ""), "batch": b,
                        "kv_len": L, "kv_dtype": dt, "page_size": args.page_size or 1, "q_len": args.q_len,
                        "kv_bytes_per_call": kv_bytes, "l2": "flushed before every timed call (256 MiB write)",
-                       "plan": {k: plan.as_dict()[k] for k in ("num_work", "grid", "chunk_tokens", "splits_max")},
+                       "plan": {k: plan.as_dict()[k] for k in ("num_work", "grid", "chunk_tokens", "splits_max",
+                                                                "tokens_fused")},
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "kv_gbs": round(kv_bytes / (us * 1e-6) / 1e9, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

@@ -119,7 +119,9 @@ typedef struct {
   int32_t num_pages;      /* paged: pages in the cache tensor; 0 otherwise */
   int32_t unit_cost;      /* schedule 1: U, empty tile positions between consecutive sequences */
   int32_t q_len;          /* query tokens per sequence (0 or 1: one; see mla_decode_plan_multi) */
-  int32_t reserved[3];
+  int32_t tokens_fused;   /* 2: a two-token e4m3 plan whose split kernel reads each cache row once
+                             for both tokens (see mla_decode_plan_multi); 0 otherwise */
+  int32_t reserved[2];
 } mla_plan;
 
 /*
@@ -205,16 +207,23 @@ MLA_API int mla_decode_poll_error(void* workspace, void* stream);
  * (i < q_len), the last q_len of its L_b cached rows are those tokens' own
  * entries, and token i attends to the first L_b - (q_len - 1 - i) rows
  * [kv_indptr[b], kv_indptr[b+1] - (q_len - 1 - i)) (none when that is not
- * positive: out = 0, lse = -inf).  The decode treats each token as a sequence
- * of its own over its visible rows, so the cache rows of a sequence are read
- * once per token.
+ * positive: out = 0, lse = -inf).
+ *
+ * Two forms.  With e4m3 KV and q_len = 2 the plan is fused (tokens_fused = 2):
+ * the rule applies to the sequences' full row ranges, one work unit serves both
+ * tokens, and the split kernel reads each cache row once, masking token 0's
+ * last row; partial slot of token i of unit s of sequence b is
+ * 2 sum_{b' < b} S_b' + i S_b + s (num_work counts slots, 2 per unit).
+ * Otherwise each token is decoded as a sequence of its own over its visible
+ * rows, so the cache rows of a sequence are read once per token.
  *
  * mla_decode_plan_multi -- as mla_decode_plan for num_seqs sequences of
  * q_len (1..16) tokens each; the plan's batch is num_seqs * q_len (one output
  * row per token) and its rule applies to the tokens' row ranges in (b, i)
- * order.  mla_decode_fwd with such a plan reads q rows qo_indptr[b] + i and
- * writes out [num_seqs * q_len, 16, 512] and lse [num_seqs * q_len, 16] in
- * (b, i) order.  Returns the status codes of mla_decode_plan.
+ * order (fused form: to the sequences' rows).  mla_decode_fwd with such a
+ * plan reads q rows qo_indptr[b] + i and writes out [num_seqs * q_len, 16, 512]
+ * and lse [num_seqs * q_len, 16] in (b, i) order.  Returns the status codes of
+ * mla_decode_plan.
  */
 MLA_API int mla_decode_plan_multi(const int32_t* kv_indptr_host, int32_t num_seqs, int32_t q_len, int32_t kv_dtype,
                                   int32_t num_sms, int32_t num_splits, mla_plan* plan);

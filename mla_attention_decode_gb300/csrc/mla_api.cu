@@ -342,10 +342,18 @@ int mla_decode_plan_multi(const int32_t* kv_indptr_host, int32_t num_seqs, int32
   if (kv_dtype < MLA_KV_BF16 || kv_dtype > MLA_KV_MXFP4) return MLA_ERR_UNSUPPORTED;
   if (num_splits < 0) return MLA_ERR_INVALID_ARG;
   if (kv_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
-  std::vector<int64_t> lens(static_cast<size_t>(num_seqs) * q_len);
+  // e4m3, two tokens: one unit list over the sequences' rows serves both
+  // tokens (the split kernel reads each row once); otherwise one entry per
+  // token over the rows up to its own entry
+  const bool fused = q_len == 2 && kv_dtype == MLA_KV_FP8_E4M3;
+  std::vector<int64_t> lens(static_cast<size_t>(num_seqs) * (fused ? 1 : q_len));
   for (int32_t b = 0; b < num_seqs; ++b) {
     const int64_t L = (int64_t)kv_indptr_host[b + 1] - kv_indptr_host[b];
     if (L < 0) return MLA_ERR_INVALID_ARG;
+    if (fused) {
+      lens[static_cast<size_t>(b)] = L;
+      continue;
+    }
     for (int32_t i = 0; i < q_len; ++i) {
       const int64_t Li = L - (q_len - 1 - i);  // the rows up to token i's own entry
       lens[static_cast<size_t>(b) * q_len + i] = Li > 0 ? Li : 0;
@@ -354,6 +362,12 @@ int mla_decode_plan_multi(const int32_t* kv_indptr_host, int32_t num_seqs, int32
   mla_plan p;
   const int rc = plan_lengths(lens, kv_indptr_host[num_seqs], kv_dtype, num_sms, num_splits, &p);
   if (rc != MLA_OK) return rc;
+  if (fused) {
+    if (2 * (int64_t)p.num_work > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+    p.batch = 2 * num_seqs;
+    p.num_work *= 2;  // partial slots: two per work unit
+    p.tokens_fused = 2;
+  }
   p.q_len = q_len;
   *plan = p;
   return MLA_OK;
@@ -474,9 +488,15 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   p->unit_cost = plan->unit_cost;
   p->q_len = plan->q_len > 1 ? plan->q_len : 1;
   if (plan->q_len > 16 || (p->q_len > 1 && (paged || plan->batch % p->q_len != 0))) return MLA_ERR_INVALID_ARG;
+  // a two-token plan: e4m3 KV, q_len 2, two partial slots per work unit
+  p->tok = plan->tokens_fused == 2 ? 2 : 1;
+  if (plan->tokens_fused != 0 && (plan->tokens_fused != 2 || plan->kv_dtype != MLA_KV_FP8_E4M3 ||
+                                  plan->q_len != 2 || plan->num_work % 2 != 0))
+    return MLA_ERR_INVALID_ARG;
+  const int32_t entries = plan->batch / p->tok;  // sequences in the unit list
   if (plan->schedule != 0 && (plan->schedule != 1 || plan->total_tiles < plan->grid)) return MLA_ERR_INVALID_ARG;
   if (plan->unit_cost < 0 || (plan->schedule == 1 && (int64_t)plan->total_tiles +
-                              (int64_t)plan->unit_cost * (plan->batch > 0 ? plan->batch - 1 : 0) > INT32_MAX))
+                              (int64_t)plan->unit_cost * (entries > 0 ? entries - 1 : 0) > INT32_MAX))
     return MLA_ERR_INVALID_ARG;
   if (plan->kv_dtype == MLA_KV_FP8_E4M3) {
     if (!encode_kv_map_tc(&p->tmap_kv64, kv, cache_rows, 128)) return MLA_ERR_CUDA;

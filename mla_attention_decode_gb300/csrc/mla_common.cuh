@@ -13,10 +13,13 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s: a wait this long means a lost copy
 
 struct UnitDesc {
-  int32_t b, start, end, u;  // u: work unit index; bit 31 set when the sequence has one split
-  int32_t qrow;              // qo_indptr[b]: the sequence's query row
+  int32_t b, start, end, u;  // u: work unit index (two tokens per unit: token 0's partial slot);
+                             // bit 31 set when the sequence has one split
+  int32_t qrow;              // qo_indptr[b]: the sequence's query row; two tokens per unit:
+                             // S_b, plus kLastUnitBit on the sequence's last unit
 };
 constexpr int32_t kFinalFlag = (int32_t)0x80000000;
+constexpr int32_t kLastUnitBit = 1 << 30;
 
 // Bounded mbarrier wait.  Returns false (after flagging the error) if the phase
 // did not complete within kWaitTimeoutNs, or immediately if another thread of
@@ -77,6 +80,23 @@ __device__ __forceinline__ int query_row(const Stage1Params& p, int b) {
     return p.qo_indptr[s] + (b - s * p.q_len);
   }
   return p.qo_indptr[b];
+}
+
+// Rows and query check of unit-list entry b: output row b (its own rows,
+// query row qo_indptr-derived), or with TOK = 2 tokens per unit sequence b,
+// whose full rows both tokens' units cover; qrow < 0 flags a bad query row.
+template <int TOK>
+__device__ __forceinline__ bool entry_rows(const Stage1Params& p, int b, int& start, int& end, int& qrow) {
+  if constexpr (TOK > 1) {
+    const int a = p.kv_indptr[b], z = p.kv_indptr[b + 1];
+    start = a;
+    end = z;
+    qrow = query_row(p, TOK * b);  // the sequence's tokens are query rows qrow, qrow + 1, ...
+    return a >= 0 && z >= a;
+  } else {
+    qrow = query_row(p, b);
+    return seq_rows(p, b, start, end);
+  }
 }
 
 // Cache row of row-space position v (a row of some sequence): v itself, or for
@@ -154,22 +174,23 @@ __device__ __forceinline__ int splits_of(int len, int chunk, int cap) {
 // tiles, laid end to end with unit_cost empty positions between consecutive
 // sequences (C positions in all); CTA c owns positions [c C / G, (c+1) C / G)
 // and takes one unit from every sequence whose tiles overlap its range.
-template <int TILE, int MAX_UNITS>
+template <int TILE, int MAX_UNITS, int TOK>
 __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, UnitDesc* units, int* s_nunits,
                                                       int lane) {
   const long long T = p.total_tiles, G = p.grid, c = blockIdx.x, U = p.unit_cost;
-  const long long C = T + U * (p.batch > 0 ? p.batch - 1 : 0);
+  const int nseq = p.batch / TOK;       // unit-list entries: sequences of a two-token plan
+  const int nunits = p.num_work / TOK;  // work units (num_work counts partial slots)
+  const long long C = T + U * (nseq > 0 ? nseq - 1 : 0);
   const long long lo = c * C / G, hi = (c + 1) * C / G;
   auto cta_of = [&](long long x) { return ((x + 1) * G - 1) / C; };
   long long tprefix = 0;  // tiles of the sequences before this chunk of 32
   int uprefix = 0, count = 0;
   bool bad = false;
-  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+  for (int b0 = 0; b0 < nseq; b0 += 32) {
     const int b = b0 + lane;
     int start = 0, end = 0, qrow = 0, w = 0;
-    if (b < p.batch) {
-      qrow = query_row(p, b);
-      if (!seq_rows(p, b, start, end) || end > p.total_kv || qrow < 0) {
+    if (b < nseq) {
+      if (!entry_rows<TOK>(p, b, start, end, qrow) || end > p.total_kv || qrow < 0) {
         bad = true;
         start = end = qrow = 0;
       }
@@ -184,7 +205,7 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
     const long long P = tprefix + wincl - w;  // tiles before sequence b
     const long long X = P + U * b;            // position of its first tile
     int sb = 0, cf = 0;
-    if (b < p.batch) {
+    if (b < nseq) {
       if (P + w > T) {
         bad = true;  // the device kv_indptr holds more tiles than the plan
       } else {
@@ -199,18 +220,22 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
       if (lane >= o) sincl += t;
     }
     const int ub = uprefix + sincl - sb;  // first unit of sequence b
-    if (blockIdx.x == 0 && b < p.batch) {
-      // split table for the combine kernel; never point past the plan's slots
-      const bool fits = ub + sb <= p.num_work;
-      p.ws_seq[2 * b] = fits ? ub : 0;
-      p.ws_seq[2 * b + 1] = fits ? sb : 0;
+    if (blockIdx.x == 0 && b < nseq) {
+      // split table for the combine kernel, per output row (token i of a
+      // two-token entry: slots TOK ub + i S_b ..); never point past the plan's slots
+      const bool fits = ub + sb <= nunits;
+#pragma unroll
+      for (int i = 0; i < TOK; ++i) {
+        p.ws_seq[2 * (TOK * b + i)] = fits ? TOK * ub + i * sb : 0;
+        p.ws_seq[2 * (TOK * b + i) + 1] = fits ? sb : 0;
+      }
     }
     const bool mine = sb > 0 && c >= cf && c < cf + sb;
     const unsigned m = __ballot_sync(0xffffffffu, mine);
     if (mine) {
       const int pos = count + __popc(m & ((1u << lane) - 1));
       const int u = ub + (int)(c - cf);
-      if (pos >= MAX_UNITS || u >= p.num_work) {
+      if (pos >= MAX_UNITS || u >= nunits) {
         bad = true;
       } else {
         const long long a = (lo > X ? lo : X) - X, e = (hi < X + w ? hi : X + w) - X;  // the sequence's tiles here
@@ -218,8 +243,8 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
         d.b = b;
         d.start = end > start ? start + TILE * (int)a : start;
         d.end = end > start ? min(end, start + TILE * (int)e) : start;
-        d.u = u | (sb == 1 ? kFinalFlag : 0);
-        d.qrow = qrow;
+        d.u = (TOK * ub + (u - ub)) | (sb == 1 ? kFinalFlag : 0);
+        d.qrow = TOK > 1 ? (sb | (c == cf + sb - 1 ? kLastUnitBit : 0)) : qrow;
         units[pos] = d;
       }
     }
@@ -227,7 +252,7 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
     tprefix += __shfl_sync(0xffffffffu, wincl, 31);
     uprefix += __shfl_sync(0xffffffffu, sincl, 31);
   }
-  if (tprefix != T || uprefix != p.num_work) bad = true;
+  if (tprefix != T || uprefix != nunits) bad = true;
   bad = __any_sync(0xffffffffu, bad);
   if (lane == 0) {
     if (bad) atomicCAS(p.ws_err, 0, kErrDeviceIndex);
@@ -235,20 +260,24 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
   }
 }
 
-template <int TILE, int MAX_UNITS = kMaxUnitsPerCta>
+// TOK: output rows per unit-list entry (2: a two-token plan, whose entries are
+// sequences and whose units serve both tokens; compile-time, so that the
+// one-token scan carries none of it).
+template <int TILE, int MAX_UNITS = kMaxUnitsPerCta, int TOK = 1>
 __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* units, int* s_nunits, int lane) {
   if (p.schedule == 1) {
-    scan_units_contiguous<TILE, MAX_UNITS>(p, units, s_nunits, lane);
+    scan_units_contiguous<TILE, MAX_UNITS, TOK>(p, units, s_nunits, lane);
     return;
   }
+  const int nseq = p.batch / TOK;       // unit-list entries: sequences of a two-token plan
+  const int nunits = p.num_work / TOK;  // work units (num_work counts partial slots)
   int prefix = 0, count = 0;
   bool bad = false;
-  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+  for (int b0 = 0; b0 < nseq; b0 += 32) {
     const int b = b0 + lane;
     int start = 0, end = 0, sb = 0, qrow = 0;
-    if (b < p.batch) {
-      qrow = query_row(p, b);
-      if (!seq_rows(p, b, start, end) || end > p.total_kv || qrow < 0) {
+    if (b < nseq) {
+      if (!entry_rows<TOK>(p, b, start, end, qrow) || end > p.total_kv || qrow < 0) {
         bad = true;
         start = end = 0;
         qrow = 0;
@@ -262,14 +291,18 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
       if (lane >= o) incl += t;
     }
     const int pb = prefix + incl - sb;
-    if (blockIdx.x == 0 && b < p.batch) {
-      // split table for the combine kernel; never point past the plan's slots
-      const bool fits = pb + sb <= p.num_work;
-      p.ws_seq[2 * b] = fits ? pb : 0;
-      p.ws_seq[2 * b + 1] = fits ? sb : 0;
+    if (blockIdx.x == 0 && b < nseq) {
+      // split table for the combine kernel (as in the contiguous schedule);
+      // never point past the plan's slots
+      const bool fits = pb + sb <= nunits;
+#pragma unroll
+      for (int i = 0; i < TOK; ++i) {
+        p.ws_seq[2 * (TOK * b + i)] = fits ? TOK * pb + i * sb : 0;
+        p.ws_seq[2 * (TOK * b + i) + 1] = fits ? sb : 0;
+      }
     }
     int n = 0, first = 0;
-    if (b < p.batch) {
+    if (b < nseq) {
       int off = (int)(((long long)blockIdx.x - pb) % p.grid);
       if (off < 0) off += p.grid;
       first = pb + off;
@@ -286,7 +319,7 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
     for (int k = 0; k < n; ++k) {
       const int u = first + k * p.grid;
       const int s = u - pb;
-      if (pos + k >= MAX_UNITS || u >= p.num_work) {
+      if (pos + k >= MAX_UNITS || u >= nunits) {
         bad = true;
         continue;
       }
@@ -294,14 +327,14 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
       d.b = b;
       d.start = start + TILE * (int)((long long)s * tiles / sb);
       d.end = min(end, start + TILE * (int)((long long)(s + 1) * tiles / sb));
-      d.u = u | (sb == 1 ? kFinalFlag : 0);
-      d.qrow = qrow;
+      d.u = (TOK * pb + s) | (sb == 1 ? kFinalFlag : 0);
+      d.qrow = TOK > 1 ? (sb | (s == sb - 1 ? kLastUnitBit : 0)) : qrow;
       units[pos + k] = d;
     }
     count += __shfl_sync(0xffffffffu, nincl, 31);
     prefix += __shfl_sync(0xffffffffu, incl, 31);
   }
-  if (prefix != p.num_work) bad = true;
+  if (prefix != nunits) bad = true;
   bad = __any_sync(0xffffffffu, bad);
   if (lane == 0) {
     if (bad) atomicCAS(p.ws_err, 0, kErrDeviceIndex);

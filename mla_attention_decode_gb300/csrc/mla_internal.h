@@ -80,6 +80,8 @@ struct Stage1Params {
   int32_t total_tiles;  // schedule 1: sum of the sequences' weights in tiles
   int32_t unit_cost;    // schedule 1: empty positions between consecutive sequences
   int32_t q_len;        // query tokens per sequence; batch counts tokens
+  int32_t tok;          // tokens one work unit serves (2: fused two-token e4m3 plan, else 1);
+                        // num_work then counts partial slots, tok per unit
 };
 
 struct CombineParams {
@@ -97,6 +99,7 @@ constexpr int32_t kErrDeviceTimeout = 6;
 
 cudaError_t launch_stage1_bf16(const Stage1Params& p, cudaStream_t s);
 cudaError_t launch_stage1_fp8(const Stage1Params& p, cudaStream_t s);
+cudaError_t launch_stage1_fp8_t2(const Stage1Params& p, cudaStream_t s);  // p.tok == 2
 cudaError_t launch_stage1_mxfp4(const Stage1Params& p, cudaStream_t s);
 // Two-term e4m3 query of every sequence into the workspace (e4m3 / MXFP4 KV).
 cudaError_t launch_prep_q(const Stage1Params& p, bool mx, cudaStream_t s);

@@ -37,6 +37,12 @@
 // [32 (w mod 4), +32)).  Hand-offs are mbarriers (TMA transaction bytes,
 // tcgen05.commit, thread arrivals).
 //
+// Two query tokens per unit (kTok = 2, e4m3; several tokens per sequence,
+// the causal reading): each tile feeds two QKs and two P.V chains, one per
+// token, into their own TMEM columns, and warps 8-11 form a second softmax
+// group for token 1, so the cache rows are read once for both tokens.  Token
+// 0 does not see its sequence's last row (token 1's own entry).
+//
 // MXFP4 KV (kMx): rows arrive packed (288 B of e2m1 pairs, element 2i in the low
 // nibble of byte i) by 1-D bulk copies of 64-row halves into a staging ring,
 // and eight converter warps (8-15, four per half tile) write them into the same e4m3 ring layout
@@ -60,10 +66,15 @@ namespace tcfp8 {
 constexpr int kTileRows = 128;
 constexpr int kChunkBytes = kTileRows * 64;  // one 64-byte feature column block of a tile
 constexpr int kPairBytes = 2 * kChunkBytes;  // two column blocks = features [128 f, 128 f + 128)
-template <bool kMx>
+// kTok: query tokens one work unit serves (2: the fused two-token e4m3 form,
+// which holds a second query image and a second pair of P buffers in shared
+// memory at the cost of two ring slots).
+template <bool kMx, int kTok = 1>
 struct Geo {
-  static constexpr int pair_slots = kMx ? 8 : 11;  // ring of V column-block pairs (4 per tile)
-  static constexpr int threads = kMx ? 512 : 256;
+  static_assert(kTok == 1 || (kTok == 2 && !kMx), "two tokens per unit: e4m3 KV only");
+  static constexpr int pair_slots = kMx ? 8 : (kTok == 1 ? 11 : 9);  // ring of V column-block pairs (4 per tile)
+  // roles: 4 single-thread warps, 4 softmax warps per token, MXFP4: 8 converter warps
+  static constexpr int threads = kMx ? 512 : 128 * (1 + kTok);
   static constexpr int max_units = kMx ? kMaxUnitsPerCtaMx : kMaxUnitsPerCta;  // work units one CTA may own
 };
 constexpr int kRopeSlots = 2;                // ring of the rope column block (features 512..575)
@@ -73,29 +84,36 @@ constexpr int kHalfRows = 64;                        // MXFP4 staging unit: 64 p
 constexpr int kPackedRowBytes = 288;
 constexpr int kStageBytes = kHalfRows * kPackedRowBytes;  // 18 KB
 constexpr int kStageSlots = 3;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;   // S^T double buffer: columns [0, 32) and [32, 64)
-constexpr uint32_t kColO = 64;  // O^T: 4 feature blocks x 32 columns
+// TMEM columns: the S^T double buffer [blk (t mod 2), +blk), then O^T, 4
+// feature blocks of blk columns; token i of a unit owns columns [32 i, +32) of
+// each buffer and block.
+template <int kTok>
+struct Tmem {
+  static constexpr uint32_t blk = 32 * kTok;
+  static constexpr uint32_t cols = kTok == 1 ? 256 : 512;
+  static constexpr uint32_t s = 0;
+  static constexpr uint32_t o = 2 * blk;
+};
 constexpr float kRescaleLog2 = 8.f;
-constexpr uint32_t kBarSoftmax = 1;  // named barrier of the softmax warps (128 threads)
+constexpr uint32_t kBarSoftmax = 1;  // named barrier of softmax group 0 (128 threads); group 1: 2
 constexpr uint32_t kIdescQK = tc::idesc_e4m3(128, 32, 0, 0);
 constexpr uint32_t kIdescPV = tc::idesc_e4m3(128, 32, 1, 1);
 
-template <bool kMx>
+template <bool kMx, int kTok = 1>
 struct Layout {
-  static constexpr int kPairSlots = Geo<kMx>::pair_slots;
+  static constexpr int kPairSlots = Geo<kMx, kTok>::pair_slots;
   static constexpr int pairs = 0;                             // 1024-aligned
   static constexpr int rope = pairs + kPairSlots * kPairBytes;
   static constexpr int stage = rope + kRopeSlots * kChunkBytes;      // MXFP4 only: packed rows
   static constexpr int qs = stage + (kMx ? kStageSlots * kStageBytes : 0);
-  static constexpr int pb = qs + kQsBytes;                    // [2]
-  static constexpr int rq = pb + 2 * kPBytes;                 // float [16] score factor per head
-  static constexpr int red = rq + 16 * 4;                     // float [2][4 warps][16]
-  static constexpr int gred = red + 2 * 4 * 16 * 4;           // int [2][4] tile max of the row exponents
+  static constexpr int pb = qs + kQsBytes * kTok;             // [2 tiles][kTok]
+  static constexpr int rq = pb + 2 * kPBytes * kTok;          // float [kTok][16] score factor per head
+  static constexpr int red = rq + 16 * 4 * kTok;              // float [2][4 warps][16 kTok]
+  static constexpr int gred = red + 2 * 4 * 16 * 4 * kTok;    // int [2][4] tile max of the row exponents
   static constexpr int grow = gred + 2 * 4 * 4;               // int8 [2][128] row exponent G - 127 (MXFP4)
   static constexpr int lut = grow + (kMx ? 2 * 128 : 0);      // u8 [32][8] e2m1 magnitude -> e4m3 per shift
   static constexpr int units = lut + (kMx ? 256 : 0);
-  static constexpr int bars = units + Geo<kMx>::max_units * (int)sizeof(UnitDesc);
+  static constexpr int bars = units + Geo<kMx, kTok>::max_units * (int)sizeof(UnitDesc);
   static constexpr int nbars = 49;
   static constexpr int misc = bars + nbars * 8;  // tmem slot, abort flag, unit count
   static constexpr int total = misc + 16;
@@ -140,12 +158,14 @@ __device__ __forceinline__ int tiles_of(const UnitDesc& d) { return (d.end - d.s
 // slot (4t + f) mod S (S = 11 for e4m3, 7 for MXFP4), the rope block to rope
 // slot t mod 2; each slot is re-filled as soon as the MMA that read it has
 // completed.
-template <bool kMx>
-__device__ __forceinline__ int pair_slot(int t, int f) { return (4 * t + f) % Geo<kMx>::pair_slots; }
-template <bool kMx>
-__device__ __forceinline__ int pair_use(int t, int f) { return (4 * t + f) / Geo<kMx>::pair_slots; }
-template <bool kMx>
-__device__ __forceinline__ int wrap_slot(int s) { return s >= Geo<kMx>::pair_slots ? s - Geo<kMx>::pair_slots : s; }
+template <bool kMx, int kTok = 1>
+__device__ __forceinline__ int pair_slot(int t, int f) { return (4 * t + f) % Geo<kMx, kTok>::pair_slots; }
+template <bool kMx, int kTok = 1>
+__device__ __forceinline__ int pair_use(int t, int f) { return (4 * t + f) / Geo<kMx, kTok>::pair_slots; }
+template <bool kMx, int kTok = 1>
+__device__ __forceinline__ int wrap_slot(int s) {
+  return s >= Geo<kMx, kTok>::pair_slots ? s - Geo<kMx, kTok>::pair_slots : s;
+}
 
 // The CTA's tiles in order (unit by unit): each tile's first row-space
 // position and its unit's end.
@@ -181,9 +201,10 @@ __device__ __forceinline__ TileRows tile_rows(const Stage1Params& p, int t0, int
   return r;
 }
 
-static __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
-  using L = Layout<false>;
-  constexpr int kPairSlots = Geo<false>::pair_slots;
+template <int kTok>
+__device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
+  using L = Layout<false, kTok>;
+  constexpr int kPairSlots = Geo<false, kTok>::pair_slots;
   const uint64_t pol = policy_evict_first();  // KV rows are read once
   const bool paged64 = p.page_shift == 6;
   // one 64-byte column block of the tile (and the bytes it brings)
@@ -209,7 +230,7 @@ static __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
     if (have) nrows = tile_rows(p, nt0, nend);
     const uint32_t block_bytes = (paged64 && rows.r1 < 0) ? kChunkBytes / 2 : kChunkBytes;
     for (int f = 0; f < 4; ++f) {
-      const int sl = pair_slot<false>(it, f), use = pair_use<false>(it, f);
+      const int sl = pair_slot<false, kTok>(it, f), use = pair_use<false, kTok>(it, f);
       if (use >= 1) wait_phase(&x.bar[kPairEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
       uint8_t* dst = x.smem + L::pairs + sl * kPairBytes;
@@ -455,13 +476,14 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
 // ---------------------------------------------------------- query loader
 // One thread: the query of unit k, prepared by mla_prep_q_kernel as the exact
 // shared-memory image (two-term e4m3, 64-byte swizzle) plus its 16 score
-// factors, comes in by two bulk copies once the last QK of unit k-1 has
-// completed and the softmax has taken unit k-1's factors.  The prepared
-// queries are the one input written by the preceding grid, so this is the one
-// thread that waits for it.
-template <bool kMx>
+// factors, comes in by two bulk copies per token once the last QK of unit k-1
+// has completed and the softmax has taken unit k-1's factors (token i of a
+// two-token unit of sequence b: the prepared output row 2 b + i).  The
+// prepared queries are the one input written by the preceding grid, so this
+// is the one thread that waits for it.
+template <bool kMx, int kTok>
 __device__ void q_loader(const Stage1Params& p, const Ctx& x) {
-  using L = Layout<kMx>;
+  using L = Layout<kMx, kTok>;
   const uint64_t pol = policy_evict_last();  // a query serves every split of its sequence
   pdl_wait_primary();
   int uses = 0;
@@ -471,10 +493,14 @@ __device__ void q_loader(const Stage1Params& p, const Ctx& x) {
       wait_phase(&x.bar[kRFree], (k - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
     }
-    const uint8_t* src = p.ws_q + (size_t)x.units[k].b * kQPrepBytes;
-    mbar_arrive_expect_tx(&x.bar[kQFull], (uint32_t)kQPrepBytes);
-    bulk_g2s(x.smem + L::qs, src, (uint32_t)kQImageBytes, &x.bar[kQFull], pol);
-    bulk_g2s(x.smem + L::rq, src + kQImageBytes, 16 * sizeof(float), &x.bar[kQFull], pol);
+    mbar_arrive_expect_tx(&x.bar[kQFull], (uint32_t)(kTok * kQPrepBytes));
+#pragma unroll
+    for (int i = 0; i < kTok; ++i) {
+      const uint8_t* src = p.ws_q + ((size_t)x.units[k].b * kTok + i) * kQPrepBytes;
+      bulk_g2s(x.smem + L::qs + i * kQsBytes, src, (uint32_t)kQImageBytes, &x.bar[kQFull], pol);
+      bulk_g2s(x.smem + L::rq + i * 16 * sizeof(float), src + kQImageBytes, 16 * sizeof(float), &x.bar[kQFull],
+               pol);
+    }
     ++uses;
   }
   if (*x.abort_flag && uses > 0) {
@@ -501,11 +527,13 @@ __host__ __device__ constexpr uint32_t lo_word(uint64_t d) { return (uint32_t)d;
 __host__ __device__ constexpr uint32_t hi_word(uint64_t d) { return (uint32_t)(d >> 32); }
 
 
-// QK of every tile: S^T(t) into TMEM columns [32 (t mod 2), +32).
-template <bool kMx>
+// QK of every tile: S^T(t) into TMEM columns [blk (t mod 2), +blk), token i's
+// scores at +32 i from its own query image.
+template <bool kMx, int kTok>
 __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
-  using L = Layout<kMx>;
-  constexpr int kPairSlots = Geo<kMx>::pair_slots;
+  using L = Layout<kMx, kTok>;
+  using TM = Tmem<kTok>;
+  constexpr int kPairSlots = Geo<kMx, kTok>::pair_slots;
   const uint32_t pairs0 = smem_u32(x.smem + L::pairs), rope0 = smem_u32(x.smem + L::rope);
   const uint32_t bq = lo_word(kTplK64) + (smem_u32(x.smem + L::qs) >> 4);
   int it = 0;
@@ -521,7 +549,7 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
 #pragma unroll
         for (int f = 0; f < 4; ++f) {
           const int sl = s0 + f;
-          wait_phase(&x.bar[kPairFull + wrap_slot<kMx>(sl)], (use0 + (sl >= kPairSlots)) & 1, x.abort_flag,
+          wait_phase(&x.bar[kPairFull + wrap_slot<kMx, kTok>(sl)], (use0 + (sl >= kPairSlots)) & 1, x.abort_flag,
                      p.ws_err);
         }
         wait_phase(&x.bar[kRopeFull + it % kRopeSlots], (it / kRopeSlots) & 1, x.abort_flag, p.ws_err);
@@ -532,16 +560,18 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
       uint32_t ap[4];
 #pragma unroll
       for (int f = 0; f < 4; ++f)
-        ap[f] = lo_word(kTplK64) + ((pairs0 + (uint32_t)wrap_slot<kMx>(s0 + f) * kPairBytes) >> 4);
+        ap[f] = lo_word(kTplK64) + ((pairs0 + (uint32_t)wrap_slot<kMx, kTok>(s0 + f) * kPairBytes) >> 4);
       const uint32_t ar = lo_word(kTplK64) + ((rope0 + (uint32_t)(it % kRopeSlots) * kChunkBytes) >> 4);
-      const uint32_t d = x.tmem + kColS + 32 * (it & 1);
+      const uint32_t d = x.tmem + TM::s + TM::blk * (it & 1);
 #pragma unroll
       for (int ks = 0; ks < 18; ++ks) {
         const int c = ks >> 1, half = ks & 1;
         const uint32_t a =
             c < 8 ? ap[c >> 1] + (((c & 1) * kChunkBytes + 32 * half) >> 4) : ar + ((32 * half) >> 4);
-        tc::mma_f8_words(d, a, hi_word(kTplK64), bq + ((c * 2048 + 32 * half) >> 4), hi_word(kTplK64), kIdescQK,
-                         ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int i = 0; i < kTok; ++i)
+          tc::mma_f8_words(d + 32 * i, a, hi_word(kTplK64), bq + ((i * kQsBytes + c * 2048 + 32 * half) >> 4),
+                           hi_word(kTplK64), kIdescQK, ks > 0 ? 1u : 0u);
       }
       tc::commit(&x.bar[kSFull + (it & 1)]);
       tc::commit(&x.bar[kRopeEmpty + it % kRopeSlots]);
@@ -550,12 +580,14 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
   }
 }
 
-// P.V of every tile: O^T += V^T(t) . P^T(t); releases the tile's ring slots, its
-// P buffer and, on a unit's last tile, the unit's O^T.
-template <bool kMx>
+// P.V of every tile: O^T += V^T(t) . P^T(t) (token i: its own P buffer and O^T
+// columns); releases the tile's ring slots, its P buffers and, on a unit's
+// last tile, the unit's O^T.
+template <bool kMx, int kTok>
 __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
-  using L = Layout<kMx>;
-  constexpr int kPairSlots = Geo<kMx>::pair_slots;
+  using L = Layout<kMx, kTok>;
+  using TM = Tmem<kTok>;
+  constexpr int kPairSlots = Geo<kMx, kTok>::pair_slots;
   const uint32_t pairs0 = smem_u32(x.smem + L::pairs), pb0 = smem_u32(x.smem + L::pb);
   int it = 0, ordinal = 0;
   for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
@@ -567,17 +599,20 @@ __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
       if (t == 0 && ordinal > 0) wait_phase(&x.bar[kOFree], (ordinal - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
       tc::fence_after();
-      const uint32_t bp = lo_word(kTplP) + ((pb0 + (uint32_t)(it & 1) * kPBytes) >> 4);
+      const uint32_t bp = lo_word(kTplP) + ((pb0 + (uint32_t)(it & 1) * kTok * kPBytes) >> 4);
       const int s0 = (4 * it) % kPairSlots;
 #pragma unroll
       for (int fb = 0; fb < 4; ++fb) {
-        const int sl = wrap_slot<kMx>(s0 + fb);
+        const int sl = wrap_slot<kMx, kTok>(s0 + fb);
         // V^T block: features [128 fb, 128 fb + 128) = the slot's two column blocks (LBO)
         const uint32_t av = lo_word(kTplV) + ((pairs0 + (uint32_t)sl * kPairBytes) >> 4);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)  // rows [32 q, 32 q + 32): +2048 B of V^T, +1024 B of P^T
-          tc::mma_f8_words(x.tmem + kColO + 32 * fb, av + q * (2048 >> 4), hi_word(kTplV), bp + q * (1024 >> 4),
-                           hi_word(kTplP), kIdescPV, (t == 0 && q == 0) ? 0u : 1u);
+        for (int i = 0; i < kTok; ++i)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)  // rows [32 q, 32 q + 32): +2048 B of V^T, +1024 B of P^T
+            tc::mma_f8_words(x.tmem + TM::o + TM::blk * fb + 32 * i, av + q * (2048 >> 4), hi_word(kTplV),
+                             bp + ((i * kPBytes + q * 1024) >> 4), hi_word(kTplP), kIdescPV,
+                             (t == 0 && q == 0) ? 0u : 1u);
         tc::commit(&x.bar[kPairEmpty + sl]);
       }
       tc::commit(&x.bar[kODone]);
@@ -592,7 +627,7 @@ __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
 // Max (or sum) over the 128 rows of the tile for 16 heads: butterfly within the
 // warp, then across the 4 warps through smem.
 template <bool kMax>
-__device__ __forceinline__ void group_reduce16(float (&v)[16], float* red, int ww, int lane) {
+__device__ __forceinline__ void group_reduce16(float (&v)[16], float* red, int ww, int lane, uint32_t bar) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
@@ -605,7 +640,7 @@ __device__ __forceinline__ void group_reduce16(float (&v)[16], float* red, int w
     for (int h = 0; h < 16; h += 4)
       *reinterpret_cast<float4*>(red + ww * 16 + h) = make_float4(v[h], v[h + 1], v[h + 2], v[h + 3]);
   }
-  named_bar_sync(kBarSoftmax, 128);
+  named_bar_sync(bar, 128);
 #pragma unroll
   for (int h = 0; h < 16; h += 4) {
     float4 r = *reinterpret_cast<const float4*>(red + h);
@@ -627,17 +662,24 @@ __device__ __forceinline__ void group_reduce16(float (&v)[16], float* red, int w
 // 2^e for an integer e in [-126, 127] (exact).
 __device__ __forceinline__ float exp2_int(int e) { return __int_as_float((e + 127) << 23); }
 
-template <bool kMx>
-__device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, int lane) {
-  using L = Layout<kMx>;
+// Softmax group ti (four warps; one group per query token of the unit):
+// thread `row` owns tile row `row` (its TMEM lane) for the token's 16 heads,
+// in TMEM columns [32 ti, +32) of the S^T buffers and O^T blocks.  With two
+// tokens, token 0 does not see the last row of its sequence (token 1's own
+// entry), and token ti's partial slot is u + ti S_b.
+template <bool kMx, int kTok>
+__device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, int lane, int ti) {
+  using L = Layout<kMx, kTok>;
+  using TM = Tmem<kTok>;
   constexpr int kGvNone = -1000;   // no MXFP4 reference yet
   const int row = 32 * ww + lane;  // tile row == TMEM lane of this thread
-  const uint32_t tl = x.tmem + ((uint32_t)(32 * ww) << 16);
+  const uint32_t tl = x.tmem + ((uint32_t)(32 * ww) << 16) + 32 * ti;
+  const uint32_t bar = kBarSoftmax + ti;  // the group's named barrier
   const float kv_scale = kMx ? 1.f : *static_cast<const float*>(p.kv_scale);
   const int8_t* grow = reinterpret_cast<const int8_t*>(x.smem + L::grow);
   int* gred = reinterpret_cast<int*>(x.smem + L::gred);
-  const float* rq = reinterpret_cast<const float*>(x.smem + L::rq);
-  float* redbuf = reinterpret_cast<float*>(x.smem + L::red);
+  const float* rq = reinterpret_cast<const float*>(x.smem + L::rq) + 16 * ti;
+  float* redbuf = reinterpret_cast<float*>(x.smem + L::red) + 128 * ti;
   int it = 0, red_par = 0, ordinal = 0;
   for (int k = 0; k < x.nunits; ++k) {
     const UnitDesc d = x.units[k];
@@ -648,19 +690,23 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
     __syncwarp();
     if (lane == 0) mbar_arrive(&x.bar[kRFree]);
     const bool final_out = (d.u & kFinalFlag) != 0;
-    const int u = d.u & ~kFinalFlag;
+    // output row and partial slot of this group's token; the rows it does not
+    // see at the end of the sequence's last unit
+    const int ob = d.b * kTok + ti;
+    const int u = (d.u & ~kFinalFlag) + (kTok > 1 ? ti * (d.qrow & ~kLastUnitBit) : 0);
+    const int hidden = (kTok > 1 && (d.qrow & kLastUnitBit) != 0) ? kTok - 1 - ti : 0;
     const int nt = tiles_of(d);
     if (nt == 0) {
       // empty sequence: out = 0, lse = -inf
       for (int i = row; i < kHeads * kVDim; i += 128) {
         if (final_out)
-          p.out[(size_t)d.b * kHeads * kVDim + i] = 0;
+          p.out[(size_t)ob * kHeads * kVDim + i] = 0;
         else
           p.ws_o[(size_t)u * kHeads * kVDim + i] = 0.f;
       }
       if (row < kHeads) {
         if (final_out) {
-          if (p.lse) p.lse[d.b * kHeads + row] = -INFINITY;
+          if (p.lse) p.lse[ob * kHeads + row] = -INFINITY;
         } else {
           p.ws_lse[(size_t)u * kHeads + row] = -INFINITY;
         }
@@ -678,10 +724,11 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       const int sb = it & 1;
       const int t0 = d.start + t * kTileRows;
       const int valid = min(kTileRows, d.end - t0);
+      const int vis = min(valid, d.end - hidden - t0);  // rows of the tile this token sees
       wait_phase(&x.bar[kSFull + sb], (it >> 1) & 1, x.abort_flag, p.ws_err);
       tc::fence_after();
       uint32_t acc[32];
-      tc::ld32(tl + kColS + 32 * sb, acc);
+      tc::ld32(tl + TM::s + TM::blk * sb, acc);
       tc::wait_ld();
       tc::fence_before();
       __syncwarp();
@@ -695,8 +742,8 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       uint32_t need = 0;  // heads with a score above m_ref + 8 in this row (bit 16: G above gv)
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
-        sv[h] = row < valid ? (__uint_as_float(acc[h]) + __uint_as_float(acc[16 + h])) * (r[h] * row_fac)
-                            : -INFINITY;
+        sv[h] = row < vis ? (__uint_as_float(acc[h]) + __uint_as_float(acc[16 + h])) * (r[h] * row_fac)
+                          : -INFINITY;
         need |= (sv[h] > m_ref[h] + kRescaleLog2 ? 1u : 0u) << h;
       }
       if (kMx && row < valid && gsh > gv) need |= 1u << 16;
@@ -705,7 +752,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       {
         uint32_t* fl = reinterpret_cast<uint32_t*>(redbuf + red_par * 64);
         if (lane == 0) fl[ww] = need;
-        named_bar_sync(kBarSoftmax, 128);
+        named_bar_sync(bar, 128);
         need = fl[0] | fl[1] | fl[2] | fl[3];
         red_par ^= 1;
       }
@@ -729,7 +776,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
           const int w = __reduce_max_sync(0xffffffffu, row < valid ? gsh : kGvNone);
           if (lane == 0) gred[red_par * 4 + ww] = w;
         }
-        named_bar_sync(kBarSoftmax, 128);
+        named_bar_sync(bar, 128);
         float fac[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
@@ -758,14 +805,14 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
 #pragma unroll 1
           for (int fb = 0; fb < 4; ++fb) {
             uint32_t o[32];
-            tc::ld32(tl + kColO + 32 * fb, o);
+            tc::ld32(tl + TM::o + TM::blk * fb, o);
             tc::wait_ld();
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
               o[h] = __float_as_uint(__uint_as_float(o[h]) * fac[h]);
               o[16 + h] = __float_as_uint(__uint_as_float(o[16 + h]) * fac[h]);
             }
-            tc::st32(tl + kColO + 32 * fb, o);
+            tc::st32(tl + TM::o + TM::blk * fb, o);
           }
           tc::wait_st();
         }
@@ -786,16 +833,17 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
         }
         two_term_e4m3(pv[0], pv[1], pv[2], pv[3], hi[g], lo[g]);
       }
-      uint8_t* pbuf = x.smem + L::pb + sb * kPBytes + row * 32;
+      uint8_t* pbuf = x.smem + L::pb + (sb * kTok + ti) * kPBytes + row * 32;
       const int xr = (row >> 2) & 1;  // 32 B swizzle: the 16-byte units of the row swap
       *reinterpret_cast<uint4*>(pbuf + 16 * xr) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(pbuf + 16 * (xr ^ 1)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      if (!kMx && row >= valid) {
+      if (!kMx && ti == 0 && row >= valid) {
         // rows past the unit's end hold other rows' data: zero their V part so
         // that P = 0 cannot meet a non-finite value (the MXFP4 converters write zeros)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          uint8_t* blk = x.smem + L::pairs + pair_slot<kMx>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes;
+          uint8_t* blk =
+              x.smem + L::pairs + pair_slot<kMx, kTok>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes;
 #pragma unroll
           for (int uu = 0; uu < 4; ++uu)
             *reinterpret_cast<uint4*>(blk + sw64_off(row, 16 * uu)) = make_uint4(0, 0, 0, 0);
@@ -807,7 +855,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       if (lane == 0) mbar_arrive(&x.bar[kPFull + sb]);
     }
     // unit epilogue: l per head over the 128 rows, O^T -> output
-    group_reduce16<false>(l_part, redbuf + red_par * 64, ww, lane);
+    group_reduce16<false>(l_part, redbuf + red_par * 64, ww, lane, bar);
     red_par ^= 1;
     // the unit's last P.V: its own barrier completes once per unit, so the parity
     // of the unit's ordinal names it exactly (o_done may be a phase further on)
@@ -821,20 +869,20 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
 #pragma unroll 1
     for (int fb = 0; fb < 4; ++fb) {
       uint32_t o[32];
-      tc::ld32(tl + kColO + 32 * fb, o);
+      tc::ld32(tl + TM::o + TM::blk * fb, o);
       tc::wait_ld();
       const int f = 128 * fb + row;
       if (final_out) {
-        uint16_t* ob = p.out + (size_t)d.b * kHeads * kVDim + f;
+        uint16_t* op = p.out + (size_t)ob * kHeads * kVDim + f;
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
           const float v = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h])) * inv[h];
-          ob[h * kVDim] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xffffu);
+          op[h * kVDim] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xffffu);
         }
       } else {
-        float* ob = p.ws_o + (size_t)u * kHeads * kVDim + f;
+        float* op = p.ws_o + (size_t)u * kHeads * kVDim + f;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) ob[h * kVDim] = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h])) * inv[h];
+        for (int h = 0; h < 16; ++h) op[h * kVDim] = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h])) * inv[h];
       }
     }
     // lse of head h is written by row h (every row holds all 16 values): pick
@@ -848,7 +896,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       }
       const float lse = lh > 0.f ? (mh + fast_log2(lh)) * kLn2 : -INFINITY;
       if (final_out) {
-        if (p.lse) p.lse[d.b * kHeads + row] = lse;
+        if (p.lse) p.lse[ob * kHeads + row] = lse;
       } else {
         p.ws_lse[(size_t)u * kHeads + row] = lse;
       }
@@ -859,9 +907,10 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
   }
 }
 
-template <bool kMx>
-__global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(const __grid_constant__ Stage1Params p) {
-  using L = Layout<kMx>;
+template <bool kMx, int kTok>
+__global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
+    mla_split_tc_kernel(const __grid_constant__ Stage1Params p) {
+  using L = Layout<kMx, kTok>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Ctx x;
@@ -878,10 +927,10 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     for (int i = 0; i < L::nbars; ++i) counts[i] = 1;
     counts[kQFull] = 1;
     counts[kFinal] = 2;
-    counts[kSEmpty] = counts[kSEmpty + 1] = 4;
-    counts[kPFull] = counts[kPFull + 1] = 4;
-    counts[kOFree] = 4;
-    counts[kRFree] = 4;
+    counts[kSEmpty] = counts[kSEmpty + 1] = 4 * kTok;  // every softmax warp
+    counts[kPFull] = counts[kPFull + 1] = 4 * kTok;
+    counts[kOFree] = 4 * kTok;
+    counts[kRFree] = 4 * kTok;
     for (int i = 0; i < kStageSlots; ++i) counts[kStageEmpty + i] = 4;
     counts[kConvFull] = counts[kConvFull + 1] = 8;
     for (int i = 0; i < L::nbars; ++i) mbar_init(&x.bar[i], counts[i]);
@@ -892,7 +941,8 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     // no grid-dependency wait here: this kernel is launched only once the
     // query-preparation grid has itself waited for all earlier work, so every
     // input but the prepared queries is complete (the query loader waits for those)
-    scan_units<kTileRows, Geo<kMx>::max_units>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits, lane);
+    scan_units<kTileRows, Geo<kMx, kTok>::max_units, kTok>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits,
+                                                     lane);
     if (lane == 0 && !kMx) prefetch_tensormap(&p.tmap_kv64);
   }
   if (kMx && threadIdx.x >= 128 && threadIdx.x < 384) {
@@ -903,7 +953,7 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
     smem[L::lut + i] = shift < 16 ? (uint8_t)(f32x2_to_e4m3x2(ldexpf(mag, -shift), 0.f) & 0xffu) : (uint8_t)0;
   }
   if (warp == 1) {
-    tc::alloc(tmem_slot, kTmemCols);
+    tc::alloc(tmem_slot, Tmem<kTok>::cols);
     tc::relinquish();
   }
   // __syncthreads is an aligned barrier: every warp must reach it converged
@@ -921,18 +971,20 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
       if constexpr (kMx)
         producer_mx(p, x);
       else
-        producer_e4m3(p, x);
+        producer_e4m3<kTok>(p, x);
     }
   } else if (warp == 1) {
-    if (lane == 0) qk_issuer<kMx>(p, x);
+    if (lane == 0) qk_issuer<kMx, kTok>(p, x);
   } else if (warp == 2) {
-    if (lane == 0) pv_issuer<kMx>(p, x);
+    if (lane == 0) pv_issuer<kMx, kTok>(p, x);
   } else if (warp == 3) {
-    if (lane == 0) q_loader<kMx>(p, x);
-  } else if (warp < 8) {
-    softmax_epilogue<kMx>(p, x, warp & 3, lane);
+    if (lane == 0) q_loader<kMx, kTok>(p, x);
+  } else if (warp < 4 + 4 * (kMx ? 1 : kTok)) {
+    // softmax group (warp - 4) / 4: one per query token of the unit (one call
+    // site, so that both groups run the same code)
+    softmax_epilogue<kMx, kTok>(p, x, warp & 3, lane, kTok == 1 ? 0 : (warp - 4) >> 2);
   } else {
-    converter_mx(p, x, warp - 8, lane);
+    if constexpr (kMx) converter_mx(p, x, warp - 8, lane);
   }
 
   if ((warp == 1 || warp == 2) && lane == 0) {
@@ -946,21 +998,21 @@ __global__ void __launch_bounds__(Geo<kMx>::threads, 1) mla_split_tc_kernel(cons
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (warp == 1) tc::dealloc(x.tmem, kTmemCols);
+  if (warp == 1) tc::dealloc(x.tmem, Tmem<kTok>::cols);
 }
 
 }  // namespace tcfp8
 
-template <bool kMx>
+template <bool kMx, int kTok = 1>
 inline cudaError_t launch_split_tc(const Stage1Params& p, cudaStream_t stream) {
-  using L = tcfp8::Layout<kMx>;
+  using L = tcfp8::Layout<kMx, kTok>;
   static_assert(L::total <= 232448, "shared memory carve-up exceeds the 227 KB per-CTA limit");
   static_assert(L::qs % 1024 == 0 && L::pb % 1024 == 0 && L::rope % 1024 == 0, "swizzled operand alignment");
   static_assert(L::stage % 16 == 0, "bulk-copy destination alignment");
-  cudaError_t e = smem_opt_in<tcfp8::mla_split_tc_kernel<kMx>>(L::total);
+  cudaError_t e = smem_opt_in<tcfp8::mla_split_tc_kernel<kMx, kTok>>(L::total);
   if (e != cudaSuccess) return e;
-  e = launch_overlapped(tcfp8::mla_split_tc_kernel<kMx>, dim3(p.grid), dim3(tcfp8::Geo<kMx>::threads), L::total,
-                        stream, p);
+  e = launch_overlapped(tcfp8::mla_split_tc_kernel<kMx, kTok>, dim3(p.grid), dim3(tcfp8::Geo<kMx, kTok>::threads),
+                        L::total, stream, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -316,3 +316,40 @@ def test_multi_token(orc, dtype, q_len, lens, num_splits):
     vmax = np.repeat(v_absmax(inp), q_len, axis=0)
     assert_parity(out.double().cpu().numpy(), ref, lse.double().cpu().numpy(), ref_lse,
                   f"multi-token {dtype} q_len={q_len}", vmax)
+
+
+@pytest.mark.parametrize("lens,num_sms,num_splits,qstride", [
+    ([1000, 1, 0, 64, 2500, 2, 129, 128, 257], 0, 0, 2),
+    ([1000, 1, 0, 64, 2500, 2, 129, 128, 257], 0, 3, 3),
+    ([1000, 1, 0, 64, 2500, 2, 129, 128, 257], 0, 17, 2),
+    ([8192] * 6 + [1, 0, 130], 7, 0, 2),
+    ([300] * 40, 3, 0, 2),
+])
+def test_two_token_fused(orc, lens, num_sms, num_splits, qstride):
+    """e4m3 with two tokens per sequence: one work unit serves both tokens, so
+    the cache rows are read once; token 0 does not see its sequence's last row
+    (token 1's own entry).  Ragged tails of one row, sequences of one and two
+    rows, forced splits that leave a one-row last unit, the contiguous schedule
+    with several units per CTA, and query rows at a stride of 3 (qo_indptr)."""
+    inp = synth.make_inputs(lens, "fp8", seed=131)
+    g = torch.Generator("cpu").manual_seed(7)
+    q = torch.randn(len(lens) * qstride, 16, 576, generator=g).to(torch.bfloat16)
+    qo = torch.arange(len(lens) + 1, dtype=torch.int32) * qstride
+    dev = torch.device("cuda:0")
+    dec = binding.MLADecoder(inp.kv_indptr, "fp8", device=dev, num_sms=num_sms, num_splits=num_splits, q_len=2)
+    assert dec.plan.tokens_fused == 2 and dec.plan.batch == 2 * len(lens)
+    if num_sms == 7:
+        assert dec.plan.schedule == 1 and dec.plan.units_per_cta > 1
+    runs = []
+    for _ in range(2):
+        out, lse = dec(q.to(dev), inp.kv.to(dev), inp.kv_indptr.to(dev), qo.to(dev), kv_scale=inp.kv_scale.to(dev))
+        torch.cuda.synchronize()
+        runs.append((out.double().cpu().numpy(), lse.double().cpu().numpy()))
+    assert np.array_equal(runs[0][0], runs[1][0]) and np.array_equal(runs[0][1], runs[1][1])
+    assert dec.poll_error() == 0
+    ref, ref_lse = orc.decode_multi(CODES["fp8"], q, inp.kv, inp.kv_indptr, 2, qo, kv_scale=inp.kv_scale.numpy())
+    vmax = np.repeat(v_absmax(inp), 2, axis=0)
+    assert_parity(runs[0][0], ref, runs[0][1], ref_lse, f"two-token fused {lens[:3]} splits={num_splits}", vmax)
+    for b, L in enumerate(lens):
+        if L <= 1:  # token 0 sees no row
+            assert np.all(runs[0][0][2 * b] == 0) and np.all(np.isneginf(runs[0][1][2 * b]))

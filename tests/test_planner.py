@@ -219,13 +219,41 @@ def test_multi_token_plan_matches_token_lengths():
         sms = rng.choice([7, 152])
         ind = np.cumsum([0] + lens).astype(np.int32)
         plan = binding.mla_decode_plan_multi(ind, q_len, dtype, num_sms=sms)
+        if q_len == 2 and dtype == "fp8":
+            continue  # the fused form (test below)
         tok = [max(0, L - (q_len - 1 - i)) for L in lens for i in range(q_len)]
         ref = binding.mla_decode_plan(np.cumsum([0] + tok).astype(np.int32), dtype, num_sms=sms)
         d, r = plan.as_dict(), ref.as_dict()
         assert d.pop("q_len") == q_len and r.pop("q_len") == 0
         assert d.pop("total_kv") == ind[-1]
         r.pop("total_kv")
+        assert d.pop("tokens_fused") == 0 and r.pop("tokens_fused") == 0
         assert d == r and plan.batch == b * q_len
+
+
+def test_two_token_e4m3_plan_is_fused():
+    """e4m3 with two tokens per sequence: the unit list is the one-token plan
+    of the sequences' full lengths, each unit serving both tokens (two output
+    rows and two partial slots per unit)."""
+    rng = random.Random(12)
+    for _ in range(60):
+        b = rng.randint(1, 40)
+        lens = [rng.choice([0, 1, 2, 129, rng.randint(1, 300), rng.randint(1, 9000)]) for _ in range(b)]
+        sms = rng.choice([3, 7, 152])
+        splits = rng.choice([0, 0, 1, 3, 17])
+        ind = np.cumsum([0] + lens).astype(np.int32)
+        plan = binding.mla_decode_plan_multi(ind, 2, "fp8", num_sms=sms, num_splits=splits)
+        ref = binding.mla_decode_plan(ind, "fp8", num_sms=sms, num_splits=splits)
+        d, r = plan.as_dict(), ref.as_dict()
+        assert (d.pop("q_len"), d.pop("tokens_fused"), d.pop("batch"), d.pop("num_work")) == \
+            (2, 2, 2 * b, 2 * ref.num_work)
+        for k in ("q_len", "tokens_fused", "batch", "num_work"):
+            r.pop(k)
+        assert d == r
+        assert binding.mla_decode_workspace_bytes(plan) > binding.mla_decode_workspace_bytes(ref)
+    for dtype in ("bf16", "mxfp4"):
+        assert binding.mla_decode_plan_multi([0, 300], 2, dtype, num_sms=152).tokens_fused == 0
+    assert binding.mla_decode_plan_multi([0, 300], 3, "fp8", num_sms=152).tokens_fused == 0
 
 
 def test_multi_token_plan_rules():
