@@ -112,16 +112,17 @@ def kernel_source_sha(kv_dtype: str) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """dram bytes per split-kernel launch from the committed ncu summary, if it
-    was taken on the current kernel source (else None)."""
+def profiled_traffic(workload: str, kv_dtype: str):
+    """dram bytes per split-kernel launch from the committed ncu summary of this
+    workload key (e.g. "bs64_kv8192_fp8_q2"), if it was taken on the current
+    kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("kernel_sha") != kernel_source_sha(synth.WORKLOADS[workload][2]):
+    if not e or e.get("kernel_sha") != kernel_source_sha(kv_dtype):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -454,7 +455,8 @@ def main():
             "kv_gbs": round(kv_bytes / (us * 1e-6) / 1e9, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
-                         "traffic": profiled_traffic(name) if paged is None else None,
+                         "traffic": (profiled_traffic(name + (f"_q{args.q_len}" if args.q_len > 1 else ""), dt)
+                                     if paged is None else None),
                          "kernel": KERNEL_NAMES[dt] if paged is None else "whole paged call",
                          "kernel_us": round(t_split, 3),
                          "combine_us": round(t_comb, 3), "peak_kind": f"{peak_kind} (HBM copy)"},
