@@ -98,6 +98,9 @@ constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kBarSoftmax = 1;  // named barrier of softmax group 0 (128 threads); group 1: 2
 constexpr uint32_t kIdescQK = tc::idesc_e4m3(128, 32, 0, 0);
 constexpr uint32_t kIdescPV = tc::idesc_e4m3(128, 32, 1, 1);
+// two tokens per unit: one MMA with N = 64 covers both tokens' columns
+constexpr uint32_t kIdescQK2 = tc::idesc_e4m3(128, 64, 0, 0);
+constexpr uint32_t kIdescPV2 = tc::idesc_e4m3(128, 64, 1, 1);
 
 template <bool kMx, int kTok = 1>
 struct Layout {
@@ -497,7 +500,13 @@ __device__ void q_loader(const Stage1Params& p, const Ctx& x) {
 #pragma unroll
     for (int i = 0; i < kTok; ++i) {
       const uint8_t* src = p.ws_q + ((size_t)x.units[k].b * kTok + i) * kQPrepBytes;
-      bulk_g2s(x.smem + L::qs + i * kQsBytes, src, (uint32_t)kQImageBytes, &x.bar[kQFull], pol);
+      if constexpr (kTok == 1) {
+        bulk_g2s(x.smem + L::qs, src, (uint32_t)kQImageBytes, &x.bar[kQFull], pol);
+      } else {
+        // K block c of both tokens side by side (rows 32 i + r): the N = 64 B operand
+        for (int c = 0; c < 9; ++c)
+          bulk_g2s(x.smem + L::qs + c * 2048 * kTok + i * 2048, src + c * 2048, 2048u, &x.bar[kQFull], pol);
+      }
       bulk_g2s(x.smem + L::rq + i * 16 * sizeof(float), src + kQImageBytes, 16 * sizeof(float), &x.bar[kQFull],
                pol);
     }
@@ -523,12 +532,13 @@ __device__ void q_loader(const Stage1Params& p, const Ctx& x) {
 constexpr uint64_t kTplK64 = tc::desc_template(16, 512, 4);          // K-major, 64 B swizzle
 constexpr uint64_t kTplV = tc::desc_template(kChunkBytes, 512, 4);   // V^T, MN-major, 64 B swizzle
 constexpr uint64_t kTplP = tc::desc_template(1024, 256, 6);          // P^T, MN-major, 32 B swizzle
+constexpr uint64_t kTplP2 = tc::desc_template(kPBytes, 256, 6);      // two tokens' P^T: 32-byte atoms kPBytes apart
 __host__ __device__ constexpr uint32_t lo_word(uint64_t d) { return (uint32_t)d; }
 __host__ __device__ constexpr uint32_t hi_word(uint64_t d) { return (uint32_t)(d >> 32); }
 
 
 // QK of every tile: S^T(t) into TMEM columns [blk (t mod 2), +blk), token i's
-// scores at +32 i from its own query image.
+// scores at +32 i (two tokens: one N = 64 MMA per k step over both query images).
 template <bool kMx, int kTok>
 __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
   using L = Layout<kMx, kTok>;
@@ -568,10 +578,9 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
         const int c = ks >> 1, half = ks & 1;
         const uint32_t a =
             c < 8 ? ap[c >> 1] + (((c & 1) * kChunkBytes + 32 * half) >> 4) : ar + ((32 * half) >> 4);
-#pragma unroll
-        for (int i = 0; i < kTok; ++i)
-          tc::mma_f8_words(d + 32 * i, a, hi_word(kTplK64), bq + ((i * kQsBytes + c * 2048 + 32 * half) >> 4),
-                           hi_word(kTplK64), kIdescQK, ks > 0 ? 1u : 0u);
+        // both tokens' query rows form one B operand (block c: 32 kTok rows of 64 B)
+        tc::mma_f8_words(d, a, hi_word(kTplK64), bq + ((c * 2048 * kTok + 32 * half) >> 4), hi_word(kTplK64),
+                         kTok == 1 ? kIdescQK : kIdescQK2, ks > 0 ? 1u : 0u);
       }
       tc::commit(&x.bar[kSFull + (it & 1)]);
       tc::commit(&x.bar[kRopeEmpty + it % kRopeSlots]);
@@ -581,8 +590,8 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
 }
 
 // P.V of every tile: O^T += V^T(t) . P^T(t) (token i: its own P buffer and O^T
-// columns); releases the tile's ring slots, its P buffers and, on a unit's
-// last tile, the unit's O^T.
+// columns, both in one N = 64 MMA); releases the tile's ring slots, its P
+// buffers and, on a unit's last tile, the unit's O^T.
 template <bool kMx, int kTok>
 __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
   using L = Layout<kMx, kTok>;
@@ -599,7 +608,8 @@ __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
       if (t == 0 && ordinal > 0) wait_phase(&x.bar[kOFree], (ordinal - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
       tc::fence_after();
-      const uint32_t bp = lo_word(kTplP) + ((pb0 + (uint32_t)(it & 1) * kTok * kPBytes) >> 4);
+      constexpr uint64_t kTplPT = kTok == 1 ? kTplP : kTplP2;
+      const uint32_t bp = lo_word(kTplPT) + ((pb0 + (uint32_t)(it & 1) * kTok * kPBytes) >> 4);
       const int s0 = (4 * it) % kPairSlots;
 #pragma unroll
       for (int fb = 0; fb < 4; ++fb) {
@@ -607,12 +617,9 @@ __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
         // V^T block: features [128 fb, 128 fb + 128) = the slot's two column blocks (LBO)
         const uint32_t av = lo_word(kTplV) + ((pairs0 + (uint32_t)sl * kPairBytes) >> 4);
 #pragma unroll
-        for (int i = 0; i < kTok; ++i)
-#pragma unroll
-          for (int q = 0; q < 4; ++q)  // rows [32 q, 32 q + 32): +2048 B of V^T, +1024 B of P^T
-            tc::mma_f8_words(x.tmem + TM::o + TM::blk * fb + 32 * i, av + q * (2048 >> 4), hi_word(kTplV),
-                             bp + ((i * kPBytes + q * 1024) >> 4), hi_word(kTplP), kIdescPV,
-                             (t == 0 && q == 0) ? 0u : 1u);
+        for (int q = 0; q < 4; ++q)  // rows [32 q, 32 q + 32): +2048 B of V^T, +1024 B of P^T (every token)
+          tc::mma_f8_words(x.tmem + TM::o + TM::blk * fb, av + q * (2048 >> 4), hi_word(kTplV), bp + q * (1024 >> 4),
+                           hi_word(kTplPT), kTok == 1 ? kIdescPV : kIdescPV2, (t == 0 && q == 0) ? 0u : 1u);
         tc::commit(&x.bar[kPairEmpty + sl]);
       }
       tc::commit(&x.bar[kODone]);
