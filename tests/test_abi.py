@@ -75,3 +75,27 @@ def test_empty_batch_is_a_noop(lib):
     assert plan.batch == 0 and plan.num_work == 0
     assert lib.mla_decode_fwd(None, None, None, 0, None, None, None, None, 1 / 24, ctypes.byref(plan), None, 0,
                               None) == 0
+
+
+def test_plan_struct_layout_matches_header(tmp_path):
+    """The ctypes mirror of mla_plan has the C header's size and field offsets
+    (a plain C program built against include/mla_decode.h prints them)."""
+    import shutil
+    import subprocess
+    from mla_attention_decode_gb300 import binding
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [name for name, _ in binding.mla_plan._fields_]
+    src = tmp_path / "plan_layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "mla_decode.h"\nint main(void) {\n'
+                   '  printf("size %zu\\n", sizeof(mla_plan));\n' +
+                   "".join(f'  printf("{f} %zu\\n", offsetof(mla_plan, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "plan_layout"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = dict(line.split() for line in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                         text=True).stdout.splitlines())
+    assert int(out.pop("size")) == ctypes.sizeof(binding.mla_plan)
+    for f in fields:
+        assert int(out[f]) == getattr(binding.mla_plan, f).offset, f
