@@ -99,3 +99,26 @@ def test_plan_struct_layout_matches_header(tmp_path):
     assert int(out.pop("size")) == ctypes.sizeof(binding.mla_plan)
     for f in fields:
         assert int(out[f]) == getattr(binding.mla_plan, f).offset, f
+
+
+def test_fwd_rejects_inconsistent_two_token_plans_without_cuda(lib):
+    """A two-token plan is e4m3 with q_len 2 and two partial slots per unit;
+    any other combination is refused on the host before any CUDA call."""
+    from mla_attention_decode_gb300 import binding
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+
+    def fwd(plan):
+        return lib.mla_decode_fwd(fake, fake, fake, 0, fake, fake, fake, None, 1 / 24, ctypes.byref(plan), fake,
+                                  1 << 30, None)
+
+    good = binding.mla_decode_plan_multi([0, 300, 700], 2, "fp8", num_sms=152)
+    assert good.tokens_fused == 2 and good.q_len == 2 and good.num_work % 2 == 0
+    for field, value in (("tokens_fused", 3), ("tokens_fused", 1), ("q_len", 3), ("kv_dtype", 0), ("num_work", 3)):
+        bad = binding.mla_plan.from_buffer_copy(good)
+        setattr(bad, field, value)
+        assert fwd(bad) == binding.MLA_ERR_INVALID_ARG, (field, value)
+    # a one-token plan may not claim two tokens per unit
+    one = binding.mla_decode_plan([0, 300, 700], "fp8", num_sms=152)
+    one.tokens_fused = 2
+    assert fwd(one) == binding.MLA_ERR_INVALID_ARG
