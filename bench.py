@@ -195,56 +195,71 @@ def time_calls(fn, steps, flush, stream):
     return [a.elapsed_time(b) * 1e3 for a, b in ev]
 
 
-def cpu_baseline(inp: synth.MLAInputs, budget_s: float = 20.0):
-    """Times the oracle as it stands on the host cores; returns (us per full call, cores, sample text)."""
+def oracle_decoder(inp: synth.MLAInputs, q_len: int = 1, paged=None):
+    """The fp64 C oracle as it stands, on the host cores: returns (decode(n), cores),
+    decode(n) evaluating the first n sequences of the workload in its form
+    (q_len tokens per sequence, or read through the page table)."""
     import oracle
     orc = oracle.load()
     cores = os.cpu_count() or 1
-    lens = (inp.kv_indptr[1:] - inp.kv_indptr[:-1]).tolist()
+    code = CODES[inp.kv_dtype]
     kvs = None if inp.kv_scale is None else inp.kv_scale.numpy()
     bs = None if inp.block_scales is None else inp.block_scales.numpy()
+
+    def decode(n):
+        qo = inp.qo_indptr[:n + 1].numpy()
+        if paged is not None:
+            pbs = None if paged.block_scales is None else paged.block_scales.numpy()
+            return orc.decode_paged(code, inp.q, paged.kv, paged.page_indptr[:n + 1].numpy(),
+                                    paged.kv_indices.numpy(), paged.last_page_len[:n].numpy(), paged.page_size,
+                                    qo, kvs, pbs, num_threads=cores)
+        if q_len > 1:
+            return orc.decode_multi(code, inp.q, inp.kv, inp.kv_indptr[:n + 1].numpy(), q_len, qo, kvs, bs,
+                                    num_threads=cores)
+        return orc.decode(code, inp.q, inp.kv, inp.kv_indptr[:n + 1].numpy(), qo, kvs, bs, num_threads=cores)
+
+    return decode, cores
+
+
+def cpu_baseline(inp: synth.MLAInputs, q_len: int = 1, paged=None, budget_s: float = 20.0):
+    """Times the oracle as it stands on the host cores; returns (us per full call, cores, sample text)."""
+    decode, cores = oracle_decoder(inp, q_len, paged)
+    lens = (inp.kv_indptr[1:] - inp.kv_indptr[:-1]).tolist()
     # probe one sequence to size the sample
     t0 = time.perf_counter()
-    orc.decode(CODES[inp.kv_dtype], inp.q, inp.kv, inp.kv_indptr[:2].numpy(), inp.qo_indptr[:2].numpy(), kvs, bs,
-               num_threads=cores)
+    decode(1)
     per_seq = max(time.perf_counter() - t0, 1e-4)
     nseq = max(1, min(inp.batch, int(budget_s / per_seq)))
-    ind = inp.kv_indptr[:nseq + 1].numpy()
     t0 = time.perf_counter()
-    orc.decode(CODES[inp.kv_dtype], inp.q, inp.kv, ind, inp.qo_indptr[:nseq + 1].numpy(), kvs, bs, num_threads=cores)
+    decode(nseq)
     dt = time.perf_counter() - t0
     us_call = dt * 1e6 * (sum(lens) / max(1, sum(lens[:nseq])))
-    sample = (f"{nseq} of {inp.batch} sequences (all 16 heads), fp64 C oracle with OpenMP, "
+    form = (f", {q_len} tokens each" if q_len > 1 else "") + (", through the page table" if paged is not None else "")
+    sample = (f"{nseq} of {inp.batch} sequences (all 16 heads{form}), fp64 C oracle with OpenMP, "
               f"scaled by KV rows to the full call")
     return us_call, cores, sample
 
 
-def run_reference(args, inp, name):
+def run_reference(args, inp, name, paged=None):
     rank, world, _ = dist_env()
     if world > 1 and rank != 0:
         return
-    import oracle
-    orc = oracle.load()
-    cores = os.cpu_count() or 1
-    kvs = None if inp.kv_scale is None else inp.kv_scale.numpy()
-    bs = None if inp.block_scales is None else inp.block_scales.numpy()
+    decode, cores = oracle_decoder(inp, args.q_len, paged)
     lens = (inp.kv_indptr[1:] - inp.kv_indptr[:-1]).tolist()
+
     # bound each step to ~2 s of CPU work: a sample of sequences, scaled by rows
     t0 = time.perf_counter()
-    orc.decode(CODES[inp.kv_dtype], inp.q, inp.kv, inp.kv_indptr[:2].numpy(), inp.qo_indptr[:2].numpy(), kvs, bs,
-               num_threads=cores)
+    decode(1)
     per_seq = max(time.perf_counter() - t0, 1e-4)
     budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
     nseq = max(1, min(inp.batch, int(budget / per_seq)))
-    ind = inp.kv_indptr[:nseq + 1].numpy()
-    qo = inp.qo_indptr[:nseq + 1].numpy()
     scale = sum(lens) / max(1, sum(lens[:nseq]))
     for _ in range(args.warmup):
-        orc.decode(CODES[inp.kv_dtype], inp.q, inp.kv, ind, qo, kvs, bs, num_threads=cores)
+        decode(nseq)
     ts = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        orc.decode(CODES[inp.kv_dtype], inp.q, inp.kv, ind, qo, kvs, bs, num_threads=cores)
+        decode(nseq)
         ts.append((time.perf_counter() - t0) * 1e6 * scale)
     us = statistics.mean(ts)
     b, L, dt = synth.WORKLOADS[name]
@@ -252,7 +267,9 @@ def run_reference(args, inp, name):
         "impl": "reference", "metric": "us_per_mla_decode_call", "value": round(us, 2), "unit": "us/call",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": name, "batch": b, "kv_len": L, "kv_dtype": dt},
+        "config": {"workload": name + (f"_paged{args.page_size}" if paged is not None else "") +
+                               (f"_q{args.q_len}" if args.q_len > 1 else ""), "batch": b, "kv_len": L,
+                   "kv_dtype": dt, "page_size": args.page_size or 1, "q_len": args.q_len},
         "cpu_baseline": {"value": round(us, 2), "unit": "us/call", "cores": cores, "kind": "oracle",
                          "sample": f"{nseq} of {inp.batch} sequences per step, scaled by KV rows"},
         "e2e": {"value": round(us, 2), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -266,8 +283,16 @@ def main():
     name = args.workload
     b, L, dt = synth.WORKLOADS[name]
     inp = synth.make_inputs([L] * b, dt, seed=rank)
+    assert args.page_size == 0 or args.q_len == 1, "--page-size and --q-len are not combined"
+    if args.q_len > 1:
+        # q_len tokens per sequence: query rows b * q_len + i
+        g = torch.Generator("cpu").manual_seed(1000 + rank)
+        inp.q = torch.randn(b * args.q_len, 16, 576, generator=g).to(torch.bfloat16)
+        inp.qo_indptr = torch.arange(b + 1, dtype=torch.int32) * args.q_len
+    # the same rows in a paged cache: pages at random positions (no spare pages)
+    paged = synth.make_paged(inp, args.page_size, seed=rank, spare_pages=0) if args.page_size else None
     if args.impl == "reference":
-        run_reference(args, inp, name)
+        run_reference(args, inp, name, paged)
         return
 
     from mla_attention_decode_gb300 import binding, build
@@ -286,16 +311,8 @@ def main():
             pg.barrier()
         torch.cuda.synchronize()
 
-    if args.q_len > 1:
-        # q_len tokens per sequence: query rows b * q_len + i
-        g = torch.Generator("cpu").manual_seed(1000 + rank)
-        inp.q = torch.randn(b * args.q_len, 16, 576, generator=g).to(torch.bfloat16)
-        inp.qo_indptr = torch.arange(b + 1, dtype=torch.int32) * args.q_len
     d = to_device(inp, dev)
-    paged = None
-    if args.page_size:
-        # the same rows in a paged cache: pages at random positions (no spare pages)
-        paged = synth.make_paged(inp, args.page_size, seed=rank, spare_pages=0)
+    if paged is not None:
         d["kv"] = paged.kv.to(dev)
         if dt == "mxfp4":
             d["kv_scale"] = paged.block_scales.to(dev)
@@ -306,7 +323,6 @@ def main():
                                       device=dev)
     else:
         dec = binding.MLADecoder(inp.kv_indptr, dt, device=dev, q_len=args.q_len)
-    assert paged is None or args.q_len == 1, "--page-size and --q-len are not combined"
     plan = dec.plan
     out = torch.empty(plan.batch, 16, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(plan.batch, 16, dtype=torch.float32, device=dev)
@@ -437,8 +453,8 @@ def main():
 
     if rank == 0:
         cpu = None
-        if not args.no_cpu_baseline and world == 1 and args.q_len == 1:
-            us_cpu, cores, sample = cpu_baseline(inp)
+        if not args.no_cpu_baseline and world == 1:
+            us_cpu, cores, sample = cpu_baseline(inp, args.q_len, paged)
             cpu = {"value": round(us_cpu, 1), "unit": "us/call", "cores": cores, "kind": "oracle", "sample": sample}
         line = {
             "metric": "us_per_mla_decode_call", "value": round(us, 3), "unit": "us/call", "n_gpus": world,
