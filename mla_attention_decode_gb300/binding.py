@@ -233,7 +233,9 @@ class MLADecoder:
     """Plan + workspace for one batch layout; call it with device tensors.
 
     The workspace is allocated once here (torch device memory) and zeroed; the
-    library itself never allocates."""
+    library itself never allocates.  ``q_len > 1``: that many query tokens per
+    sequence (rows ``qo_indptr[b] + i``, output rows ``b * q_len + i``); e4m3 KV
+    with ``q_len == 2`` gets the single-pass plan (``plan.tokens_fused == 2``)."""
 
     def __init__(self, kv_indptr_host, kv_dtype, device="cuda", num_sms: int = 0, num_splits: int = 0,
                  q_len: int = 1):
