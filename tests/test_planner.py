@@ -261,3 +261,41 @@ def test_multi_token_plan_rules():
         with pytest.raises(binding.MLAError) as e:
             binding.mla_decode_plan_multi([0, 10], q_len, "fp8", num_sms=152)
         assert e.value.status == binding.MLA_ERR_UNSUPPORTED
+
+
+def test_two_token_slots_partition_the_workspace():
+    """Two-token plans (mla_decode.h): token i of unit s of sequence b writes
+    partial slot 2 ub + i S_b + s (ub = the sequence's first unit).  Over a
+    batch the slots are a partition of [0, num_work), each token's slots are
+    contiguous (what the combine kernel reads), and a token's last unit is
+    the unit that holds its sequence's last row."""
+    rng = random.Random(13)
+    for _ in range(40):
+        b = rng.randint(1, 50)
+        lens = [rng.choice([0, 1, 2, 129, rng.randint(1, 4000), rng.randint(1, 20000)]) for _ in range(b)]
+        sms = rng.choice([4, 9, 152])
+        splits = rng.choice([0, 0, 3, 17])
+        ind = np.cumsum([0] + lens).astype(np.int32)
+        plan = binding.mla_decode_plan_multi(ind, 2, "fp8", num_sms=sms, num_splits=splits)
+        one = binding.mla_decode_plan(ind, "fp8", num_sms=sms, num_splits=splits)
+        S = n_splits_of(one, lens)
+        assert sum(S) * 2 == plan.num_work
+        seen = []
+        ub = 0
+        for Sb in S:
+            for i in range(2):
+                slots = [2 * ub + i * Sb + s for s in range(Sb)]
+                assert slots == list(range(slots[0], slots[0] + Sb))
+                seen += slots
+            ub += Sb
+        assert sorted(seen) == list(range(plan.num_work))
+        units = units_of(one, lens)
+        u = 0
+        for bi, (L, Sb) in enumerate(zip(lens, S)):
+            # the sequence's units tile its rows in order; the last one ends at its
+            # last row, the only row token 0 does not see
+            mine = units[u:u + Sb]
+            assert mine[0][0] == ind[bi] and mine[-1][1] == ind[bi + 1]
+            assert all(x[1] == y[0] for x, y in zip(mine, mine[1:]))
+            assert all(x[1] > x[0] for x in mine) or L == 0
+            u += Sb
