@@ -67,3 +67,22 @@ def test_reference_arm_runs_on_rank0_only():
     line = json.loads(r0.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.parametrize("extra,suffix", [
+    ([], ""),
+    (["--q-len", "2"], "_q2"),
+    (["--page-size", "64"], "_paged64"),
+])
+def test_reference_arm_times_the_same_form(extra, suffix):
+    """--impl reference times the oracle on the workload in the form the GPU arm
+    decodes it (several tokens per sequence, or through a page table) and names
+    it the same way."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--workload", "bs4_kv1024_bf16", *extra],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    assert line["impl"] == "reference" and line["config"]["workload"] == "bs4_kv1024_bf16" + suffix
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
