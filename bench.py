@@ -1,23 +1,30 @@
-"""Benchmark: microseconds per MLA decode call on one synthetic workload.
+"""Benchmark: microseconds per MLA decode call on the synthetic workloads.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step = one mla_decode_fwd call (split kernel + log-sum-exp combine) over one
-batch, inputs resident in HBM, with the L2 flushed (a 256 MiB device write)
-before every timed call; each call is bracketed by CUDA events on its stream.
-Under torchrun (N > 1) every rank decodes its own batch of the same shape
+One step = one mla_decode_fwd call (query preparation, split kernel and
+log-sum-exp combine) over one batch, inputs resident in HBM, with the L2
+flushed before every timed call (a 256 MiB device write); each call is
+bracketed by CUDA events on its stream.  The headline workload is the
+largest one, bs=64, kv_len=8192, e4m3 KV (302 MB of cache per call).  Under
+torchrun (N > 1) every rank decodes its own batch of the same shape
 (independent sequences, no collective on the data path: weak scaling); the
 timed loop is bracketed by a barrier and synchronize, the per-call time is the
 max over ranks.  Rank 0 prints one JSON line.
 
 Extra keys:
-  roofline     the split kernel alone (timed in a second pass through the
-               split/combine entry points, events on the launch stream) against
-               the measured HBM copy bandwidth; algorithmic bytes = KV bytes.
-  cpu_baseline the fp64 C oracle on the host cores (full workload when it takes
-               seconds, else a bounded sample of sequences, scaled).
-  e2e          the same metric through the public call with pinned host q /
-               indptrs copied in and out / lse copied back inside the timed region.
+  roofline     the split stage alone (query preparation + split kernel, timed
+               in a second pass through the split/combine entry points, events
+               on the launch stream) against the measured HBM copy bandwidth;
+               algorithmic bytes = KV bytes.
+  per_config   (one GPU) every one of the five workloads timed the same way in
+               the same run: us per call, split stage, combine, roofline
+               fraction, and the oracle's CPU time on a bounded sample.
+  cpu_baseline the fp64 C oracle on the host cores (a bounded sample of
+               sequences, scaled by KV rows to the full call).
+  e2e          the same metric through the public call with the step's inputs
+               (q and the index arrays) copied in from pinned host memory and
+               out/lse copied back inside the timed region.
   clocks       nvidia-smi samples taken during the timed region.
 
 --impl reference times the oracle (the pages' definition evaluated in fp64 on the
@@ -41,8 +48,9 @@ import torch  # noqa: E402
 
 from mla_attention_decode_gb300 import synth  # noqa: E402
 
-DEFAULT_WORKLOAD = "bs32_kv1024_fp8"
+DEFAULT_WORKLOAD = "bs64_kv8192_fp8"
 L2_FLUSH_BYTES = 256 << 20
+L2_TEXT = "flushed before every timed call (256 MiB write)"
 CODES = {"bf16": 0, "fp8": 1, "mxfp4": 2}
 DTYPE_LABEL = {"bf16": "bf16 x bf16 -> f32", "fp8": "e4m3 x e4m3 -> f32", "mxfp4": "e4m3 x e4m3 -> f32 (e2m1 KV)"}
 _CSRC = "mla_attention_decode_gb300/csrc/"
@@ -59,9 +67,11 @@ KERNEL_NAMES = {"bf16": "mla_split_kernel (mma.sync, bf16)",
                 "mxfp4": "mla_prep_q_kernel + mla_split_tc_kernel (tcgen05, e2m1 dequantised to e4m3), "
                          "launches overlapped"}
 CLOCK_SOAK_S = 1.0
+CPU_BUDGET_HEADLINE_S = 15.0
+CPU_BUDGET_PER_CONFIG_S = 4.0
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
@@ -69,13 +79,15 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOAD_ORDER)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the headline workload (per_config is otherwise added on one GPU)")
     ap.add_argument("--q-len", type=int, default=1,
                     help="query tokens per sequence (mla_decode_plan_multi; each token attends to the rows up "
                          "to its own entry)")
     ap.add_argument("--page-size", type=int, default=0,
                     help="decode the workload's rows from a paged cache with pages of this many rows "
                          "(pages scattered at random; mla_decode_fwd_paged); 0 = contiguous cache")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -125,6 +137,25 @@ def profiled_traffic(workload: str, kv_dtype: str):
     if not e or e.get("kernel_sha") != kernel_source_sha(kv_dtype):
         return None
     return e.get("dram_bytes_per_launch")
+
+
+def workload_key(name: str, args) -> str:
+    return name + (f"_paged{args.page_size}" if args.page_size else "") + (f"_q{args.q_len}" if args.q_len > 1 else "")
+
+
+def workload_kv_bytes(name: str) -> int:
+    """KV bytes (with scales) one call reads: the algorithmic bytes of the workload."""
+    b, L, dt = synth.WORKLOADS[name]
+    rows = b * L
+    return {"bf16": rows * 1152, "fp8": rows * 576 + 4, "mxfp4": rows * (288 + 18)}[dt]
+
+
+def workload_config(name: str, args, world: int) -> dict:
+    """The `config` object of the JSON line; both arms print the same one."""
+    b, L, dt = synth.WORKLOADS[name]
+    return {"workload": workload_key(name, args), "batch": b, "kv_len": L, "kv_dtype": dt,
+            "page_size": args.page_size or 1, "q_len": args.q_len, "kv_bytes_per_call": workload_kv_bytes(name),
+            "l2": L2_TEXT, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 class ClockSampler:
@@ -177,6 +208,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class L2Flush:
+    """Evicts the L2 between timed calls: a write of 256 MiB, twice the L2."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def __call__(self, i: int):
+        self.w.fill_(i & 0xFF)
+
+
 def to_device(inp: synth.MLAInputs, dev):
     scale = inp.kv_scale if inp.kv_dtype == "fp8" else inp.block_scales
     return dict(q=inp.q.to(dev), kv=inp.kv.to(dev), kv_scale=None if scale is None else scale.to(dev),
@@ -187,7 +228,7 @@ def time_calls(fn, steps, flush, stream):
     """Per-call device times (us) of `steps` calls, L2 flushed before each."""
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for i in range(steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         ev[i][0].record(stream)
         fn()
         ev[i][1].record(stream)
@@ -221,7 +262,7 @@ def oracle_decoder(inp: synth.MLAInputs, q_len: int = 1, paged=None):
     return decode, cores
 
 
-def cpu_baseline(inp: synth.MLAInputs, q_len: int = 1, paged=None, budget_s: float = 20.0):
+def cpu_baseline(inp: synth.MLAInputs, q_len: int = 1, paged=None, budget_s: float = CPU_BUDGET_HEADLINE_S):
     """Times the oracle as it stands on the host cores; returns (us per full call, cores, sample text)."""
     decode, cores = oracle_decoder(inp, q_len, paged)
     lens = (inp.kv_indptr[1:] - inp.kv_indptr[:-1]).tolist()
@@ -240,6 +281,20 @@ def cpu_baseline(inp: synth.MLAInputs, q_len: int = 1, paged=None, budget_s: flo
     return us_call, cores, sample
 
 
+def make_workload_inputs(name, args, rank):
+    """The seeded inputs of a workload in the form the run decodes it."""
+    b, L, dt = synth.WORKLOADS[name]
+    inp = synth.make_inputs([L] * b, dt, seed=rank)
+    if args.q_len > 1:
+        # q_len tokens per sequence: query rows b * q_len + i
+        g = torch.Generator("cpu").manual_seed(1000 + rank)
+        inp.q = torch.randn(b * args.q_len, 16, 576, generator=g).to(torch.bfloat16)
+        inp.qo_indptr = torch.arange(b + 1, dtype=torch.int32) * args.q_len
+    # the same rows in a paged cache: pages at random positions (no spare pages)
+    paged = synth.make_paged(inp, args.page_size, seed=rank, spare_pages=0) if args.page_size else None
+    return inp, paged
+
+
 def run_reference(args, inp, name, paged=None):
     rank, world, _ = dist_env()
     if world > 1 and rank != 0:
@@ -247,11 +302,12 @@ def run_reference(args, inp, name, paged=None):
     decode, cores = oracle_decoder(inp, args.q_len, paged)
     lens = (inp.kv_indptr[1:] - inp.kv_indptr[:-1]).tolist()
 
-    # bound each step to ~2 s of CPU work: a sample of sequences, scaled by rows
+    # bound the whole run to about 100 s of CPU work: a sample of sequences per
+    # step, scaled by rows
     t0 = time.perf_counter()
     decode(1)
     per_seq = max(time.perf_counter() - t0, 1e-4)
-    budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    budget = max(0.05, 100.0 / max(1, args.steps + args.warmup))
     nseq = max(1, min(inp.batch, int(budget / per_seq)))
     scale = sum(lens) / max(1, sum(lens[:nseq]))
     for _ in range(args.warmup):
@@ -262,14 +318,11 @@ def run_reference(args, inp, name, paged=None):
         decode(nseq)
         ts.append((time.perf_counter() - t0) * 1e6 * scale)
     us = statistics.mean(ts)
-    b, L, dt = synth.WORKLOADS[name]
     line = {
         "impl": "reference", "metric": "us_per_mla_decode_call", "value": round(us, 2), "unit": "us/call",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": name + (f"_paged{args.page_size}" if paged is not None else "") +
-                               (f"_q{args.q_len}" if args.q_len > 1 else ""), "batch": b, "kv_len": L,
-                   "kv_dtype": dt, "page_size": args.page_size or 1, "q_len": args.q_len},
+        "config": workload_config(name, args, world),
         "cpu_baseline": {"value": round(us, 2), "unit": "us/call", "cores": cores, "kind": "oracle",
                          "sample": f"{nseq} of {inp.batch} sequences per step, scaled by KV rows"},
         "e2e": {"value": round(us, 2), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -277,21 +330,127 @@ def run_reference(args, inp, name, paged=None):
     print(json.dumps(line), flush=True)
 
 
-def main():
-    args = parse()
+class Workload:
+    """One workload resident on the device, with its plan, workspace and the
+    calls the bench times."""
+
+    def __init__(self, name, args, rank, dev):
+        from mla_attention_decode_gb300 import binding
+        self.binding = binding
+        self.name = name
+        b, L, self.dt = synth.WORKLOADS[name]
+        self.inp, self.paged = make_workload_inputs(name, args, rank)
+        dt = self.dt
+        d = to_device(self.inp, dev)
+        if self.paged is not None:
+            pg_ = self.paged
+            d["kv"] = pg_.kv.to(dev)
+            if dt == "mxfp4":
+                d["kv_scale"] = pg_.block_scales.to(dev)
+            d["page_indptr"] = pg_.page_indptr.to(dev)
+            d["kv_indices"] = pg_.kv_indices.to(dev)
+            d["last_page_len"] = pg_.last_page_len.to(dev)
+            self.dec = binding.PagedMLADecoder(pg_.page_indptr, pg_.last_page_len, pg_.page_size, pg_.num_pages, dt,
+                                               device=dev)
+        else:
+            self.dec = binding.MLADecoder(self.inp.kv_indptr, dt, device=dev, q_len=args.q_len)
+        self.d = d
+        self.plan = self.dec.plan
+        self.out = torch.empty(self.plan.batch, 16, 512, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(self.plan.batch, 16, dtype=torch.float32, device=dev)
+        self.scale_stride = int(d["kv_scale"].stride(0)) if dt == "mxfp4" else 0
+        # query preparation (e4m3 and MXFP4 KV), split kernel, combine when split
+        self.launches_per_call = (1 if dt == "bf16" else 2) + (1 if self.plan.splits_max > 1 else 0)
+
+    def call(self, stream, src=None, out=None, lse=None):
+        """One mla_decode_fwd (or _paged) call; src/out/lse override the inputs
+        and results (host buffers for the end-to-end forms)."""
+        b, d = self.binding, self.d
+        s = d if src is None else src
+        o = self.out if out is None else out
+        l_ = self.lse if lse is None else lse
+        if self.paged is not None:
+            b.mla_decode_fwd_paged(s["q"], d["kv"], d["kv_scale"], s["page_indptr"], s["kv_indices"],
+                                   s["last_page_len"], s["qo_indptr"], o, l_, self.plan, self.dec.workspace,
+                                   scale_stride=self.scale_stride, stream=stream)
+        else:
+            b.mla_decode_fwd(s["q"], d["kv"], d["kv_scale"], s["kv_indptr"], s["qo_indptr"], o, l_, self.plan,
+                             self.dec.workspace, scale_stride=self.scale_stride, stream=stream)
+
+    def time_stages(self, steps, flush, stream, us_call):
+        """(split stage us, combine us): the two entry points timed separately,
+        L2 flushed before each call (the paged entry point has no separate
+        stages: the whole call stands in)."""
+        if self.paged is not None:
+            return us_call, 0.0
+        b, d = self.binding, self.d
+        ev_split, ev_comb = [], []
+        for i in range(steps):
+            flush(i)
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            b.mla_decode_split(d["q"], d["kv"], d["kv_scale"], d["kv_indptr"], d["qo_indptr"], self.out, self.lse,
+                               self.plan, self.dec.workspace, scale_stride=self.scale_stride, stream=stream)
+            e1.record(stream)
+            b.mla_decode_combine(self.out, self.lse, self.plan, self.dec.workspace, stream=stream)
+            e2.record(stream)
+            ev_split.append((e0, e1))
+            ev_comb.append((e1, e2))
+        torch.cuda.synchronize()
+        return (statistics.mean(a.elapsed_time(c) * 1e3 for a, c in ev_split),
+                statistics.mean(a.elapsed_time(c) * 1e3 for a, c in ev_comb))
+
+
+def roofline_entry(w: Workload, args, t_split: float, t_comb: float, peak: float, peak_kind: str) -> dict:
+    kv_bytes = w.inp.kv_bytes()
+    achieved = kv_bytes / (t_split * 1e-6) / 1e9
+    key = w.name + (f"_q{args.q_len}" if args.q_len > 1 else "")
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(key, w.dt) if w.paged is None else None,
+            "kernel": KERNEL_NAMES[w.dt] if w.paged is None else "whole paged call",
+            "kernel_us": round(t_split, 3), "combine_us": round(t_comb, 3),
+            "peak_kind": f"{peak_kind} (HBM copy)"}
+
+
+def measure_per_config(args, rank, dev, stream, flush, peak, peak_kind, headline: dict) -> dict:
+    """Every workload timed as the headline is (same flush, same events), one
+    after another; the headline's own entry is the headline's numbers."""
+    res = {}
+    for name in synth.WORKLOAD_ORDER:
+        if name == args.workload:
+            res[name] = headline
+            continue
+        w = Workload(name, args, rank, dev)
+        for _ in range(max(3, args.warmup)):
+            w.call(stream)
+        assert w.dec.poll_error() == 0, f"{name}: device error"
+        us = statistics.mean(time_calls(lambda: w.call(stream), args.steps, flush, stream))
+        t_split, t_comb = w.time_stages(args.steps, flush, stream, us)
+        assert w.dec.poll_error() == 0, f"{name}: device error"
+        entry = {"value": round(us, 3), "unit": "us/call", "kv_bytes_per_call": w.inp.kv_bytes(),
+                 "kv_gbs": round(w.inp.kv_bytes() / (us * 1e-6) / 1e9, 1),
+                 "roofline": roofline_entry(w, args, t_split, t_comb, peak, peak_kind),
+                 "gpu_launches": args.steps * w.launches_per_call,
+                 "plan": {k: w.plan.as_dict()[k] for k in ("num_work", "grid", "chunk_tokens", "splits_max",
+                                                          "schedule")}}
+        if not args.no_cpu_baseline:
+            us_cpu, cores, sample = cpu_baseline(w.inp, args.q_len, w.paged, budget_s=CPU_BUDGET_PER_CONFIG_S)
+            entry["cpu_baseline"] = {"value": round(us_cpu, 1), "unit": "us/call", "cores": cores, "kind": "oracle",
+                                     "sample": sample}
+        res[name] = entry
+        del w
+        torch.cuda.empty_cache()
+    return res
+
+
+def main(argv=None):
+    args = parse(argv)
     rank, world, local = dist_env()
     name = args.workload
-    b, L, dt = synth.WORKLOADS[name]
-    inp = synth.make_inputs([L] * b, dt, seed=rank)
     assert args.page_size == 0 or args.q_len == 1, "--page-size and --q-len are not combined"
-    if args.q_len > 1:
-        # q_len tokens per sequence: query rows b * q_len + i
-        g = torch.Generator("cpu").manual_seed(1000 + rank)
-        inp.q = torch.randn(b * args.q_len, 16, 576, generator=g).to(torch.bfloat16)
-        inp.qo_indptr = torch.arange(b + 1, dtype=torch.int32) * args.q_len
-    # the same rows in a paged cache: pages at random positions (no spare pages)
-    paged = synth.make_paged(inp, args.page_size, seed=rank, spare_pages=0) if args.page_size else None
     if args.impl == "reference":
+        inp, paged = make_workload_inputs(name, args, rank)
         run_reference(args, inp, name, paged)
         return
 
@@ -311,39 +470,12 @@ def main():
             pg.barrier()
         torch.cuda.synchronize()
 
-    d = to_device(inp, dev)
-    if paged is not None:
-        d["kv"] = paged.kv.to(dev)
-        if dt == "mxfp4":
-            d["kv_scale"] = paged.block_scales.to(dev)
-        d["page_indptr"] = paged.page_indptr.to(dev)
-        d["kv_indices"] = paged.kv_indices.to(dev)
-        d["last_page_len"] = paged.last_page_len.to(dev)
-        dec = binding.PagedMLADecoder(paged.page_indptr, paged.last_page_len, paged.page_size, paged.num_pages, dt,
-                                      device=dev)
-    else:
-        dec = binding.MLADecoder(inp.kv_indptr, dt, device=dev, q_len=args.q_len)
-    plan = dec.plan
-    out = torch.empty(plan.batch, 16, 512, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(plan.batch, 16, dtype=torch.float32, device=dev)
+    w = Workload(name, args, rank, dev)
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    scale_stride = int(d["kv_scale"].stride(0)) if dt == "mxfp4" else 0
-    # query preparation (e4m3 and MXFP4 KV), split kernel, combine when split
-    launches_per_call = (1 if dt == "bf16" else 2) + (1 if plan.splits_max > 1 else 0)
-
-    def call():
-        if paged is not None:
-            binding.mla_decode_fwd_paged(d["q"], d["kv"], d["kv_scale"], d["page_indptr"], d["kv_indices"],
-                                         d["last_page_len"], d["qo_indptr"], out, lse, plan, dec.workspace,
-                                         scale_stride=scale_stride, stream=stream)
-        else:
-            binding.mla_decode_fwd(d["q"], d["kv"], d["kv_scale"], d["kv_indptr"], d["qo_indptr"], out, lse, plan,
-                                   dec.workspace, scale_stride=scale_stride, stream=stream)
-
+    flush = L2Flush(dev)
     for _ in range(max(3, args.warmup)):
-        call()
-    assert dec.poll_error() == 0
+        w.call(stream)
+    assert w.dec.poll_error() == 0
 
     # ---- headline: whole call, device time, L2 flushed before each call.  The
     # clock samples cover the timed steps and a soak of the same flushed calls
@@ -352,8 +484,8 @@ def main():
         t_end = time.perf_counter() + seconds
         while time.perf_counter() < t_end:
             for i in range(20):
-                flush.fill_(i)
-                call()
+                flush(i)
+                w.call(stream)
             torch.cuda.synchronize()
 
     barrier()
@@ -361,44 +493,25 @@ def main():
         soak(CLOCK_SOAK_S / 2)
         barrier()
         t_wall = time.perf_counter()
-        per_call = time_calls(call, args.steps, flush, stream)
+        per_call = time_calls(lambda: w.call(stream), args.steps, flush, stream)
         barrier()
         t_wall = time.perf_counter() - t_wall
         soak(CLOCK_SOAK_S / 2)
     us = max_over_ranks([statistics.mean(per_call)], pg, dev)[0]
 
-    # ---- the split kernel alone (roofline) and the combine, events on the launch stream
-    ev_split, ev_comb = [], []
-    for i in range(args.steps if paged is None else 0):
-        flush.fill_(i & 0xFF)
-        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        e0.record(stream)
-        binding.mla_decode_split(d["q"], d["kv"], d["kv_scale"], d["kv_indptr"], d["qo_indptr"], out, lse, plan,
-                                 dec.workspace, scale_stride=scale_stride, stream=stream)
-        e1.record(stream)
-        binding.mla_decode_combine(out, lse, plan, dec.workspace, stream=stream)
-        e2.record(stream)
-        ev_split.append((e0, e1))
-        ev_comb.append((e1, e2))
-    torch.cuda.synchronize()
-    if paged is None:
-        t_split = statistics.mean(a.elapsed_time(c) * 1e3 for a, c in ev_split)
-        t_comb = statistics.mean(a.elapsed_time(c) * 1e3 for a, c in ev_comb)
-    else:
-        # the paged entry point has no separate stages: the whole call stands in
-        t_split, t_comb = us, 0.0
-    kv_bytes = inp.kv_bytes()
+    # ---- the split stage alone (roofline) and the combine, events on the launch stream
+    t_split, t_comb = w.time_stages(args.steps, flush, stream, us)
     peak, peak_kind = measured_peaks()
-    achieved = kv_bytes / (t_split * 1e-6) / 1e9
 
     # ---- end to end through the public call, with the step's inputs (q and the
     # index arrays) in pinned host memory and out/lse read back to it.  Two
-    # forms, both timed: "staged" moves each group by one explicit copy
-    # (binding.PackedBuffers); "host" passes the pinned host buffers to the call
+    # forms, both timed; the headline e2e value is always the "staged" form:
+    # one host-to-device copy of the inputs, the call, one device-to-host copy
+    # of out/lse.  "host_buffers" passes the pinned host buffers to the call
     # itself, so the kernels read the inputs and write the results over the
     # host link (NVLink-C2C on Grace) -- except q of bf16 KV, which that kernel
     # fetches with bulk copies and is therefore copied in first.
-    idx_names = ["kv_indptr"] if paged is None else ["page_indptr", "kv_indices", "last_page_len"]
+    inp, paged = w.inp, w.paged
     host_src = {"q": inp.q, "qo_indptr": inp.qo_indptr}
     if paged is None:
         host_src["kv_indptr"] = inp.kv_indptr
@@ -408,20 +521,12 @@ def main():
     ins = binding.PackedBuffers([(k, tuple(v.shape), v.dtype) for k, v in host_src.items()], dev)
     for k, v in host_src.items():
         ins.host[k].copy_(v)
-    outs = binding.PackedBuffers([("out", tuple(out.shape), out.dtype), ("lse", tuple(lse.shape), lse.dtype)], dev)
-
-    def decode_with(src, out_t, lse_t):
-        if paged is not None:
-            binding.mla_decode_fwd_paged(src["q"], d["kv"], d["kv_scale"], src["page_indptr"], src["kv_indices"],
-                                         src["last_page_len"], src["qo_indptr"], out_t, lse_t, plan, dec.workspace,
-                                         scale_stride=scale_stride, stream=stream)
-        else:
-            binding.mla_decode_fwd(src["q"], d["kv"], d["kv_scale"], src["kv_indptr"], src["qo_indptr"], out_t,
-                                   lse_t, plan, dec.workspace, scale_stride=scale_stride, stream=stream)
+    outs = binding.PackedBuffers([("out", tuple(w.out.shape), w.out.dtype), ("lse", tuple(w.lse.shape),
+                                                                             w.lse.dtype)], dev)
 
     def staged_call():
         ins.to_device(stream)
-        decode_with(ins.dev, outs.dev["out"], outs.dev["lse"])
+        w.call(stream, ins.dev, outs.dev["out"], outs.dev["lse"])
         outs.to_host(stream)
 
     host_in = dict(ins.host)
@@ -429,10 +534,10 @@ def main():
 
     def host_call():
         src = host_in
-        if dt == "bf16":
+        if w.dt == "bf16":
             q_dev.copy_(ins.host["q"], non_blocking=True)
             src = dict(host_in, q=q_dev)
-        decode_with(src, outs.host["out"], outs.host["lse"])
+        w.call(stream, src, outs.host["out"], outs.host["lse"])
 
     e2e_forms = {}
     for form, fn in (("staged", staged_call), ("host", host_call)):
@@ -441,52 +546,54 @@ def main():
         barrier()
         times = time_calls(fn, args.steps, flush, stream)
         torch.cuda.synchronize()
-        assert torch.equal(outs.host["out"], out.cpu()), f"end-to-end ({form}) output differs from the device call"
+        assert torch.equal(outs.host["out"], w.out.cpu()), f"end-to-end ({form}) output differs from the device call"
         e2e_forms[form] = statistics.mean(times)
-    e2e_times = [min(e2e_forms.values())]
-    e2e_form = min(e2e_forms, key=e2e_forms.get)
-    e2e_us = statistics.mean(e2e_times)
     h2d, d2h = ins.nbytes, outs.nbytes
-    assert dec.poll_error() == 0
-    e2e_us, e2e_staged, e2e_host, t_split, t_comb = max_over_ranks(
-        [e2e_us, e2e_forms["staged"], e2e_forms["host"], t_split, t_comb], pg, dev)
+    assert w.dec.poll_error() == 0
+    e2e_staged, e2e_host, t_split, t_comb = max_over_ranks(
+        [e2e_forms["staged"], e2e_forms["host"], t_split, t_comb], pg, dev)
+    roof = roofline_entry(w, args, t_split, t_comb, peak, peak_kind)
+    headline = {"value": round(us, 3), "unit": "us/call", "kv_bytes_per_call": inp.kv_bytes(),
+                "kv_gbs": round(inp.kv_bytes() / (us * 1e-6) / 1e9, 1), "roofline": roof,
+                "gpu_launches": args.steps * w.launches_per_call,
+                "plan": {k: w.plan.as_dict()[k] for k in ("num_work", "grid", "chunk_tokens", "splits_max",
+                                                         "schedule")}}
+    plan_dict = {k: w.plan.as_dict()[k] for k in ("num_work", "grid", "chunk_tokens", "splits_max", "schedule",
+                                                  "tokens_fused")}
+    del w
+    torch.cuda.empty_cache()
 
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             us_cpu, cores, sample = cpu_baseline(inp, args.q_len, paged)
             cpu = {"value": round(us_cpu, 1), "unit": "us/call", "cores": cores, "kind": "oracle", "sample": sample}
+            headline["cpu_baseline"] = cpu
+        per_config = None
+        if world == 1 and not args.no_per_config and args.q_len == 1 and args.page_size == 0:
+            per_config = measure_per_config(args, rank, dev, stream, flush, peak, peak_kind, headline)
         line = {
             "metric": "us_per_mla_decode_call", "value": round(us, 3), "unit": "us/call", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-            "dtype": DTYPE_LABEL[dt], "data": "synthetic (seeded N(0,1) q and KV, quantised as stated)",
-            "config": {"workload": name + (f"_paged{args.page_size}" if paged is not None else "") +
-                                   (f"_q{args.q_len}" if args.q_len > 1 else ""), "batch": b,
-                       "kv_len": L, "kv_dtype": dt, "page_size": args.page_size or 1, "q_len": args.q_len,
-                       "kv_bytes_per_call": kv_bytes, "l2": "flushed before every timed call (256 MiB write)",
-                       "plan": {k: plan.as_dict()[k] for k in ("num_work", "grid", "chunk_tokens", "splits_max",
-                                                                "tokens_fused")},
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "kv_gbs": round(kv_bytes / (us * 1e-6) / 1e9, 1),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4),
-                         "traffic": (profiled_traffic(name + (f"_q{args.q_len}" if args.q_len > 1 else ""), dt)
-                                     if paged is None else None),
-                         "kernel": KERNEL_NAMES[dt] if paged is None else "whole paged call",
-                         "kernel_us": round(t_split, 3),
-                         "combine_us": round(t_comb, 3), "peak_kind": f"{peak_kind} (HBM copy)"},
-            "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "form": e2e_form,
+            "dtype": DTYPE_LABEL[synth.WORKLOADS[name][2]],
+            "data": "synthetic (seeded N(0,1) q and KV, quantised as stated)",
+            "config": workload_config(name, args, world),
+            "plan": plan_dict,
+            "kv_gbs": headline["kv_gbs"],
+            "roofline": roof,
+            "e2e": {"value": round(e2e_staged, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "form": "staged",
                     "staged_us": round(e2e_staged, 3), "host_buffers_us": round(e2e_host, 3),
-                    "forms": "staged: one pinned-host-to-device copy of q and the index arrays and one copy "
-                             "of out/lse back, around the call; host_buffers: the call gets the pinned host "
-                             "buffers and its kernels read and write them over the host link (q of bf16 KV "
+                    "forms": "staged (the value): one pinned-host-to-device copy of q and the index arrays and "
+                             "one copy of out/lse back, around the call; host_buffers: the call gets the pinned "
+                             "host buffers and its kernels read and write them over the host link (q of bf16 KV "
                              "copied in first)"},
-            "gpu_launches": args.steps * launches_per_call,
+            "gpu_launches": headline["gpu_launches"],
             "clocks": dict(clk.summary(), window="timed steps plus a 1 s soak of the same calls"),
             "wall_s_timed_loop": round(t_wall, 4),
             "cpu_baseline": cpu,
+            "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     if pg is not None:

@@ -293,7 +293,11 @@ MLA_API int mla_decode_fwd_paged(const void* q, const void* kv_pages, const void
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  Each call clears the array's error word and overwrites the rest,
+ * capture.  The address is kept with the id of the device's context: after
+ * the context changes (the application called cudaDeviceReset, or released
+ * and re-created the primary context) the next call looks it up again, so
+ * that call, too, belongs before any capture.  Each call clears the array's
+ * error word and overwrites the rest,
  * so nothing carries over between calls -- but every call on a device shares
  * the one array: calls that may overlap on the GPU (different streams without
  * ordering, or several host threads) race and give wrong results.
@@ -307,6 +311,24 @@ MLA_API int mla_decode_fwd_paged(const void* q, const void* kv_pages, const void
 MLA_API int mla_decode_fwd_static(const void* q, const void* kv, const void* kv_scale, int32_t scale_stride,
                                   const int32_t* kv_indptr, const int32_t* qo_indptr, void* out, float* lse,
                                   float sm_scale, const mla_plan* plan, int32_t* device_error, void* stream);
+
+/*
+ * mla_decode_set_trace -- diagnostics, for the library's trace build only
+ * (compiled with MLA_TRACE=1; the normal build returns MLA_ERR_UNSUPPORTED for
+ * a non-null buffer and records nothing).  The pages have no counterpart.
+ * While `buffer` is set, every launch of the tensor-core split kernel (e4m3
+ * and MXFP4 KV) writes global-timer stamps (ns) into
+ *   buffer[cta * MLA_TRACE_SLOTS + slot]   (device uint64, grid * MLA_TRACE_SLOTS entries)
+ * for slot: 0 kernel entry, 1 set-up done, 2 first KV copy issued, 3 query
+ * preparation complete, 4 the CTA's unit count (a count, not a time),
+ * 5 its tile count (a count), 6 exit, 7 unit list built, 8 + k unit k's
+ * epilogue written (k < 8), 16 + t tile t's scores ready for the softmax
+ * (t < 64), 80 + t tile t's KV landed with its score buffer free (t < 32),
+ * 112 + k unit k's last P.V complete (k < 8).  Slots a launch does not reach
+ * keep their old contents.  Process-wide; not thread-safe; NULL turns it off.
+ */
+#define MLA_TRACE_SLOTS 128
+MLA_API int mla_decode_set_trace(uint64_t* buffer);
 
 /* Static, NUL-terminated description of a status code. */
 MLA_API const char* mla_status_string(int status);

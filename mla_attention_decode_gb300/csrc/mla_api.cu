@@ -105,7 +105,10 @@ struct BalancedPlan {
 // query and the refill of the ring) costs about two tiles of pipeline time;
 // schedule 1 gives each boundary that weight when the CTAs have at least
 // four tiles each (below that the weight would leave CTAs without tiles).
-constexpr int32_t kScheduleUnitCost = 2;
+#ifndef MLA_UNIT_COST
+#define MLA_UNIT_COST 2
+#endif
+constexpr int32_t kScheduleUnitCost = MLA_UNIT_COST;
 
 // The busiest CTA's tiles plus kUnitCost per unit it owns, plus the combine
 // (same model as plan_cost).
@@ -216,6 +219,9 @@ int device_sm_count(int32_t* out) {
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Trace builds: the stamp buffer of the split kernel's launches (null: off).
+uint64_t* g_trace = nullptr;
 
 // The plan of a batch of sequences with lengths `lens` whose rows span
 // [0, total_kv) of the row space the kernels walk (see mla_decode.h).
@@ -486,6 +492,7 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   p->schedule = plan->schedule;
   p->total_tiles = plan->total_tiles;
   p->unit_cost = plan->unit_cost;
+  p->trace = g_trace;
   p->q_len = plan->q_len > 1 ? plan->q_len : 1;
   if (plan->q_len > 16 || (p->q_len > 1 && (paged || plan->batch % p->q_len != 0))) return MLA_ERR_INVALID_ARG;
   // a two-token plan: e4m3 KV, q_len 2, two partial slots per work unit
@@ -654,6 +661,17 @@ const char* mla_status_string(int status) {
   }
 }
 
-const char* mla_decode_version(void) { return "0.1.0"; }
+const char* mla_decode_version(void) { return "0.2.0"; }
+
+int mla_decode_set_trace(uint64_t* buffer) {
+#if defined(MLA_TRACE) && MLA_TRACE
+  g_trace = buffer;
+  return MLA_OK;
+#else
+  if (buffer) return MLA_ERR_UNSUPPORTED;
+  g_trace = nullptr;
+  return MLA_OK;
+#endif
+}
 
 }  // extern "C"

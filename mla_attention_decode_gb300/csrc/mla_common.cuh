@@ -8,6 +8,31 @@
 
 namespace mla {
 
+#ifndef MLA_TRACE
+#define MLA_TRACE 0
+#endif
+
+// Trace builds: the global time (ns) at `slot` of this CTA's stamp row, or a
+// count when `value` is given.  Compiled out of normal builds.
+__device__ __forceinline__ void trace_stamp(const Stage1Params& p, int slot) {
+#if MLA_TRACE
+  if (p.trace != nullptr && slot >= 0 && slot < kTraceSlots)
+    p.trace[(size_t)blockIdx.x * kTraceSlots + slot] = global_timer_ns();
+#else
+  (void)p;
+  (void)slot;
+#endif
+}
+__device__ __forceinline__ void trace_value(const Stage1Params& p, int slot, uint64_t value) {
+#if MLA_TRACE
+  if (p.trace != nullptr && slot >= 0 && slot < kTraceSlots) p.trace[(size_t)blockIdx.x * kTraceSlots + slot] = value;
+#else
+  (void)p;
+  (void)slot;
+  (void)value;
+#endif
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s: a wait this long means a lost copy

@@ -82,6 +82,24 @@ struct Stage1Params {
   int32_t q_len;        // query tokens per sequence; batch counts tokens
   int32_t tok;          // tokens one work unit serves (2: fused two-token e4m3 plan, else 1);
                         // num_work then counts partial slots, tok per unit
+  uint64_t* trace;      // trace builds only: [grid][kTraceSlots] global-timer stamps (else null)
+};
+
+// Per-CTA stamp slots of a trace build (compiled with MLA_TRACE=1).
+constexpr int kTraceSlots = 128;
+enum TraceSlot {
+  kTrEntry = 0,        // kernel entry
+  kTrSetup = 1,        // set-up done (barriers, unit list, TMEM)
+  kTrFirstLoad = 2,    // producer issued the first KV copy
+  kTrQueryReady = 3,   // query loader: the query-preparation grid is complete
+  kTrUnits = 4,        // (a count) work units of the CTA
+  kTrTiles = 5,        // (a count) tiles of the CTA
+  kTrExit = 6,         // every role done, before TMEM is freed
+  kTrScanDone = 7,     // the unit list is in shared memory
+  kTrUnitDone = 8,     // [8] unit k's epilogue written
+  kTrTileS = 16,       // [64] softmax: tile t's scores ready
+  kTrTileData = 80,    // [32] QK issuer: tile t's data landed and its S buffer free
+  kTrUnitLastPV = 112, // [8] unit k's last P.V complete (its epilogue starts)
 };
 
 struct CombineParams {

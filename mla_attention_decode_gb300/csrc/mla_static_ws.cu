@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "mla_decode.h"
@@ -17,11 +18,60 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_workspace[MLA_STATIC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_address[kMaxDevices] = {};  // device address of g_static_workspace, per device ordinal
 
-// Device address of the shared workspace on the current device; looked up once
-// per device (the first call on a device does it) and cached.
+// The device address of g_static_workspace is looked up once per device and
+// kept together with the id of the context it belongs to.  A new context on
+// the device (the application called cudaDeviceReset, or the primary context
+// was released and created again) loads the module again, possibly at another
+// address: the id then differs and the address is looked up again.
+struct Entry {
+  void* address = nullptr;
+  unsigned long long ctx_id = 0;
+};
+std::mutex g_mutex;
+Entry g_entry[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Driver entry points for the current context's id, fetched through the
+// runtime once (the library links only the runtime).
+struct CtxIdApi {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+const CtxIdApi& ctx_api() {
+  static const CtxIdApi api = []() {
+    CtxIdApi a;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      a.get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      a.get_id = reinterpret_cast<CtxGetIdFn>(f);
+    cudaGetLastError();
+    return a;
+  }();
+  return api;
+}
+
+// Id of the current context (0 when there is none or it cannot be read).
+unsigned long long current_ctx_id() {
+  const CtxIdApi& a = ctx_api();
+  if (!a.get_current || !a.get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (a.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (a.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the shared workspace on the current device.  The first
+// call on a device (and the first after its context changed) looks it up with
+// cudaGetSymbolAddress, which also loads the module into the context.
 int static_workspace(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -30,16 +80,21 @@ int static_workspace(void** out) {
   }
   if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_address[dev]) {
+  Entry& e = g_entry[dev];
+  const unsigned long long id = current_ctx_id();
+  if (!e.address || id == 0 || id != e.ctx_id) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
-    if (e != cudaSuccess || p == nullptr) {
+    const cudaError_t rc = cudaGetSymbolAddress(&p, g_static_workspace);
+    if (rc != cudaSuccess || p == nullptr) {
       cudaGetLastError();
+      e.address = nullptr;
       return MLA_ERR_CUDA;
     }
-    g_address[dev] = p;
+    e.address = p;
+    // the look-up made the device's primary context current if none was
+    e.ctx_id = current_ctx_id();
   }
-  *out = g_address[dev];
+  *out = e.address;
   return MLA_OK;
 }
 

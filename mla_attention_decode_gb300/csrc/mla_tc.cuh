@@ -94,6 +94,9 @@ struct Tmem {
   static constexpr uint32_t s = 0;
   static constexpr uint32_t o = 2 * blk;
 };
+#ifndef MLA_FIRST_TILE_WAIT
+#define MLA_FIRST_TILE_WAIT 0
+#endif
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kBarSoftmax = 1;  // named barrier of softmax group 0 (128 threads); group 1: 2
 constexpr uint32_t kIdescQK = tc::idesc_e4m3(128, 32, 0, 0);
@@ -228,6 +231,11 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
   bool have = walk.next(x, nt0, nend);
   TileRows nrows = have ? tile_rows(p, nt0, nend) : TileRows{0, -1};
   for (int it = 0; have && !*x.abort_flag; ++it) {
+    if (MLA_FIRST_TILE_WAIT && it == 1) {
+      // the first tile lands before the rest of the ring is requested
+      for (int f = 0; f < 4; ++f) wait_phase(&x.bar[kPairFull + f], 0, x.abort_flag, p.ws_err);
+      wait_phase(&x.bar[kRopeFull], 0, x.abort_flag, p.ws_err);
+    }
     const TileRows rows = nrows;
     have = walk.next(x, nt0, nend);
     if (have) nrows = tile_rows(p, nt0, nend);
@@ -241,6 +249,7 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
       load_block(dst, 128 * f, rows, &x.bar[kPairFull + sl]);
       load_block(dst + kChunkBytes, 128 * f + 64, rows, &x.bar[kPairFull + sl]);
       ++armed[sl];
+      if (it == 0 && f == 0) trace_stamp(p, kTrFirstLoad);
     }
     const int rs = it % kRopeSlots, ruse = it / kRopeSlots;
     if (ruse >= 1) wait_phase(&x.bar[kRopeEmpty + rs], (ruse - 1) & 1, x.abort_flag, p.ws_err);
@@ -340,6 +349,7 @@ static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
       mbar_arrive_expect_tx(&x.bar[kStageFull + sl], (uint32_t)(rows * kPackedRowBytes));
       bulk_g2s(x.smem + L::stage + sl * kStageBytes, p.kv + (size_t)crow * kPackedRowBytes,
                (uint32_t)(rows * kPackedRowBytes), &x.bar[kStageFull + sl], pol);
+      if (hh == 0) trace_stamp(p, kTrFirstLoad);
     } else {
       mbar_arrive(&x.bar[kStageFull + sl]);
     }
@@ -489,6 +499,7 @@ __device__ void q_loader(const Stage1Params& p, const Ctx& x) {
   using L = Layout<kMx, kTok>;
   const uint64_t pol = policy_evict_last();  // a query serves every split of its sequence
   pdl_wait_primary();
+  trace_stamp(p, kTrQueryReady);
   int uses = 0;
   for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
     if (k >= 1) {
@@ -566,6 +577,7 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
       }
       if (it >= 2) wait_phase(&x.bar[kSEmpty + (it & 1)], ((it >> 1) - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
+      if (it < 32) trace_stamp(p, kTrTileData + it);
       tc::fence_after();
       uint32_t ap[4];
 #pragma unroll
@@ -733,6 +745,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       const int valid = min(kTileRows, d.end - t0);
       const int vis = min(valid, d.end - hidden - t0);  // rows of the tile this token sees
       wait_phase(&x.bar[kSFull + sb], (it >> 1) & 1, x.abort_flag, p.ws_err);
+      if (row == 0 && ti == 0 && it < 64) trace_stamp(p, kTrTileS + it);
       tc::fence_after();
       uint32_t acc[32];
       tc::ld32(tl + TM::s + TM::blk * sb, acc);
@@ -867,6 +880,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
     // the unit's last P.V: its own barrier completes once per unit, so the parity
     // of the unit's ordinal names it exactly (o_done may be a phase further on)
     wait_phase(&x.bar[kOLast], ordinal & 1, x.abort_flag, p.ws_err);
+    if (row == 0 && ti == 0 && k < 8) trace_stamp(p, kTrUnitLastPV + k);
     ++ordinal;
     tc::fence_after();
     float inv[16];
@@ -908,10 +922,12 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
         p.ws_lse[(size_t)u * kHeads + row] = lse;
       }
     }
+    if (row == 0 && ti == 0 && k < 8) trace_stamp(p, kTrUnitDone + k);
     tc::fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&x.bar[kOFree]);
   }
+  if (row == 0 && ti == 0) trace_value(p, kTrTiles, (uint64_t)it);
 }
 
 template <bool kMx, int kTok>
@@ -928,6 +944,7 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
   int* misc = reinterpret_cast<int*>(smem + L::misc);
   x.abort_flag = misc + 1;
   int* s_nunits = misc + 2;
+  if (threadIdx.x == 0) trace_stamp(p, kTrEntry);
 
   if (threadIdx.x == 0) {
     uint32_t counts[L::nbars];
@@ -950,6 +967,7 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
     // input but the prepared queries is complete (the query loader waits for those)
     scan_units<kTileRows, Geo<kMx, kTok>::max_units, kTok>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits,
                                                      lane);
+    if (lane == 0) trace_stamp(p, kTrScanDone);
     if (lane == 0 && !kMx) prefetch_tensormap(&p.tmap_kv64);
   }
   if (kMx && threadIdx.x >= 128 && threadIdx.x < 384) {
@@ -972,6 +990,10 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
   pdl_launch_dependents();
   x.tmem = *tmem_slot;
   x.nunits = *s_nunits;
+  if (threadIdx.x == 0) {
+    trace_stamp(p, kTrSetup);
+    trace_value(p, kTrUnits, (uint64_t)x.nunits);
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1005,6 +1027,7 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
+  if (threadIdx.x == 0) trace_stamp(p, kTrExit);
   if (warp == 1) tc::dealloc(x.tmem, Tmem<kTok>::cols);
 }
 

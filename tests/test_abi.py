@@ -69,6 +69,15 @@ def test_fwd_rejects_bad_arguments_without_cuda(lib):
                               1 << 30, None) == 1
 
 
+def test_trace_is_off_in_the_normal_build(lib):
+    """mla_decode_set_trace records only in the trace build: the normal library
+    refuses a buffer and accepts NULL (off)."""
+    lib.mla_decode_set_trace.argtypes = [ctypes.c_void_p]
+    lib.mla_decode_set_trace.restype = ctypes.c_int
+    assert lib.mla_decode_set_trace(ctypes.c_void_p(1 << 20)) == 2
+    assert lib.mla_decode_set_trace(None) == 0
+
+
 def test_empty_batch_is_a_noop(lib):
     from mla_attention_decode_gb300 import binding
     plan = binding.mla_decode_plan([0], "bf16", num_sms=152)

@@ -86,3 +86,18 @@ def test_reference_arm_times_the_same_form(extra, suffix):
     assert line["impl"] == "reference" and line["config"]["workload"] == "bs4_kv1024_bf16" + suffix
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+    # the reference arm names the workload with the same config object as the GPU arm
+    import bench
+    assert line["config"] == bench.workload_config("bs4_kv1024_bf16", bench.parse(["--workload", "bs4_kv1024_bf16",
+                                                                                    *extra]), 1)
+
+
+def test_default_workload_is_the_largest():
+    """The bench's headline is bs=64, kv_len=8192, e4m3 KV (the most KV bytes per call)."""
+    import bench
+    from mla_attention_decode_gb300 import synth
+    args = bench.parse([])
+    assert args.workload == "bs64_kv8192_fp8"
+    assert max(synth.WORKLOAD_ORDER, key=bench.workload_kv_bytes) == args.workload
+    cfg = bench.workload_config(args.workload, args, 1)
+    assert cfg["kv_bytes_per_call"] == 64 * 8192 * 576 + 4 and cfg["batch"] == 64 and cfg["kv_len"] == 8192

@@ -5,14 +5,25 @@ output, and every case checks it.  Each case also holds a tighter internal gate
 derived from the arithmetic of the kernels:
   * the output is rounded to bf16:            <= 2^-9 |oracle|
   * the softmax weights enter P.V as bf16 (bf16 KV) or as two e4m3 terms
-    (fp8 KV), a relative error <= 2^-8 per weight, so feature j moves by at
-    most 2^-8 max_t |v[t, j]| over the sequence's rows
-  * fp32 accumulation, two-term (bf16-exact) query: 1e-3 absolute slack
-so |out - oracle| <= 1e-3 + 2^-9 |oracle| + 2^-8 max_t |v[t, j]| per element,
-plus relative Frobenius error <= 1e-2 and |lse - oracle| <= 2e-3.  For long
-sequences (outputs O(0.05)) this is within ~2e-3 absolute, so a wrong but
-plausible kernel cannot pass.
+    (fp8 and MXFP4 KV), a relative error <= 2^-8 per weight, so feature j
+    of head h moves by at most 2^-8 sum_t w_t |v[t, j]|, with w_t the
+    softmax weight of row t (from the oracle's lse and an independent
+    dequantisation of the rows)
+  * fp32 accumulation, two-term (bf16-exact) query, and the weights too small
+    for the two-term encoding's relative bound: 1e-3 absolute slack
+so |out - oracle| <= 1e-3 + 2^-9 |oracle| + 2^-8 sum_t w_t |v[t, j]| per element,
+plus relative Frobenius error <= 1e-2 and |lse - oracle| <= 2e-3.  For N(0,1)
+rows the weighted mean of |v| is about 0.8, so long sequences (outputs
+O(0.05)) are held to about 4e-3 absolute.  MXFP4 rows whose block exponents
+lie far below the row's largest (test_mxfp4_wide_block_exponents) are held to
+the looser 2^-8 max_t |v[t, j]|: the kernel's e4m3 copy of such blocks rounds
+to e4m3's subnormal grid.  Set MLA_PARITY_LOG to a file path to record each
+case's max |error|, relative Frobenius error, max |lse error| and the largest
+ratio of error to bound.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -26,6 +37,43 @@ CODES = {"bf16": 0, "fp8": 1, "mxfp4": 2}
 ABS_SLACK = 1e-3
 REL_FRO = 1e-2
 LSE_ABS = 2e-3
+
+
+def _rows(inp, a, e):
+    """KV rows [a, e) of inp as float64 [e - a, 576], dequantised without the oracle."""
+    from oracle_pins import lib_dequant
+    sub = synth.MLAInputs(inp.kv_dtype, inp.q, inp.kv_bf16, inp.kv[a:e], inp.kv_scale,
+                          None if inp.block_scales is None else inp.block_scales[a:e],
+                          torch.tensor([0, e - a], dtype=torch.int32), inp.qo_indptr[:2])
+    return lib_dequant(sub)
+
+
+def weighted_vabs(inp, ref_lse, q=None, qo=None, q_len=1):
+    """sum_t w_t |v[t, j]| per output row, head and feature: the softmax-weighted
+    mean of |v| that bounds the effect of relative errors in the weights.
+    w_t = exp(s_t - lse) with the oracle's lse and s_t = q . k_t / 24 from an
+    independent dequantisation; token i of a sequence (q_len > 1) sees its
+    sequence's rows up to its own entry."""
+    q = inp.q if q is None else q
+    qo = (inp.qo_indptr if qo is None else qo).tolist()
+    ind = inp.kv_indptr.tolist()
+    nseq = len(ind) - 1
+    qf = q.to(torch.float64).numpy()
+    out = np.zeros((nseq * q_len, 16, 512))
+    for b in range(nseq):
+        a, e = ind[b], ind[b + 1]
+        if e <= a:
+            continue
+        k = _rows(inp, a, e)
+        vabs = np.abs(k[:, :512])
+        for i in range(q_len):
+            r = b * q_len + i
+            n = e - a - (q_len - 1 - i)
+            if n <= 0 or not np.all(np.isfinite(ref_lse[r])):
+                continue
+            s = qf[qo[b] + i] @ k[:n].T / 24.0
+            out[r] = np.exp(s - ref_lse[r][:, None]) @ vabs[:n]
+    return out
 
 
 def v_absmax(inp, seqs=None):
@@ -89,26 +137,39 @@ def oracle_decode(orc, inp, q=None, qo=None, seqs=None):
                       block_scales=None if inp.block_scales is None else inp.block_scales.numpy())
 
 
-def assert_parity(got, ref, lse, ref_lse, what, vmax=None):
-    """vmax: [B, 512] per-sequence max |v| (None: use the output scale only)."""
+def assert_parity(got, ref, lse, ref_lse, what, wabs=None, vmax=None):
+    """wabs: [B, 16, 512] softmax-weighted |v| (weighted_vabs); vmax: [B, 512]
+    per-sequence max |v|, the looser form (None for both: the output scale only)."""
     assert got.shape == ref.shape
     err = np.abs(got - ref)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     assert np.all(err <= 2e-2 + 2e-2 * np.abs(ref)), f"{what}: outside rtol=atol=2e-2"
     bound = ABS_SLACK + 2.0 ** -9 * np.abs(ref)
-    if vmax is not None:
+    if wabs is not None:
+        bound = bound + 2.0 ** -8 * wabs
+    elif vmax is not None:
         bound = bound + 2.0 ** -8 * vmax[:, None, :]
     worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    nrm = np.linalg.norm(ref)
+    rel_fro = float(np.linalg.norm(got - ref) / nrm) if nrm > 0 else 0.0
+    fin = np.isfinite(ref_lse)
+    lse_err = float(np.max(np.abs(lse[fin] - ref_lse[fin]))) if fin.any() and np.array_equal(
+        fin, np.isfinite(lse)) else float("nan")
+    log = os.environ.get("MLA_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"case": what, "max_abs_err": float(err.max()) if err.size else 0.0,
+                                "rel_fro": rel_fro, "max_lse_err": lse_err,
+                                "max_err_over_bound": float(np.max(err / bound)) if err.size else 0.0,
+                                "gate": "weighted" if wabs is not None else ("max" if vmax is not None else
+                                                                             "output")}) + "\n")
     assert np.all(err <= bound), (f"{what}: internal gate: err {err[worst]:.3e} > bound {bound[worst]:.3e} at "
                                   f"{worst} (ref {ref[worst]:.4f}, got {got[worst]:.4f})")
-    nrm = np.linalg.norm(ref)
-    if nrm > 0:
-        assert np.linalg.norm(got - ref) / nrm <= REL_FRO, f"{what}: rel fro {np.linalg.norm(got - ref) / nrm:.3e}"
-    fin = np.isfinite(ref_lse)
+    assert rel_fro <= REL_FRO, f"{what}: rel fro {rel_fro:.3e}"
     assert np.array_equal(fin, np.isfinite(lse)), f"{what}: lse finiteness differs"
     assert np.all(np.isneginf(lse[~fin])), f"{what}: empty sequence lse must be -inf"
     if fin.any():
-        assert np.max(np.abs(lse[fin] - ref_lse[fin])) <= LSE_ABS, f"{what}: lse err"
+        assert lse_err <= LSE_ABS, f"{what}: lse err {lse_err:.3e}"
 
 
 DTYPES = ["bf16", "fp8", "mxfp4"]
@@ -120,7 +181,7 @@ def test_ragged_small(orc, dtype, num_splits):
     inp = synth.make_inputs([1, 33, 70, 0, 129, 200, 64, 2], dtype, seed=31)
     got, lse, dec = gpu_decode(inp, num_splits=num_splits)
     ref, ref_lse = oracle_decode(orc, inp)
-    assert_parity(got, ref, lse, ref_lse, f"ragged {dtype} splits={num_splits}", v_absmax(inp))
+    assert_parity(got, ref, lse, ref_lse, f"ragged {dtype} splits={num_splits}", weighted_vabs(inp, ref_lse))
     assert got[3].max() == 0 and got[3].min() == 0, "empty sequence output must be exactly 0"
     assert dec.poll_error() == 0
 
@@ -132,7 +193,7 @@ def test_many_short_sequences(orc, dtype):
     inp = synth.make_inputs(lens, dtype, seed=37)
     got, lse, dec = gpu_decode(inp)
     ref, ref_lse = oracle_decode(orc, inp)
-    assert_parity(got, ref, lse, ref_lse, f"300 short {dtype}", v_absmax(inp))
+    assert_parity(got, ref, lse, ref_lse, f"300 short {dtype}", weighted_vabs(inp, ref_lse))
     assert dec.poll_error() == 0
 
 
@@ -161,7 +222,7 @@ def test_many_units_per_cta(orc, dtype, lens, num_sms, num_splits):
         runs.append((out.double().cpu().numpy(), lse.double().cpu().numpy()))
     assert np.array_equal(runs[0][0], runs[1][0]) and np.array_equal(runs[0][1], runs[1][1])
     ref, ref_lse = oracle_decode(orc, inp)
-    assert_parity(runs[0][0], ref, runs[0][1], ref_lse, f"units/CTA {dtype} {lens}", v_absmax(inp))
+    assert_parity(runs[0][0], ref, runs[0][1], ref_lse, f"units/CTA {dtype} {lens}", weighted_vabs(inp, ref_lse))
     assert dec.poll_error() == 0
 
 
@@ -185,7 +246,7 @@ def test_contiguous_schedule(orc, dtype, lens, num_sms):
     torch.cuda.synchronize()
     got, got_lse = out.double().cpu().numpy(), lse.double().cpu().numpy()
     ref, ref_lse = oracle_decode(orc, inp)
-    assert_parity(got, ref, got_lse, ref_lse, f"contiguous {dtype} {lens[:3]}", v_absmax(inp))
+    assert_parity(got, ref, got_lse, ref_lse, f"contiguous {dtype} {lens[:3]}", weighted_vabs(inp, ref_lse))
     for b, L in enumerate(lens):
         if L == 0:
             assert got[b].max() == 0 and got[b].min() == 0
@@ -197,7 +258,7 @@ def test_one_long_sequence(orc, dtype):
     inp = synth.make_inputs([40001], dtype, seed=41)
     got, lse, _ = gpu_decode(inp)
     ref, ref_lse = oracle_decode(orc, inp)
-    assert_parity(got, ref, lse, ref_lse, f"long {dtype}", v_absmax(inp))
+    assert_parity(got, ref, lse, ref_lse, f"long {dtype}", weighted_vabs(inp, ref_lse))
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -219,7 +280,7 @@ def test_qo_indptr_and_large_logits(orc, dtype):
     qo = torch.tensor([2, 3, 0, 4], dtype=torch.int32)
     got, lse, _ = gpu_decode(inp, q=q, qo=qo)
     ref, ref_lse = oracle_decode(orc, inp, q=q, qo=qo)
-    assert_parity(got, ref, lse, ref_lse, f"qo_indptr x8 logits {dtype}", v_absmax(inp))
+    assert_parity(got, ref, lse, ref_lse, f"qo_indptr x8 logits {dtype}", weighted_vabs(inp, ref_lse, q=q, qo=qo))
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -246,34 +307,15 @@ def test_device_index_error_is_reported():
     assert dec.poll_error() == 0  # cleared by the first poll
 
 
-@pytest.mark.parametrize("name", ["bs4_kv1024_bf16", "bs32_kv1024_fp8", "bs4_kv8192_fp8"])
+@pytest.mark.parametrize("name", synth.WORKLOAD_ORDER)
 def test_benchmark_workloads_full(orc, name):
+    """Each of the five benchmark workloads at full size, in the benchmark's
+    launch configuration, compared with the oracle on every sequence, head and
+    feature."""
     inp = synth.make_workload(name)
     got, lse, dec = gpu_decode(inp)
     ref, ref_lse = oracle_decode(orc, inp)
-    assert_parity(got, ref, lse, ref_lse, name, v_absmax(inp))
-    assert dec.poll_error() == 0
-
-
-def test_benchmark_workload_bs32_kv8192_mxfp4_sampled(orc):
-    """The MXFP4 workload at full size in the benchmark's launch configuration;
-    the oracle checks a sample of 8 sequences (all 16 heads)."""
-    inp = synth.make_workload("bs32_kv8192_mxfp4")
-    got, lse, dec = gpu_decode(inp)
-    seqs = [0, 1, 9, 15, 16, 22, 30, 31]
-    ref, ref_lse = oracle_decode(orc, inp, seqs=seqs)
-    assert_parity(got[seqs], ref, lse[seqs], ref_lse, "bs32_kv8192_mxfp4 sampled", v_absmax(inp, seqs))
-    assert dec.poll_error() == 0
-
-
-def test_benchmark_workload_bs64_kv8192_fp8_sampled(orc):
-    """The largest workload at full size, in the benchmark's launch
-    configuration; the oracle checks a sample of 12 sequences (all 16 heads)."""
-    inp = synth.make_workload("bs64_kv8192_fp8")
-    got, lse, dec = gpu_decode(inp)
-    seqs = [0, 1, 7, 13, 21, 30, 31, 32, 44, 50, 62, 63]
-    ref, ref_lse = oracle_decode(orc, inp, seqs=seqs)
-    assert_parity(got[seqs], ref, lse[seqs], ref_lse, "bs64_kv8192_fp8 sampled", v_absmax(inp, seqs))
+    assert_parity(got, ref, lse, ref_lse, name, weighted_vabs(inp, ref_lse))
     assert dec.poll_error() == 0
 
 
@@ -285,7 +327,7 @@ def test_mxfp4_wide_block_exponents(orc, spread):
     inp = synth.make_inputs([700, 1, 2500, 130], "mxfp4", seed=spread, block_spread=spread)
     got, lse, _ = gpu_decode(inp)
     ref, ref_lse = oracle_decode(orc, inp)
-    assert_parity(got, ref, lse, ref_lse, f"mxfp4 block spread {spread}", v_absmax(inp))
+    assert_parity(got, ref, lse, ref_lse, f"mxfp4 block spread {spread}", vmax=v_absmax(inp))
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -313,9 +355,8 @@ def test_multi_token(orc, dtype, q_len, lens, num_splits):
     ref, ref_lse = orc.decode_multi(CODES[dtype], q, inp.kv, inp.kv_indptr, q_len, qo,
                                     kv_scale=None if inp.kv_scale is None else inp.kv_scale.numpy(),
                                     block_scales=None if inp.block_scales is None else inp.block_scales.numpy())
-    vmax = np.repeat(v_absmax(inp), q_len, axis=0)
     assert_parity(out.double().cpu().numpy(), ref, lse.double().cpu().numpy(), ref_lse,
-                  f"multi-token {dtype} q_len={q_len}", vmax)
+                  f"multi-token {dtype} q_len={q_len}", weighted_vabs(inp, ref_lse, q=q, qo=qo, q_len=q_len))
 
 
 @pytest.mark.parametrize("lens,num_sms,num_splits,qstride", [
@@ -348,8 +389,8 @@ def test_two_token_fused(orc, lens, num_sms, num_splits, qstride):
     assert np.array_equal(runs[0][0], runs[1][0]) and np.array_equal(runs[0][1], runs[1][1])
     assert dec.poll_error() == 0
     ref, ref_lse = orc.decode_multi(CODES["fp8"], q, inp.kv, inp.kv_indptr, 2, qo, kv_scale=inp.kv_scale.numpy())
-    vmax = np.repeat(v_absmax(inp), 2, axis=0)
-    assert_parity(runs[0][0], ref, runs[0][1], ref_lse, f"two-token fused {lens[:3]} splits={num_splits}", vmax)
+    assert_parity(runs[0][0], ref, runs[0][1], ref_lse, f"two-token fused {lens[:3]} splits={num_splits}",
+                  weighted_vabs(inp, ref_lse, q=q, qo=qo, q_len=2))
     for b, L in enumerate(lens):
         if L <= 1:  # token 0 sees no row
             assert np.all(runs[0][0][2 * b] == 0) and np.all(np.isneginf(runs[0][1][2 * b]))
