@@ -73,8 +73,13 @@ template <bool kMx, int kTok = 1>
 struct Geo {
   static_assert(kTok == 1 || (kTok == 2 && !kMx), "two tokens per unit: e4m3 KV only");
   static constexpr int pair_slots = kMx ? 8 : (kTok == 1 ? 11 : 9);  // ring of V column-block pairs (4 per tile)
-  // roles: 4 single-thread warps, 4 softmax warps per token, MXFP4: 8 converter warps
-  static constexpr int threads = kMx ? 512 : 128 * (1 + kTok);
+  // e4m3, one token per unit: a separate epilogue group (warps 8-11) drains
+  // each unit's O^T from its own TMEM buffer, two buffers in turn, so that the
+  // softmax warps and the next unit's P.V do not wait for the epilogue
+  static constexpr bool epi = !kMx && kTok == 1;
+  // roles: 4 single-thread warps, 4 softmax warps per token, MXFP4: 8 converter
+  // warps, e4m3 one token: 4 epilogue warps
+  static constexpr int threads = kMx ? 512 : 384;
   static constexpr int max_units = kMx ? kMaxUnitsPerCtaMx : kMaxUnitsPerCta;  // work units one CTA may own
 };
 constexpr int kRopeSlots = 2;                // ring of the rope column block (features 512..575)
@@ -86,13 +91,16 @@ constexpr int kStageBytes = kHalfRows * kPackedRowBytes;  // 18 KB
 constexpr int kStageSlots = 3;
 // TMEM columns: the S^T double buffer [blk (t mod 2), +blk), then O^T, 4
 // feature blocks of blk columns; token i of a unit owns columns [32 i, +32) of
-// each buffer and block.
+// each buffer and block.  With a separate epilogue group (one token) there are
+// two O^T buffers, obuf columns apart, used by a CTA's units in turn.
 template <int kTok>
 struct Tmem {
   static constexpr uint32_t blk = 32 * kTok;
-  static constexpr uint32_t cols = kTok == 1 ? 256 : 512;
+  static constexpr uint32_t cols = 512;
   static constexpr uint32_t s = 0;
   static constexpr uint32_t o = 2 * blk;
+  static constexpr uint32_t obuf = 4 * blk;
+  static_assert(kTok == 2 || o + 2 * obuf <= cols, "two O^T buffers");
 };
 #ifndef MLA_FIRST_TILE_WAIT
 #define MLA_FIRST_TILE_WAIT 0
@@ -118,9 +126,10 @@ struct Layout {
   static constexpr int gred = red + 2 * 4 * 16 * 4 * kTok;    // int [2][4] tile max of the row exponents
   static constexpr int grow = gred + 2 * 4 * 4;               // int8 [2][128] row exponent G - 127 (MXFP4)
   static constexpr int lut = grow + (kMx ? 2 * 128 : 0);      // u8 [32][8] e2m1 magnitude -> e4m3 per shift
-  static constexpr int units = lut + (kMx ? 256 : 0);
+  static constexpr int hand = lut + (kMx ? 256 : 0);          // float [2][32] l, m handed to the epilogue group
+  static constexpr int units = hand + (Geo<kMx, kTok>::epi ? 256 : 0);
   static constexpr int bars = units + Geo<kMx, kTok>::max_units * (int)sizeof(UnitDesc);
-  static constexpr int nbars = 49;
+  static constexpr int nbars = Geo<kMx, kTok>::epi ? 53 : 49;  // the last four serve the epilogue group
   static constexpr int misc = bars + nbars * 8;  // tmem slot, abort flag, unit count
   static constexpr int total = misc + 16;
 };
@@ -145,7 +154,12 @@ enum {
   kStageFull = 41,  // [3]  MXFP4: bytes of a staged half tile (or the producer's arrival)
   kStageEmpty = 44, // [3]  MXFP4: the converter warps of that half read it (4 warps)
   kConvFull = 47,   // [2]  MXFP4: tile t converted into the ring (8 warps)
+  kOFree2 = 49,     // epilogue group: kOFree of the second O^T buffer
+  kOLast2 = 50,     // epilogue group: kOLast of the second O^T buffer
+  kEpiReady = 51,   // [2]  epilogue group: a unit's l and m handed over, per O^T buffer (1)
 };
+__device__ __forceinline__ int ofree_bar(int obuf) { return obuf ? kOFree2 : kOFree; }
+__device__ __forceinline__ int olast_bar(int obuf) { return obuf ? kOLast2 : kOLast; }
 
 
 struct Ctx {
@@ -610,14 +624,18 @@ __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
   using TM = Tmem<kTok>;
   constexpr int kPairSlots = Geo<kMx, kTok>::pair_slots;
   const uint32_t pairs0 = smem_u32(x.smem + L::pairs), pb0 = smem_u32(x.smem + L::pb);
+  constexpr bool kEpi = Geo<kMx, kTok>::epi;
   int it = 0, ordinal = 0;
   for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
     const int nt = tiles_of(x.units[k]);
     if (nt == 0) continue;
+    // the unit's O^T buffer, and how many units used it before
+    const int obuf = kEpi ? (ordinal & 1) : 0, use = kEpi ? (ordinal >> 1) : ordinal;
+    const uint32_t od = x.tmem + TM::o + obuf * TM::obuf;
     for (int t = 0; t < nt; ++t, ++it) {
       wait_phase(&x.bar[kPFull + (it & 1)], (it >> 1) & 1, x.abort_flag, p.ws_err);
-      // a unit's first P.V overwrites O^T: the previous unit's epilogue must have read it
-      if (t == 0 && ordinal > 0) wait_phase(&x.bar[kOFree], (ordinal - 1) & 1, x.abort_flag, p.ws_err);
+      // a unit's first P.V overwrites O^T: the epilogue of the buffer's previous unit must have read it
+      if (t == 0 && use > 0) wait_phase(&x.bar[ofree_bar(obuf)], (use - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
       tc::fence_after();
       constexpr uint64_t kTplPT = kTok == 1 ? kTplP : kTplP2;
@@ -630,14 +648,100 @@ __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
         const uint32_t av = lo_word(kTplV) + ((pairs0 + (uint32_t)sl * kPairBytes) >> 4);
 #pragma unroll
         for (int q = 0; q < 4; ++q)  // rows [32 q, 32 q + 32): +2048 B of V^T, +1024 B of P^T (every token)
-          tc::mma_f8_words(x.tmem + TM::o + TM::blk * fb, av + q * (2048 >> 4), hi_word(kTplV), bp + q * (1024 >> 4),
+          tc::mma_f8_words(od + TM::blk * fb, av + q * (2048 >> 4), hi_word(kTplV), bp + q * (1024 >> 4),
                            hi_word(kTplPT), kTok == 1 ? kIdescPV : kIdescPV2, (t == 0 && q == 0) ? 0u : 1u);
         tc::commit(&x.bar[kPairEmpty + sl]);
       }
       tc::commit(&x.bar[kODone]);
       tc::commit(&x.bar[kPFree + (it & 1)]);
-      if (t == nt - 1) tc::commit(&x.bar[kOLast]);
+      if (t == nt - 1) tc::commit(&x.bar[olast_bar(obuf)]);
     }
+    ++ordinal;
+  }
+}
+
+// ------------------------------------------------------------------ unit output
+// A unit's output from O^T in TMEM: this thread's lane is feature row `row` of
+// each 128-feature block, the block's 32 columns at tl_o + blk fb (16 heads x
+// the query's two terms).  An unsplit sequence gets bf16 out and lse; a split
+// one an fp32 partial and lse in partial slot u.  l, m: the unit's softmax sum
+// and reference per head (log2 units); out_scale: the factor O^T carries.
+__device__ __forceinline__ void write_unit(const Stage1Params& p, uint32_t tl_o, uint32_t blk, int row, bool final_out,
+                                           int ob, int u, const float (&l)[16], const float (&m)[16],
+                                           float out_scale) {
+  float inv[16];
+#pragma unroll
+  for (int h = 0; h < 16; ++h) inv[h] = l[h] > 0.f ? out_scale * __frcp_rn(l[h]) : 0.f;
+#pragma unroll 1
+  for (int fb = 0; fb < 4; ++fb) {
+    uint32_t o[32];
+    tc::ld32(tl_o + blk * fb, o);
+    tc::wait_ld();
+    const int f = 128 * fb + row;
+    if (final_out) {
+      uint16_t* op = p.out + (size_t)ob * kHeads * kVDim + f;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const float v = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h])) * inv[h];
+        op[h * kVDim] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xffffu);
+      }
+    } else {
+      float* op = p.ws_o + (size_t)u * kHeads * kVDim + f;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) op[h * kVDim] = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h])) * inv[h];
+    }
+  }
+  // lse of head h is written by row h (every row holds all 16 values): pick
+  // this row's head with selects, no divergent branches
+  if (row < kHeads) {
+    float lh = l[0], mh = m[0];
+#pragma unroll
+    for (int h = 1; h < 16; ++h) {
+      lh = row == h ? l[h] : lh;
+      mh = row == h ? m[h] : mh;
+    }
+    const float lse = lh > 0.f ? (mh + fast_log2(lh)) * kLn2 : -INFINITY;
+    if (final_out) {
+      if (p.lse) p.lse[ob * kHeads + row] = lse;
+    } else {
+      p.ws_lse[(size_t)u * kHeads + row] = lse;
+    }
+  }
+}
+
+// Epilogue group (e4m3, one token per unit; warps 8-11, warp w reading TMEM
+// lanes [32 (w mod 4), +32)): for each unit with tiles, in order, takes the
+// softmax's l and m (kEpiReady), waits for the unit's last P.V, writes the
+// unit's output from its O^T buffer and frees the buffer.
+template <bool kMx, int kTok>
+__device__ void epilogue_group(const Stage1Params& p, const Ctx& x, int ww, int lane) {
+  using L = Layout<kMx, kTok>;
+  using TM = Tmem<kTok>;
+  const int row = 32 * ww + lane;
+  const uint32_t tl = x.tmem + ((uint32_t)(32 * ww) << 16);
+  const float kv_scale = *static_cast<const float*>(p.kv_scale);
+  const float* hand = reinterpret_cast<const float*>(x.smem + L::hand);
+  int ordinal = 0;
+  for (int k = 0; k < x.nunits; ++k) {
+    const UnitDesc d = x.units[k];
+    if (tiles_of(d) == 0) continue;
+    const int obuf = ordinal & 1, use = ordinal >> 1;
+    wait_phase(&x.bar[kEpiReady + obuf], use & 1, x.abort_flag, p.ws_err);
+    float l[16], m[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      l[h] = hand[32 * obuf + h];
+      m[h] = hand[32 * obuf + 16 + h];
+    }
+    wait_phase(&x.bar[olast_bar(obuf)], use & 1, x.abort_flag, p.ws_err);
+    if (row == 0 && k < 8) trace_stamp(p, kTrUnitLastPV + k);
+    tc::fence_after();
+    write_unit(p, tl + TM::o + obuf * TM::obuf, TM::blk, row, (d.u & kFinalFlag) != 0, d.b, d.u & ~kFinalFlag, l, m,
+               kv_scale);
+    if (row == 0 && k < 8) trace_stamp(p, kTrUnitDone + k);
+    tc::fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&x.bar[ofree_bar(obuf)]);
     ++ordinal;
   }
 }
@@ -699,6 +803,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
   int* gred = reinterpret_cast<int*>(x.smem + L::gred);
   const float* rq = reinterpret_cast<const float*>(x.smem + L::rq) + 16 * ti;
   float* redbuf = reinterpret_cast<float*>(x.smem + L::red) + 128 * ti;
+  constexpr bool kEpi = Geo<kMx, kTok>::epi;
   int it = 0, red_par = 0, ordinal = 0;
   for (int k = 0; k < x.nunits; ++k) {
     const UnitDesc d = x.units[k];
@@ -739,6 +844,8 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       l_part[h] = 0.f;
     }
     int gv = kGvNone;  // MXFP4: P.V reference exponent of the unit
+    const int obuf = kEpi ? (ordinal & 1) : 0;  // the unit's O^T buffer
+    const uint32_t tl_o = tl + TM::o + obuf * TM::obuf;
     for (int t = 0; t < nt; ++t, ++it) {
       const int sb = it & 1;
       const int t0 = d.start + t * kTileRows;
@@ -825,14 +932,14 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
 #pragma unroll 1
           for (int fb = 0; fb < 4; ++fb) {
             uint32_t o[32];
-            tc::ld32(tl + TM::o + TM::blk * fb, o);
+            tc::ld32(tl_o + TM::blk * fb, o);
             tc::wait_ld();
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
               o[h] = __float_as_uint(__uint_as_float(o[h]) * fac[h]);
               o[16 + h] = __float_as_uint(__uint_as_float(o[16 + h]) * fac[h]);
             }
-            tc::st32(tl + TM::o + TM::blk * fb, o);
+            tc::st32(tl_o + TM::blk * fb, o);
           }
           tc::wait_st();
         }
@@ -877,55 +984,34 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
     // unit epilogue: l per head over the 128 rows, O^T -> output
     group_reduce16<false>(l_part, redbuf + red_par * 64, ww, lane, bar);
     red_par ^= 1;
-    // the unit's last P.V: its own barrier completes once per unit, so the parity
-    // of the unit's ordinal names it exactly (o_done may be a phase further on)
-    wait_phase(&x.bar[kOLast], ordinal & 1, x.abort_flag, p.ws_err);
-    if (row == 0 && ti == 0 && k < 8) trace_stamp(p, kTrUnitLastPV + k);
-    ++ordinal;
-    tc::fence_after();
-    float inv[16];
-    const float out_scale = kMx ? exp2_int(max(-126, min(127, gv))) : kv_scale;
-#pragma unroll
-    for (int h = 0; h < 16; ++h) inv[h] = l_part[h] > 0.f ? out_scale * __frcp_rn(l_part[h]) : 0.f;
-#pragma unroll 1
-    for (int fb = 0; fb < 4; ++fb) {
-      uint32_t o[32];
-      tc::ld32(tl + TM::o + TM::blk * fb, o);
-      tc::wait_ld();
-      const int f = 128 * fb + row;
-      if (final_out) {
-        uint16_t* op = p.out + (size_t)ob * kHeads * kVDim + f;
+    if constexpr (kEpi) {
+      // hand l and m to the epilogue group (its buffer slot is free once the
+      // epilogue of the slot's previous unit has run) and go on to the next unit
+      if (row == 0) {
+        if (ordinal >= 2) wait_phase(&x.bar[ofree_bar(obuf)], ((ordinal >> 1) - 1) & 1, x.abort_flag, p.ws_err);
+        float* hand = reinterpret_cast<float*>(x.smem + L::hand) + 32 * obuf;
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
-          const float v = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h])) * inv[h];
-          op[h * kVDim] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xffffu);
+          hand[h] = l_part[h];
+          hand[16 + h] = m_ref[h];
         }
-      } else {
-        float* op = p.ws_o + (size_t)u * kHeads * kVDim + f;
-#pragma unroll
-        for (int h = 0; h < 16; ++h) op[h * kVDim] = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h])) * inv[h];
+        mbar_arrive(&x.bar[kEpiReady + obuf]);
       }
+      ++ordinal;
+    } else {
+      // the unit's last P.V: its own barrier completes once per unit, so the parity
+      // of the unit's ordinal names it exactly (o_done may be a phase further on)
+      wait_phase(&x.bar[kOLast], ordinal & 1, x.abort_flag, p.ws_err);
+      if (row == 0 && ti == 0 && k < 8) trace_stamp(p, kTrUnitLastPV + k);
+      ++ordinal;
+      tc::fence_after();
+      const float out_scale = kMx ? exp2_int(max(-126, min(127, gv))) : kv_scale;
+      write_unit(p, tl_o, TM::blk, row, final_out, ob, u, l_part, m_ref, out_scale);
+      if (row == 0 && ti == 0 && k < 8) trace_stamp(p, kTrUnitDone + k);
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&x.bar[kOFree]);
     }
-    // lse of head h is written by row h (every row holds all 16 values): pick
-    // this row's head with selects, no divergent branches
-    if (row < kHeads) {
-      float lh = l_part[0], mh = m_ref[0];
-#pragma unroll
-      for (int h = 1; h < 16; ++h) {
-        lh = row == h ? l_part[h] : lh;
-        mh = row == h ? m_ref[h] : mh;
-      }
-      const float lse = lh > 0.f ? (mh + fast_log2(lh)) * kLn2 : -INFINITY;
-      if (final_out) {
-        if (p.lse) p.lse[ob * kHeads + row] = lse;
-      } else {
-        p.ws_lse[(size_t)u * kHeads + row] = lse;
-      }
-    }
-    if (row == 0 && ti == 0 && k < 8) trace_stamp(p, kTrUnitDone + k);
-    tc::fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&x.bar[kOFree]);
   }
   if (row == 0 && ti == 0) trace_value(p, kTrTiles, (uint64_t)it);
 }
@@ -954,6 +1040,7 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
     counts[kSEmpty] = counts[kSEmpty + 1] = 4 * kTok;  // every softmax warp
     counts[kPFull] = counts[kPFull + 1] = 4 * kTok;
     counts[kOFree] = 4 * kTok;
+    if constexpr (Geo<kMx, kTok>::epi) counts[kOFree2] = 4 * kTok;
     counts[kRFree] = 4 * kTok;
     for (int i = 0; i < kStageSlots; ++i) counts[kStageEmpty + i] = 4;
     counts[kConvFull] = counts[kConvFull + 1] = 8;
@@ -1013,7 +1100,10 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
     // site, so that both groups run the same code)
     softmax_epilogue<kMx, kTok>(p, x, warp & 3, lane, kTok == 1 ? 0 : (warp - 4) >> 2);
   } else {
-    if constexpr (kMx) converter_mx(p, x, warp - 8, lane);
+    if constexpr (kMx)
+      converter_mx(p, x, warp - 8, lane);
+    else if constexpr (Geo<kMx, kTok>::epi)
+      epilogue_group<kMx, kTok>(p, x, warp & 3, lane);
   }
 
   if ((warp == 1 || warp == 2) && lane == 0) {

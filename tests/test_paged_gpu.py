@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from mla_attention_decode_gb300 import binding, synth
-from test_parity_gpu import CODES, assert_parity, orc, built, weighted_vabs  # noqa: F401 (fixtures)
+from test_parity_gpu import CODES, assert_parity, gate_terms, orc, built  # noqa: F401 (fixtures)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,7 @@ def test_paged_parity(orc, dtype, page_size):
     assert dec.poll_error() == 0
     ref, ref_lse = paged_oracle(orc, inp, pg)
     assert_parity(out.double().cpu().numpy(), ref, lse.double().cpu().numpy(), ref_lse,
-                  f"paged {dtype} P={page_size}", weighted_vabs(inp, ref_lse))
+                  f"paged {dtype} P={page_size}", gate_terms(inp, ref, ref_lse))
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp8", "mxfp4"])
@@ -79,7 +79,7 @@ def test_paged_long_sequences_split(orc):
     assert dec.poll_error() == 0
     ref, ref_lse = paged_oracle(orc, inp, pg)
     assert_parity(out.double().cpu().numpy(), ref, lse.double().cpu().numpy(), ref_lse, "paged long",
-                  weighted_vabs(inp, ref_lse))
+                  gate_terms(inp, ref, ref_lse))
 
 
 def test_paged_bad_page_index_is_reported():
