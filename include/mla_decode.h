@@ -324,7 +324,7 @@ MLA_API int mla_decode_fwd_static(const void* q, const void* kv, const void* kv_
  * 5 its tile count (a count), 6 exit, 7 unit list built, 8 + k unit k's
  * epilogue written (k < 8), 16 + t tile t's scores ready for the softmax
  * (t < 64), 80 + t tile t's KV landed with its score buffer free (t < 32),
- * 112 + k unit k's last P.V complete (k < 8).  Slots a launch does not reach
+ * 112 + k unit k's last P.V complete (k < 8), 127 the SM id (a value).  Slots a launch does not reach
  * keep their old contents.  Process-wide; not thread-safe; NULL turns it off.
  */
 #define MLA_TRACE_SLOTS 128

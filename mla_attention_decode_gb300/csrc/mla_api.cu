@@ -385,7 +385,7 @@ int mla_decode_plan_paged(const int32_t* kv_page_indptr_host, const int32_t* kv_
   if (!kv_page_indptr_host || !plan || (batch > 0 && !kv_last_page_len_host)) return MLA_ERR_INVALID_ARG;
   if (batch < 0 || batch > MLA_MAX_BATCH || num_pages < 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
   if (kv_dtype < MLA_KV_BF16 || kv_dtype > MLA_KV_MXFP4) return MLA_ERR_UNSUPPORTED;
-  if (page_size < 64 || page_size > (1 << 20) || (page_size & (page_size - 1)) != 0) return MLA_ERR_UNSUPPORTED;
+  if (page_size < 1 || page_size > (1 << 20) || (page_size & (page_size - 1)) != 0) return MLA_ERR_UNSUPPORTED;
   if (kv_page_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
   if ((int64_t)kv_page_indptr_host[batch] * page_size > INT32_MAX || (int64_t)num_pages * page_size > INT32_MAX)
     return MLA_ERR_UNSUPPORTED;
@@ -438,7 +438,7 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   int32_t page_shift = 0;
   if (paged) {
     const int32_t P = plan->page_size;
-    if (P < 64 || (P & (P - 1)) != 0 || plan->num_pages < 0 || (int64_t)plan->num_pages * P > INT32_MAX)
+    if (P < 1 || (P & (P - 1)) != 0 || plan->num_pages < 0 || (int64_t)plan->num_pages * P > INT32_MAX)
       return MLA_ERR_INVALID_ARG;
     if (plan->total_kv > 0 && plan->num_pages == 0) return MLA_ERR_INVALID_ARG;  // pages with no cache
     if (plan->total_kv > 0 && (!paged->kv_indices || !paged->kv_last_page_len ||
@@ -473,6 +473,7 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   p->qo_indptr = qo_indptr;
   p->kv_indices = paged ? paged->kv_indices : nullptr;
   p->kv_last = paged ? paged->kv_last_page_len : nullptr;
+  p->paged = paged ? 1 : 0;
   p->page_shift = page_shift;
   p->num_pages = paged ? plan->num_pages : 0;
   p->out = static_cast<uint16_t*>(out);
@@ -507,9 +508,12 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
     return MLA_ERR_INVALID_ARG;
   if (plan->kv_dtype == MLA_KV_FP8_E4M3) {
     if (!encode_kv_map_tc(&p->tmap_kv64, kv, cache_rows, 128)) return MLA_ERR_CUDA;
-    if (page_shift == 6) {
+    if (paged && page_shift == 6) {
       // 64-row pages: a tile is two 64-row boxes
       if (!encode_kv_map_tc(&p->tmap_kv16, kv, cache_rows, 64)) return MLA_ERR_CUDA;
+    } else if (paged && page_shift < 6) {
+      // smaller pages: rows come in by four-row gathers of one-row boxes
+      if (!encode_kv_map_tc(&p->tmap_kv16, kv, cache_rows, 1)) return MLA_ERR_CUDA;
     } else {
       std::memcpy(&p->tmap_kv16, &p->tmap_kv64, sizeof(CUtensorMap));
     }
@@ -517,9 +521,13 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
     // packed rows are fetched by 1-D bulk copies: no tensor map
     std::memset(&p->tmap_kv64, 0, sizeof(CUtensorMap));
     std::memset(&p->tmap_kv16, 0, sizeof(CUtensorMap));
-  } else if (!encode_kv_map(&p->tmap_kv64, kv, plan->kv_dtype, cache_rows, 64) ||
-             !encode_kv_map(&p->tmap_kv16, kv, plan->kv_dtype, cache_rows, 16)) {
-    return MLA_ERR_CUDA;
+  } else {
+    // bf16: 64-row boxes, and 16-row boxes for short tails; pages of fewer
+    // than 16 rows come in one page per box
+    const uint32_t small = (paged && page_shift < 4) ? (1u << page_shift) : 16u;
+    if (!encode_kv_map(&p->tmap_kv64, kv, plan->kv_dtype, cache_rows, 64) ||
+        !encode_kv_map(&p->tmap_kv16, kv, plan->kv_dtype, cache_rows, small))
+      return MLA_ERR_CUDA;
   }
   return MLA_OK;
 }

@@ -81,7 +81,7 @@ __device__ __forceinline__ bool seq_rows(const Stage1Params& p, int b, int& star
     return a >= 0 && z >= a;
   }
   const int a = p.kv_indptr[b], z = p.kv_indptr[b + 1];
-  if (p.page_shift == 0) {
+  if (!p.paged) {
     start = a;
     end = z;
     return a >= 0 && z >= a;
@@ -128,7 +128,7 @@ __device__ __forceinline__ bool entry_rows(const Stage1Params& p, int b, int& st
 // a paged cache row v % P of page kv_indices[v / P].  A page index outside
 // [0, num_pages) is flagged and page 0 is read instead.
 __device__ __forceinline__ int cache_row(const Stage1Params& p, int v) {
-  if (p.page_shift == 0) return v;
+  if (!p.paged) return v;
   int pg = __ldg(p.kv_indices + (v >> p.page_shift));
   if ((unsigned)pg >= (unsigned)p.num_pages) {
     atomicCAS(p.ws_err, 0, kErrDeviceIndex);

@@ -60,6 +60,7 @@ struct Stage1Params {
   const int32_t* qo_indptr;
   const int32_t* kv_indices; // paged cache: the page table (else null)
   const int32_t* kv_last;    // paged cache: rows in each sequence's last page
+  int32_t paged;             // 1: a paged cache (kv_indices, kv_last); 0: contiguous rows
   int32_t page_shift;        // paged cache: log2(page size); 0 for a contiguous cache
   int32_t num_pages;         // paged cache: pages in the cache tensor
   uint16_t* out;             // bf16 [batch, 16, 512]
@@ -100,6 +101,7 @@ enum TraceSlot {
   kTrTileS = 16,       // [64] softmax: tile t's scores ready
   kTrTileData = 80,    // [32] QK issuer: tile t's data landed and its S buffer free
   kTrUnitLastPV = 112, // [8] unit k's last P.V complete (its epilogue starts)
+  kTrSmid = 127,       // (a value) the SM the CTA ran on
 };
 
 struct CombineParams {

@@ -321,6 +321,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int c0, 
       "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Four rows (r0..r3, any order) of a 2-D tensor map whose box is one row high,
+// at column c0, into four consecutive box rows of shared memory (the map's
+// swizzle applies); completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_gather4(void* dst, const void* map, int c0, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

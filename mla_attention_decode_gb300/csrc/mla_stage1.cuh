@@ -30,15 +30,9 @@
 //   Hand-offs between the groups are mbarriers (P buffer full / empty, double
 //   buffered); the score group's internal steps use named barriers.
 //
-// Tensor-core operands:
-//   bf16 KV : mma.sync m16n8k16 bf16, Q and P in bf16.
-//   fp8 KV  : mma.sync m16n8k32 e4m3 straight from the stored bytes (the
-//             per-tensor scale is folded into the score factor and the final
-//             normalisation, as on submission 703488's "_exact_vtile" kernels).
-//             Q and P are each carried as two e4m3 terms, x ~= hi + lo with
-//             hi = e4m3(x), lo = e4m3(x - hi) (Q with a power-of-two scale per
-//             head and query half), which keeps ~8 significant bits -- the
-//             precision of bf16 -- instead of fp8's 4.
+// Tensor-core operands: mma.sync m16n8k16 bf16, Q and P in bf16.  This is the
+// bf16 KV kernel; e4m3 and MXFP4 KV run the tcgen05 kernel of mla_tc.cuh.  The
+// template parameter is the KV storage format, 0 (bf16) being the only one.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -57,38 +51,24 @@ constexpr uint32_t kBarScore = 1;   // named barrier of the score group (128 thr
 constexpr uint32_t kBarPair0 = 2;   // named barriers of the two pairs (64 threads)
 
 template <int KV>
-struct KvTraits;
+struct KvTraits;  // defined for KV = 0 (bf16) only
 template <>
 struct KvTraits<0> {  // bf16 rows of 576 x 2 B, 9 chunks of 128 B, 128 B swizzle
   static constexpr int kRowBytes = 1152, kSpan = 128, kStages = 2;
 };
-template <>
-struct KvTraits<1> {  // e4m3 rows of 576 B, 9 chunks of 64 B, 64 B swizzle
-  static constexpr int kRowBytes = 576, kSpan = 64, kStages = 4;
-};
-template <>
-struct KvTraits<2> {  // packed e2m1 rows of 288 B, 9 chunks of 32 B, 32 B swizzle
-  static constexpr int kRowBytes = 288, kSpan = 32, kStages = 6;
-};
 
 // Byte offset of (row, byte column) inside a stage written by the swizzled TMA
-// copy: the row is 9 consecutive "span" lines (line index rho = 9 row + chunk);
-// the 16-byte unit inside a line is XOR-ed with bits of the line address, as
-// the hardware swizzle of that span does (128 B: 3 bits, 64 B: 2, 32 B: 1).
+// copy: the row is 9 consecutive 128-byte lines (line index rho = 9 row +
+// chunk); the 16-byte unit inside a line is XOR-ed with the low 3 bits of the
+// line index, as the hardware's 128-byte swizzle does.
 template <int KV>
 __device__ __forceinline__ uint32_t swz(int row, int col) {
   constexpr int span = KvTraits<KV>::kSpan;
+  static_assert(span == 128, "bf16 rows: 128-byte lines");
   const int chunk = col / span;
   const int u = (col % span) >> 4;
   const int rho = 9 * row + chunk;
-  int x;
-  if constexpr (span == 128)
-    x = rho & 7;
-  else if constexpr (span == 64)
-    x = (rho >> 1) & 3;
-  else
-    x = (rho >> 2) & 1;
-  return (uint32_t)(rho * span + ((u ^ x) << 4) + (col & 15));
+  return (uint32_t)(rho * span + ((u ^ (rho & 7)) << 4) + (col & 15));
 }
 
 // Shared-memory carve-up (byte offsets).
@@ -115,14 +95,32 @@ struct Smem {
 
 // One thread: arms a stage's mbarrier and issues the tensor-map copies of the
 // tile whose first row is cache row `crow` (a 64-row box, or 16-row boxes for
-// a short tail; a paged cache keeps a tile inside one page).  Rows past the
-// unit's end come from the next rows of the tensor (or are zero past its end);
-// the kernel masks them.
+// a short tail; pages of 64 rows or more keep a tile inside one page).  Pages
+// of fewer than 64 rows: one box per page (16 rows per box for 16- and 32-row
+// pages), each page looked up from the tile's first row-space position `pos`.
+// Rows past the unit's end come from the next rows of the tensor or page (or
+// are zero past the tensor's end); the kernel masks them.
 template <int KV>
 __device__ __forceinline__ void issue_tile(const Stage1Params& p, uint8_t* st, uint64_t* bar, int crow, int rows,
-                                           int* armed_count) {
+                                           int* armed_count, int pos) {
   using T = KvTraits<KV>;
   const uint64_t pol = policy_evict_first();  // KV rows are read once
+  if (p.paged && p.page_shift < 6) {
+    const int bp = min(1 << p.page_shift, 16);  // rows per box; a tile starts on a page boundary
+    const int nbox = (rows + bp - 1) / bp;
+    ++*armed_count;
+    mbar_arrive_expect_tx(bar, (uint32_t)(nbox * bp * T::kRowBytes));
+    // the page lookups of 16 boxes are independent loads, issued before their copies
+    for (int i0 = 0; i0 < nbox; i0 += 16) {
+      int cr[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) cr[i] = i0 + i < nbox ? cache_row(p, pos + (i0 + i) * bp) : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (i0 + i < nbox) tma_load_3d(st + (i0 + i) * bp * T::kRowBytes, &p.tmap_kv16, 0, 0, cr[i], bar, pol);
+    }
+    return;
+  }
   const int boxes16 = (rows + 15) / 16;
   const bool big = boxes16 == 4;
   const uint32_t bytes = (big ? kTile : 16 * boxes16) * T::kRowBytes;
@@ -152,13 +150,9 @@ template <>
 struct QFrag<0> {
   uint32_t a[18][4];  // 18 k16 steps, bf16 A fragments
 };
-template <>
-struct QFrag<1> {
-  uint32_t hi[9][4], lo[9][4];  // 9 k32 steps, two-term e4m3 A fragments
-};
 
 // Loads this warp's query half into registers.  rf: per-row score factors
-// (rows g and g+8): sm_scale * log2(e) * (fp8 kv scale) / (query scale).
+// (rows g and g+8): sm_scale * log2(e).
 template <int KV>
 __device__ __forceinline__ void load_q(const uint8_t* qs, int hf, int lane, float base_factor, QFrag<KV>& qf,
                                        float (&rf)[2]) {
@@ -169,42 +163,6 @@ __device__ __forceinline__ void load_q(const uint8_t* qs, int hf, int lane, floa
 #pragma unroll
     for (int kk = 0; kk < 18; ++kk) ldsm_x4(a0 + 32 * kk, qf.a[kk][0], qf.a[kk][1], qf.a[kk][2], qf.a[kk][3]);
     rf[0] = rf[1] = base_factor;
-  } else {
-    float amax[2] = {0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < 9; ++kk)
-#pragma unroll
-      for (int q16 = 0; q16 < 2; ++q16)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float4 v = bf16x4_to_f4(*reinterpret_cast<const uint2*>(
-              qs + (g + 8 * r) * kQRowStride + 2 * (288 * hf + 32 * kk + 16 * q16 + 4 * c)));
-          amax[r] = fmaxf(amax[r], fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-        }
-    float sc[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      amax[r] = quad_max(amax[r]);
-      // power-of-two scale with amax * scale <= 448 (e4m3 max); 1 for an all-zero half
-      float s = 1.f;
-      if (amax[r] > 0.f) {
-        s = exp2f(floorf(log2f(448.f / amax[r])));
-        if (amax[r] * s > 448.f) s *= 0.5f;
-      }
-      sc[r] = s;
-      rf[r] = base_factor / s;
-    }
-#pragma unroll
-    for (int kk = 0; kk < 9; ++kk)
-#pragma unroll
-      for (int q16 = 0; q16 < 2; ++q16)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float4 v = bf16x4_to_f4(*reinterpret_cast<const uint2*>(
-              qs + (g + 8 * r) * kQRowStride + 2 * (288 * hf + 32 * kk + 16 * q16 + 4 * c)));
-          two_term_e4m3(v.x * sc[r], v.y * sc[r], v.z * sc[r], v.w * sc[r], qf.hi[kk][2 * q16 + r],
-                        qf.lo[kk][2 * q16 + r]);
-        }
   }
 }
 
@@ -240,32 +198,6 @@ __device__ __forceinline__ void qk_tile(const uint8_t* st, int pr, int hf, int l
 #pragma unroll
       for (int j = 0; j < 4; ++j) mma_bf16_16816(a2[1][j], qf.a[2 * kp + 1], b[j][2], b[j][3]);
     }
-  } else {
-    // x4 = 8 rows x 64 bytes: matrices = 16-byte feature blocks (k32 steps 2kp, 2kp+1)
-#pragma unroll
-    for (int kp = 0; kp < 4; ++kp) {
-      uint32_t b[4][4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        ldsm_x4(sbase + swz<KV>(rbase + 8 * j, 288 * hf + 64 * kp + 16 * mi), b[j][0], b[j][1], b[j][2], b[j][3]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mma_e4m3_16832(a2[0][j], qf.hi[2 * kp], b[j][0], b[j][1]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mma_e4m3_16832(a2[1][j], qf.lo[2 * kp], b[j][0], b[j][1]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mma_e4m3_16832(a2[0][j], qf.hi[2 * kp + 1], b[j][2], b[j][3]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mma_e4m3_16832(a2[1][j], qf.lo[2 * kp + 1], b[j][2], b[j][3]);
-    }
-    // last k32 step: x2 (lanes 0..15 address; the rest repeat them in-row)
-    uint32_t b[4][2];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      ldsm_x2(sbase + swz<KV>(rbase + 8 * j, 288 * hf + 256 + 16 * (mi & 1)), b[j][0], b[j][1]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) mma_e4m3_16832(a2[0][j], qf.hi[8], b[j][0], b[j][1]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) mma_e4m3_16832(a2[1][j], qf.lo[8], b[j][0], b[j][1]);
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j)
@@ -285,21 +217,10 @@ __device__ __forceinline__ void store_p(uint8_t* pb, int pr, int hf, int lane, c
                                  pack_bf16x2(pv[2 * jj + 1][0], pv[2 * jj + 1][1]));
       *reinterpret_cast<uint2*>(pb + ((2 * pr + jj) * 32 + lane) * 16 + 8 * hf) = w;
     }
-  } else {
-    // uint4 [2 k32 steps][2 terms][32 lanes] = {a0, a2, a1, a3}; step = p; P scaled by 256
-    uint32_t hi0, lo0, hi1, lo1;
-    two_term_e4m3(pv[0][0] * 256.f, pv[0][1] * 256.f, pv[1][0] * 256.f, pv[1][1] * 256.f, hi0, lo0);
-    two_term_e4m3(pv[2][0] * 256.f, pv[2][1] * 256.f, pv[3][0] * 256.f, pv[3][1] * 256.f, hi1, lo1);
-    *reinterpret_cast<uint2*>(pb + ((pr * 2 + 0) * 32 + lane) * 16 + 8 * hf) = make_uint2(hi0, hi1);
-    *reinterpret_cast<uint2*>(pb + ((pr * 2 + 1) * 32 + lane) * 16 + 8 * hf) = make_uint2(lo0, lo1);
   }
 }
 
 // ---------------------------------------------------------------- P.V group
-__device__ __forceinline__ uint32_t byte_mask4(int t0, int t1, int t2, int t3, int valid) {
-  return (t0 < valid ? 0x000000ffu : 0u) | (t1 < valid ? 0x0000ff00u : 0u) | (t2 < valid ? 0x00ff0000u : 0u) |
-         (t3 < valid ? 0xff000000u : 0u);
-}
 __device__ __forceinline__ uint32_t half_mask2(int t0, int t1, int valid) {
   return (t0 < valid ? 0x0000ffffu : 0u) | (t1 < valid ? 0xffff0000u : 0u);
 }
@@ -333,41 +254,6 @@ __device__ __forceinline__ void pv_tile(const uint8_t* st, const uint8_t* pb, in
 #pragma unroll
       for (int fg = 0; fg < 4; ++fg) mma_bf16_16816(o[2 * fg + 1], a, r[fg][2] & m0, r[fg][3] & m1);
     }
-  } else {
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint4 wh = *reinterpret_cast<const uint4*>(pb + ((q * 2 + 0) * 32 + lane) * 16);
-      const uint4 wl = *reinterpret_cast<const uint4*>(pb + ((q * 2 + 1) * 32 + lane) * 16);
-      const uint32_t ah[4] = {wh.x, wh.z, wh.y, wh.w};
-      const uint32_t al[4] = {wl.x, wl.z, wl.y, wl.w};
-      const int row = 32 * q + 8 * (lane >> 3) + (lane & 7);
-      uint32_t m0 = 0xffffffffu, m1 = 0xffffffffu;
-      if (valid < kTile) {
-        const int tb = 32 * q + 2 * c;
-        m0 = byte_mask4(tb, tb + 1, tb + 8, tb + 9, valid);
-        m1 = byte_mask4(tb + 16, tb + 17, tb + 24, tb + 25, valid);
-      }
-      uint32_t be[4][2], bo[4][2];
-#pragma unroll
-      for (int fg = 0; fg < 4; ++fg) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4_t(sbase + swz<KV>(row, 64 * v + 16 * fg), r0, r1, r2, r3);
-        be[fg][0] = prmt(r0, r1, 0x6420) & m0;
-        be[fg][1] = prmt(r2, r3, 0x6420) & m1;
-        bo[fg][0] = prmt(r0, r1, 0x7531) & m0;
-        bo[fg][1] = prmt(r2, r3, 0x7531) & m1;
-      }
-#pragma unroll
-      for (int fg = 0; fg < 4; ++fg) {
-        mma_e4m3_16832(o[2 * fg], ah, be[fg][0], be[fg][1]);
-        mma_e4m3_16832(o[2 * fg + 1], ah, bo[fg][0], bo[fg][1]);
-      }
-#pragma unroll
-      for (int fg = 0; fg < 4; ++fg) {
-        mma_e4m3_16832(o[2 * fg], al, be[fg][0], be[fg][1]);
-        mma_e4m3_16832(o[2 * fg + 1], al, bo[fg][0], bo[fg][1]);
-      }
-    }
   }
 }
 
@@ -390,25 +276,6 @@ __device__ __forceinline__ void store_out(const Stage1Params& p, const UnitDesc&
         float* ob = p.ws_o + (size_t)u * kHeads * kVDim;
         *reinterpret_cast<float2*>(ob + g * kVDim + f) = make_float2(o[nt][0] * s0, o[nt][1] * s0);
         *reinterpret_cast<float2*>(ob + (g + 8) * kVDim + f) = make_float2(o[nt][2] * s1, o[nt][3] * s1);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int fg = 0; fg < 4; ++fg) {
-      const int f = 64 * v + 16 * fg + 4 * c;
-      const float4 r0 =
-          make_float4(o[2 * fg][0] * s0, o[2 * fg + 1][0] * s0, o[2 * fg][1] * s0, o[2 * fg + 1][1] * s0);
-      const float4 r1 =
-          make_float4(o[2 * fg][2] * s1, o[2 * fg + 1][2] * s1, o[2 * fg][3] * s1, o[2 * fg + 1][3] * s1);
-      if (final_out) {
-        uint16_t* ob = p.out + (size_t)d.b * kHeads * kVDim;
-        *reinterpret_cast<uint2*>(ob + g * kVDim + f) = make_uint2(pack_bf16x2(r0.x, r0.y), pack_bf16x2(r0.z, r0.w));
-        *reinterpret_cast<uint2*>(ob + (g + 8) * kVDim + f) =
-            make_uint2(pack_bf16x2(r1.x, r1.y), pack_bf16x2(r1.z, r1.w));
-      } else {
-        float* ob = p.ws_o + (size_t)u * kHeads * kVDim;
-        *reinterpret_cast<float4*>(ob + g * kVDim + f) = r0;
-        *reinterpret_cast<float4*>(ob + (g + 8) * kVDim + f) = r1;
       }
     }
   }
@@ -439,8 +306,7 @@ __device__ __forceinline__ void score_loop(const Stage1Params& p, const Ctx& x, 
   float* tmax = reinterpret_cast<float*>(smem + L::tmax);
   float* lsum = reinterpret_cast<float*>(smem + L::lsum);
   float* qsc = reinterpret_cast<float*>(smem + L::qsc);
-  const float kv_scale = (KV == 1) ? *static_cast<const float*>(p.kv_scale) : 1.f;
-  const float base_factor = p.sm_scale * kLog2e * kv_scale;
+  const float base_factor = p.sm_scale * kLog2e;
   const uint64_t pol_keep = policy_evict_last();
 
   int it = 0;
@@ -558,9 +424,7 @@ __device__ __forceinline__ void pv_loop(const Stage1Params& p, const Ctx& x, int
   uint8_t* smem = x.smem;
   const int g = lane >> 2;
   int* tickets = reinterpret_cast<int*>(smem + L::tickets);
-  const float kv_scale = (KV == 1) ? *static_cast<const float*>(p.kv_scale) : 1.f;
-  // final normalisation constant: fp8 P carries a factor 256 and V its kv scale
-  const float out_mult = (KV == 1) ? kv_scale / 256.f : 1.f;
+  const float out_mult = 1.f;  // bf16 P and V carry no extra factor
   // refill cursor: the tile kStages ahead of the one being consumed
   TileCursor cur;
   cur.k = 0;
@@ -607,7 +471,7 @@ __device__ __forceinline__ void pv_loop(const Stage1Params& p, const Ctx& x, int
           tickets[s] = 0;
           if (cur.k < x.nunits && !*x.abort_flag)
             issue_tile<KV>(p, smem + L::stages + s * L::kStageBytes, &x.full[s], refill_row,
-                           min(kTile, x.units[cur.k].end - cur.t0), &x.armed[s]);
+                           min(kTile, x.units[cur.k].end - cur.t0), &x.armed[s], cur.t0);
         }
       }
       if (cur.k < x.nunits) cursor_next<kTile>(cur, x.units, x.nunits);
@@ -669,12 +533,13 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
       cur.k = 0;
       cursor_skip_empty(cur, units, nu);
       // all the first tiles' cache rows are looked up before any is issued
-      int crow[T::kStages], rows[T::kStages];
+      int crow[T::kStages], rows[T::kStages], pos[T::kStages];
       int nfirst = 0;
 #pragma unroll
       for (int s = 0; s < T::kStages; ++s) {
         if (cur.k < nu) {
           crow[s] = cache_row(p, cur.t0);
+          pos[s] = cur.t0;
           rows[s] = min(kTile, units[cur.k].end - cur.t0);
           nfirst = s + 1;
           cursor_next<kTile>(cur, units, nu);
@@ -683,7 +548,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
 #pragma unroll
       for (int s = 0; s < T::kStages; ++s)
         if (s < nfirst)
-          issue_tile<KV>(p, smem + L::stages + s * L::kStageBytes, &x.full[s], crow[s], rows[s], &x.armed[s]);
+          issue_tile<KV>(p, smem + L::stages + s * L::kStageBytes, &x.full[s], crow[s], rows[s], &x.armed[s],
+                         pos[s]);
     }
   }
   __syncwarp();  // lane 0's prologue copies rejoin the warp before the aligned CTA barrier

@@ -217,7 +217,7 @@ struct TileRows {
 __device__ __forceinline__ TileRows tile_rows(const Stage1Params& p, int t0, int end) {
   TileRows r;
   r.r0 = cache_row(p, t0);
-  r.r1 = (p.page_shift == 6 && t0 + 64 < end) ? cache_row(p, t0 + 64) : -1;
+  r.r1 = (p.paged && p.page_shift == 6 && t0 + 64 < end) ? cache_row(p, t0 + 64) : -1;
   return r;
 }
 
@@ -226,7 +226,7 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
   using L = Layout<false, kTok>;
   constexpr int kPairSlots = Geo<false, kTok>::pair_slots;
   const uint64_t pol = policy_evict_first();  // KV rows are read once
-  const bool paged64 = p.page_shift == 6;
+  const bool paged64 = p.paged && p.page_shift == 6;
   // one 64-byte column block of the tile (and the bytes it brings)
   auto load_block = [&](uint8_t* dst, int col, const TileRows& r, uint64_t* bar) {
     if (!paged64) {
@@ -285,6 +285,70 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
 }
 
 
+// Pages of fewer than 64 rows: a tile's rows lie in many pages, so the 32
+// lanes of warp 0 fetch them together.  Lane l looks up the cache rows of tile
+// rows [4 l, 4 l + 4) and issues one four-row gather per 64-byte column block
+// (nine per tile, the 2-D map's box one row high) into those rows' places in
+// the ring, once lane 0 has waited for the tile's slots and armed their
+// barriers.  Rows past the unit's end repeat its last row (the softmax masks
+// them and zeroes their V part).
+template <int kTok>
+__device__ void producer_e4m3_gather(const Stage1Params& p, const Ctx& x, int lane) {
+  using L = Layout<false, kTok>;
+  constexpr int kPairSlots = Geo<false, kTok>::pair_slots;
+  const uint64_t pol = policy_evict_first();  // KV rows are read once
+  int armed[kPairSlots + kRopeSlots];         // lane 0: fills issued per slot
+  for (int i = 0; i < kPairSlots + kRopeSlots; ++i) armed[i] = 0;
+  TileWalk walk;
+  int t0 = 0, end = 0;
+  for (int it = 0; walk.next(x, t0, end); ++it) {
+    int cr[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cr[j] = cache_row(p, min(t0 + 4 * lane + j, end - 1));
+    int sl[4];
+#pragma unroll
+    for (int f = 0; f < 4; ++f) sl[f] = pair_slot<false, kTok>(it, f);
+    const int rs = it % kRopeSlots;
+    if (lane == 0) {
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+        const int use = pair_use<false, kTok>(it, f);
+        if (use >= 1) wait_phase(&x.bar[kPairEmpty + sl[f]], (use - 1) & 1, x.abort_flag, p.ws_err);
+      }
+      const int ruse = it / kRopeSlots;
+      if (ruse >= 1) wait_phase(&x.bar[kRopeEmpty + rs], (ruse - 1) & 1, x.abort_flag, p.ws_err);
+      if (!*x.abort_flag) {
+#pragma unroll
+        for (int f = 0; f < 4; ++f) {
+          mbar_arrive_expect_tx(&x.bar[kPairFull + sl[f]], 2 * kChunkBytes);
+          ++armed[sl[f]];
+        }
+        mbar_arrive_expect_tx(&x.bar[kRopeFull + rs], kChunkBytes);
+        ++armed[kPairSlots + rs];
+      }
+    }
+    if (__shfl_sync(0xffffffffu, lane == 0 ? *x.abort_flag : 0, 0)) break;
+#pragma unroll
+    for (int c = 0; c < 9; ++c) {
+      uint8_t* blk = c < 8 ? x.smem + L::pairs + sl[c >> 1] * kPairBytes + (c & 1) * kChunkBytes
+                           : x.smem + L::rope + rs * kChunkBytes;
+      uint64_t* bar = c < 8 ? &x.bar[kPairFull + sl[c >> 1]] : &x.bar[kRopeFull + rs];
+      tma_gather4(blk + 256 * lane, &p.tmap_kv16, 64 * c, cr[0], cr[1], cr[2], cr[3], bar, pol);
+    }
+    if (it == 0 && lane == 0) trace_stamp(p, kTrFirstLoad);
+  }
+  if (lane == 0 && *x.abort_flag) {
+    // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
+    for (int i = 0; i < kPairSlots + kRopeSlots; ++i) {
+      if (armed[i] == 0) continue;
+      uint64_t* bar = i < kPairSlots ? &x.bar[kPairFull + i] : &x.bar[kRopeFull + i - kPairSlots];
+      const uint64_t tw = global_timer_ns();
+      while (!mbar_try_wait(bar, (armed[i] - 1) & 1) && global_timer_ns() - tw < kWaitTimeoutNs) {
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------- MXFP4 converters
 // Walks the CTA's half tiles in order: unit k, rows [t0 + 64 h, ...) of its
 // tile starting at t0.
@@ -317,8 +381,12 @@ struct HalfCursor {
 // copies (rows of a unit are contiguous); the rows' scale bytes are prefetched
 // into L2 for the converter warps.  A half with no rows (the second half of a
 // short tile) is signalled by a plain arrival.
-static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
+static __device__ void producer_mx(const Stage1Params& p, const Ctx& x, int lane) {
   using L = Layout<true>;
+  // pages of fewer than 64 rows: a half's rows lie in several pages, and the
+  // 32 lanes copy two rows each (their own page-table lookups); otherwise lane
+  // 0 copies the half at once
+  const bool rows_apart = p.paged && p.page_shift < 6;
   const uint64_t pol = policy_evict_first();  // KV rows are read once
   const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
   const size_t ss = (size_t)p.scale_stride;
@@ -328,7 +396,7 @@ static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
   constexpr int kScalePrefetch = 6;
   // one bulk L2 prefetch per half: the 16-byte-aligned part of its scale rows
   // that lies inside the tensor (the base is 16-byte aligned)
-  const int cache_rows = p.page_shift ? (p.num_pages << p.page_shift) : p.total_kv;
+  const int cache_rows = p.paged ? (p.num_pages << p.page_shift) : p.total_kv;
   const size_t scale_end = ((size_t)cache_rows * ss) & ~(size_t)15;
   auto prefetch_scales = [&](int c0, int rows) {
     if (rows <= 0) return;
@@ -347,30 +415,49 @@ static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
     pf_rows = pre.next(x, r0, rows) ? rows : 0;
     pf_row = pf_rows > 0 ? cache_row(p, r0) : 0;
   };
-  for (int i = 0; i <= kScalePrefetch; ++i) advance_prefetch();
+  if (lane == 0 && !rows_apart)
+    for (int i = 0; i <= kScalePrefetch; ++i) advance_prefetch();
   HalfCursor cur;
   int nr0 = 0, nrows = 0;
   bool have = cur.next(x, nr0, nrows);
   int ncrow = (have && nrows > 0) ? cache_row(p, nr0) : 0;
-  for (int hh = 0; have && !*x.abort_flag; ++hh) {
-    const int rows = nrows, crow = ncrow;
+  for (int hh = 0; have; ++hh) {
+    if (__shfl_sync(0xffffffffu, lane == 0 ? *x.abort_flag : 0, 0)) break;
+    const int rows = nrows, crow = ncrow, r0 = nr0;
     have = cur.next(x, nr0, nrows);
-    if (have) ncrow = nrows > 0 ? cache_row(p, nr0) : 0;
+    if (have && !rows_apart) ncrow = nrows > 0 ? cache_row(p, nr0) : 0;
     const int sl = hh % kStageSlots, use = hh / kStageSlots;
-    if (use >= 1) wait_phase(&x.bar[kStageEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
-    if (*x.abort_flag) break;
-    if (rows > 0) {
-      mbar_arrive_expect_tx(&x.bar[kStageFull + sl], (uint32_t)(rows * kPackedRowBytes));
-      bulk_g2s(x.smem + L::stage + sl * kStageBytes, p.kv + (size_t)crow * kPackedRowBytes,
-               (uint32_t)(rows * kPackedRowBytes), &x.bar[kStageFull + sl], pol);
-      if (hh == 0) trace_stamp(p, kTrFirstLoad);
-    } else {
-      mbar_arrive(&x.bar[kStageFull + sl]);
+    int armed_ok = 0;
+    if (lane == 0) {
+      if (use >= 1) wait_phase(&x.bar[kStageEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
+      if (!*x.abort_flag) {
+        armed_ok = 1;
+        if (rows > 0) {
+          mbar_arrive_expect_tx(&x.bar[kStageFull + sl], (uint32_t)(rows * kPackedRowBytes));
+          if (!rows_apart)
+            bulk_g2s(x.smem + L::stage + sl * kStageBytes, p.kv + (size_t)crow * kPackedRowBytes,
+                     (uint32_t)(rows * kPackedRowBytes), &x.bar[kStageFull + sl], pol);
+          if (hh == 0) trace_stamp(p, kTrFirstLoad);
+        } else {
+          mbar_arrive(&x.bar[kStageFull + sl]);
+        }
+        ++uses[sl];
+      }
     }
-    ++uses[sl];
-    advance_prefetch();
+    if (!__shfl_sync(0xffffffffu, armed_ok, 0)) break;
+    if (rows_apart) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int r = 2 * lane + j;
+        if (r < rows)
+          bulk_g2s(x.smem + L::stage + sl * kStageBytes + r * kPackedRowBytes,
+                   p.kv + (size_t)cache_row(p, r0 + r) * kPackedRowBytes, (uint32_t)kPackedRowBytes,
+                   &x.bar[kStageFull + sl], pol);
+      }
+    }
+    if (lane == 0 && !rows_apart) advance_prefetch();
   }
-  if (*x.abort_flag) {
+  if (lane == 0 && *x.abort_flag) {
     // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
     for (int i = 0; i < kStageSlots; ++i) {
       if (uses[i] == 0) continue;
@@ -436,7 +523,7 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
   auto load_next_scales = [&](uint32_t (&dst)[9]) {
     while (pre.next(x, pr0, prows)) {
       if ((pre_hh++ & 1) != hsel) continue;  // the other half's rows
-      load_row_scales(sc, ss, (prows > 0 ? cache_row(p, pr0) : 0) + lr, lr < prows, dst);
+      load_row_scales(sc, ss, lr < prows ? cache_row(p, pr0 + lr) : 0, lr < prows, dst);
       return;
     }
   };
@@ -1030,7 +1117,12 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
   int* misc = reinterpret_cast<int*>(smem + L::misc);
   x.abort_flag = misc + 1;
   int* s_nunits = misc + 2;
-  if (threadIdx.x == 0) trace_stamp(p, kTrEntry);
+  if (threadIdx.x == 0) {
+    trace_stamp(p, kTrEntry);
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    trace_value(p, kTrSmid, smid);
+  }
 
   if (threadIdx.x == 0) {
     uint32_t counts[L::nbars];
@@ -1083,10 +1175,12 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
   }
 
   if (warp == 0) {
-    if (lane == 0) {
-      if constexpr (kMx)
-        producer_mx(p, x);
-      else
+    if constexpr (kMx) {
+      producer_mx(p, x, lane);
+    } else {
+      if (p.paged && p.page_shift < 6)
+        producer_e4m3_gather<kTok>(p, x, lane);
+      else if (lane == 0)
         producer_e4m3<kTok>(p, x);
     }
   } else if (warp == 1) {

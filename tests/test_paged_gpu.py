@@ -3,7 +3,8 @@ paged decode, and identity with the contiguous decode of the same rows.
 
 The page layout is the one the pages' AITER call takes (kernelindex
 "amd-mixed-mla" submission 703488: kv.view(num_pages, page_size, 1, 576), a
-page-counted kv_indptr, kv_indices and kv_last_page_lens).  Every case scatters
+page-counted kv_indptr, kv_indices and kv_last_page_lens; submission 616673
+calls it with pages of 2 and 8 rows).  Page sizes run from 1 to 256 rows.  Every case scatters
 a contiguous cache into pages at random positions, with partial last pages, an
 empty sequence, and NaN poison in every row that no sequence owns (spare pages
 and the tail of each last page): a kernel that reads anything else gives a
@@ -41,7 +42,7 @@ def paged_oracle(orc, inp, pg):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp8", "mxfp4"])
-@pytest.mark.parametrize("page_size", [64, 128, 256])
+@pytest.mark.parametrize("page_size", [1, 2, 4, 8, 16, 32, 64, 128, 256])
 def test_paged_parity(orc, dtype, page_size):
     inp = synth.make_inputs(LENS, dtype, seed=page_size + 5)
     pg = synth.make_paged(inp, page_size, seed=page_size)
@@ -53,7 +54,7 @@ def test_paged_parity(orc, dtype, page_size):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp8", "mxfp4"])
-@pytest.mark.parametrize("page_size,num_splits", [(64, 0), (64, 3), (128, 5)])
+@pytest.mark.parametrize("page_size,num_splits", [(1, 0), (2, 3), (8, 0), (16, 5), (64, 0), (64, 3), (128, 5)])
 def test_paged_equals_contiguous(dtype, page_size, num_splits):
     """The same rows in pages or in one block, with the same splits: identical bits."""
     inp = synth.make_inputs(LENS, dtype, seed=11)
@@ -80,6 +81,23 @@ def test_paged_long_sequences_split(orc):
     ref, ref_lse = paged_oracle(orc, inp, pg)
     assert_parity(out.double().cpu().numpy(), ref, lse.double().cpu().numpy(), ref_lse, "paged long",
                   gate_terms(inp, ref, ref_lse))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "mxfp4"])
+@pytest.mark.parametrize("page_size", [1, 2, 8, 16])
+def test_small_pages_long_sequences(orc, dtype, page_size):
+    """Pages of 1 to 16 rows with a shuffled page table under sequences of
+    thousands of rows, split over several CTAs (the pages' own paged call uses
+    pages of 2 and 8 rows)."""
+    lens = [3000, 1, 2047, 0, 700]
+    inp = synth.make_inputs(lens, dtype, seed=page_size + 29)
+    pg = synth.make_paged(inp, page_size, seed=page_size + 3)
+    out, lse, dec = paged_gpu(inp, pg)
+    assert dec.plan.splits_max > 1
+    assert dec.poll_error() == 0
+    ref, ref_lse = paged_oracle(orc, inp, pg)
+    assert_parity(out.double().cpu().numpy(), ref, lse.double().cpu().numpy(), ref_lse,
+                  f"small pages {dtype} P={page_size}", gate_terms(inp, ref, ref_lse))
 
 
 def test_paged_bad_page_index_is_reported():

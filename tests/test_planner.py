@@ -179,7 +179,7 @@ def test_paged_plan_matches_lengths():
     rng = random.Random(5)
     for _ in range(60):
         b = rng.randint(1, 40)
-        P = rng.choice([64, 128, 256, 1024])
+        P = rng.choice([1, 2, 8, 16, 32, 64, 128, 256, 1024])
         npages = [rng.choice([0, 1, 2, rng.randint(1, 40)]) for _ in range(b)]
         last = [rng.randint(1, P) if n else 0 for n in npages]
         lens = [(n - 1) * P + l if n else 0 for n, l in zip(npages, last)]
@@ -195,10 +195,13 @@ def test_paged_plan_matches_lengths():
 
 
 def test_paged_plan_rules():
-    for P in (1, 8, 32, 96):  # not a power of two >= 64
+    for P in (0, 3, 24, 96):  # not a power of two
         with pytest.raises(binding.MLAError) as e:
             binding.mla_decode_plan_paged([0, 1], [1], P, 1, "fp8", num_sms=152)
         assert e.value.status == binding.MLA_ERR_UNSUPPORTED
+    for P in (1, 2, 4, 8, 16, 32):  # small pages: a tile's rows come from many pages
+        plan = binding.mla_decode_plan_paged([0, 3], [1], P, 3, "fp8", num_sms=152)
+        assert plan.page_size == P and plan.total_kv == 3 * P
     for pind, last in (([0, 2], [65]), ([0, 2], [0]), ([1, 0], [1])):  # last page length, order
         with pytest.raises(binding.MLAError) as e:
             binding.mla_decode_plan_paged(pind, last, 64, 4, "fp8", num_sms=152)
