@@ -115,7 +115,7 @@ typedef struct {
   int32_t units_per_cta;  /* the most units any CTA owns */
   int32_t schedule;       /* 0: splits dealt round-robin (rule above); 1: contiguous tile ranges */
   int32_t total_tiles;    /* schedule 1: T = sum_b max(1, T_b) */
-  int32_t page_size;      /* 0: contiguous cache (mla_decode_plan); P >= 64: paged (mla_decode_plan_paged) */
+  int32_t page_size;      /* 0: contiguous cache (mla_decode_plan); P >= 1: paged (mla_decode_plan_paged) */
   int32_t num_pages;      /* paged: pages in the cache tensor; 0 otherwise */
   int32_t unit_cost;      /* schedule 1: U, empty tile positions between consecutive sequences */
   int32_t q_len;          /* query tokens per sequence (0 or 1: one; see mla_decode_plan_multi) */
@@ -239,9 +239,11 @@ MLA_API int mla_decode_plan_multi(const int32_t* kv_indptr_host, int32_t num_seq
  * the last, kv_last_page_len[b] (1..page_size) rows of the last.  A sequence
  * with no pages is empty (out = 0, lse = -inf).
  *
- * page_size must be a power of two >= 64 (one page holds whole 64-row boxes of
- * the tensor-memory copies; smaller pages with a non-identity table are not
- * supported: MLA_ERR_UNSUPPORTED).  The plan's splits and rule are those of
+ * page_size must be a power of two (1, 2, 4, ...; MLA_ERR_UNSUPPORTED
+ * otherwise).  Pages of 64 rows or more hold whole tiles of the copies into
+ * shared memory; smaller pages are gathered row by row (e4m3: four-row tensor
+ * gathers, MXFP4: one bulk copy per row, bf16: one box per page), each row
+ * through the page table.  The plan's splits and rule are those of
  * mla_decode_plan with start_b = kv_page_indptr[b] * page_size (a position in
  * the sequences' page-ordered row space) and L_b the token count above;
  * total_kv is kv_page_indptr[batch] * page_size.  Both that and
