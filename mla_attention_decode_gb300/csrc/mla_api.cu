@@ -512,8 +512,10 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
       // 64-row pages: a tile is two 64-row boxes
       if (!encode_kv_map_tc(&p->tmap_kv16, kv, cache_rows, 64)) return MLA_ERR_CUDA;
     } else if (paged && page_shift < 6) {
-      // smaller pages: rows come in by four-row gathers of one-row boxes
-      if (!encode_kv_map_tc(&p->tmap_kv16, kv, cache_rows, 1)) return MLA_ERR_CUDA;
+      // smaller pages: one box per page of 8 to 32 rows, four-row gathers of
+      // one-row boxes for pages of 1 to 4 rows
+      if (!encode_kv_map_tc(&p->tmap_kv16, kv, cache_rows, page_shift >= 3 ? (1u << page_shift) : 1u))
+        return MLA_ERR_CUDA;
     } else {
       std::memcpy(&p->tmap_kv16, &p->tmap_kv64, sizeof(CUtensorMap));
     }

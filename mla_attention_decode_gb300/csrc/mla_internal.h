@@ -121,6 +121,8 @@ cudaError_t launch_stage1_bf16(const Stage1Params& p, cudaStream_t s);
 cudaError_t launch_stage1_fp8(const Stage1Params& p, cudaStream_t s);
 cudaError_t launch_stage1_fp8_t2(const Stage1Params& p, cudaStream_t s);  // p.tok == 2
 cudaError_t launch_stage1_mxfp4(const Stage1Params& p, cudaStream_t s);
+// paged caches with pages of fewer than 64 rows (e4m3 or MXFP4, one token)
+cudaError_t launch_stage1_small_pages(const Stage1Params& p, bool mx, cudaStream_t s);
 // Two-term e4m3 query of every sequence into the workspace (e4m3 / MXFP4 KV).
 cudaError_t launch_prep_q(const Stage1Params& p, bool mx, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s, bool pdl);

@@ -286,11 +286,15 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
 
 
 // Pages of fewer than 64 rows: a tile's rows lie in many pages, so the 32
-// lanes of warp 0 fetch them together.  Lane l looks up the cache rows of tile
-// rows [4 l, 4 l + 4) and issues one four-row gather per 64-byte column block
-// (nine per tile, the 2-D map's box one row high) into those rows' places in
-// the ring, once lane 0 has waited for the tile's slots and armed their
-// barriers.  Rows past the unit's end repeat its last row (the softmax masks
+// lanes of warp 0 fetch them together, once lane 0 has waited for the tile's
+// slots and armed their barriers.
+// - Pages of 8 to 32 rows: lane l < 128 / P looks up page l of the tile and
+//   issues one box per 64-byte column block (the 2-D map's box is one page
+//   high), 9 x 128 / P copies per tile.
+// - Pages of 1 to 4 rows: lane l looks up the cache rows of tile rows
+//   [4 l, 4 l + 4) and issues one four-row gather per column block (the box
+//   one row high), 288 copies per tile.
+// Rows past the unit's end repeat its last row, or page (the softmax masks
 // them and zeroes their V part).
 template <int kTok>
 __device__ void producer_e4m3_gather(const Stage1Params& p, const Ctx& x, int lane) {
@@ -299,12 +303,20 @@ __device__ void producer_e4m3_gather(const Stage1Params& p, const Ctx& x, int la
   const uint64_t pol = policy_evict_first();  // KV rows are read once
   int armed[kPairSlots + kRopeSlots];         // lane 0: fills issued per slot
   for (int i = 0; i < kPairSlots + kRopeSlots; ++i) armed[i] = 0;
+  const bool per_page = p.page_shift >= 3;
+  const int page_mask = (1 << p.page_shift) - 1;
   TileWalk walk;
   int t0 = 0, end = 0;
   for (int it = 0; walk.next(x, t0, end); ++it) {
     int cr[4];
+    if (per_page) {
+      // the first cache row of page `lane` of the tile (tiles start on page boundaries)
+      const int v = min(t0 + (lane << p.page_shift), end - 1);
+      cr[0] = cache_row(p, v) - (v & page_mask);
+    } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) cr[j] = cache_row(p, min(t0 + 4 * lane + j, end - 1));
+      for (int j = 0; j < 4; ++j) cr[j] = cache_row(p, min(t0 + 4 * lane + j, end - 1));
+    }
     int sl[4];
 #pragma unroll
     for (int f = 0; f < 4; ++f) sl[f] = pair_slot<false, kTok>(it, f);
@@ -328,12 +340,24 @@ __device__ void producer_e4m3_gather(const Stage1Params& p, const Ctx& x, int la
       }
     }
     if (__shfl_sync(0xffffffffu, lane == 0 ? *x.abort_flag : 0, 0)) break;
+    if (per_page) {
+      if (lane < (kTileRows >> p.page_shift)) {
 #pragma unroll
-    for (int c = 0; c < 9; ++c) {
-      uint8_t* blk = c < 8 ? x.smem + L::pairs + sl[c >> 1] * kPairBytes + (c & 1) * kChunkBytes
-                           : x.smem + L::rope + rs * kChunkBytes;
-      uint64_t* bar = c < 8 ? &x.bar[kPairFull + sl[c >> 1]] : &x.bar[kRopeFull + rs];
-      tma_gather4(blk + 256 * lane, &p.tmap_kv16, 64 * c, cr[0], cr[1], cr[2], cr[3], bar, pol);
+        for (int c = 0; c < 9; ++c) {
+          uint8_t* blk = c < 8 ? x.smem + L::pairs + sl[c >> 1] * kPairBytes + (c & 1) * kChunkBytes
+                               : x.smem + L::rope + rs * kChunkBytes;
+          uint64_t* bar = c < 8 ? &x.bar[kPairFull + sl[c >> 1]] : &x.bar[kRopeFull + rs];
+          tma_load_2d(blk + ((lane << p.page_shift) << 6), &p.tmap_kv16, 64 * c, cr[0], bar, pol);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 9; ++c) {
+        uint8_t* blk = c < 8 ? x.smem + L::pairs + sl[c >> 1] * kPairBytes + (c & 1) * kChunkBytes
+                             : x.smem + L::rope + rs * kChunkBytes;
+        uint64_t* bar = c < 8 ? &x.bar[kPairFull + sl[c >> 1]] : &x.bar[kRopeFull + rs];
+        tma_gather4(blk + 256 * lane, &p.tmap_kv16, 64 * c, cr[0], cr[1], cr[2], cr[3], bar, pol);
+      }
     }
     if (it == 0 && lane == 0) trace_stamp(p, kTrFirstLoad);
   }
@@ -378,15 +402,12 @@ struct HalfCursor {
 
 // ------------------------------------------------------- MXFP4 producer
 // Half tiles (64 packed rows, 18 KB) into a ring of 3 staging slots by 1-D bulk
-// copies (rows of a unit are contiguous); the rows' scale bytes are prefetched
+// copies (a half's rows are contiguous in the cache: a unit's rows, or one page
+// of at least 64 rows); one lane issues them.  The rows' scale bytes are prefetched
 // into L2 for the converter warps.  A half with no rows (the second half of a
 // short tile) is signalled by a plain arrival.
-static __device__ void producer_mx(const Stage1Params& p, const Ctx& x, int lane) {
+static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
   using L = Layout<true>;
-  // pages of fewer than 64 rows: a half's rows lie in several pages, and the
-  // 32 lanes copy two rows each (their own page-table lookups); otherwise lane
-  // 0 copies the half at once
-  const bool rows_apart = p.paged && p.page_shift < 6;
   const uint64_t pol = policy_evict_first();  // KV rows are read once
   const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
   const size_t ss = (size_t)p.scale_stride;
@@ -415,17 +436,52 @@ static __device__ void producer_mx(const Stage1Params& p, const Ctx& x, int lane
     pf_rows = pre.next(x, r0, rows) ? rows : 0;
     pf_row = pf_rows > 0 ? cache_row(p, r0) : 0;
   };
-  if (lane == 0 && !rows_apart)
-    for (int i = 0; i <= kScalePrefetch; ++i) advance_prefetch();
+  for (int i = 0; i <= kScalePrefetch; ++i) advance_prefetch();
   HalfCursor cur;
   int nr0 = 0, nrows = 0;
   bool have = cur.next(x, nr0, nrows);
   int ncrow = (have && nrows > 0) ? cache_row(p, nr0) : 0;
-  for (int hh = 0; have; ++hh) {
-    if (__shfl_sync(0xffffffffu, lane == 0 ? *x.abort_flag : 0, 0)) break;
-    const int rows = nrows, crow = ncrow, r0 = nr0;
+  for (int hh = 0; have && !*x.abort_flag; ++hh) {
+    const int rows = nrows, crow = ncrow;
     have = cur.next(x, nr0, nrows);
-    if (have && !rows_apart) ncrow = nrows > 0 ? cache_row(p, nr0) : 0;
+    if (have) ncrow = nrows > 0 ? cache_row(p, nr0) : 0;
+    const int sl = hh % kStageSlots, use = hh / kStageSlots;
+    if (use >= 1) wait_phase(&x.bar[kStageEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
+    if (*x.abort_flag) break;
+    if (rows > 0) {
+      mbar_arrive_expect_tx(&x.bar[kStageFull + sl], (uint32_t)(rows * kPackedRowBytes));
+      bulk_g2s(x.smem + L::stage + sl * kStageBytes, p.kv + (size_t)crow * kPackedRowBytes,
+               (uint32_t)(rows * kPackedRowBytes), &x.bar[kStageFull + sl], pol);
+      if (hh == 0) trace_stamp(p, kTrFirstLoad);
+    } else {
+      mbar_arrive(&x.bar[kStageFull + sl]);
+    }
+    ++uses[sl];
+    advance_prefetch();
+  }
+  if (*x.abort_flag) {
+    // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
+    for (int i = 0; i < kStageSlots; ++i) {
+      if (uses[i] == 0) continue;
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(&x.bar[kStageFull + i], (uses[i] - 1) & 1) && global_timer_ns() - t0 < kWaitTimeoutNs) {
+      }
+    }
+  }
+}
+
+// Pages of fewer than 64 rows: a half's rows lie in 64 / P pages, so the 32
+// lanes copy one page's rows each (two pages per lane for P = 1), through
+// their own page-table lookups, once lane 0 has waited for the staging slot
+// and armed its barrier.  No scale prefetch: the converters look up their rows'
+// scales themselves.
+static __device__ void producer_mx_rows(const Stage1Params& p, const Ctx& x, int lane) {
+  using L = Layout<true>;
+  const uint64_t pol = policy_evict_first();  // KV rows are read once
+  int uses[kStageSlots] = {0, 0, 0};
+  HalfCursor cur;
+  int r0 = 0, rows = 0;
+  for (int hh = 0; cur.next(x, r0, rows); ++hh) {
     const int sl = hh % kStageSlots, use = hh / kStageSlots;
     int armed_ok = 0;
     if (lane == 0) {
@@ -434,9 +490,6 @@ static __device__ void producer_mx(const Stage1Params& p, const Ctx& x, int lane
         armed_ok = 1;
         if (rows > 0) {
           mbar_arrive_expect_tx(&x.bar[kStageFull + sl], (uint32_t)(rows * kPackedRowBytes));
-          if (!rows_apart)
-            bulk_g2s(x.smem + L::stage + sl * kStageBytes, p.kv + (size_t)crow * kPackedRowBytes,
-                     (uint32_t)(rows * kPackedRowBytes), &x.bar[kStageFull + sl], pol);
           if (hh == 0) trace_stamp(p, kTrFirstLoad);
         } else {
           mbar_arrive(&x.bar[kStageFull + sl]);
@@ -445,17 +498,13 @@ static __device__ void producer_mx(const Stage1Params& p, const Ctx& x, int lane
       }
     }
     if (!__shfl_sync(0xffffffffu, armed_ok, 0)) break;
-    if (rows_apart) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int r = 2 * lane + j;
-        if (r < rows)
-          bulk_g2s(x.smem + L::stage + sl * kStageBytes + r * kPackedRowBytes,
-                   p.kv + (size_t)cache_row(p, r0 + r) * kPackedRowBytes, (uint32_t)kPackedRowBytes,
-                   &x.bar[kStageFull + sl], pol);
-      }
+    // page k of the half: rows [k P, k P + P) (halves start on page boundaries)
+    for (int r = lane << p.page_shift; r < rows; r += 32 << p.page_shift) {
+      const int n = min(1 << p.page_shift, rows - r);
+      bulk_g2s(x.smem + L::stage + sl * kStageBytes + r * kPackedRowBytes,
+               p.kv + (size_t)cache_row(p, r0 + r) * kPackedRowBytes, (uint32_t)(n * kPackedRowBytes),
+               &x.bar[kStageFull + sl], pol);
     }
-    if (lane == 0 && !rows_apart) advance_prefetch();
   }
   if (lane == 0 && *x.abort_flag) {
     // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
@@ -507,7 +556,8 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lut_lo, uin
 // each is fixed at compile time.  Eight warps, two per SM sub-partition (one
 // per half tile): the conversion is bound by each sub-partition's integer
 // pipe, and a second warp keeps it busy while the first waits.
-static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw, int lane) {
+template <bool kSmallPages>
+__device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw, int lane) {
   using L = Layout<true>;
   const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
   const size_t ss = (size_t)p.scale_stride;
@@ -519,11 +569,14 @@ static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw,
   HalfCursor cur, pre;
   int r0 = 0, rows = 0, pr0 = 0, prows = 0, pre_hh = 0;
   // the row's scale bytes are loaded one tile ahead of their use (the producer
-  // has already brought them into L2); a half lies inside one page
+  // has already brought them into L2, except for pages of fewer than 64 rows);
+  // a half lies inside one page unless its pages are that small
   auto load_next_scales = [&](uint32_t (&dst)[9]) {
     while (pre.next(x, pr0, prows)) {
       if ((pre_hh++ & 1) != hsel) continue;  // the other half's rows
-      load_row_scales(sc, ss, lr < prows ? cache_row(p, pr0 + lr) : 0, lr < prows, dst);
+      const int crow = kSmallPages ? (lr < prows ? cache_row(p, pr0 + lr) : 0)
+                                   : (prows > 0 ? cache_row(p, pr0) : 0) + lr;
+      load_row_scales(sc, ss, crow, lr < prows, dst);
       return;
     }
   };
@@ -1103,7 +1156,10 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
   if (row == 0 && ti == 0) trace_value(p, kTrTiles, (uint64_t)it);
 }
 
-template <bool kMx, int kTok>
+// kSmallPages: the instance for paged caches with pages of fewer than 64 rows
+// (one token per unit), whose producer warp fetches rows page by page.  It is a
+// separate instance so that the others carry none of its code.
+template <bool kMx, int kTok, bool kSmallPages>
 __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
     mla_split_tc_kernel(const __grid_constant__ Stage1Params p) {
   using L = Layout<kMx, kTok>;
@@ -1175,12 +1231,15 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
   }
 
   if (warp == 0) {
-    if constexpr (kMx) {
-      producer_mx(p, x, lane);
-    } else {
-      if (p.paged && p.page_shift < 6)
+    if constexpr (kSmallPages) {
+      if constexpr (kMx)
+        producer_mx_rows(p, x, lane);
+      else
         producer_e4m3_gather<kTok>(p, x, lane);
-      else if (lane == 0)
+    } else if (lane == 0) {
+      if constexpr (kMx)
+        producer_mx(p, x);
+      else
         producer_e4m3<kTok>(p, x);
     }
   } else if (warp == 1) {
@@ -1195,7 +1254,7 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
     softmax_epilogue<kMx, kTok>(p, x, warp & 3, lane, kTok == 1 ? 0 : (warp - 4) >> 2);
   } else {
     if constexpr (kMx)
-      converter_mx(p, x, warp - 8, lane);
+      converter_mx<kSmallPages>(p, x, warp - 8, lane);
     else if constexpr (Geo<kMx, kTok>::epi)
       epilogue_group<kMx, kTok>(p, x, warp & 3, lane);
   }
@@ -1217,16 +1276,17 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
 
 }  // namespace tcfp8
 
-template <bool kMx, int kTok = 1>
+template <bool kMx, int kTok = 1, bool kSmallPages = false>
 inline cudaError_t launch_split_tc(const Stage1Params& p, cudaStream_t stream) {
   using L = tcfp8::Layout<kMx, kTok>;
   static_assert(L::total <= 232448, "shared memory carve-up exceeds the 227 KB per-CTA limit");
   static_assert(L::qs % 1024 == 0 && L::pb % 1024 == 0 && L::rope % 1024 == 0, "swizzled operand alignment");
   static_assert(L::stage % 16 == 0, "bulk-copy destination alignment");
-  cudaError_t e = smem_opt_in<tcfp8::mla_split_tc_kernel<kMx, kTok>>(L::total);
+  static_assert(!kSmallPages || kTok == 1, "paged caches take one token per sequence");
+  auto* kernel = tcfp8::mla_split_tc_kernel<kMx, kTok, kSmallPages>;
+  cudaError_t e = smem_opt_in<tcfp8::mla_split_tc_kernel<kMx, kTok, kSmallPages>>(L::total);
   if (e != cudaSuccess) return e;
-  e = launch_overlapped(tcfp8::mla_split_tc_kernel<kMx, kTok>, dim3(p.grid), dim3(tcfp8::Geo<kMx, kTok>::threads),
-                        L::total, stream, p);
+  e = launch_overlapped(kernel, dim3(p.grid), dim3(tcfp8::Geo<kMx, kTok>::threads), L::total, stream, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

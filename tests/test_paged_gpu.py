@@ -54,7 +54,7 @@ def test_paged_parity(orc, dtype, page_size):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp8", "mxfp4"])
-@pytest.mark.parametrize("page_size,num_splits", [(1, 0), (2, 3), (8, 0), (16, 5), (64, 0), (64, 3), (128, 5)])
+@pytest.mark.parametrize("page_size,num_splits", [(1, 0), (2, 3), (4, 0), (8, 0), (16, 5), (32, 2), (64, 0), (64, 3), (128, 5)])
 def test_paged_equals_contiguous(dtype, page_size, num_splits):
     """The same rows in pages or in one block, with the same splits: identical bits."""
     inp = synth.make_inputs(LENS, dtype, seed=11)
