@@ -33,6 +33,17 @@ __device__ __forceinline__ void trace_value(const Stage1Params& p, int slot, uin
 #endif
 }
 
+// Trace builds: the SM this CTA runs on.
+__device__ __forceinline__ void trace_smid(const Stage1Params& p) {
+#if MLA_TRACE
+  uint32_t smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  trace_value(p, kTrSmid, smid);
+#else
+  (void)p;
+#endif
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s: a wait this long means a lost copy

@@ -314,6 +314,7 @@ __device__ __forceinline__ void score_loop(const Stage1Params& p, const Ctx& x, 
     const UnitDesc d = x.units[k];
     const int qb = k & 1;
     wait_phase(&x.qfull[qb], (k >> 1) & 1, x.abort_flag, p.ws_err);
+    if (k == 0 && warp == 0 && lane == 0) trace_stamp(p, kTrQueryReady);
     QFrag<KV> qf;
     float rf[2];
     load_q<KV>(smem + L::qbuf + qb * kQBufBytes, hf, lane, base_factor, qf, rf);
@@ -334,6 +335,7 @@ __device__ __forceinline__ void score_loop(const Stage1Params& p, const Ctx& x, 
       const int s = it % T::kStages;
       const int pbi = it & 1;
       wait_phase(&x.full[s], (it / T::kStages) & 1, x.abort_flag, p.ws_err);
+      if (warp == 0 && lane == 0 && it < 32) trace_stamp(p, kTrTileData + it);
       const uint8_t* st = smem + L::stages + s * L::kStageBytes;
       const int valid = min(kTile, d.end - t0);
 
@@ -400,6 +402,7 @@ __device__ __forceinline__ void score_loop(const Stage1Params& p, const Ctx& x, 
         }
       }
       __syncwarp();
+      if (warp == 0 && lane == 0 && it < 64) trace_stamp(p, kTrTileS + it);
       if (lane == 0) mbar_arrive(&x.pfull[pbi]);
     }
     if (d.start >= d.end && warp == 0 && c == 0) {
@@ -415,6 +418,7 @@ __device__ __forceinline__ void score_loop(const Stage1Params& p, const Ctx& x, 
       }
     }
   }
+  if (warp == 0 && lane == 0) trace_value(p, kTrTiles, (uint64_t)it);
 }
 
 template <int KV>
@@ -479,6 +483,7 @@ __device__ __forceinline__ void pv_loop(const Stage1Params& p, const Ctx& x, int
     const float s0 = l0 > 0.f ? out_mult / l0 : 0.f;
     const float s1 = l1 > 0.f ? out_mult / l1 : 0.f;
     store_out<KV>(p, d, v, lane, o, s0, s1);
+    if (v == 0 && lane == 0 && k < 8) trace_stamp(p, kTrUnitDone + k);
   }
 }
 
@@ -502,6 +507,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
   x.armed = reinterpret_cast<int*>(smem + L::armed);
 
   if (threadIdx.x == 0) {
+    trace_stamp(p, kTrEntry);
+    trace_smid(p);
     for (int s = 0; s < T::kStages; ++s) mbar_init(&x.full[s], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&x.pfull[i], kScoreWarps);
@@ -521,6 +528,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
     scan_units<kTile>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits, lane);
     __syncwarp();
     if (lane == 0) {
+      trace_stamp(p, kTrScanDone);
       // prologue copies: queries of units 0 and 1, the first kStages tiles
       prefetch_tensormap(&p.tmap_kv64);
       prefetch_tensormap(&p.tmap_kv16);
@@ -550,6 +558,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
         if (s < nfirst)
           issue_tile<KV>(p, smem + L::stages + s * L::kStageBytes, &x.full[s], crow[s], rows[s], &x.armed[s],
                          pos[s]);
+      trace_stamp(p, kTrFirstLoad);
     }
   }
   __syncwarp();  // lane 0's prologue copies rejoin the warp before the aligned CTA barrier
@@ -557,6 +566,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
   pdl_wait_primary();
   pdl_launch_dependents();
   x.nunits = *s_nunits;
+  if (threadIdx.x == 0) {
+    trace_stamp(p, kTrSetup);
+    trace_value(p, kTrUnits, (uint64_t)x.nunits);
+  }
   if (warp < kScoreWarps)
     score_loop<KV>(p, x, warp, lane);
   else
@@ -564,6 +577,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) mla_split_kernel(const __grid_
 
   __syncwarp();
   __syncthreads();
+  if (threadIdx.x == 0) trace_stamp(p, kTrExit);
   if (*x.abort_flag && threadIdx.x == 0) {
     // a wait gave up: never leave with copies in flight (bounded wait per barrier)
     for (int s = 0; s < T::kStages + 2; ++s) {

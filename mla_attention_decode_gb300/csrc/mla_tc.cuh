@@ -1175,9 +1175,7 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
   int* s_nunits = misc + 2;
   if (threadIdx.x == 0) {
     trace_stamp(p, kTrEntry);
-    uint32_t smid;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    trace_value(p, kTrSmid, smid);
+    trace_smid(p);
   }
 
   if (threadIdx.x == 0) {

@@ -1,6 +1,7 @@
-"""Per-CTA timeline of the tensor-core split kernel (e4m3 and MXFP4 KV).
+"""Per-CTA timeline of the split kernels (bf16, e4m3 and MXFP4 KV).
 
     python -m mla_attention_decode_gb300.trace [--workload bs64_kv8192_fp8] [--runs 5] [--json PATH]
+    python -m mla_attention_decode_gb300.trace --shape 64 8192 bf16    (any uniform batch)
 
 Builds and loads the trace library (libmla_decode_trace.so: the same kernels
 with global-timer stamps compiled in, see mla_decode_set_trace), decodes one
@@ -28,17 +29,16 @@ UNIT_DONE, TILE_S, TILE_DATA, UNIT_LAST_PV = 8, 16, 80, 112
 N_TILE_S, N_TILE_DATA = 64, 32
 
 
-def run(workload: str, runs: int, flush_bytes: int = 256 << 20, lib: str | None = None):
+def run(workload: str, runs: int, flush_bytes: int = 256 << 20, lib: str | None = None, shape=None):
+    """shape: (batch, kv_len, kv_dtype) in place of a named workload."""
     binding.load_library(lib or build.build(trace=True))
     dev = torch.device("cuda:0")
-    b, L, dt = synth.WORKLOADS[workload]
+    b, L, dt = shape if shape is not None else synth.WORKLOADS[workload]
     inp = synth.make_inputs([L] * b, dt, seed=0)
-    if dt == "bf16":
-        raise SystemExit("the trace covers the tensor-core split kernel (e4m3 and MXFP4 KV)")
     dec = binding.MLADecoder(inp.kv_indptr, dt, device=dev)
-    scale = inp.kv_scale if dt == "fp8" else inp.block_scales
+    scale = {"bf16": None, "fp8": inp.kv_scale, "mxfp4": inp.block_scales}[dt]
     q, kv, ind, qo = inp.q.to(dev), inp.kv.to(dev), inp.kv_indptr.to(dev), inp.qo_indptr.to(dev)
-    sc = scale.to(dev)
+    sc = None if scale is None else scale.to(dev)
     grid = dec.plan.grid
     buf = torch.zeros(grid * SLOTS, dtype=torch.int64, device=dev)
     flush = torch.empty(flush_bytes, dtype=torch.uint8, device=dev)
@@ -153,8 +153,15 @@ def main(argv=None):
     ap.add_argument("--runs", type=int, default=5)
     ap.add_argument("--json", default=None, help="write the per-run summaries here")
     ap.add_argument("--lib", default=None, help="a prebuilt trace library (default: build libmla_decode_trace.so)")
+    ap.add_argument("--shape", nargs=3, default=None, metavar=("BATCH", "KV_LEN", "DTYPE"),
+                    help="a uniform batch in place of --workload (DTYPE: bf16, fp8 or mxfp4)")
     args = ap.parse_args(argv)
-    plan, runs = run(args.workload, args.runs, lib=args.lib)
+    shape = None
+    if args.shape is not None:
+        shape = (int(args.shape[0]), int(args.shape[1]), args.shape[2])
+        assert shape[2] in ("bf16", "fp8", "mxfp4"), "DTYPE: bf16, fp8 or mxfp4"
+        args.workload = f"bs{shape[0]}_kv{shape[1]}_{shape[2]}"
+    plan, runs = run(args.workload, args.runs, lib=args.lib, shape=shape)
     summaries = [analyse(s, ev) for s, ev in runs]
     # the median run by split-stage event time
     order = sorted(range(len(summaries)), key=lambda i: summaries[i]["event_us_split_stage"])
