@@ -565,6 +565,7 @@ int launch_combine_stage(const mla::Stage1Params& p, const mla_plan* plan, cudaS
   c.out = p.out;
   c.lse = p.lse;
   c.batch = plan->batch;
+  c.few_splits = plan->splits_max <= 4 ? 1 : 0;
   if (mla::launch_combine(c, s, true) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;

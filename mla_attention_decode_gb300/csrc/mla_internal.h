@@ -111,6 +111,7 @@ struct CombineParams {
   uint16_t* out;
   float* lse;
   int32_t batch;
+  int32_t few_splits;  // the plan splits no sequence more than 4 times
 };
 
 // Device error codes written to the workspace error word (match mla_status).
