@@ -287,10 +287,14 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
 
 // Pages of fewer than 64 rows: a tile's rows lie in many pages, so the 32
 // lanes of warp 0 fetch them together, once lane 0 has waited for the tile's
-// slots and armed their barriers.
+// slots and armed their barriers.  The pair slots hold 8-row groups outermost
+// ([16 groups][2 column blocks][8 rows x 64 B]; the MMA descriptors of this
+// instance say so), so that one copy can bring whole pages of both blocks.
 // - Pages of 8 to 32 rows: lane l < 128 / P looks up page l of the tile and
-//   issues one box per 64-byte column block (the 2-D map's box is one page
-//   high), 9 x 128 / P copies per tile.
+//   issues one 4-D box per pair (the page's P / 8 groups of both column blocks:
+//   dims 64 B, 8 rows, 9 blocks, groups of the cache, strides 576, 64 and
+//   4608 B) and one 2-D box of the page's rope block: 5 x 128 / P copies per
+//   tile.
 // - Pages of 1 to 4 rows: lane l looks up the cache rows of tile rows
 //   [4 l, 4 l + 4) and issues one four-row gather per column block (the box
 //   one row high), 288 copies per tile.
@@ -342,21 +346,24 @@ __device__ void producer_e4m3_gather(const Stage1Params& p, const Ctx& x, int la
     if (__shfl_sync(0xffffffffu, lane == 0 ? *x.abort_flag : 0, 0)) break;
     if (per_page) {
       if (lane < (kTileRows >> p.page_shift)) {
+        // page `lane`: groups [lane P / 8, (lane + 1) P / 8) of the tile
+        const int g_tile = lane << (p.page_shift - 3), g_cache = cr[0] >> 3;
 #pragma unroll
-        for (int c = 0; c < 9; ++c) {
-          uint8_t* blk = c < 8 ? x.smem + L::pairs + sl[c >> 1] * kPairBytes + (c & 1) * kChunkBytes
-                               : x.smem + L::rope + rs * kChunkBytes;
-          uint64_t* bar = c < 8 ? &x.bar[kPairFull + sl[c >> 1]] : &x.bar[kRopeFull + rs];
-          tma_load_2d(blk + ((lane << p.page_shift) << 6), &p.tmap_kv16, 64 * c, cr[0], bar, pol);
-        }
+        for (int f = 0; f < 4; ++f)
+          tma_load_4d(x.smem + L::pairs + sl[f] * kPairBytes + g_tile * 1024, &p.tmap_kv16, 0, 0, 2 * f, g_cache,
+                      &x.bar[kPairFull + sl[f]], pol);
+        tma_load_2d(x.smem + L::rope + rs * kChunkBytes + ((lane << p.page_shift) << 6), &p.tmap_kv64, 512, cr[0],
+                    &x.bar[kRopeFull + rs], pol);
       }
     } else {
+      // rows [4 lane, 4 lane + 4): half of 8-row group lane / 2
+      const int gofs = (lane >> 1) * 1024 + (lane & 1) * 256;
 #pragma unroll
       for (int c = 0; c < 9; ++c) {
-        uint8_t* blk = c < 8 ? x.smem + L::pairs + sl[c >> 1] * kPairBytes + (c & 1) * kChunkBytes
-                             : x.smem + L::rope + rs * kChunkBytes;
+        uint8_t* blk = c < 8 ? x.smem + L::pairs + sl[c >> 1] * kPairBytes + (c & 1) * 512 + gofs
+                             : x.smem + L::rope + rs * kChunkBytes + 256 * lane;
         uint64_t* bar = c < 8 ? &x.bar[kPairFull + sl[c >> 1]] : &x.bar[kRopeFull + rs];
-        tma_gather4(blk + 256 * lane, &p.tmap_kv16, 64 * c, cr[0], cr[1], cr[2], cr[3], bar, pol);
+        tma_gather4(blk, &p.tmap_kv16, 64 * c, cr[0], cr[1], cr[2], cr[3], bar, pol);
       }
     }
     if (it == 0 && lane == 0) trace_stamp(p, kTrFirstLoad);
@@ -698,15 +705,22 @@ constexpr uint64_t kTplK64 = tc::desc_template(16, 512, 4);          // K-major,
 constexpr uint64_t kTplV = tc::desc_template(kChunkBytes, 512, 4);   // V^T, MN-major, 64 B swizzle
 constexpr uint64_t kTplP = tc::desc_template(1024, 256, 6);          // P^T, MN-major, 32 B swizzle
 constexpr uint64_t kTplP2 = tc::desc_template(kPBytes, 256, 6);      // two tokens' P^T: 32-byte atoms kPBytes apart
+// pair slots with 8-row groups outermost (pages of fewer than 64 rows, e4m3):
+// [16 groups][2 column blocks][8 rows x 64 B], so column block c of the slot
+// starts at 512 c and an 8-row group is 1024 B on
+constexpr uint64_t kTplK64G = tc::desc_template(16, 1024, 4);        // K-major, 64 B swizzle, groups 1 KB apart
+constexpr uint64_t kTplVG = tc::desc_template(512, 1024, 4);         // V^T, MN-major: blocks 512 B, groups 1 KB apart
 __host__ __device__ constexpr uint32_t lo_word(uint64_t d) { return (uint32_t)d; }
 __host__ __device__ constexpr uint32_t hi_word(uint64_t d) { return (uint32_t)(d >> 32); }
 
 
 // QK of every tile: S^T(t) into TMEM columns [blk (t mod 2), +blk), token i's
 // scores at +32 i (two tokens: one N = 64 MMA per k step over both query images).
-template <bool kMx, int kTok>
+template <bool kMx, int kTok, bool kSmallPages>
 __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
   using L = Layout<kMx, kTok>;
+  constexpr bool kGM = kSmallPages && !kMx;  // group-major pair slots
+  constexpr uint64_t kTplA = kGM ? kTplK64G : kTplK64;
   using TM = Tmem<kTok>;
   constexpr int kPairSlots = Geo<kMx, kTok>::pair_slots;
   const uint32_t pairs0 = smem_u32(x.smem + L::pairs), rope0 = smem_u32(x.smem + L::rope);
@@ -736,17 +750,18 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
       uint32_t ap[4];
 #pragma unroll
       for (int f = 0; f < 4; ++f)
-        ap[f] = lo_word(kTplK64) + ((pairs0 + (uint32_t)wrap_slot<kMx, kTok>(s0 + f) * kPairBytes) >> 4);
+        ap[f] = lo_word(kTplA) + ((pairs0 + (uint32_t)wrap_slot<kMx, kTok>(s0 + f) * kPairBytes) >> 4);
       const uint32_t ar = lo_word(kTplK64) + ((rope0 + (uint32_t)(it % kRopeSlots) * kChunkBytes) >> 4);
       const uint32_t d = x.tmem + TM::s + TM::blk * (it & 1);
 #pragma unroll
       for (int ks = 0; ks < 18; ++ks) {
         const int c = ks >> 1, half = ks & 1;
+        constexpr int kBlockStride = kGM ? 512 : kChunkBytes;  // column block 2 f + 1 within pair f
         const uint32_t a =
-            c < 8 ? ap[c >> 1] + (((c & 1) * kChunkBytes + 32 * half) >> 4) : ar + ((32 * half) >> 4);
+            c < 8 ? ap[c >> 1] + (((c & 1) * kBlockStride + 32 * half) >> 4) : ar + ((32 * half) >> 4);
         // both tokens' query rows form one B operand (block c: 32 kTok rows of 64 B)
-        tc::mma_f8_words(d, a, hi_word(kTplK64), bq + ((c * 2048 * kTok + 32 * half) >> 4), hi_word(kTplK64),
-                         kTok == 1 ? kIdescQK : kIdescQK2, ks > 0 ? 1u : 0u);
+        tc::mma_f8_words(d, a, c < 8 ? hi_word(kTplA) : hi_word(kTplK64), bq + ((c * 2048 * kTok + 32 * half) >> 4),
+                         hi_word(kTplK64), kTok == 1 ? kIdescQK : kIdescQK2, ks > 0 ? 1u : 0u);
       }
       tc::commit(&x.bar[kSFull + (it & 1)]);
       tc::commit(&x.bar[kRopeEmpty + it % kRopeSlots]);
@@ -758,9 +773,12 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
 // P.V of every tile: O^T += V^T(t) . P^T(t) (token i: its own P buffer and O^T
 // columns, both in one N = 64 MMA); releases the tile's ring slots, its P
 // buffers and, on a unit's last tile, the unit's O^T.
-template <bool kMx, int kTok>
+template <bool kMx, int kTok, bool kSmallPages>
 __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
   using L = Layout<kMx, kTok>;
+  constexpr bool kGM = kSmallPages && !kMx;  // group-major pair slots
+  constexpr uint64_t kTplA = kGM ? kTplVG : kTplV;
+  constexpr uint32_t kRows32 = kGM ? 4 * 1024 : 2048;  // bytes of 32 rows of V^T in a slot
   using TM = Tmem<kTok>;
   constexpr int kPairSlots = Geo<kMx, kTok>::pair_slots;
   const uint32_t pairs0 = smem_u32(x.smem + L::pairs), pb0 = smem_u32(x.smem + L::pb);
@@ -785,10 +803,10 @@ __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
       for (int fb = 0; fb < 4; ++fb) {
         const int sl = wrap_slot<kMx, kTok>(s0 + fb);
         // V^T block: features [128 fb, 128 fb + 128) = the slot's two column blocks (LBO)
-        const uint32_t av = lo_word(kTplV) + ((pairs0 + (uint32_t)sl * kPairBytes) >> 4);
+        const uint32_t av = lo_word(kTplA) + ((pairs0 + (uint32_t)sl * kPairBytes) >> 4);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)  // rows [32 q, 32 q + 32): +2048 B of V^T, +1024 B of P^T (every token)
-          tc::mma_f8_words(od + TM::blk * fb, av + q * (2048 >> 4), hi_word(kTplV), bp + q * (1024 >> 4),
+        for (int q = 0; q < 4; ++q)  // rows [32 q, 32 q + 32): +kRows32 B of V^T, +1024 B of P^T (every token)
+          tc::mma_f8_words(od + TM::blk * fb, av + q * (kRows32 >> 4), hi_word(kTplA), bp + q * (1024 >> 4),
                            hi_word(kTplPT), kTok == 1 ? kIdescPV : kIdescPV2, (t == 0 && q == 0) ? 0u : 1u);
         tc::commit(&x.bar[kPairEmpty + sl]);
       }
@@ -930,8 +948,9 @@ __device__ __forceinline__ float exp2_int(int e) { return __int_as_float((e + 12
 // in TMEM columns [32 ti, +32) of the S^T buffers and O^T blocks.  With two
 // tokens, token 0 does not see the last row of its sequence (token 1's own
 // entry), and token ti's partial slot is u + ti S_b.
-template <bool kMx, int kTok>
+template <bool kMx, int kTok, bool kSmallPages>
 __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, int lane, int ti) {
+  constexpr bool kGM = kSmallPages && !kMx;  // group-major pair slots
   using L = Layout<kMx, kTok>;
   using TM = Tmem<kTok>;
   constexpr int kGvNone = -1000;   // no MXFP4 reference yet
@@ -1109,11 +1128,12 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
         // that P = 0 cannot meet a non-finite value (the MXFP4 converters write zeros)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          uint8_t* blk =
-              x.smem + L::pairs + pair_slot<kMx, kTok>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes;
+          uint8_t* blk = x.smem + L::pairs + pair_slot<kMx, kTok>(it, c >> 1) * kPairBytes +
+                         (kGM ? (row >> 3) * 1024 + (c & 1) * 512 : (c & 1) * kChunkBytes);
+          const int r = kGM ? (row & 7) : row;
 #pragma unroll
           for (int uu = 0; uu < 4; ++uu)
-            *reinterpret_cast<uint4*>(blk + sw64_off(row, 16 * uu)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(blk + sw64_off(r, 16 * uu)) = make_uint4(0, 0, 0, 0);
         }
       }
       tc::fence_proxy_async();
@@ -1241,15 +1261,15 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
         producer_e4m3<kTok>(p, x);
     }
   } else if (warp == 1) {
-    if (lane == 0) qk_issuer<kMx, kTok>(p, x);
+    if (lane == 0) qk_issuer<kMx, kTok, kSmallPages>(p, x);
   } else if (warp == 2) {
-    if (lane == 0) pv_issuer<kMx, kTok>(p, x);
+    if (lane == 0) pv_issuer<kMx, kTok, kSmallPages>(p, x);
   } else if (warp == 3) {
     if (lane == 0) q_loader<kMx, kTok>(p, x);
   } else if (warp < 4 + 4 * (kMx ? 1 : kTok)) {
     // softmax group (warp - 4) / 4: one per query token of the unit (one call
     // site, so that both groups run the same code)
-    softmax_epilogue<kMx, kTok>(p, x, warp & 3, lane, kTok == 1 ? 0 : (warp - 4) >> 2);
+    softmax_epilogue<kMx, kTok, kSmallPages>(p, x, warp & 3, lane, kTok == 1 ? 0 : (warp - 4) >> 2);
   } else {
     if constexpr (kMx)
       converter_mx<kSmallPages>(p, x, warp - 8, lane);
