@@ -188,20 +188,17 @@ bool encode_kv_map_tc(CUtensorMap* m, const void* kv, int32_t total_kv, uint32_t
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// e4m3 rows seen as groups of 8: dims (64 B, 8 rows, 9 column blocks, groups)
-// with strides 576 B (row), 64 B (block) and 4608 B (group); a box is both
-// blocks of a pair for `groups` whole groups, laid out in shared memory as
-// [groups][2 blocks][8 rows x 64 B] with the 64-byte swizzle.  cache_rows must
-// be a multiple of 8.
-bool encode_kv_map_pairs(CUtensorMap* m, const void* kv, int32_t cache_rows, uint32_t groups) {
+// e4m3 rows, a box of 128 B (both column blocks of a pair) x box_rows rows
+// with the 128-byte swizzle.
+bool encode_kv_map_pairs(CUtensorMap* m, const void* kv, int32_t total_kv, uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc || cache_rows % 8 != 0) return false;
-  const cuuint64_t dims[4] = {64, 8, 9, (cuuint64_t)(cache_rows > 0 ? cache_rows / 8 : 1)};
-  const cuuint64_t strides[3] = {576, 64, 8 * 576};
-  const cuuint32_t box[4] = {64, 8, 2, groups};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(kv), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {576, (cuuint64_t)(total_kv > 0 ? total_kv : 1)};
+  const cuuint64_t strides[1] = {576};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -528,16 +525,14 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
     if (paged && page_shift == 6) {
       // 64-row pages: a tile is two 64-row boxes
       if (!encode_kv_map_tc(&p->tmap_kv16, kv, cache_rows, 64)) return MLA_ERR_CUDA;
-    } else if (paged && page_shift >= 3 && page_shift < 6) {
-      // pages of 8 to 32 rows: a pair of column blocks of one page as one 4-D
-      // box (64 B, 8 rows, 2 blocks, P / 8 groups) into the group-major pair
-      // slots, and the page's rope block as a 2-D box one page high
-      if (!encode_kv_map_pairs(&p->tmap_kv16, kv, cache_rows, 1u << (page_shift - 3)) ||
-          !encode_kv_map_tc(&p->tmap_kv64, kv, cache_rows, 1u << page_shift))
+    } else if (paged && page_shift < 6) {
+      // smaller pages: a pair of column blocks (128 B) and the rope block (64 B)
+      // per box, one page high for pages of 8 to 32 rows, one row high (for
+      // four-row gathers) for pages of 1 to 4 rows
+      const uint32_t rows = page_shift >= 3 ? (1u << page_shift) : 1u;
+      if (!encode_kv_map_pairs(&p->tmap_kv16, kv, cache_rows, rows) ||
+          !encode_kv_map_tc(&p->tmap_kv64, kv, cache_rows, rows))
         return MLA_ERR_CUDA;
-    } else if (paged && page_shift < 3) {
-      // pages of 1 to 4 rows: four-row gathers of one-row boxes
-      if (!encode_kv_map_tc(&p->tmap_kv16, kv, cache_rows, 1)) return MLA_ERR_CUDA;
     } else {
       std::memcpy(&p->tmap_kv16, &p->tmap_kv64, sizeof(CUtensorMap));
     }

@@ -91,16 +91,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int c0, 
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
-// 4-D tensor-map copy global -> shared (box of the map at coordinates c0..c3),
-// completion counted in bytes on `bar`; `map` is a __grid_constant__ parameter.
-__device__ __forceinline__ void tma_load_4d(void* dst, const void* map, int c0, int c1, int c2, int c3, uint64_t* bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
 // Bulk prefetch of [src, src + bytes) into L2 by the TMA unit (src 16-byte
 // aligned, bytes a multiple of 16, the range inside the allocation).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {

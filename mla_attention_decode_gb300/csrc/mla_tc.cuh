@@ -287,17 +287,16 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
 
 // Pages of fewer than 64 rows: a tile's rows lie in many pages, so the 32
 // lanes of warp 0 fetch them together, once lane 0 has waited for the tile's
-// slots and armed their barriers.  The pair slots hold 8-row groups outermost
-// ([16 groups][2 column blocks][8 rows x 64 B]; the MMA descriptors of this
-// instance say so), so that one copy can bring whole pages of both blocks.
+// slots and armed their barriers.  The pair slots hold 128-byte rows (both
+// column blocks of a pair side by side, 128-byte swizzle; the MMA descriptors
+// of this instance say so), so that one copy brings both blocks of a pair.
 // - Pages of 8 to 32 rows: lane l < 128 / P looks up page l of the tile and
-//   issues one 4-D box per pair (the page's P / 8 groups of both column blocks:
-//   dims 64 B, 8 rows, 9 blocks, groups of the cache, strides 576, 64 and
-//   4608 B) and one 2-D box of the page's rope block: 5 x 128 / P copies per
-//   tile.
+//   issues one box of 128 B x P rows per pair and one of 64 B x P rows for the
+//   rope block: 5 x 128 / P copies per tile.
 // - Pages of 1 to 4 rows: lane l looks up the cache rows of tile rows
-//   [4 l, 4 l + 4) and issues one four-row gather per column block (the box
-//   one row high), 288 copies per tile.
+//   [4 l, 4 l + 4) and issues one four-row gather per pair (128 B wide) and
+//   one for the rope block (64 B wide), the maps' boxes one row high: 160
+//   copies per tile.
 // Rows past the unit's end repeat its last row, or page (the softmax masks
 // them and zeroes their V part).
 template <int kTok>
@@ -346,25 +345,23 @@ __device__ void producer_e4m3_gather(const Stage1Params& p, const Ctx& x, int la
     if (__shfl_sync(0xffffffffu, lane == 0 ? *x.abort_flag : 0, 0)) break;
     if (per_page) {
       if (lane < (kTileRows >> p.page_shift)) {
-        // page `lane`: groups [lane P / 8, (lane + 1) P / 8) of the tile
-        const int g_tile = lane << (p.page_shift - 3), g_cache = cr[0] >> 3;
+        // page `lane`: tile rows [lane P, lane P + P)
+        const int r_tile = lane << p.page_shift;
 #pragma unroll
         for (int f = 0; f < 4; ++f)
-          tma_load_4d(x.smem + L::pairs + sl[f] * kPairBytes + g_tile * 1024, &p.tmap_kv16, 0, 0, 2 * f, g_cache,
+          tma_load_2d(x.smem + L::pairs + sl[f] * kPairBytes + r_tile * 128, &p.tmap_kv16, 128 * f, cr[0],
                       &x.bar[kPairFull + sl[f]], pol);
-        tma_load_2d(x.smem + L::rope + rs * kChunkBytes + ((lane << p.page_shift) << 6), &p.tmap_kv64, 512, cr[0],
+        tma_load_2d(x.smem + L::rope + rs * kChunkBytes + r_tile * 64, &p.tmap_kv64, 512, cr[0],
                     &x.bar[kRopeFull + rs], pol);
       }
     } else {
-      // rows [4 lane, 4 lane + 4): half of 8-row group lane / 2
-      const int gofs = (lane >> 1) * 1024 + (lane & 1) * 256;
+      // tile rows [4 lane, 4 lane + 4)
 #pragma unroll
-      for (int c = 0; c < 9; ++c) {
-        uint8_t* blk = c < 8 ? x.smem + L::pairs + sl[c >> 1] * kPairBytes + (c & 1) * 512 + gofs
-                             : x.smem + L::rope + rs * kChunkBytes + 256 * lane;
-        uint64_t* bar = c < 8 ? &x.bar[kPairFull + sl[c >> 1]] : &x.bar[kRopeFull + rs];
-        tma_gather4(blk, &p.tmap_kv16, 64 * c, cr[0], cr[1], cr[2], cr[3], bar, pol);
-      }
+      for (int f = 0; f < 4; ++f)
+        tma_gather4(x.smem + L::pairs + sl[f] * kPairBytes + 512 * lane, &p.tmap_kv16, 128 * f, cr[0], cr[1], cr[2],
+                    cr[3], &x.bar[kPairFull + sl[f]], pol);
+      tma_gather4(x.smem + L::rope + rs * kChunkBytes + 256 * lane, &p.tmap_kv64, 512, cr[0], cr[1], cr[2], cr[3],
+                  &x.bar[kRopeFull + rs], pol);
     }
     if (it == 0 && lane == 0) trace_stamp(p, kTrFirstLoad);
   }
@@ -705,11 +702,12 @@ constexpr uint64_t kTplK64 = tc::desc_template(16, 512, 4);          // K-major,
 constexpr uint64_t kTplV = tc::desc_template(kChunkBytes, 512, 4);   // V^T, MN-major, 64 B swizzle
 constexpr uint64_t kTplP = tc::desc_template(1024, 256, 6);          // P^T, MN-major, 32 B swizzle
 constexpr uint64_t kTplP2 = tc::desc_template(kPBytes, 256, 6);      // two tokens' P^T: 32-byte atoms kPBytes apart
-// pair slots with 8-row groups outermost (pages of fewer than 64 rows, e4m3):
-// [16 groups][2 column blocks][8 rows x 64 B], so column block c of the slot
-// starts at 512 c and an 8-row group is 1024 B on
-constexpr uint64_t kTplK64G = tc::desc_template(16, 1024, 4);        // K-major, 64 B swizzle, groups 1 KB apart
-constexpr uint64_t kTplVG = tc::desc_template(512, 1024, 4);         // V^T, MN-major: blocks 512 B, groups 1 KB apart
+// pair slots as 128-byte rows (pages of fewer than 64 rows, e4m3): both column
+// blocks of a row side by side, [16 groups][8 rows x 128 B] with the 128-byte
+// swizzle; column block 2 f + 1 starts 64 B into the row, and an 8-row group
+// is 1024 B on.  The V^T block of the pair is one MN-major atom wide.
+constexpr uint64_t kTplK128 = tc::desc_template(16, 1024, 2);        // K-major, 128 B swizzle
+constexpr uint64_t kTplV128 = tc::desc_template(16, 1024, 2);        // V^T, MN-major, 128 B swizzle
 __host__ __device__ constexpr uint32_t lo_word(uint64_t d) { return (uint32_t)d; }
 __host__ __device__ constexpr uint32_t hi_word(uint64_t d) { return (uint32_t)(d >> 32); }
 
@@ -719,8 +717,8 @@ __host__ __device__ constexpr uint32_t hi_word(uint64_t d) { return (uint32_t)(d
 template <bool kMx, int kTok, bool kSmallPages>
 __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
   using L = Layout<kMx, kTok>;
-  constexpr bool kGM = kSmallPages && !kMx;  // group-major pair slots
-  constexpr uint64_t kTplA = kGM ? kTplK64G : kTplK64;
+  constexpr bool kR128 = kSmallPages && !kMx;  // pair slots of 128-byte rows
+  constexpr uint64_t kTplA = kR128 ? kTplK128 : kTplK64;
   using TM = Tmem<kTok>;
   constexpr int kPairSlots = Geo<kMx, kTok>::pair_slots;
   const uint32_t pairs0 = smem_u32(x.smem + L::pairs), rope0 = smem_u32(x.smem + L::rope);
@@ -756,7 +754,7 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
 #pragma unroll
       for (int ks = 0; ks < 18; ++ks) {
         const int c = ks >> 1, half = ks & 1;
-        constexpr int kBlockStride = kGM ? 512 : kChunkBytes;  // column block 2 f + 1 within pair f
+        constexpr int kBlockStride = kR128 ? 64 : kChunkBytes;  // column block 2 f + 1 within pair f
         const uint32_t a =
             c < 8 ? ap[c >> 1] + (((c & 1) * kBlockStride + 32 * half) >> 4) : ar + ((32 * half) >> 4);
         // both tokens' query rows form one B operand (block c: 32 kTok rows of 64 B)
@@ -776,9 +774,9 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
 template <bool kMx, int kTok, bool kSmallPages>
 __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
   using L = Layout<kMx, kTok>;
-  constexpr bool kGM = kSmallPages && !kMx;  // group-major pair slots
-  constexpr uint64_t kTplA = kGM ? kTplVG : kTplV;
-  constexpr uint32_t kRows32 = kGM ? 4 * 1024 : 2048;  // bytes of 32 rows of V^T in a slot
+  constexpr bool kR128 = kSmallPages && !kMx;  // pair slots of 128-byte rows
+  constexpr uint64_t kTplA = kR128 ? kTplV128 : kTplV;
+  constexpr uint32_t kRows32 = kR128 ? 4 * 1024 : 2048;  // bytes of 32 rows of V^T in a slot
   using TM = Tmem<kTok>;
   constexpr int kPairSlots = Geo<kMx, kTok>::pair_slots;
   const uint32_t pairs0 = smem_u32(x.smem + L::pairs), pb0 = smem_u32(x.smem + L::pb);
@@ -950,7 +948,7 @@ __device__ __forceinline__ float exp2_int(int e) { return __int_as_float((e + 12
 // entry), and token ti's partial slot is u + ti S_b.
 template <bool kMx, int kTok, bool kSmallPages>
 __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, int lane, int ti) {
-  constexpr bool kGM = kSmallPages && !kMx;  // group-major pair slots
+  constexpr bool kR128 = kSmallPages && !kMx;  // pair slots of 128-byte rows
   using L = Layout<kMx, kTok>;
   using TM = Tmem<kTok>;
   constexpr int kGvNone = -1000;   // no MXFP4 reference yet
@@ -1127,13 +1125,23 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
         // rows past the unit's end hold other rows' data: zero their V part so
         // that P = 0 cannot meet a non-finite value (the MXFP4 converters write zeros)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint8_t* blk = x.smem + L::pairs + pair_slot<kMx, kTok>(it, c >> 1) * kPairBytes +
-                         (kGM ? (row >> 3) * 1024 + (c & 1) * 512 : (c & 1) * kChunkBytes);
-          const int r = kGM ? (row & 7) : row;
+        if constexpr (kR128) {
+          // the row's 128 bytes in each pair slot (all eight 16-byte units, whatever the swizzle)
 #pragma unroll
-          for (int uu = 0; uu < 4; ++uu)
-            *reinterpret_cast<uint4*>(blk + sw64_off(r, 16 * uu)) = make_uint4(0, 0, 0, 0);
+          for (int f = 0; f < 4; ++f) {
+            uint8_t* rb = x.smem + L::pairs + pair_slot<kMx, kTok>(it, f) * kPairBytes + row * 128;
+#pragma unroll
+            for (int uu = 0; uu < 8; ++uu) *reinterpret_cast<uint4*>(rb + 16 * uu) = make_uint4(0, 0, 0, 0);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint8_t* blk =
+                x.smem + L::pairs + pair_slot<kMx, kTok>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes;
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu)
+              *reinterpret_cast<uint4*>(blk + sw64_off(row, 16 * uu)) = make_uint4(0, 0, 0, 0);
+          }
         }
       }
       tc::fence_proxy_async();
