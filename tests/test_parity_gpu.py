@@ -368,6 +368,30 @@ def test_benchmark_workloads_full(orc, name):
     assert dec.poll_error() == 0
 
 
+@pytest.mark.parametrize("name", synth.WORKLOAD_ORDER)
+def test_repeated_calls_are_identical(name):
+    """Twenty calls of each benchmark workload, with the L2 flushed between
+    them as the benchmark does: the same bits every time and no device error
+    (the split kernel's CTAs finish in a different order on every call)."""
+    inp = synth.make_workload(name)
+    dev = torch.device("cuda:0")
+    dec = binding.MLADecoder(inp.kv_indptr, inp.kv_dtype, device=dev)
+    scale = {"bf16": None, "fp8": inp.kv_scale, "mxfp4": inp.block_scales}[inp.kv_dtype]
+    args = (inp.q.to(dev), inp.kv.to(dev), inp.kv_indptr.to(dev), inp.qo_indptr.to(dev))
+    sc = None if scale is None else scale.to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    first = None
+    for i in range(20):
+        flush.fill_(i & 0xFF)
+        out, lse = dec(*args, kv_scale=sc)
+        torch.cuda.synchronize()
+        assert dec.poll_error() == 0, f"{name} call {i}: device error"
+        if first is None:
+            first = (out.clone(), lse.clone())
+        else:
+            assert torch.equal(out, first[0]) and torch.equal(lse, first[1]), f"{name} call {i} differs"
+
+
 @pytest.mark.parametrize("spread", [6, 12])
 def test_mxfp4_wide_block_exponents(orc, spread):
     """MXFP4 rows whose block scales lie up to 2 x spread below the row's
