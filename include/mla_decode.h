@@ -58,6 +58,7 @@ extern "C" {
 #define MLA_MX_BLOCK 32
 #define MLA_MX_SCALES_PER_ROW 18
 #define MLA_MAX_BATCH 65536
+#define MLA_PLAN_FIRST_ROWS 256
 
 typedef enum {
   MLA_KV_BF16 = 0,
@@ -122,6 +123,12 @@ typedef struct {
   int32_t tokens_fused;   /* 2: a two-token e4m3 plan whose split kernel reads each cache row once
                              for both tokens (see mla_decode_plan_multi); 0 otherwise */
   int32_t reserved[2];
+  /* first_row[c] (c < MLA_PLAN_FIRST_ROWS): the row-space row of the first tile
+   * CTA c of the split kernel reads, -1 when it reads none or the plan does not
+   * say (paged and multi-token plans).  The e4m3 split kernel starts that
+   * tile's copy on entry, before its unit scan; the device kv_indptr must then
+   * hold the values the plan was made from (as it must anyway). */
+  int32_t first_row[MLA_PLAN_FIRST_ROWS];
 } mla_plan;
 
 /*

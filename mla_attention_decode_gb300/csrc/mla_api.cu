@@ -234,6 +234,42 @@ int device_sm_count(int32_t* out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// plan->first_row (mla_decode.h): the first row of the first non-empty unit of
+// each CTA, by the unit rules of the plan's schedule (contiguous single-token
+// plans; the others say -1).
+void fill_first_rows(mla_plan* plan, const int32_t* kv_indptr_host) {
+  for (int c = 0; c < MLA_PLAN_FIRST_ROWS; ++c) plan->first_row[c] = -1;
+  if (!kv_indptr_host || plan->batch <= 0 || plan->grid <= 0) return;
+  const int64_t B = plan->batch, G = plan->grid, R = plan->tile_tokens;
+  auto set = [&](int64_t c, int64_t row) {
+    if (c >= 0 && c < MLA_PLAN_FIRST_ROWS && plan->first_row[c] < 0) plan->first_row[c] = static_cast<int32_t>(row);
+  };
+  if (plan->schedule == 1) {
+    const int64_t U = plan->unit_cost, T = plan->total_tiles, C = T + U * (B - 1);
+    int64_t P = 0;
+    for (int64_t b = 0; b < B; ++b) {
+      const int64_t L = (int64_t)kv_indptr_host[b + 1] - kv_indptr_host[b];
+      const int64_t w = L > 0 ? (L + R - 1) / R : 1;
+      const int64_t X = P + U * b;
+      if (L > 0)
+        for (int64_t c = cta_of(X, C, G); c <= cta_of(X + w - 1, C, G); ++c) {
+          const int64_t lo = c * C / G;
+          set(c, kv_indptr_host[b] + R * ((lo > X ? lo : X) - X));
+        }
+      P += w;
+    }
+  } else {
+    int64_t u = 0;
+    for (int64_t b = 0; b < B; ++b) {
+      const int64_t L = (int64_t)kv_indptr_host[b + 1] - kv_indptr_host[b];
+      const int32_t S = splits_for(L, plan->chunk_tokens, plan->max_splits, static_cast<int>(R));
+      const int64_t t = (L + R - 1) / R;
+      for (int32_t sp = 0; sp < S; ++sp, ++u)
+        if (L > 0) set(u % G, kv_indptr_host[b] + R * ((int64_t)sp * t / S));
+    }
+  }
+}
+
 // Trace builds: the stamp buffer of the split kernel's launches (null: off).
 uint64_t* g_trace = nullptr;
 
@@ -306,6 +342,7 @@ int plan_lengths(const std::vector<int64_t>& lens, int32_t total_kv, int32_t kv_
       p.schedule = 1;
       p.total_tiles = static_cast<int32_t>(bp.T);
       p.unit_cost = bp.unit_cost;
+      for (int c = 0; c < MLA_PLAN_FIRST_ROWS; ++c) p.first_row[c] = -1;
       *plan = p;
       return MLA_OK;
     }
@@ -330,6 +367,7 @@ int plan_lengths(const std::vector<int64_t>& lens, int32_t total_kv, int32_t kv_
   p.splits_max = smax;
   p.tile_tokens = tile_rows(kv_dtype);
   p.units_per_cta = p.grid > 0 ? (p.num_work + p.grid - 1) / p.grid : 0;
+  for (int c = 0; c < MLA_PLAN_FIRST_ROWS; ++c) p.first_row[c] = -1;
   *plan = p;
   return MLA_OK;
 }
@@ -351,7 +389,9 @@ int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dty
     if (L < 0) return MLA_ERR_INVALID_ARG;
     lens[static_cast<size_t>(b)] = L;
   }
-  return plan_lengths(lens, kv_indptr_host[batch], kv_dtype, num_sms, num_splits, plan);
+  const int rc = plan_lengths(lens, kv_indptr_host[batch], kv_dtype, num_sms, num_splits, plan);
+  if (rc == MLA_OK) fill_first_rows(plan, kv_indptr_host);
+  return rc;
 }
 
 int mla_decode_plan_multi(const int32_t* kv_indptr_host, int32_t num_seqs, int32_t q_len, int32_t kv_dtype,
@@ -512,6 +552,14 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   if (plan->q_len > 16 || (p->q_len > 1 && (paged || plan->batch % p->q_len != 0))) return MLA_ERR_INVALID_ARG;
   // a two-token plan: e4m3 KV, q_len 2, two partial slots per work unit
   p->tok = plan->tokens_fused == 2 ? 2 : 1;
+  // the first tile rows of a contiguous single-token plan (the e4m3 split
+  // kernel starts those copies before its unit scan)
+  const bool first_rows = !paged && p->q_len == 1 && p->tok == 1;
+  for (int c = 0; c < MLA_PLAN_FIRST_ROWS; ++c) {
+    const int32_t r = first_rows ? plan->first_row[c] : -1;
+    if (r < -1 || r >= plan->total_kv) return MLA_ERR_INVALID_ARG;  // a row of the cache, or none
+    p->first_row[c] = r;
+  }
   if (plan->tokens_fused != 0 && (plan->tokens_fused != 2 || plan->kv_dtype != MLA_KV_FP8_E4M3 ||
                                   plan->q_len != 2 || plan->num_work % 2 != 0))
     return MLA_ERR_INVALID_ARG;

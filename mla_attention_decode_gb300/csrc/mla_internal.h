@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "mla_decode.h"
+
 namespace mla {
 
 constexpr int kHeads = 16;
@@ -84,6 +86,7 @@ struct Stage1Params {
   int32_t tok;          // tokens one work unit serves (2: fused two-token e4m3 plan, else 1);
                         // num_work then counts partial slots, tok per unit
   uint64_t* trace;      // trace builds only: [grid][kTraceSlots] global-timer stamps (else null)
+  int32_t first_row[MLA_PLAN_FIRST_ROWS];  // the plan's first tile row per CTA (-1: none; see mla_plan)
 };
 
 // Per-CTA stamp slots of a trace build (compiled with MLA_TRACE=1).

@@ -169,6 +169,7 @@ struct Ctx {
   uint64_t* bar;
   volatile int* abort_flag;
   uint32_t tmem;
+  int early_row;  // e4m3, one token: the row of the first tile, copied before the unit scan (-1: none)
 };
 
 __device__ __forceinline__ int tiles_of(const UnitDesc& d) { return (d.end - d.start + kTileRows - 1) / kTileRows; }
@@ -244,7 +245,24 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
   int nt0 = 0, nend = 0;
   bool have = walk.next(x, nt0, nend);
   TileRows nrows = have ? tile_rows(p, nt0, nend) : TileRows{0, -1};
+  bool early_pending = x.early_row >= 0;  // the tile copied on entry is not yet accounted for
   for (int it = 0; have && !*x.abort_flag; ++it) {
+    if (it == 0 && early_pending) {
+      // the kernel prologue copied the tile the plan names into pair slots 0..3
+      // and rope slot 0; the scan must agree (it does unless the device
+      // kv_indptr differs from the plan's), else flag it and stop
+      early_pending = false;
+      for (int f = 0; f < 4; ++f) ++armed[f];
+      ++armed[kPairSlots];
+      if (!paged64 && nrows.r0 == x.early_row) {
+        have = walk.next(x, nt0, nend);
+        if (have) nrows = tile_rows(p, nt0, nend);
+        continue;
+      }
+      atomicCAS(p.ws_err, 0, kErrDeviceIndex);
+      *x.abort_flag = 1;
+      break;
+    }
     if (MLA_FIRST_TILE_WAIT && it == 1) {
       // the first tile lands before the rest of the ring is requested
       for (int f = 0; f < 4; ++f) wait_phase(&x.bar[kPairFull + f], 0, x.abort_flag, p.ws_err);
@@ -271,6 +289,14 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
     mbar_arrive_expect_tx(&x.bar[kRopeFull + rs], block_bytes);
     load_block(x.smem + L::rope + rs * kChunkBytes, 512, rows, &x.bar[kRopeFull + rs]);
     ++armed[kPairSlots + rs];
+  }
+  if (early_pending) {
+    // the plan named a tile that this CTA's scan does not have: flag it, and
+    // let the copy land before leaving
+    atomicCAS(p.ws_err, 0, kErrDeviceIndex);
+    *x.abort_flag = 1;
+    for (int f = 0; f < 4; ++f) ++armed[f];
+    ++armed[kPairSlots];
   }
   if (*x.abort_flag) {
     // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
@@ -1221,6 +1247,26 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
     for (int i = 0; i < L::nbars; ++i) mbar_init(&x.bar[i], counts[i]);
     *x.abort_flag = 0;
     fence_mbar_init();
+    misc[3] = -1;
+    if constexpr (!kMx && kTok == 1 && !kSmallPages) {
+      // the first tile's copy starts now, before the unit scan: the plan names
+      // its row (the producer checks it against the scan), into pair slots
+      // 0..3 and rope slot 0, where the producer would put tile 0
+      const int r0 = blockIdx.x < MLA_PLAN_FIRST_ROWS ? p.first_row[blockIdx.x] : -1;
+      if (r0 >= 0 && !p.paged) {
+        const uint64_t pol = policy_evict_first();
+        for (int f = 0; f < 4; ++f) {
+          uint8_t* dst = smem + L::pairs + f * kPairBytes;
+          mbar_arrive_expect_tx(&x.bar[kPairFull + f], 2 * kChunkBytes);
+          tma_load_2d(dst, &p.tmap_kv64, 128 * f, r0, &x.bar[kPairFull + f], pol);
+          tma_load_2d(dst + kChunkBytes, &p.tmap_kv64, 128 * f + 64, r0, &x.bar[kPairFull + f], pol);
+        }
+        mbar_arrive_expect_tx(&x.bar[kRopeFull], kChunkBytes);
+        tma_load_2d(smem + L::rope, &p.tmap_kv64, 512, r0, &x.bar[kRopeFull], pol);
+        trace_stamp(p, kTrFirstLoad);
+        misc[3] = r0;
+      }
+    }
   }
   if (warp == 0) {
     // no grid-dependency wait here: this kernel is launched only once the
@@ -1251,6 +1297,7 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
   pdl_launch_dependents();
   x.tmem = *tmem_slot;
   x.nunits = *s_nunits;
+  x.early_row = misc[3];
   if (threadIdx.x == 0) {
     trace_stamp(p, kTrSetup);
     trace_value(p, kTrUnits, (uint64_t)x.nunits);

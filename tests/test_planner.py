@@ -87,9 +87,28 @@ def n_splits_of(plan, lens):
     return [cta_of(x + wb - 1, C, G) - cta_of(x, C, G) + 1 for wb, x in zip(w, X)]
 
 
+def first_rows_of(plan, lens, ind):
+    """Per CTA, the first row of its first non-empty unit (mla_plan.first_row)."""
+    G, R = plan.grid, plan.tile_tokens
+    first = [-1] * 256
+    us = units_of(plan, lens)
+    if plan.schedule == 1:
+        w, X, C = positions(plan, lens)
+        owner = []
+        for wb, x in zip(w, X):
+            owner += list(range(cta_of(x, C, G), cta_of(x + wb - 1, C, G) + 1))
+    else:
+        owner = [u % G for u in range(len(us))]
+    for (a, b), c in zip(us, owner):
+        if b > a and c < 256 and first[c] < 0:
+            first[c] = a + ind[0]
+    return first
+
+
 def check_plan(lens, dtype="fp8", num_sms=152, num_splits=0):
     ind = [0] + list(itertools.accumulate(lens))
     plan = binding.mla_decode_plan(ind, dtype, num_sms=num_sms, num_splits=num_splits)
+    assert list(plan.first_row) == first_rows_of(plan, lens, ind)
     us = units_of(plan, lens)
     assert plan.num_work == len(us)
     assert plan.batch == len(lens) and plan.total_kv == ind[-1]
@@ -302,3 +321,22 @@ def test_two_token_slots_partition_the_workspace():
             assert all(x[1] == y[0] for x, y in zip(mine, mine[1:]))
             assert all(x[1] > x[0] for x in mine) or L == 0
             u += Sb
+
+
+def test_first_rows_follow_the_units():
+    """mla_plan.first_row: per CTA, the first row of its first non-empty unit
+    (rows of the device kv_indptr, which may start above 0); -1 for CTAs
+    without one and for paged and multi-token plans."""
+    rng = random.Random(17)
+    for _ in range(60):
+        lens = [rng.choice([0, 1, 130, rng.randint(1, 5000), rng.randint(1, 40000)]) for _ in range(rng.randint(1, 70))]
+        base = rng.choice([0, 0, 7, 1000])
+        ind = [base] + [base + x for x in itertools.accumulate(lens)]
+        for dtype in ("bf16", "fp8", "mxfp4"):
+            plan = binding.mla_decode_plan(ind, dtype, num_sms=rng.choice([5, 152]),
+                                           num_splits=rng.choice([0, 0, 3]))
+            assert list(plan.first_row) == first_rows_of(plan, lens, ind)
+    m = binding.mla_decode_plan_multi([0, 300, 700], 2, "fp8", num_sms=152)
+    assert set(m.first_row) == {-1}
+    pg = binding.mla_decode_plan_paged([0, 2, 5], [7, 3], 8, 8, "fp8", num_sms=152)
+    assert set(pg.first_row) == {-1}
