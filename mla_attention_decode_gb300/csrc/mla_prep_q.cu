@@ -19,16 +19,15 @@
 
 namespace mla {
 
-// One CTA of 64 threads per sequence: thread j handles head j/4, features
-// [144 (j%4), 144 (j%4) + 144).  At most 112 registers per thread (the launch
-// bound of 9 CTAs per SM): then a CTA of this grid fits on an SM beside an e4m3
-// split CTA (149 registers x 384 threads), and the split CTAs on the SMs this grid
-// occupies start at once instead of after it (measured: 1.9 us off a bs32 /
-// kv1024 call, 0.8 us off bs64 / kv8192).  The row is read twice: all 18
-// loads in flight for the head maximum, then again (L1 hits) for the
-// conversion, so that it never sits in registers whole.
+// One CTA of 128 threads per sequence: thread j handles head j/8, features
+// [72 (j%8), 72 (j%8) + 72), all nine 16-byte loads in flight for the head
+// maximum, then the same row again (L1 hits) for the conversion, in 53
+// registers.  Measured against one CTA of 64 threads at 174 registers (a
+// thread per 144 features): calls 1.4-1.9 us faster at bs32/kv1024 and
+// bs64/kv8192.  The split CTAs placed on this grid's SMs still start when its
+// CTAs have finished (a per-CTA trace shows them entering about 3.3 us late).
 template <bool kMx>
-__global__ void __launch_bounds__(64, 9) mla_prep_q_kernel(const __grid_constant__ Stage1Params p) {
+__global__ void __launch_bounds__(128, 9) mla_prep_q_kernel(const __grid_constant__ Stage1Params p) {
   pdl_wait_primary();      // q and qo_indptr written by earlier work are visible
   pdl_launch_dependents();  // the split kernel may begin its set-up
   const int b = blockIdx.x, j = threadIdx.x;
@@ -37,23 +36,24 @@ __global__ void __launch_bounds__(64, 9) mla_prep_q_kernel(const __grid_constant
   // scan (the comparison only keeps the load; offsets are never negative)
   if (j == 0 && __ldg(p.kv_indptr + (p.q_len > 1 ? b / p.q_len : b)) < 0) p.ws_err[1] = 1;
   if (qrow < 0) return;  // the split kernel reports the bad index
-  const int h = j >> 2, part = j & 3;
+  const int h = j >> 3, part = j & 7;  // 8 threads per head, 72 features each
   const float kv_scale = kMx ? 1.f : *static_cast<const float*>(p.kv_scale);
-  const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)qrow * kHeads + h) * kQkDim + 144 * part) * 2);
+  const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)qrow * kHeads + h) * kQkDim + 72 * part) * 2);
   float amax = 0.f;
   {
-    uint4 raw[18];
+    uint4 raw[9];
 #pragma unroll
-    for (int i = 0; i < 18; ++i) raw[i] = __ldg(src + i);
+    for (int i = 0; i < 9; ++i) raw[i] = __ldg(src + i);
 #pragma unroll
-    for (int i = 0; i < 18; ++i) {
+    for (int i = 0; i < 9; ++i) {
       const float4 a = bf16x4_to_f4(make_uint2(raw[i].x, raw[i].y));
       const float4 c = bf16x4_to_f4(make_uint2(raw[i].z, raw[i].w));
       amax = fmaxf(amax, fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
                                fmaxf(fmaxf(fabsf(c.x), fabsf(c.y)), fmaxf(fabsf(c.z), fabsf(c.w)))));
     }
   }
-  amax = quad_max(amax);
+  amax = quad_max(amax);  // over the head's 8 threads
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
   // power-of-two scale with amax * scale <= 448 (e4m3 max); 1 for an all-zero head
   float sc = 1.f;
   if (amax > 0.f) {
@@ -61,9 +61,9 @@ __global__ void __launch_bounds__(64, 9) mla_prep_q_kernel(const __grid_constant
     if (amax * sc > 448.f) sc *= 0.5f;
   }
   uint8_t* dst = p.ws_q + (size_t)b * kQPrepBytes;
-#pragma unroll 6
-  for (int i = 0; i < 18; ++i) {
-    const int f0 = 144 * part + 8 * i;  // 8 features, inside one 16-byte unit of a 64-byte block
+#pragma unroll 3
+  for (int i = 0; i < 9; ++i) {
+    const int f0 = 72 * part + 8 * i;  // 8 features, inside one 16-byte unit of a 64-byte block
     const uint4 r = __ldg(src + i);
     const float4 a = bf16x4_to_f4(make_uint2(r.x, r.y));
     const float4 c = bf16x4_to_f4(make_uint2(r.z, r.w));
@@ -79,8 +79,8 @@ __global__ void __launch_bounds__(64, 9) mla_prep_q_kernel(const __grid_constant
 
 cudaError_t launch_prep_q(const Stage1Params& p, bool mx, cudaStream_t s) {
   if (p.batch <= 0) return cudaSuccess;
-  cudaError_t e = mx ? launch_overlapped(mla_prep_q_kernel<true>, dim3(p.batch), dim3(64), 0, s, p)
-                     : launch_overlapped(mla_prep_q_kernel<false>, dim3(p.batch), dim3(64), 0, s, p);
+  cudaError_t e = mx ? launch_overlapped(mla_prep_q_kernel<true>, dim3(p.batch), dim3(128), 0, s, p)
+                     : launch_overlapped(mla_prep_q_kernel<false>, dim3(p.batch), dim3(128), 0, s, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
