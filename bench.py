@@ -61,11 +61,17 @@ KERNEL_SOURCES = {
     "fp8": [_CSRC + f for f in ("mla_tc.cuh", "mla_common.cuh", "mla_ptx.cuh", "mla_internal.h")],
     "mxfp4": [_CSRC + f for f in ("mla_tc.cuh", "mla_common.cuh", "mla_ptx.cuh", "mla_internal.h",
                                   "mla_split_mxfp4.cu")],
+    "mxfp4_bs": [_CSRC + f for f in ("mla_tc.cuh", "mla_common.cuh", "mla_ptx.cuh", "mla_internal.h",
+                                     "mla_split_mxfp4_bs.cu")],
 }
 KERNEL_NAMES = {"bf16": "mla_split_kernel (mma.sync, bf16)",
                 "fp8": "mla_prep_q_kernel + mla_split_tc_kernel (tcgen05, e4m3), launches overlapped",
                 "mxfp4": "mla_prep_q_kernel + mla_split_tc_kernel (tcgen05, e2m1 dequantised to e4m3), "
-                         "launches overlapped"}
+                         "launches overlapped",
+                "mxfp4_bs": "mla_prep_q_kernel + mla_split_tc_kernel (tcgen05 block-scaled e2m1 x e4m3 scores, "
+                            "V dequantised to e4m3), launches overlapped"}
+# the block-scaled form of the MXFP4 workload, timed beside the five in per_config
+MX_BS_SUFFIX = "_block_scaled"
 CLOCK_SOAK_S = 1.0
 CPU_BUDGET_HEADLINE_S = 15.0
 CPU_BUDGET_PER_CONFIG_S = 4.0
@@ -334,11 +340,13 @@ class Workload:
     """One workload resident on the device, with its plan, workspace and the
     calls the bench times."""
 
-    def __init__(self, name, args, rank, dev):
+    def __init__(self, name, args, rank, dev, mx_bs=False):
         from mla_attention_decode_gb300 import binding
         self.binding = binding
-        self.name = name
+        self.name = name + (MX_BS_SUFFIX if mx_bs else "")
         b, L, self.dt = synth.WORKLOADS[name]
+        assert not mx_bs or self.dt == "mxfp4"
+        self.kind = "mxfp4_bs" if mx_bs else self.dt  # which kernel sources and name the roofline cites
         self.inp, self.paged = make_workload_inputs(name, args, rank)
         dt = self.dt
         d = to_device(self.inp, dev)
@@ -351,9 +359,10 @@ class Workload:
             d["kv_indices"] = pg_.kv_indices.to(dev)
             d["last_page_len"] = pg_.last_page_len.to(dev)
             self.dec = binding.PagedMLADecoder(pg_.page_indptr, pg_.last_page_len, pg_.page_size, pg_.num_pages, dt,
-                                               device=dev)
+                                               device=dev, mx_block_scaled=mx_bs)
         else:
-            self.dec = binding.MLADecoder(self.inp.kv_indptr, dt, device=dev, q_len=args.q_len)
+            self.dec = binding.MLADecoder(self.inp.kv_indptr, dt, device=dev, q_len=args.q_len,
+                                          mx_block_scaled=mx_bs)
         self.d = d
         self.plan = self.dec.plan
         self.out = torch.empty(self.plan.batch, 16, 512, dtype=torch.bfloat16, device=dev)
@@ -407,8 +416,8 @@ def roofline_entry(w: Workload, args, t_split: float, t_comb: float, peak: float
     key = w.name + (f"_q{args.q_len}" if args.q_len > 1 else "")
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(key, w.dt) if w.paged is None else None,
-            "kernel": KERNEL_NAMES[w.dt] if w.paged is None else "whole paged call",
+            "traffic": profiled_traffic(key, w.kind) if w.paged is None else None,
+            "kernel": KERNEL_NAMES[w.kind] if w.paged is None else "whole paged call",
             "kernel_us": round(t_split, 3), "combine_us": round(t_comb, 3),
             "peak_kind": f"{peak_kind} (HBM copy)"}
 
@@ -417,11 +426,12 @@ def measure_per_config(args, rank, dev, stream, flush, peak, peak_kind, headline
     """Every workload timed as the headline is (same flush, same events), one
     after another; the headline's own entry is the headline's numbers."""
     res = {}
-    for name in synth.WORKLOAD_ORDER:
-        if name == args.workload:
+    mx_name = next(n for n in synth.WORKLOAD_ORDER if synth.WORKLOADS[n][2] == "mxfp4")
+    for name, mx_bs in [(n, False) for n in synth.WORKLOAD_ORDER] + [(mx_name, True)]:
+        if name == args.workload and not mx_bs:
             res[name] = headline
             continue
-        w = Workload(name, args, rank, dev)
+        w = Workload(name, args, rank, dev, mx_bs=mx_bs)
         for _ in range(max(3, args.warmup)):
             w.call(stream)
         assert w.dec.poll_error() == 0, f"{name}: device error"
@@ -434,11 +444,13 @@ def measure_per_config(args, rank, dev, stream, flush, peak, peak_kind, headline
                  "gpu_launches": args.steps * w.launches_per_call,
                  "plan": {k: w.plan.as_dict()[k] for k in ("num_work", "grid", "chunk_tokens", "splits_max",
                                                           "schedule")}}
-        if not args.no_cpu_baseline:
+        if mx_bs:
+            entry["form"] = "MXFP4 scores by block-scaled MMAs on the e2m1 tile (plan.mx_scores = 1)"
+        if not args.no_cpu_baseline and not mx_bs:
             us_cpu, cores, sample = cpu_baseline(w.inp, args.q_len, w.paged, budget_s=CPU_BUDGET_PER_CONFIG_S)
             entry["cpu_baseline"] = {"value": round(us_cpu, 1), "unit": "us/call", "cores": cores, "kind": "oracle",
                                      "sample": sample}
-        res[name] = entry
+        res[w.name] = entry
         del w
         torch.cuda.empty_cache()
     return res

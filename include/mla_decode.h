@@ -122,7 +122,14 @@ typedef struct {
   int32_t q_len;          /* query tokens per sequence (0 or 1: one; see mla_decode_plan_multi) */
   int32_t tokens_fused;   /* 2: a two-token e4m3 plan whose split kernel reads each cache row once
                              for both tokens (see mla_decode_plan_multi); 0 otherwise */
-  int32_t reserved[2];
+  int32_t mx_scores;      /* mxfp4 only, set by the caller after planning (the planners write 0):
+                             0: both tensor-core products read an e4m3 copy of each tile made
+                             in shared memory; 1: the scores q.k come from block-scaled MMAs
+                             (tcgen05 kind::mxf8f6f4) on the e2m1 tile with the cache's e8m0
+                             block scales, only the V part being converted for P.V (needs kv
+                             32-byte aligned).  Paged caches with pages of fewer than 64 rows
+                             always take the copy. */
+  int32_t reserved;
   /* first_row[c] (c < MLA_PLAN_FIRST_ROWS): the row-space row of the first tile
    * CTA c of the split kernel reads, -1 when it reads none or the plan does not
    * say (paged and multi-token plans).  The e4m3 split kernel starts that
@@ -161,7 +168,8 @@ MLA_API size_t mla_decode_workspace_bytes(const mla_plan* plan);
  *   q          device, bf16 [*, 16, 576] row-major; sequence b uses row qo_indptr[b].
  *              16-byte aligned.
  *   kv         device, see the storage table above; rows [0, plan->total_kv) are read.
- *              16-byte aligned.
+ *              16-byte aligned; 32-byte aligned for mxfp4 (the 4-bit tensor-map
+ *              form the block-scaled kernel reads).
  *   kv_scale   device: NULL for bf16; fp32[1] for fp8 (dequant = e4m3 * kv_scale[0]);
  *              uint8 e8m0 [plan->total_kv, scale_stride] for mxfp4 (16-byte aligned).
  *   scale_stride  mxfp4: bytes between scale rows, >= 18; otherwise 0.
@@ -269,7 +277,8 @@ MLA_API int mla_decode_plan_paged(const int32_t* kv_page_indptr_host, const int3
 /*
  * mla_decode_fwd_paged -- mla_decode_fwd over a paged cache; the plan must come
  * from mla_decode_plan_paged.  Arguments as for mla_decode_fwd, except
- *   kv_pages          device, the cache: num_pages * page_size rows, 16-byte aligned.
+ *   kv_pages          device, the cache: num_pages * page_size rows, 16-byte aligned
+ *                     (mxfp4 with pages of 64 rows or more: 32-byte aligned).
  *   kv_scale          fp8: fp32[1]; mxfp4: uint8 e8m0 [num_pages * page_size, scale_stride].
  *   kv_page_indptr    device int32 [batch+1], equal to the host copy the plan was made from.
  *   kv_indices        device int32 [kv_page_indptr[batch]], each in [0, num_pages).

@@ -38,7 +38,8 @@ class mla_plan(ctypes.Structure):
                 ("tile_tokens", ctypes.c_int32), ("units_per_cta", ctypes.c_int32),
                 ("schedule", ctypes.c_int32), ("total_tiles", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("num_pages", ctypes.c_int32), ("unit_cost", ctypes.c_int32), ("q_len", ctypes.c_int32),
-                ("tokens_fused", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2),
+                ("tokens_fused", ctypes.c_int32), ("mx_scores", ctypes.c_int32),
+                ("reserved", ctypes.c_int32),
                 ("first_row", ctypes.c_int32 * 256)]
 
     def as_dict(self) -> dict:
@@ -236,15 +237,19 @@ class MLADecoder:
     The workspace is allocated once here (torch device memory) and zeroed; the
     library itself never allocates.  ``q_len > 1``: that many query tokens per
     sequence (rows ``qo_indptr[b] + i``, output rows ``b * q_len + i``); e4m3 KV
-    with ``q_len == 2`` gets the single-pass plan (``plan.tokens_fused == 2``)."""
+    with ``q_len == 2`` gets the single-pass plan (``plan.tokens_fused == 2``).
+    ``mx_block_scaled``: MXFP4 scores from block-scaled MMAs on the e2m1 tile
+    (``plan.mx_scores = 1``) instead of the e4m3 copy."""
 
     def __init__(self, kv_indptr_host, kv_dtype, device="cuda", num_sms: int = 0, num_splits: int = 0,
-                 q_len: int = 1):
+                 q_len: int = 1, mx_block_scaled: bool = False):
         self.kv_dtype = _dtype_code(kv_dtype)
         if q_len > 1:
             self.plan = mla_decode_plan_multi(kv_indptr_host, q_len, self.kv_dtype, num_sms, num_splits)
         else:
             self.plan = mla_decode_plan(kv_indptr_host, self.kv_dtype, num_sms, num_splits)
+        if mx_block_scaled:
+            self.plan.mx_scores = 1
         nbytes = max(256, mla_decode_workspace_bytes(self.plan))
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=device)
 
@@ -268,10 +273,12 @@ class PagedMLADecoder:
     """Plan + workspace for one paged batch layout (see mla_decode_plan_paged)."""
 
     def __init__(self, kv_page_indptr_host, kv_last_page_len_host, page_size: int, num_pages: int, kv_dtype,
-                 device="cuda", num_sms: int = 0, num_splits: int = 0):
+                 device="cuda", num_sms: int = 0, num_splits: int = 0, mx_block_scaled: bool = False):
         self.kv_dtype = _dtype_code(kv_dtype)
         self.plan = mla_decode_plan_paged(kv_page_indptr_host, kv_last_page_len_host, page_size, num_pages,
                                           self.kv_dtype, num_sms, num_splits)
+        if mx_block_scaled:
+            self.plan.mx_scores = 1
         nbytes = max(256, mla_decode_workspace_bytes(self.plan))
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=device)
 

@@ -202,6 +202,33 @@ bool encode_kv_map_pairs(CUtensorMap* m, const void* kv, int32_t total_kv, uint3
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MXFP4 rows (288 packed bytes, element 2i in the low nibble of byte i) for the
+// block-scaled kernel: the 512 V features as 4 groups of 128 e2m1 elements in
+// the 16U4_ALIGN16B form (each 16 elements land in 16 bytes of shared memory,
+// 8 packed bytes then 8 zero bytes; 128-byte swizzle), one group x box_rows
+// rows per box (kv 32-byte aligned); and the rows as bytes, for the rope
+// block's 32 bytes (at byte 256) x box_rows rows.
+constexpr cuuint64_t kMxRowBytes = MLA_QK_DIM / 2;
+bool encode_kv_maps_mx(CUtensorMap* m4, CUtensorMap* m8, const void* kv, int32_t total_kv, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t rows = (cuuint64_t)(total_kv > 0 ? total_kv : 1);
+  const cuuint64_t dims4[3] = {128, 4, rows};
+  const cuuint64_t strides4[2] = {64, kMxRowBytes};
+  const cuuint32_t box4[3] = {128, 1, box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(m4, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(kv), dims4, strides4, box4, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const cuuint64_t dims8[2] = {kMxRowBytes, rows};
+  const cuuint64_t strides8[1] = {kMxRowBytes};
+  const cuuint32_t box8[2] = {32, box_rows};
+  return enc(m8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), dims8, strides8, box8, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_kv_map(CUtensorMap* m, const void* kv, int kv_dtype, int32_t total_kv, uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
@@ -552,6 +579,9 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
   if (plan->q_len > 16 || (p->q_len > 1 && (paged || plan->batch % p->q_len != 0))) return MLA_ERR_INVALID_ARG;
   // a two-token plan: e4m3 KV, q_len 2, two partial slots per work unit
   p->tok = plan->tokens_fused == 2 ? 2 : 1;
+  // MXFP4 scores by block-scaled MMAs (pages of fewer than 64 rows take the copy)
+  if (plan->mx_scores != 0 && (plan->mx_scores != 1 || plan->kv_dtype != MLA_KV_MXFP4)) return MLA_ERR_INVALID_ARG;
+  p->mx_bs = (plan->mx_scores == 1 && !(paged && page_shift < 6)) ? 1 : 0;
   // the first tile rows of a contiguous single-token plan (the e4m3 split
   // kernel starts those copies before its unit scan)
   const bool first_rows = !paged && p->q_len == 1 && p->tok == 1;
@@ -585,9 +615,16 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
       std::memcpy(&p->tmap_kv16, &p->tmap_kv64, sizeof(CUtensorMap));
     }
   } else if (plan->kv_dtype == MLA_KV_MXFP4) {
-    // packed rows are fetched by 1-D bulk copies: no tensor map
-    std::memset(&p->tmap_kv64, 0, sizeof(CUtensorMap));
-    std::memset(&p->tmap_kv16, 0, sizeof(CUtensorMap));
+    if (!p->mx_bs) {
+      // the e4m3 copy: packed rows by 1-D bulk copies, no tensor map
+      std::memset(&p->tmap_kv64, 0, sizeof(CUtensorMap));
+      std::memset(&p->tmap_kv16, 0, sizeof(CUtensorMap));
+    } else {
+      // the block-scaled kernel: 128-row boxes (two 64-row boxes per tile for 64-row pages)
+      if (!aligned(kv, 32)) return MLA_ERR_INVALID_ARG;
+      if (!encode_kv_maps_mx(&p->tmap_kv64, &p->tmap_kv16, kv, cache_rows, (paged && page_shift == 6) ? 64u : 128u))
+        return MLA_ERR_CUDA;
+    }
   } else {
     // bf16: 64-row boxes, and 16-row boxes for short tails; pages of fewer
     // than 16 rows come in one page per box

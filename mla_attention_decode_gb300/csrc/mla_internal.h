@@ -85,6 +85,7 @@ struct Stage1Params {
   int32_t q_len;        // query tokens per sequence; batch counts tokens
   int32_t tok;          // tokens one work unit serves (2: fused two-token e4m3 plan, else 1);
                         // num_work then counts partial slots, tok per unit
+  int32_t mx_bs;        // MXFP4 (contiguous, pages >= 64 rows): 1 = scores by block-scaled MMAs
   uint64_t* trace;      // trace builds only: [grid][kTraceSlots] global-timer stamps (else null)
   int32_t first_row[MLA_PLAN_FIRST_ROWS];  // the plan's first tile row per CTA (-1: none; see mla_plan)
 };
@@ -127,6 +128,8 @@ cudaError_t launch_stage1_fp8_t2(const Stage1Params& p, cudaStream_t s);  // p.t
 cudaError_t launch_stage1_mxfp4(const Stage1Params& p, cudaStream_t s);
 // paged caches with pages of fewer than 64 rows (e4m3 or MXFP4, one token)
 cudaError_t launch_stage1_small_pages(const Stage1Params& p, bool mx, cudaStream_t s);
+// MXFP4 scores by block-scaled MMAs on the e2m1 tile (p.mx_bs)
+cudaError_t launch_stage1_mxfp4_bs(const Stage1Params& p, cudaStream_t s);
 // Two-term e4m3 query of every sequence into the workspace (e4m3 / MXFP4 KV).
 cudaError_t launch_prep_q(const Stage1Params& p, bool mx, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s, bool pdl);

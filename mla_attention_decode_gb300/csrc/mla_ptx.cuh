@@ -1,6 +1,8 @@
 // mla_ptx.cuh -- thin inline-PTX wrappers used by the sm_103a decode kernels:
 // mbarriers, bulk async copies (TMA engine), ldmatrix, warp-level tensor-core
-// MMA (bf16 and e4m3), fp8 conversions, named barriers, PDL controls.
+// MMA (bf16 and e4m3), tcgen05 (MMAs with TMEM accumulators, block-scaled
+// MMAs, shared-memory-to-TMEM copies), fp8 conversions, named barriers, PDL
+// controls.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -244,6 +246,14 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, int a_mn, int b_
          ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: A e2m1, B e4m3,
+// both K-major (4-bit operands cannot be MN-major), fp32 accumulator, ue8m0
+// scale factors; a_sf / b_sf: the byte of each 32-bit scale-factor column that
+// this MMA's K block (32 elements) uses.
+__host__ __device__ constexpr uint32_t idesc_mx_e2m1_e4m3(int M, int N, int a_sf, int b_sf) {
+  return ((uint32_t)b_sf << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24) | ((uint32_t)a_sf << 29);
+}
 __device__ __forceinline__ void alloc(uint32_t* slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
                "r"(ncols)
@@ -279,6 +289,29 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+// D[tmem] (+)= (A x 2^(sfa - 127)) . (B x 2^(sfb - 127))^T, one k32 step of
+// kind::mxf8f6f4: row m of A scaled by its factor in the TMEM scale columns at
+// sfa, row n of B by its factor at sfb (the bytes the instruction descriptor
+// selects).  Descriptors as low and high 32-bit words.
+__device__ __forceinline__ void mma_mx_words(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                             uint32_t b_hi, uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+      "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
+      "setp.ne.b32 p, %8, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], ad, bd, %5, [%6], [%7], p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Shared memory -> TMEM: 32 rows of 128 bits (the descriptor's source, no
+// swizzle) into lanes [0, 32) x 4 columns at taddr, repeated in each of the
+// four lane quarters.  Executes in order before tensor-core MMAs issued after
+// it by the same thread.
+__device__ __forceinline__ void cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread is complete.
 __device__ __forceinline__ void commit(uint64_t* bar) {

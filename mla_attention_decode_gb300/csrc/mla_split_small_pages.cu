@@ -8,6 +8,7 @@
 
 namespace mla {
 cudaError_t launch_stage1_small_pages(const Stage1Params& p, bool mx, cudaStream_t s) {
-  return mx ? launch_split_tc<true, 1, true>(p, s) : launch_split_tc<false, 1, true>(p, s);
+  return mx ? launch_split_tc<true, 1, tcfp8::kPathSmallPages>(p, s)
+            : launch_split_tc<false, 1, tcfp8::kPathSmallPages>(p, s);
 }
 }  // namespace mla

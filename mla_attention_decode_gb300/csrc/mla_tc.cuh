@@ -68,11 +68,18 @@ constexpr int kChunkBytes = kTileRows * 64;  // one 64-byte feature column block
 constexpr int kPairBytes = 2 * kChunkBytes;  // two column blocks = features [128 f, 128 f + 128)
 // kTok: query tokens one work unit serves (2: the fused two-token e4m3 form,
 // which holds a second query image and a second pair of P buffers in shared
-// memory at the cost of two ring slots).
-template <bool kMx, int kTok = 1>
+// memory at the cost of two ring slots).  kPath: which instance -- the
+// contiguous cache and pages of 64 rows or more (kPathRows), pages of fewer
+// rows (kPathSmallPages), or MXFP4 scores from block-scaled MMAs on the e2m1
+// tile itself (kPathBlockScaled; otherwise MXFP4 is converted to e4m3 from a
+// staging ring for both MMAs).
+constexpr int kPathRows = 0, kPathSmallPages = 1, kPathBlockScaled = 2;
+template <bool kMx, int kTok = 1, int kPath = kPathRows>
 struct Geo {
   static_assert(kTok == 1 || (kTok == 2 && !kMx), "two tokens per unit: e4m3 KV only");
-  static constexpr int pair_slots = kMx ? 8 : (kTok == 1 ? 11 : 9);  // ring of V column-block pairs (4 per tile)
+  static_assert(kPath != kPathBlockScaled || (kMx && kTok == 1), "block-scaled scores: MXFP4, one token");
+  static constexpr bool bs = kPath == kPathBlockScaled;
+  static constexpr int pair_slots = kMx ? (bs ? 10 : 8) : (kTok == 1 ? 11 : 9);  // ring of column-block pairs (4 per tile)
   // e4m3, one token per unit: a separate epilogue group (warps 8-11) drains
   // each unit's O^T from its own TMEM buffer, two buffers in turn, so that the
   // softmax warps and the next unit's P.V do not wait for the epilogue
@@ -89,6 +96,14 @@ constexpr int kHalfRows = 64;                        // MXFP4 staging unit: 64 p
 constexpr int kPackedRowBytes = 288;
 constexpr int kStageBytes = kHalfRows * kPackedRowBytes;  // 18 KB
 constexpr int kStageSlots = 3;
+// block-scaled MXFP4: the rope block's packed bytes (128 rows x 32 B) are staged
+// for the converters, which lay them out as the tensor core's 4-bit operand;
+// the tile's scale bytes go to shared memory as five 512-byte chunks of 4
+// K-blocks (the 32 x 128-bit source of one tcgen05.cp each: chunk word
+// (m mod 32) x 4 + m / 32 holds the scale bytes of row m)
+constexpr int kRopeStageBytes = kTileRows * 32;
+constexpr int kSfChunks = 5;
+constexpr int kSfTileBytes = kSfChunks * 512;
 // TMEM columns: the S^T double buffer [blk (t mod 2), +blk), then O^T, 4
 // feature blocks of blk columns; token i of a unit owns columns [32 i, +32) of
 // each buffer and block.  With a separate epilogue group (one token) there are
@@ -101,6 +116,11 @@ struct Tmem {
   static constexpr uint32_t o = 2 * blk;
   static constexpr uint32_t obuf = 4 * blk;
   static_assert(kTok == 2 || o + 2 * obuf <= cols, "two O^T buffers");
+  // block-scaled MXFP4 (one O^T buffer): the A scale factors of tile t at
+  // sfa + 32 (t mod 2), chunk g at +4 g (4 columns, replicated over the four
+  // lane quarters), the B scale factors (all 2^0) at sfb
+  static constexpr uint32_t sfa = 256;
+  static constexpr uint32_t sfb = 320;
 };
 #ifndef MLA_FIRST_TILE_WAIT
 #define MLA_FIRST_TILE_WAIT 0
@@ -113,13 +133,19 @@ constexpr uint32_t kIdescPV = tc::idesc_e4m3(128, 32, 1, 1);
 constexpr uint32_t kIdescQK2 = tc::idesc_e4m3(128, 64, 0, 0);
 constexpr uint32_t kIdescPV2 = tc::idesc_e4m3(128, 64, 1, 1);
 
-template <bool kMx, int kTok = 1>
+
+__host__ __device__ constexpr int round_up_1024(int v) { return (v + 1023) / 1024 * 1024; }
+template <bool kMx, int kTok = 1, int kPath = kPathRows>
 struct Layout {
-  static constexpr int kPairSlots = Geo<kMx, kTok>::pair_slots;
+  using G = Geo<kMx, kTok, kPath>;
+  static constexpr int kPairSlots = G::pair_slots;
   static constexpr int pairs = 0;                             // 1024-aligned
   static constexpr int rope = pairs + kPairSlots * kPairBytes;
-  static constexpr int stage = rope + kRopeSlots * kChunkBytes;      // MXFP4 only: packed rows
-  static constexpr int qs = stage + (kMx ? kStageSlots * kStageBytes : 0);
+  // MXFP4: packed rows (staging ring), or the rope blocks (block-scaled)
+  static constexpr int stage = rope + kRopeSlots * kChunkBytes;
+  static constexpr int sf = stage + (kMx ? (G::bs ? kRopeSlots * kRopeStageBytes : kStageSlots * kStageBytes) : 0);
+  static constexpr int sfb = sf + (G::bs ? 2 * kSfTileBytes : 0);  // block-scaled: [2 tiles] A chunks, then B
+  static constexpr int qs = round_up_1024(sfb + (G::bs ? 512 : 0));
   static constexpr int pb = qs + kQsBytes * kTok;             // [2 tiles][kTok]
   static constexpr int rq = pb + 2 * kPBytes * kTok;          // float [kTok][16] score factor per head
   static constexpr int red = rq + 16 * 4 * kTok;              // float [2][4 warps][16 kTok]
@@ -127,9 +153,10 @@ struct Layout {
   static constexpr int grow = gred + 2 * 4 * 4;               // int8 [2][128] row exponent G - 127 (MXFP4)
   static constexpr int lut = grow + (kMx ? 2 * 128 : 0);      // u8 [32][8] e2m1 magnitude -> e4m3 per shift
   static constexpr int hand = lut + (kMx ? 256 : 0);          // float [2][32] l, m handed to the epilogue group
-  static constexpr int units = hand + (Geo<kMx, kTok>::epi ? 256 : 0);
-  static constexpr int bars = units + Geo<kMx, kTok>::max_units * (int)sizeof(UnitDesc);
-  static constexpr int nbars = Geo<kMx, kTok>::epi ? 53 : 49;  // the last four serve the epilogue group
+  static constexpr int units = hand + (G::epi ? 256 : 0);
+  static constexpr int bars = units + G::max_units * (int)sizeof(UnitDesc);
+  // the epilogue group's four (e4m3, one token), then the two of block-scaled MXFP4
+  static constexpr int nbars = G::bs ? 55 : (G::epi ? 53 : 49);
   static constexpr int misc = bars + nbars * 8;  // tmem slot, abort flag, unit count
   static constexpr int total = misc + 16;
 };
@@ -157,7 +184,11 @@ enum {
   kOFree2 = 49,     // epilogue group: kOFree of the second O^T buffer
   kOLast2 = 50,     // epilogue group: kOLast of the second O^T buffer
   kEpiReady = 51,   // [2]  epilogue group: a unit's l and m handed over, per O^T buffer (1)
+  kConvQK = 53,     // [2]  block-scaled MXFP4: tile t's scale chunks, row exponents and rope block written (8 warps)
 };
+// block-scaled MXFP4 reuses the staging barriers for the rope block: kStageFull
+// + (t mod 2) counts its TMA bytes, kStageEmpty + (t mod 2) the 8 converter
+// warps that laid it out
 __device__ __forceinline__ int ofree_bar(int obuf) { return obuf ? kOFree2 : kOFree; }
 __device__ __forceinline__ int olast_bar(int obuf) { return obuf ? kOLast2 : kOLast; }
 
@@ -176,16 +207,17 @@ __device__ __forceinline__ int tiles_of(const UnitDesc& d) { return (d.end - d.s
 
 // ------------------------------------------------------------------ producer
 // Column blocks of tile t: pair f (features [128 f, 128 f + 128)) goes to pair
-// slot (4t + f) mod S (S = 11 for e4m3, 7 for MXFP4), the rope block to rope
+// slot (4t + f) mod S (S = 11 for e4m3, 9 with two tokens, 10 for block-scaled
+// MXFP4, 8 for MXFP4 converted from staging), the rope block to rope
 // slot t mod 2; each slot is re-filled as soon as the MMA that read it has
 // completed.
-template <bool kMx, int kTok = 1>
-__device__ __forceinline__ int pair_slot(int t, int f) { return (4 * t + f) % Geo<kMx, kTok>::pair_slots; }
-template <bool kMx, int kTok = 1>
-__device__ __forceinline__ int pair_use(int t, int f) { return (4 * t + f) / Geo<kMx, kTok>::pair_slots; }
-template <bool kMx, int kTok = 1>
+template <bool kMx, int kTok = 1, int kPath = kPathRows>
+__device__ __forceinline__ int pair_slot(int t, int f) { return (4 * t + f) % Geo<kMx, kTok, kPath>::pair_slots; }
+template <bool kMx, int kTok = 1, int kPath = kPathRows>
+__device__ __forceinline__ int pair_use(int t, int f) { return (4 * t + f) / Geo<kMx, kTok, kPath>::pair_slots; }
+template <bool kMx, int kTok = 1, int kPath = kPathRows>
 __device__ __forceinline__ int wrap_slot(int s) {
-  return s >= Geo<kMx, kTok>::pair_slots ? s - Geo<kMx, kTok>::pair_slots : s;
+  return s >= Geo<kMx, kTok, kPath>::pair_slots ? s - Geo<kMx, kTok, kPath>::pair_slots : s;
 }
 
 // The CTA's tiles in order (unit by unit): each tile's first row-space
@@ -430,10 +462,113 @@ struct HalfCursor {
   }
 };
 
-// ------------------------------------------------------- MXFP4 producer
-// Half tiles (64 packed rows, 18 KB) into a ring of 3 staging slots by 1-D bulk
-// copies (a half's rows are contiguous in the cache: a unit's rows, or one page
-// of at least 64 rows); one lane issues them.  The rows' scale bytes are prefetched
+// ------------------------------------------------------- MXFP4 producers
+// Block-scaled MXFP4 (contiguous caches, pages of 64 rows or more), one lane:
+// per tile, each 128-feature pair of e2m1 as one box of the 16U4_ALIGN16B map
+// (tmap_kv64: 16 elements = 8 packed bytes land in 16 bytes of shared memory,
+// the upper 8 zero, which is the tensor core's layout for a 4-bit operand;
+// the barrier counts the 8 packed bytes), into the pair ring as 128-byte rows
+// with the 128-byte swizzle; the rope block's 32 packed bytes a row as one box
+// of the byte map (tmap_kv16) into a staging slot, which the converter warps
+// lay out for the tensor core.  Pages of 64 rows: two 64-row boxes per tile.  The scale rows of the tile
+// three ahead are prefetched into L2 for the converter warps.
+static __device__ void producer_mx_bs(const Stage1Params& p, const Ctx& x) {
+  using L = Layout<true, 1, kPathBlockScaled>;
+  constexpr int kPairSlots = Geo<true, 1, kPathBlockScaled>::pair_slots;
+  const uint64_t pol = policy_evict_first();  // KV rows are read once
+  const bool paged64 = p.paged && p.page_shift == 6;
+  const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
+  const size_t ss = (size_t)p.scale_stride;
+  const int cache_rows = p.paged ? (p.num_pages << p.page_shift) : p.total_kv;
+  const size_t scale_end = ((size_t)cache_rows * ss) & ~(size_t)15;
+  // one bulk L2 prefetch per box: the 16-byte-aligned part of its scale rows
+  // that lies inside the tensor (the scale base is 16-byte aligned)
+  auto prefetch_scales = [&](int c0, int rows) {
+    if (c0 < 0 || rows <= 0) return;
+    const size_t lo = ((size_t)c0 * ss) & ~(size_t)15;
+    size_t hi = ((size_t)(c0 + rows) * ss + 15) & ~(size_t)15;
+    if (hi > scale_end) hi = scale_end;
+    if (hi > lo) bulk_prefetch_l2(sc + lo, (uint32_t)(hi - lo));
+  };
+  constexpr int kScaleAhead = 3;  // tiles
+  TileWalk pre;
+  auto prefetch_next = [&]() {
+    int t0, end;
+    if (!pre.next(x, t0, end)) return;
+    const TileRows r = tile_rows(p, t0, end);
+    if (!paged64) {
+      prefetch_scales(r.r0, min(kTileRows, cache_rows - r.r0));
+    } else {
+      prefetch_scales(r.r0, 64);
+      if (r.r1 >= 0) prefetch_scales(r.r1, 64);
+    }
+  };
+  for (int i = 0; i < kScaleAhead; ++i) prefetch_next();
+  int armed[kPairSlots + kRopeSlots];
+  for (int i = 0; i < kPairSlots + kRopeSlots; ++i) armed[i] = 0;
+  // the rope block of tile t + 2 is requested before the pairs of tile t: its
+  // staging slot was laid out by the converters' step 1 for tile t, which
+  // needs nothing requested later than tile t - 2, while the pairs of tile t
+  // wait for the P.V of tiles t - 2 and t - 3
+  TileWalk rope_walk;
+  int rope_it = 0;
+  auto request_rope = [&]() {
+    int t0, end;
+    if (!rope_walk.next(x, t0, end)) return;
+    const TileRows rows = tile_rows(p, t0, end);
+    const int rs = rope_it % kRopeSlots, ruse = rope_it / kRopeSlots;
+    ++rope_it;
+    if (ruse >= 1) wait_phase(&x.bar[kStageEmpty + rs], (ruse - 1) & 1, x.abort_flag, p.ws_err);
+    if (*x.abort_flag) return;
+    const uint32_t box_rows = (paged64 && rows.r1 < 0) ? 64u : 128u;
+    uint8_t* dst = x.smem + L::stage + rs * kRopeStageBytes;
+    mbar_arrive_expect_tx(&x.bar[kStageFull + rs], box_rows * 32);
+    tma_load_2d(dst, &p.tmap_kv16, 256, rows.r0, &x.bar[kStageFull + rs], pol);
+    if (paged64 && rows.r1 >= 0) tma_load_2d(dst + 64 * 32, &p.tmap_kv16, 256, rows.r1, &x.bar[kStageFull + rs], pol);
+    ++armed[kPairSlots + rs];
+  };
+  request_rope();
+  request_rope();
+  TileWalk walk;
+  int nt0 = 0, nend = 0;
+  bool have = walk.next(x, nt0, nend);
+  TileRows nrows = have ? tile_rows(p, nt0, nend) : TileRows{0, -1};
+  for (int it = 0; have && !*x.abort_flag; ++it) {
+    const TileRows rows = nrows;
+    have = walk.next(x, nt0, nend);
+    if (have) nrows = tile_rows(p, nt0, nend);
+    prefetch_next();
+    request_rope();
+    if (*x.abort_flag) break;
+    const uint32_t box_rows = (paged64 && rows.r1 < 0) ? 64u : 128u;  // rows the copies bring
+    for (int f = 0; f < 4; ++f) {
+      const int sl = pair_slot<true, 1, kPathBlockScaled>(it, f), use = pair_use<true, 1, kPathBlockScaled>(it, f);
+      if (use >= 1) wait_phase(&x.bar[kPairEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
+      if (*x.abort_flag) break;
+      uint8_t* dst = x.smem + L::pairs + sl * kPairBytes;
+      mbar_arrive_expect_tx(&x.bar[kPairFull + sl], box_rows * 64);
+      tma_load_3d(dst, &p.tmap_kv64, 0, f, rows.r0, &x.bar[kPairFull + sl], pol);
+      if (paged64 && rows.r1 >= 0) tma_load_3d(dst + 64 * 128, &p.tmap_kv64, 0, f, rows.r1, &x.bar[kPairFull + sl], pol);
+      ++armed[sl];
+      if (it == 0 && f == 0) trace_stamp(p, kTrFirstLoad);
+    }
+  }
+  if (*x.abort_flag) {
+    // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
+    for (int i = 0; i < kPairSlots + kRopeSlots; ++i) {
+      if (armed[i] == 0) continue;
+      uint64_t* bar = i < kPairSlots ? &x.bar[kPairFull + i] : &x.bar[kStageFull + i - kPairSlots];
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(bar, (armed[i] - 1) & 1) && global_timer_ns() - t0 < kWaitTimeoutNs) {
+      }
+    }
+  }
+}
+
+// Converted MXFP4, contiguous caches and pages of 64 rows or more: half tiles
+// (64 packed rows, 18 KB) into a ring of 3 staging slots by 1-D bulk copies (a
+// half's rows are contiguous in the cache: a unit's rows, or one page of at
+// least 64 rows); one lane issues them.  The rows' scale bytes are prefetched
 // into L2 for the converter warps.  A half with no rows (the second half of a
 // short tile) is signalled by a plain arrival.
 static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
@@ -500,13 +635,14 @@ static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
   }
 }
 
-// Pages of fewer than 64 rows: a half's rows lie in 64 / P pages, so the 32
-// lanes copy one page's rows each (two pages per lane for P = 1), through
-// their own page-table lookups, once lane 0 has waited for the staging slot
-// and armed its barrier.  No scale prefetch: the converters look up their rows'
-// scales themselves.
+// Converted MXFP4, pages of fewer than 64 rows: half tiles as above.  A half's rows
+// lie in 64 / P pages, so the 32 lanes copy one page's rows each (two pages per
+// lane for P = 1), through their own page-table lookups, once lane 0 has
+// waited for the staging slot and armed its barrier; a half with no rows (the
+// second half of a short tile) is signalled by a plain arrival.  No scale
+// prefetch: the converters look up their rows' scales themselves.
 static __device__ void producer_mx_rows(const Stage1Params& p, const Ctx& x, int lane) {
-  using L = Layout<true>;
+  using L = Layout<true, 1, kPathSmallPages>;
   const uint64_t pol = policy_evict_first();  // KV rows are read once
   int uses[kStageSlots] = {0, 0, 0};
   HalfCursor cur;
@@ -578,7 +714,7 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lut_lo, uin
   return make_uint2(m0 | ((s0 << 1) & 0x80808080u), m1 | ((s1 << 1) & 0x80808080u));
 }
 
-// Converter warp cw (0..7) converts half cw / 4 of every tile (tile rows
+// Converted MXFP4: converter warp cw (0..7) converts half cw / 4 of every tile (tile rows
 // [64 (cw / 4), +64)): rows [16 (cw % 4), +16) of that half.  Lane pair
 // (2i, 2i+1) shares row 16 (cw % 4) + i, lane 2i + hp taking the row's blocks
 // 2j + hp (j = 0..8).  Block 2j + hp holds features [64 j + 32 hp, +32),
@@ -587,7 +723,7 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lut_lo, uin
 // per half tile): the conversion is bound by each sub-partition's integer
 // pipe, and a second warp keeps it busy while the first waits.
 template <bool kSmallPages>
-__device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw, int lane) {
+static __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw, int lane) {
   using L = Layout<true>;
   const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
   const size_t ss = (size_t)p.scale_stride;
@@ -670,6 +806,121 @@ __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw, int la
   }
 }
 
+// Block-scaled MXFP4: converter warp cw (0..7) serves tile rows [16 cw, +16);
+// lane 2i + hp takes row 16 cw + i and, of each of the row's 16 V blocks kb
+// (32 features), the 16 features [32 kb + 16 hp, +16).  Per tile t:
+//  1. for tile t + 1, first (so that its QK can overlap the conversion of
+//     tile t): the row's scale bytes into that tile's five chunks, its row
+//     exponent G - 127 (G: the largest scale byte of its 16 V blocks) and its
+//     rope bytes laid out as the 4-bit operand (8 packed bytes, then 8 zero
+//     bytes, per 16 elements) in the rope slot; then kConvQK;
+//  2. once the QK of tile t is complete (its e2m1 bytes have been read), each
+//     16-element group of the row's V blocks is rewritten in place as 16 e4m3
+//     bytes n * 2^(e-G) (element n of a block with scale byte e; exact while
+//     e is within 8 of G, smaller ones rounding to e4m3's subnormal grid) for
+//     the P.V; then kConvFull.
+// The scale chunks, rope slot and row exponents of tile t + 1 are those of
+// tile t - 1: its QK completed before its conversion, and its softmax had
+// read the row exponents (kSEmpty).  A row past the unit's end takes scale
+// bytes 127 and the all-zero conversion table.
+__device__ __forceinline__ uint32_t bs_scale_word(const uint32_t (&e)[9], int g) {
+  return g < 4 ? (e[2 * g] | (e[2 * g + 1] << 16)) : (e[8] | 0x7f7f0000u);
+}
+static __device__ void converter_mx_bs(const Stage1Params& p, const Ctx& x, int cw, int lane) {
+  using L = Layout<true, 1, kPathBlockScaled>;
+  const uint8_t* sc = static_cast<const uint8_t*>(p.kv_scale);
+  const size_t ss = (size_t)p.scale_stride;
+  const uint32_t lut0 = smem_u32(x.smem + L::lut), pairs0 = smem_u32(x.smem + L::pairs);
+  const uint32_t rope0 = smem_u32(x.smem + L::rope), stage0 = smem_u32(x.smem + L::stage);
+  int8_t* grow = reinterpret_cast<int8_t*>(x.smem + L::grow);
+  const int row = 16 * cw + (lane >> 1), hp = lane & 1;
+  // the scale bytes of the row, two tiles ahead of the conversion
+  TileWalk wl;
+  auto next_scales = [&](uint32_t (&e)[9], bool& v) -> bool {
+    int t0, end;
+    if (!wl.next(x, t0, end)) return false;
+    v = t0 + row < end;
+    load_row_scales(sc, ss, v ? cache_row(p, t0 + row) : 0, v, e);
+    return true;
+  };
+  // step 1 for tile t (scale bytes e, row valid v): returns G
+  auto prepare = [&](int t, const uint32_t (&e)[9], bool v) -> uint32_t {
+    const int sb = t & 1;
+    uint32_t g = 1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g = max(g, max(e[i] & 0xffu, e[i] >> 8));
+    // the softmax of tile t - 2 has read its row exponents
+    if (t >= 2) wait_phase(&x.bar[kSEmpty + sb], ((t >> 1) - 1) & 1, x.abort_flag, p.ws_err);
+    if (hp == 0) grow[sb * 128 + row] = (int8_t)(v ? (int)min(g, 254u) - 127 : 0);
+    uint8_t* chunk = x.smem + L::sf + sb * kSfTileBytes + (row & 31) * 16 + (row >> 5) * 4;
+    if (hp == 0) {
+#pragma unroll
+      for (int c = 0; c < 3; ++c) *reinterpret_cast<uint32_t*>(chunk + 512 * c) = bs_scale_word(e, c);
+    } else {
+#pragma unroll
+      for (int c = 3; c < kSfChunks; ++c) *reinterpret_cast<uint32_t*>(chunk + 512 * c) = bs_scale_word(e, c);
+    }
+    // the rope block: 16 packed bytes (32 elements) of the row per lane
+    wait_phase(&x.bar[kStageFull + sb], (t >> 1) & 1, x.abort_flag, p.ws_err);
+    const uint4 w = lds128(stage0 + sb * kRopeStageBytes + row * 32 + 16 * hp);
+    const uint32_t rb = rope0 + sb * kChunkBytes;
+    sts128(rb + sw64_off(row, 32 * hp), w.x, w.y, 0u, 0u);
+    sts128(rb + sw64_off(row, 32 * hp + 16), w.z, w.w, 0u, 0u);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&x.bar[kStageEmpty + sb]);
+    tc::fence_proxy_async();  // the tensor core reads the chunks and the rope slot through the async proxy
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&x.bar[kConvQK + sb]);
+    return g;
+  };
+  uint32_t ec[9], en[9];
+  bool vc = false, vn = false;
+  bool hc = next_scales(ec, vc);
+  uint32_t gc = hc ? prepare(0, ec, vc) : 1u;
+  bool hn = next_scales(en, vn);
+  for (int it = 0; hc && !*x.abort_flag; ++it) {
+    uint32_t e2[9];
+    bool v2 = false;
+    const bool h2 = hn && next_scales(e2, v2);
+    const uint32_t gn = hn ? prepare(it + 1, en, vn) : 1u;
+    // step 2 for tile it
+    const int sb = it & 1;
+    wait_phase(&x.bar[kSFull + sb], (it >> 1) & 1, x.abort_flag, p.ws_err);
+    uint32_t base[4];
+#pragma unroll
+    for (int f = 0; f < 4; ++f) {
+      const int sl = pair_slot<true, 1, kPathBlockScaled>(it, f);
+      wait_phase(&x.bar[kPairFull + sl], pair_use<true, 1, kPathBlockScaled>(it, f) & 1, x.abort_flag, p.ws_err);
+      base[f] = pairs0 + (uint32_t)sl * kPairBytes + row * 128;
+    }
+    if (*x.abort_flag) break;
+    const uint32_t lutv = lut0 + (vc ? 0u : 128u);
+#pragma unroll
+    for (int kb = 0; kb < 16; ++kb) {
+      const int u = 2 * (kb & 3) + hp;  // 16-element group of the 128-byte row
+      const uint32_t a = base[kb >> 2] + ((u ^ (row & 7)) << 4);
+      const uint2 w = lds64(a);
+      const uint32_t eb = (ec[kb >> 1] >> (8 * (kb & 1))) & 0xffu;
+      const uint2 lt = lds64(lutv + 8 * min(gc - eb, 15u));
+      const uint2 lo = e2m1x8_to_e4m3(w.x, lt.x, lt.y), hi = e2m1x8_to_e4m3(w.y, lt.x, lt.y);
+      sts128(a, lo.x, lo.y, hi.x, hi.y);
+    }
+    tc::fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&x.bar[kConvFull + sb]);
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      ec[i] = en[i];
+      en[i] = e2[i];
+    }
+    vc = vn;
+    vn = v2;
+    gc = gn;
+    hc = hn;
+    hn = h2;
+  }
+}
+
 // ---------------------------------------------------------- query loader
 // One thread: the query of unit k, prepared by mla_prep_q_kernel as the exact
 // shared-memory image (two-term e4m3, 64-byte swizzle) plus its 16 score
@@ -678,9 +929,9 @@ __device__ void converter_mx(const Stage1Params& p, const Ctx& x, int cw, int la
 // two-token unit of sequence b: the prepared output row 2 b + i).  The
 // prepared queries are the one input written by the preceding grid, so this
 // is the one thread that waits for it.
-template <bool kMx, int kTok>
+template <bool kMx, int kTok, int kPath>
 __device__ void q_loader(const Stage1Params& p, const Ctx& x) {
-  using L = Layout<kMx, kTok>;
+  using L = Layout<kMx, kTok, kPath>;
   const uint64_t pol = policy_evict_last();  // a query serves every split of its sequence
   pdl_wait_primary();
   trace_stamp(p, kTrQueryReady);
@@ -740,13 +991,15 @@ __host__ __device__ constexpr uint32_t hi_word(uint64_t d) { return (uint32_t)(d
 
 // QK of every tile: S^T(t) into TMEM columns [blk (t mod 2), +blk), token i's
 // scores at +32 i (two tokens: one N = 64 MMA per k step over both query images).
-template <bool kMx, int kTok, bool kSmallPages>
+template <bool kMx, int kTok, int kPath>
 __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
-  using L = Layout<kMx, kTok>;
-  constexpr bool kR128 = kSmallPages && !kMx;  // pair slots of 128-byte rows
+  constexpr bool kSmallPages = kPath == kPathSmallPages;
+  using L = Layout<kMx, kTok, kPath>;
+  constexpr bool kBs = Geo<kMx, kTok, kPath>::bs;  // block-scaled e2m1 scores
+  constexpr bool kR128 = (kSmallPages && !kMx) || kBs;    // pair slots of 128-byte rows
   constexpr uint64_t kTplA = kR128 ? kTplK128 : kTplK64;
   using TM = Tmem<kTok>;
-  constexpr int kPairSlots = Geo<kMx, kTok>::pair_slots;
+  constexpr int kPairSlots = Geo<kMx, kTok, kPath>::pair_slots;
   const uint32_t pairs0 = smem_u32(x.smem + L::pairs), rope0 = smem_u32(x.smem + L::rope);
   const uint32_t bq = lo_word(kTplK64) + (smem_u32(x.smem + L::qs) >> 4);
   int it = 0;
@@ -755,17 +1008,20 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
     wait_phase(&x.bar[kQFull], k & 1, x.abort_flag, p.ws_err);
     for (int t = 0; t < nt; ++t, ++it) {
       const int s0 = (4 * it) % kPairSlots, use0 = (4 * it) / kPairSlots;
-      if constexpr (kMx) {
+      if constexpr (kMx && !kBs) {
         // the converter warps filled all of the tile's slots
         wait_phase(&x.bar[kConvFull + (it & 1)], (it >> 1) & 1, x.abort_flag, p.ws_err);
       } else {
 #pragma unroll
         for (int f = 0; f < 4; ++f) {
           const int sl = s0 + f;
-          wait_phase(&x.bar[kPairFull + wrap_slot<kMx, kTok>(sl)], (use0 + (sl >= kPairSlots)) & 1, x.abort_flag,
-                     p.ws_err);
+          wait_phase(&x.bar[kPairFull + wrap_slot<kMx, kTok, kPath>(sl)], (use0 + (sl >= kPairSlots)) & 1,
+                     x.abort_flag, p.ws_err);
         }
-        wait_phase(&x.bar[kRopeFull + it % kRopeSlots], (it / kRopeSlots) & 1, x.abort_flag, p.ws_err);
+        if constexpr (kBs)  // the tile's scale chunks and rope block are laid out
+          wait_phase(&x.bar[kConvQK + (it & 1)], (it >> 1) & 1, x.abort_flag, p.ws_err);
+        else
+          wait_phase(&x.bar[kRopeFull + it % kRopeSlots], (it / kRopeSlots) & 1, x.abort_flag, p.ws_err);
       }
       if (it >= 2) wait_phase(&x.bar[kSEmpty + (it & 1)], ((it >> 1) - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
@@ -774,21 +1030,43 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
       uint32_t ap[4];
 #pragma unroll
       for (int f = 0; f < 4; ++f)
-        ap[f] = lo_word(kTplA) + ((pairs0 + (uint32_t)wrap_slot<kMx, kTok>(s0 + f) * kPairBytes) >> 4);
+        ap[f] = lo_word(kTplA) + ((pairs0 + (uint32_t)wrap_slot<kMx, kTok, kPath>(s0 + f) * kPairBytes) >> 4);
       const uint32_t ar = lo_word(kTplK64) + ((rope0 + (uint32_t)(it % kRopeSlots) * kChunkBytes) >> 4);
       const uint32_t d = x.tmem + TM::s + TM::blk * (it & 1);
+      if constexpr (kBs) {
+        // scale factors into TMEM (executed before the MMAs that follow):
+        // the B factors (all 2^0) once, the tile's A chunks per tile
+        const uint32_t sfa = x.tmem + TM::sfa + 32 * (it & 1), sfb = x.tmem + TM::sfb;
+        if (it == 0) tc::cp_32x128b_warpx4(sfb, tc::smem_desc(smem_u32(x.smem + L::sfb), 128, 128, 0));
+        const uint32_t chunks = smem_u32(x.smem + L::sf + (it & 1) * kSfTileBytes);
 #pragma unroll
-      for (int ks = 0; ks < 18; ++ks) {
-        const int c = ks >> 1, half = ks & 1;
-        constexpr int kBlockStride = kR128 ? 64 : kChunkBytes;  // column block 2 f + 1 within pair f
-        const uint32_t a =
-            c < 8 ? ap[c >> 1] + (((c & 1) * kBlockStride + 32 * half) >> 4) : ar + ((32 * half) >> 4);
-        // both tokens' query rows form one B operand (block c: 32 kTok rows of 64 B)
-        tc::mma_f8_words(d, a, c < 8 ? hi_word(kTplA) : hi_word(kTplK64), bq + ((c * 2048 * kTok + 32 * half) >> 4),
-                         hi_word(kTplK64), kTok == 1 ? kIdescQK : kIdescQK2, ks > 0 ? 1u : 0u);
+        for (int g = 0; g < kSfChunks; ++g)
+          tc::cp_32x128b_warpx4(sfa + 4 * g, tc::smem_desc(chunks + 512 * g, 128, 128, 0));
+        // 18 k32 steps, K-block kb's scales in byte kb mod 4 of chunk kb / 4:
+        // the pairs' e2m1 (128-byte rows), then the rope block (64-byte rows)
+#pragma unroll
+        for (int kb = 0; kb < 18; ++kb) {
+          const uint32_t a = kb < 16 ? ap[kb >> 2] + ((32 * (kb & 3)) >> 4) : ar + ((32 * (kb - 16)) >> 4);
+          tc::mma_mx_words(d, a, kb < 16 ? hi_word(kTplK128) : hi_word(kTplK64),
+                           bq + (((kb >> 1) * 2048 + 32 * (kb & 1)) >> 4), hi_word(kTplK64),
+                           tc::idesc_mx_e2m1_e4m3(128, 32, kb & 3, 0), sfa + 4 * (kb >> 2), sfb, kb > 0 ? 1u : 0u);
+        }
+        tc::commit(&x.bar[kSFull + (it & 1)]);
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < 18; ++ks) {
+          const int c = ks >> 1, half = ks & 1;
+          constexpr int kBlockStride = kR128 ? 64 : kChunkBytes;  // column block 2 f + 1 within pair f
+          const uint32_t a =
+              c < 8 ? ap[c >> 1] + (((c & 1) * kBlockStride + 32 * half) >> 4) : ar + ((32 * half) >> 4);
+          // both tokens' query rows form one B operand (block c: 32 kTok rows of 64 B)
+          tc::mma_f8_words(d, a, c < 8 ? hi_word(kTplA) : hi_word(kTplK64),
+                           bq + ((c * 2048 * kTok + 32 * half) >> 4), hi_word(kTplK64),
+                           kTok == 1 ? kIdescQK : kIdescQK2, ks > 0 ? 1u : 0u);
+        }
+        tc::commit(&x.bar[kSFull + (it & 1)]);
+        tc::commit(&x.bar[kRopeEmpty + it % kRopeSlots]);
       }
-      tc::commit(&x.bar[kSFull + (it & 1)]);
-      tc::commit(&x.bar[kRopeEmpty + it % kRopeSlots]);
     }
     tc::commit(&x.bar[kQEmpty]);  // the query buffer may be refilled
   }
@@ -797,16 +1075,18 @@ __device__ void qk_issuer(const Stage1Params& p, const Ctx& x) {
 // P.V of every tile: O^T += V^T(t) . P^T(t) (token i: its own P buffer and O^T
 // columns, both in one N = 64 MMA); releases the tile's ring slots, its P
 // buffers and, on a unit's last tile, the unit's O^T.
-template <bool kMx, int kTok, bool kSmallPages>
+template <bool kMx, int kTok, int kPath>
 __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
-  using L = Layout<kMx, kTok>;
-  constexpr bool kR128 = kSmallPages && !kMx;  // pair slots of 128-byte rows
+  constexpr bool kSmallPages = kPath == kPathSmallPages;
+  using L = Layout<kMx, kTok, kPath>;
+  constexpr bool kBs = Geo<kMx, kTok, kPath>::bs;  // block-scaled e2m1 scores, V converted in place
+  constexpr bool kR128 = (kSmallPages && !kMx) || kBs;    // pair slots of 128-byte rows
   constexpr uint64_t kTplA = kR128 ? kTplV128 : kTplV;
   constexpr uint32_t kRows32 = kR128 ? 4 * 1024 : 2048;  // bytes of 32 rows of V^T in a slot
   using TM = Tmem<kTok>;
-  constexpr int kPairSlots = Geo<kMx, kTok>::pair_slots;
+  constexpr int kPairSlots = Geo<kMx, kTok, kPath>::pair_slots;
   const uint32_t pairs0 = smem_u32(x.smem + L::pairs), pb0 = smem_u32(x.smem + L::pb);
-  constexpr bool kEpi = Geo<kMx, kTok>::epi;
+  constexpr bool kEpi = Geo<kMx, kTok, kPath>::epi;
   int it = 0, ordinal = 0;
   for (int k = 0; k < x.nunits && !*x.abort_flag; ++k) {
     const int nt = tiles_of(x.units[k]);
@@ -816,6 +1096,8 @@ __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
     const uint32_t od = x.tmem + TM::o + obuf * TM::obuf;
     for (int t = 0; t < nt; ++t, ++it) {
       wait_phase(&x.bar[kPFull + (it & 1)], (it >> 1) & 1, x.abort_flag, p.ws_err);
+      // block-scaled MXFP4: the converter warps have rewritten the tile's V as e4m3
+      if (kBs) wait_phase(&x.bar[kConvFull + (it & 1)], (it >> 1) & 1, x.abort_flag, p.ws_err);
       // a unit's first P.V overwrites O^T: the epilogue of the buffer's previous unit must have read it
       if (t == 0 && use > 0) wait_phase(&x.bar[ofree_bar(obuf)], (use - 1) & 1, x.abort_flag, p.ws_err);
       if (*x.abort_flag) break;
@@ -825,7 +1107,8 @@ __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
       const int s0 = (4 * it) % kPairSlots;
 #pragma unroll
       for (int fb = 0; fb < 4; ++fb) {
-        const int sl = wrap_slot<kMx, kTok>(s0 + fb);
+        const int sl = wrap_slot<kMx, kTok, kPath>(s0 + fb);
+
         // V^T block: features [128 fb, 128 fb + 128) = the slot's two column blocks (LBO)
         const uint32_t av = lo_word(kTplA) + ((pairs0 + (uint32_t)sl * kPairBytes) >> 4);
 #pragma unroll
@@ -972,10 +1255,12 @@ __device__ __forceinline__ float exp2_int(int e) { return __int_as_float((e + 12
 // in TMEM columns [32 ti, +32) of the S^T buffers and O^T blocks.  With two
 // tokens, token 0 does not see the last row of its sequence (token 1's own
 // entry), and token ti's partial slot is u + ti S_b.
-template <bool kMx, int kTok, bool kSmallPages>
+template <bool kMx, int kTok, int kPath>
 __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, int lane, int ti) {
-  constexpr bool kR128 = kSmallPages && !kMx;  // pair slots of 128-byte rows
-  using L = Layout<kMx, kTok>;
+  constexpr bool kSmallPages = kPath == kPathSmallPages;
+  constexpr bool kR128 = kSmallPages && !kMx;  // e4m3 pair slots of 128-byte rows
+  constexpr bool kBs = Geo<kMx, kTok, kPath>::bs;  // block-scaled e2m1 scores
+  using L = Layout<kMx, kTok, kPath>;
   using TM = Tmem<kTok>;
   constexpr int kGvNone = -1000;   // no MXFP4 reference yet
   const int row = 32 * ww + lane;  // tile row == TMEM lane of this thread
@@ -986,7 +1271,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
   int* gred = reinterpret_cast<int*>(x.smem + L::gred);
   const float* rq = reinterpret_cast<const float*>(x.smem + L::rq) + 16 * ti;
   float* redbuf = reinterpret_cast<float*>(x.smem + L::red) + 128 * ti;
-  constexpr bool kEpi = Geo<kMx, kTok>::epi;
+  constexpr bool kEpi = Geo<kMx, kTok, kPath>::epi;
   int it = 0, red_par = 0, ordinal = 0;
   for (int k = 0; k < x.nunits; ++k) {
     const UnitDesc d = x.units[k];
@@ -1040,14 +1325,18 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       uint32_t acc[32];
       tc::ld32(tl + TM::s + TM::blk * sb, acc);
       tc::wait_ld();
+      // MXFP4: the row's exponent G - 127, written by the converter warps before
+      // they released the tile (waited for here too, so that the bytes are
+      // visible); block-scaled: read before kSEmpty, which lets them reuse it
+      if (kBs) wait_phase(&x.bar[kConvQK + sb], (it >> 1) & 1, x.abort_flag, p.ws_err);
+      const int gsh_bs = kBs ? max(-126, (int)grow[sb * 128 + row]) : 0;
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&x.bar[kSEmpty + sb]);
-      // MXFP4: the row's exponent G - 127, written by the converter warps before
-      // they released the tile (waited for here too, so that the bytes are visible)
-      if (kMx) wait_phase(&x.bar[kConvFull + sb], (it >> 1) & 1, x.abort_flag, p.ws_err);
-      const int gsh = kMx ? max(-126, (int)grow[sb * 128 + row]) : 0;
-      const float row_fac = kMx ? exp2_int(gsh) : 1.f;
+      if (kMx && !kBs) wait_phase(&x.bar[kConvFull + sb], (it >> 1) & 1, x.abort_flag, p.ws_err);
+      const int gsh = kBs ? gsh_bs : (kMx ? max(-126, (int)grow[sb * 128 + row]) : 0);
+      // the scores of block-scaled MMAs carry no row factor
+      const float row_fac = (kMx && !kBs) ? exp2_int(gsh) : 1.f;
       float sv[16];
       uint32_t need = 0;  // heads with a score above m_ref + 8 in this row (bit 16: G above gv)
 #pragma unroll
@@ -1150,12 +1439,11 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       if (!kMx && ti == 0 && row >= valid) {
         // rows past the unit's end hold other rows' data: zero their V part so
         // that P = 0 cannot meet a non-finite value (the MXFP4 converters write zeros)
-#pragma unroll
         if constexpr (kR128) {
           // the row's 128 bytes in each pair slot (all eight 16-byte units, whatever the swizzle)
 #pragma unroll
           for (int f = 0; f < 4; ++f) {
-            uint8_t* rb = x.smem + L::pairs + pair_slot<kMx, kTok>(it, f) * kPairBytes + row * 128;
+            uint8_t* rb = x.smem + L::pairs + pair_slot<kMx, kTok, kPath>(it, f) * kPairBytes + row * 128;
 #pragma unroll
             for (int uu = 0; uu < 8; ++uu) *reinterpret_cast<uint4*>(rb + 16 * uu) = make_uint4(0, 0, 0, 0);
           }
@@ -1163,7 +1451,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint8_t* blk =
-                x.smem + L::pairs + pair_slot<kMx, kTok>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes;
+                x.smem + L::pairs + pair_slot<kMx, kTok, kPath>(it, c >> 1) * kPairBytes + (c & 1) * kChunkBytes;
 #pragma unroll
             for (int uu = 0; uu < 4; ++uu)
               *reinterpret_cast<uint4*>(blk + sw64_off(row, 16 * uu)) = make_uint4(0, 0, 0, 0);
@@ -1210,13 +1498,16 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
   if (row == 0 && ti == 0) trace_value(p, kTrTiles, (uint64_t)it);
 }
 
-// kSmallPages: the instance for paged caches with pages of fewer than 64 rows
-// (one token per unit), whose producer warp fetches rows page by page.  It is a
-// separate instance so that the others carry none of its code.
-template <bool kMx, int kTok, bool kSmallPages>
-__global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
+// kPath: the instance -- kPathSmallPages for paged caches with pages of fewer
+// than 64 rows (one token per unit), whose producer warp fetches rows page by
+// page; kPathBlockScaled for MXFP4 scores from block-scaled MMAs.  Separate
+// instances, so that the others carry none of their code.
+template <bool kMx, int kTok, int kPath>
+__global__ void __launch_bounds__(Geo<kMx, kTok, kPath>::threads, 1)
     mla_split_tc_kernel(const __grid_constant__ Stage1Params p) {
-  using L = Layout<kMx, kTok>;
+  constexpr bool kSmallPages = kPath == kPathSmallPages;
+  using L = Layout<kMx, kTok, kPath>;
+  constexpr bool kBs = Geo<kMx, kTok, kPath>::bs;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Ctx x;
@@ -1240,10 +1531,12 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
     counts[kSEmpty] = counts[kSEmpty + 1] = 4 * kTok;  // every softmax warp
     counts[kPFull] = counts[kPFull + 1] = 4 * kTok;
     counts[kOFree] = 4 * kTok;
-    if constexpr (Geo<kMx, kTok>::epi) counts[kOFree2] = 4 * kTok;
+    if constexpr (Geo<kMx, kTok, kPath>::epi) counts[kOFree2] = 4 * kTok;
     counts[kRFree] = 4 * kTok;
-    for (int i = 0; i < kStageSlots; ++i) counts[kStageEmpty + i] = 4;
+    // staging halves: the 4 converter warps of a half; rope blocks (block-scaled): all 8
+    for (int i = 0; i < kStageSlots; ++i) counts[kStageEmpty + i] = kBs ? 8 : 4;
     counts[kConvFull] = counts[kConvFull + 1] = 8;
+    if constexpr (kBs) counts[kConvQK] = counts[kConvQK + 1] = 8;
     for (int i = 0; i < L::nbars; ++i) mbar_init(&x.bar[i], counts[i]);
     *x.abort_flag = 0;
     fence_mbar_init();
@@ -1272,7 +1565,7 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
     // no grid-dependency wait here: this kernel is launched only once the
     // query-preparation grid has itself waited for all earlier work, so every
     // input but the prepared queries is complete (the query loader waits for those)
-    scan_units<kTileRows, Geo<kMx, kTok>::max_units, kTok>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits,
+    scan_units<kTileRows, Geo<kMx, kTok, kPath>::max_units, kTok>(p, reinterpret_cast<UnitDesc*>(smem + L::units), s_nunits,
                                                      lane);
     if (lane == 0) trace_stamp(p, kTrScanDone);
     if (lane == 0 && !kMx) prefetch_tensormap(&p.tmap_kv64);
@@ -1283,6 +1576,11 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
     const int i = threadIdx.x - 128, shift = i >> 3, m = i & 7;
     const float mag = m < 4 ? 0.5f * (float)m : (float)(2 << ((m - 4) >> 1)) * ((m & 1) ? 1.5f : 1.f);
     smem[L::lut + i] = shift < 16 ? (uint8_t)(f32x2_to_e4m3x2(ldexpf(mag, -shift), 0.f) & 0xffu) : (uint8_t)0;
+  }
+  if (kBs && threadIdx.x >= 384) {
+    // the query's scale factors, all 2^0 (e8m0 127): one 512-byte chunk
+    reinterpret_cast<uint32_t*>(smem + L::sfb)[threadIdx.x - 384] = 0x7f7f7f7fu;
+    tc::fence_proxy_async();  // read by tcgen05.cp (async proxy)
   }
   if (warp == 1) {
     tc::alloc(tmem_slot, Tmem<kTok>::cols);
@@ -1310,25 +1608,29 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
       else
         producer_e4m3_gather<kTok>(p, x, lane);
     } else if (lane == 0) {
-      if constexpr (kMx)
+      if constexpr (kBs)
+        producer_mx_bs(p, x);
+      else if constexpr (kMx)
         producer_mx(p, x);
       else
         producer_e4m3<kTok>(p, x);
     }
   } else if (warp == 1) {
-    if (lane == 0) qk_issuer<kMx, kTok, kSmallPages>(p, x);
+    if (lane == 0) qk_issuer<kMx, kTok, kPath>(p, x);
   } else if (warp == 2) {
-    if (lane == 0) pv_issuer<kMx, kTok, kSmallPages>(p, x);
+    if (lane == 0) pv_issuer<kMx, kTok, kPath>(p, x);
   } else if (warp == 3) {
-    if (lane == 0) q_loader<kMx, kTok>(p, x);
+    if (lane == 0) q_loader<kMx, kTok, kPath>(p, x);
   } else if (warp < 4 + 4 * (kMx ? 1 : kTok)) {
     // softmax group (warp - 4) / 4: one per query token of the unit (one call
     // site, so that both groups run the same code)
-    softmax_epilogue<kMx, kTok, kSmallPages>(p, x, warp & 3, lane, kTok == 1 ? 0 : (warp - 4) >> 2);
+    softmax_epilogue<kMx, kTok, kPath>(p, x, warp & 3, lane, kTok == 1 ? 0 : (warp - 4) >> 2);
   } else {
-    if constexpr (kMx)
+    if constexpr (kBs)
+      converter_mx_bs(p, x, warp - 8, lane);
+    else if constexpr (kMx)
       converter_mx<kSmallPages>(p, x, warp - 8, lane);
-    else if constexpr (Geo<kMx, kTok>::epi)
+    else if constexpr (Geo<kMx, kTok, kPath>::epi)
       epilogue_group<kMx, kTok>(p, x, warp & 3, lane);
   }
 
@@ -1349,17 +1651,17 @@ __global__ void __launch_bounds__(Geo<kMx, kTok>::threads, 1)
 
 }  // namespace tcfp8
 
-template <bool kMx, int kTok = 1, bool kSmallPages = false>
+template <bool kMx, int kTok = 1, int kPath = tcfp8::kPathRows>
 inline cudaError_t launch_split_tc(const Stage1Params& p, cudaStream_t stream) {
-  using L = tcfp8::Layout<kMx, kTok>;
+  using L = tcfp8::Layout<kMx, kTok, kPath>;
   static_assert(L::total <= 232448, "shared memory carve-up exceeds the 227 KB per-CTA limit");
   static_assert(L::qs % 1024 == 0 && L::pb % 1024 == 0 && L::rope % 1024 == 0, "swizzled operand alignment");
-  static_assert(L::stage % 16 == 0, "bulk-copy destination alignment");
-  static_assert(!kSmallPages || kTok == 1, "paged caches take one token per sequence");
-  auto* kernel = tcfp8::mla_split_tc_kernel<kMx, kTok, kSmallPages>;
-  cudaError_t e = smem_opt_in<tcfp8::mla_split_tc_kernel<kMx, kTok, kSmallPages>>(L::total);
+  static_assert(L::stage % 128 == 0 && L::sf % 16 == 0 && L::sfb % 16 == 0, "copy source / destination alignment");
+  static_assert(kPath != tcfp8::kPathSmallPages || kTok == 1, "paged caches take one token per sequence");
+  auto* kernel = tcfp8::mla_split_tc_kernel<kMx, kTok, kPath>;
+  cudaError_t e = smem_opt_in<tcfp8::mla_split_tc_kernel<kMx, kTok, kPath>>(L::total);
   if (e != cudaSuccess) return e;
-  e = launch_overlapped(kernel, dim3(p.grid), dim3(tcfp8::Geo<kMx, kTok>::threads), L::total, stream, p);
+  e = launch_overlapped(kernel, dim3(p.grid), dim3(tcfp8::Geo<kMx, kTok, kPath>::threads), L::total, stream, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

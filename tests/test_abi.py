@@ -131,3 +131,28 @@ def test_fwd_rejects_inconsistent_two_token_plans_without_cuda(lib):
     one = binding.mla_decode_plan([0, 300, 700], "fp8", num_sms=152)
     one.tokens_fused = 2
     assert fwd(one) == binding.MLA_ERR_INVALID_ARG
+
+
+def test_fwd_checks_the_mx_scores_field_without_cuda(lib):
+    """plan.mx_scores: 0 or 1, and 1 only for MXFP4; the block-scaled form reads
+    the cache through a 4-bit tensor map, which needs kv 32-byte aligned."""
+    from mla_attention_decode_gb300 import binding
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+
+    def fwd(plan, kv=fake):
+        return lib.mla_decode_fwd(fake, kv, fake, 18, fake, fake, fake, None, 1 / 24, ctypes.byref(plan), fake,
+                                  1 << 30, None)
+
+    mx = binding.mla_decode_plan([0, 300, 700], "mxfp4", num_sms=152)
+    assert mx.mx_scores == 0
+    for value in (2, -1):
+        bad = binding.mla_plan.from_buffer_copy(mx)
+        bad.mx_scores = value
+        assert fwd(bad) == binding.MLA_ERR_INVALID_ARG, value
+    fp8 = binding.mla_decode_plan([0, 300, 700], "fp8", num_sms=152)
+    fp8.mx_scores = 1
+    assert fwd(fp8) == binding.MLA_ERR_INVALID_ARG
+    bs = binding.mla_plan.from_buffer_copy(mx)
+    bs.mx_scores = 1
+    assert fwd(bs, kv=P((1 << 20) + 16)) == binding.MLA_ERR_INVALID_ARG

@@ -23,9 +23,9 @@ DEV = torch.device("cuda:0")
 LENS = [130, 0, 64, 5, 1000, 257, 128, 1]
 
 
-def paged_gpu(inp, pg, num_splits=0, kv_indices=None):
+def paged_gpu(inp, pg, num_splits=0, kv_indices=None, mx_block_scaled=False):
     dec = binding.PagedMLADecoder(pg.page_indptr, pg.last_page_len, pg.page_size, pg.num_pages, inp.kv_dtype,
-                                  device=DEV, num_splits=num_splits)
+                                  device=DEV, num_splits=num_splits, mx_block_scaled=mx_block_scaled)
     scale = inp.kv_scale if inp.kv_dtype == "fp8" else pg.block_scales
     idx = pg.kv_indices if kv_indices is None else kv_indices
     out, lse = dec(inp.q.to(DEV), pg.kv.to(DEV), pg.page_indptr.to(DEV), idx.to(DEV), pg.last_page_len.to(DEV),

@@ -152,9 +152,10 @@ def built():
     assert torch.cuda.is_available()
 
 
-def gpu_decode(inp, num_splits=0, q=None, qo=None, kv_indptr_dev=None):
+def gpu_decode(inp, num_splits=0, q=None, qo=None, kv_indptr_dev=None, num_sms=0, mx_block_scaled=False):
     dev = torch.device("cuda:0")
-    dec = binding.MLADecoder(inp.kv_indptr, inp.kv_dtype, device=dev, num_splits=num_splits)
+    dec = binding.MLADecoder(inp.kv_indptr, inp.kv_dtype, device=dev, num_splits=num_splits, num_sms=num_sms,
+                             mx_block_scaled=mx_block_scaled)
     scale = inp.kv_scale if inp.kv_dtype == "fp8" else inp.block_scales
     qq = inp.q if q is None else q
     qo_ = inp.qo_indptr if qo is None else qo
