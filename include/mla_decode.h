@@ -93,9 +93,14 @@ typedef enum {
  * end, each sequence weighing w_b = max(1, T_b) tiles, T = sum_b w_b, with
  * U = unit_cost empty positions between consecutive sequences (the weight of
  * a unit boundary), C = T + U (batch - 1) positions in all, and gives CTA c of
- * G = grid the positions [floor(c C / G), floor((c+1) C / G)).  Sequence b's
- * tiles sit at positions X_b + i, X_b = P_b + U b with P_b = sum_{b' < b} w_b';
- * it is split where CTA ranges cut it: with cta(x) = floor(((x + 1) G - 1) / C),
+ * G = grid the positions [B(c), B(c+1)) with
+ *   B(c) = floor(c C' / G) - D max(0, c - (G - L)),  C' = C + L D,
+ * D = late_tiles and L = min(G, max(0, G + batch - num_sms)) when D > 0 (else
+ * L = 0): the last L CTAs, which the hardware places on the SMs the
+ * query-preparation grid (one CTA per output row) holds and so start later,
+ * own D positions fewer.  Sequence b's tiles sit at positions X_b + i,
+ * X_b = P_b + U b with P_b = sum_{b' < b} w_b'; it is split where CTA ranges
+ * cut it: with cta(x) the CTA whose range holds x,
  * S_b = cta(X_b + w_b - 1) - cta(X_b) + 1, split s covers the sequence's tiles
  * in CTA cta(X_b) + s's range, and unit u = sum_{b' < b} S_b' + s.  The planner takes whichever schedule its cost
  * model (the busiest CTA's tiles and units, plus the combine) prefers; a forced
@@ -129,7 +134,7 @@ typedef struct {
                              block scales, only the V part being converted for P.V (needs kv
                              32-byte aligned).  Paged caches with pages of fewer than 64 rows
                              always take the copy. */
-  int32_t reserved;
+  int32_t late_tiles;     /* schedule 1: D, the positions each late CTA gives up (rule above); 0: none */
   /* first_row[c] (c < MLA_PLAN_FIRST_ROWS): the row-space row of the first tile
    * CTA c of the split kernel reads, -1 when it reads none or the plan does not
    * say (paged and multi-token plans).  The e4m3 split kernel starts that

@@ -39,11 +39,11 @@ class mla_plan(ctypes.Structure):
                 ("schedule", ctypes.c_int32), ("total_tiles", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("num_pages", ctypes.c_int32), ("unit_cost", ctypes.c_int32), ("q_len", ctypes.c_int32),
                 ("tokens_fused", ctypes.c_int32), ("mx_scores", ctypes.c_int32),
-                ("reserved", ctypes.c_int32),
+                ("late_tiles", ctypes.c_int32),
                 ("first_row", ctypes.c_int32 * 256)]
 
     def as_dict(self) -> dict:
-        return {k: getattr(self, k) for k, _ in self._fields_ if k not in ("reserved", "first_row")}
+        return {k: getattr(self, k) for k, _ in self._fields_ if k != "first_row"}
 
 
 _lock = threading.Lock()

@@ -91,12 +91,33 @@ double plan_cost(const std::vector<int64_t>& lens, int32_t chunk, int32_t cap, i
 
 // Schedule 1 (contiguous tile ranges, see mla_decode.h): the sequences' tiles
 // laid end to end with unit_cost empty positions between consecutive
-// sequences; CTA c of G owns positions [c C / G, (c+1) C / G) of the C in
-// all, and cta_of(x) is the CTA owning position x.
-int64_t cta_of(int64_t x, int64_t C, int64_t G) { return ((x + 1) * G - 1) / C; }
+// sequences, C positions in all; CTA c of G owns positions [lo(c), lo(c+1)),
+// the last L CTAs (late_ctas) D positions (late_tiles) fewer than the others,
+// and cta(x) is the CTA owning position x.
+struct Partition {
+  int64_t C, G, L, D;
+  int64_t lo(int64_t c) const {
+    const int64_t Cp = C + L * D;
+    return c * Cp / G - D * (c > G - L ? c - (G - L) : 0);
+  }
+  int64_t cta(int64_t x) const {
+    const int64_t Cp = C + L * D;
+    if (D == 0 || x < lo(G - L)) return ((x + 1) * G - 1) / Cp;
+    return ((x - D * (G - L) + 1) * G - 1) / (Cp - D * G);
+  }
+};
+// The late CTAs: e4m3 and MXFP4 plans start the split kernel while the
+// query-preparation grid (one CTA per output row) still holds SMs, and the
+// hardware places the split CTAs of the highest indices on those SMs once
+// they are free; a per-CTA trace puts them about 3.3 us behind (two e4m3
+// tiles, one MXFP4 or two-token tile).  Those CTAs get D positions fewer.
+int64_t late_ctas(int64_t G, int64_t prep_rows, int64_t num_sms) {
+  const int64_t l = G + prep_rows - num_sms;
+  return l <= 0 ? 0 : (l < G ? l : G);
+}
 
 struct BalancedPlan {
-  int64_t T = 0, C = 0, G = 0, work = 0;
+  int64_t T = 0, C = 0, G = 0, work = 0, L = 0, D = 0;
   int32_t smax = 0, max_units = 0, unit_cost = 0;
   double cost = -1.0;
 };
@@ -112,7 +133,8 @@ constexpr int32_t kScheduleUnitCost = MLA_UNIT_COST;
 
 // The busiest CTA's tiles plus kUnitCost per unit it owns, plus the combine
 // (same model as plan_cost).
-BalancedPlan plan_balanced(const std::vector<int64_t>& lens, int num_sms, int kv_dtype) {
+BalancedPlan plan_balanced(const std::vector<int64_t>& lens, int num_sms, int kv_dtype, int64_t prep_rows,
+                           int64_t late_tiles) {
   const double kUnitCost = 0.5, kCombineFixed = 2.0;
   const int tile = tile_rows(kv_dtype);
   BalancedPlan bp;
@@ -122,6 +144,11 @@ BalancedPlan plan_balanced(const std::vector<int64_t>& lens, int num_sms, int kv
   const int64_t B = static_cast<int64_t>(lens.size());
   bp.unit_cost = bp.T >= (kScheduleUnitCost + 2) * bp.G ? kScheduleUnitCost : 0;
   bp.C = bp.T + bp.unit_cost * (B - 1);
+  // the late CTAs' share, when every CTA keeps at least two positions
+  bp.L = late_ctas(bp.G, prep_rows, num_sms);
+  bp.D = (bp.L > 0 && bp.C + bp.L * late_tiles >= (late_tiles + 2) * bp.G) ? late_tiles : 0;
+  if (bp.D == 0) bp.L = 0;
+  const Partition part{bp.C, bp.G, bp.L, bp.D};
   std::vector<int64_t> tiles(static_cast<size_t>(bp.G), 0);
   std::vector<int32_t> units(static_cast<size_t>(bp.G), 0);
   int64_t P = 0, split_units = 0;
@@ -129,13 +156,13 @@ BalancedPlan plan_balanced(const std::vector<int64_t>& lens, int num_sms, int kv
     const int64_t L = lens[static_cast<size_t>(b)];
     const int64_t w = L > 0 ? (L + tile - 1) / tile : 1;
     const int64_t x = P + bp.unit_cost * b;  // position of the sequence's first tile
-    const int64_t cf = cta_of(x, bp.C, bp.G), cl = cta_of(x + w - 1, bp.C, bp.G);
+    const int64_t cf = part.cta(x), cl = part.cta(x + w - 1);
     const int64_t s = cl - cf + 1;
     bp.work += s;
     if (s > 1) split_units += s;
     bp.smax = s > bp.smax ? static_cast<int32_t>(s) : bp.smax;
     for (int64_t c = cf; c <= cl; ++c) {
-      const int64_t lo = c * bp.C / bp.G, hi = (c + 1) * bp.C / bp.G;
+      const int64_t lo = part.lo(c), hi = part.lo(c + 1);
       tiles[static_cast<size_t>(c)] += (hi < x + w ? hi : x + w) - (lo > x ? lo : x);
       units[static_cast<size_t>(c)] += 1;
     }
@@ -273,14 +300,16 @@ void fill_first_rows(mla_plan* plan, const int32_t* kv_indptr_host) {
   };
   if (plan->schedule == 1) {
     const int64_t U = plan->unit_cost, T = plan->total_tiles, C = T + U * (B - 1);
+    const int64_t D = plan->late_tiles, L = D > 0 ? late_ctas(G, plan->batch, plan->num_sms) : 0;
+    const Partition part{C, G, L, D};
     int64_t P = 0;
     for (int64_t b = 0; b < B; ++b) {
       const int64_t L = (int64_t)kv_indptr_host[b + 1] - kv_indptr_host[b];
       const int64_t w = L > 0 ? (L + R - 1) / R : 1;
       const int64_t X = P + U * b;
       if (L > 0)
-        for (int64_t c = cta_of(X, C, G); c <= cta_of(X + w - 1, C, G); ++c) {
-          const int64_t lo = c * C / G;
+        for (int64_t c = part.cta(X); c <= part.cta(X + w - 1); ++c) {
+          const int64_t lo = part.lo(c);
           set(c, kv_indptr_host[b] + R * ((lo > X ? lo : X) - X));
         }
       P += w;
@@ -302,8 +331,22 @@ uint64_t* g_trace = nullptr;
 
 // The plan of a batch of sequences with lengths `lens` whose rows span
 // [0, total_kv) of the row space the kernels walk (see mla_decode.h).
+// Positions a late CTA gives up (see late_ctas): e4m3 one token per unit,
+// MXFP4 and the two-token e4m3 form; none for bf16 (no query preparation).
+#ifndef MLA_LATE_TILES_E4M3
+#define MLA_LATE_TILES_E4M3 2
+#endif
+#ifndef MLA_LATE_TILES_OTHER
+#define MLA_LATE_TILES_OTHER 1
+#endif
+int64_t late_tiles_for(int32_t kv_dtype, bool fused) {
+  if (kv_dtype == MLA_KV_BF16) return 0;
+  return (kv_dtype == MLA_KV_FP8_E4M3 && !fused) ? MLA_LATE_TILES_E4M3 : MLA_LATE_TILES_OTHER;
+}
+
+// prep_rows: output rows (the query-preparation grid); fused: the two-token e4m3 form
 int plan_lengths(const std::vector<int64_t>& lens, int32_t total_kv, int32_t kv_dtype, int32_t num_sms,
-                 int32_t num_splits, mla_plan* plan) {
+                 int32_t num_splits, mla_plan* plan, int64_t prep_rows, bool fused = false) {
   const int32_t batch = static_cast<int32_t>(lens.size());
   int64_t lmax = 0;
   for (int64_t L : lens) lmax = L > lmax ? L : lmax;
@@ -350,7 +393,7 @@ int plan_lengths(const std::vector<int64_t>& lens, int32_t total_kv, int32_t kv_
     rr_cost = best;
     if (best >= 0.0) plan_cost(lens, chunk, cap, sms, kv_dtype, &work);
     // the contiguous schedule, when it is cheaper (or the only one that fits)
-    const BalancedPlan bp = plan_balanced(lens, sms, kv_dtype);
+    const BalancedPlan bp = plan_balanced(lens, sms, kv_dtype, prep_rows, late_tiles_for(kv_dtype, fused));
     if (bp.cost >= 0.0 && bp.max_units <= mla::max_units_per_cta(kv_dtype) && bp.work <= INT32_MAX &&
         bp.C <= INT32_MAX && (rr_cost < 0.0 || bp.cost < rr_cost - 1e-9)) {
       mla_plan p;
@@ -369,6 +412,7 @@ int plan_lengths(const std::vector<int64_t>& lens, int32_t total_kv, int32_t kv_
       p.schedule = 1;
       p.total_tiles = static_cast<int32_t>(bp.T);
       p.unit_cost = bp.unit_cost;
+      p.late_tiles = static_cast<int32_t>(bp.D);
       for (int c = 0; c < MLA_PLAN_FIRST_ROWS; ++c) p.first_row[c] = -1;
       *plan = p;
       return MLA_OK;
@@ -416,7 +460,7 @@ int mla_decode_plan(const int32_t* kv_indptr_host, int32_t batch, int32_t kv_dty
     if (L < 0) return MLA_ERR_INVALID_ARG;
     lens[static_cast<size_t>(b)] = L;
   }
-  const int rc = plan_lengths(lens, kv_indptr_host[batch], kv_dtype, num_sms, num_splits, plan);
+  const int rc = plan_lengths(lens, kv_indptr_host[batch], kv_dtype, num_sms, num_splits, plan, batch);
   if (rc == MLA_OK) fill_first_rows(plan, kv_indptr_host);
   return rc;
 }
@@ -447,7 +491,8 @@ int mla_decode_plan_multi(const int32_t* kv_indptr_host, int32_t num_seqs, int32
     }
   }
   mla_plan p;
-  const int rc = plan_lengths(lens, kv_indptr_host[num_seqs], kv_dtype, num_sms, num_splits, &p);
+  const int rc = plan_lengths(lens, kv_indptr_host[num_seqs], kv_dtype, num_sms, num_splits, &p,
+                              (int64_t)num_seqs * q_len, fused);
   if (rc != MLA_OK) return rc;
   if (fused) {
     if (2 * (int64_t)p.num_work > INT32_MAX) return MLA_ERR_UNSUPPORTED;
@@ -484,7 +529,7 @@ int mla_decode_plan_paged(const int32_t* kv_page_indptr_host, const int32_t* kv_
   }
   const int32_t total = static_cast<int32_t>((int64_t)kv_page_indptr_host[batch] * page_size);
   mla_plan p;
-  const int rc = plan_lengths(lens, total, kv_dtype, num_sms, num_splits, &p);
+  const int rc = plan_lengths(lens, total, kv_dtype, num_sms, num_splits, &p, batch);
   if (rc != MLA_OK) return rc;
   p.page_size = page_size;
   p.num_pages = num_pages;
@@ -595,9 +640,21 @@ int prepare(const void* q, const void* kv, const void* kv_scale, int32_t scale_s
     return MLA_ERR_INVALID_ARG;
   const int32_t entries = plan->batch / p->tok;  // sequences in the unit list
   if (plan->schedule != 0 && (plan->schedule != 1 || plan->total_tiles < plan->grid)) return MLA_ERR_INVALID_ARG;
+  // schedule 1's late CTAs (see late_ctas): every CTA keeps at least two positions
+  p->late_tiles = plan->late_tiles;
+  p->late_ctas = plan->late_tiles > 0 ? static_cast<int32_t>(late_ctas(plan->grid, plan->batch, plan->num_sms)) : 0;
+  if (plan->late_tiles < 0 || (plan->late_tiles > 0 && (plan->schedule != 1 || plan->late_tiles > 64 ||
+                                                        p->late_ctas == 0 || plan->num_sms <= 0)))
+    return MLA_ERR_INVALID_ARG;
   if (plan->unit_cost < 0 || (plan->schedule == 1 && (int64_t)plan->total_tiles +
                               (int64_t)plan->unit_cost * (entries > 0 ? entries - 1 : 0) > INT32_MAX))
     return MLA_ERR_INVALID_ARG;
+  if (plan->late_tiles > 0) {
+    const int64_t C = (int64_t)plan->total_tiles + (int64_t)plan->unit_cost * (entries > 0 ? entries - 1 : 0);
+    if (C + (int64_t)p->late_ctas * plan->late_tiles < (int64_t)(plan->late_tiles + 2) * plan->grid ||
+        C + (int64_t)p->late_ctas * plan->late_tiles > INT32_MAX)
+      return MLA_ERR_INVALID_ARG;
+  }
   if (plan->kv_dtype == MLA_KV_FP8_E4M3) {
     if (!encode_kv_map_tc(&p->tmap_kv64, kv, cache_rows, 128)) return MLA_ERR_CUDA;
     if (paged && page_shift == 6) {

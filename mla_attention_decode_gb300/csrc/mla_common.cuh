@@ -208,8 +208,10 @@ __device__ __forceinline__ int splits_of(int len, int chunk, int cap) {
 
 // Schedule 1 (contiguous tile ranges): sequence b weighs w_b = max(1, T_b)
 // tiles, laid end to end with unit_cost empty positions between consecutive
-// sequences (C positions in all); CTA c owns positions [c C / G, (c+1) C / G)
-// and takes one unit from every sequence whose tiles overlap its range.
+// sequences (C positions in all); CTA c owns positions [B(c), B(c+1)) with
+// B(c) = floor(c C' / G) - D max(0, c - (G - L)), C' = C + L D (the last L =
+// late_ctas CTAs, which start behind the others, own D = late_tiles positions
+// fewer), and takes one unit from every sequence whose tiles overlap its range.
 template <int TILE, int MAX_UNITS, int TOK>
 __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, UnitDesc* units, int* s_nunits,
                                                       int lane) {
@@ -217,8 +219,12 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
   const int nseq = p.batch / TOK;       // unit-list entries: sequences of a two-token plan
   const int nunits = p.num_work / TOK;  // work units (num_work counts partial slots)
   const long long C = T + U * (nseq > 0 ? nseq - 1 : 0);
-  const long long lo = c * C / G, hi = (c + 1) * C / G;
-  auto cta_of = [&](long long x) { return ((x + 1) * G - 1) / C; };
+  const long long L = p.late_ctas, D = p.late_tiles, Cp = C + L * D;
+  auto bound = [&](long long k) { return k * Cp / G - D * (k > G - L ? k - (G - L) : 0); };
+  const long long lo = bound(c), hi = bound(c + 1), late0 = bound(G - L);
+  auto cta_of = [&](long long x) {
+    return (D == 0 || x < late0) ? ((x + 1) * G - 1) / Cp : ((x - D * (G - L) + 1) * G - 1) / (Cp - D * G);
+  };
   long long tprefix = 0;  // tiles of the sequences before this chunk of 32
   int uprefix = 0, count = 0;
   bool bad = false;

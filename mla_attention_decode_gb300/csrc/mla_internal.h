@@ -86,6 +86,8 @@ struct Stage1Params {
   int32_t tok;          // tokens one work unit serves (2: fused two-token e4m3 plan, else 1);
                         // num_work then counts partial slots, tok per unit
   int32_t mx_bs;        // MXFP4 (contiguous, pages >= 64 rows): 1 = scores by block-scaled MMAs
+  int32_t late_ctas;    // schedule 1: the last late_ctas CTAs own late_tiles positions fewer
+  int32_t late_tiles;
   uint64_t* trace;      // trace builds only: [grid][kTraceSlots] global-timer stamps (else null)
   int32_t first_row[MLA_PLAN_FIRST_ROWS];  // the plan's first tile row per CTA (-1: none; see mla_plan)
 };

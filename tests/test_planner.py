@@ -16,29 +16,47 @@ def n_splits(plan, L):
     return max(1, min(plan.max_splits, -(-L // plan.chunk_tokens), -(-L // plan.tile_tokens)))
 
 
-def cta_of(x, C, G):
-    return ((x + 1) * G - 1) // C
+class Partition:
+    """Schedule 1's CTA ranges (mla_decode.h): CTA c owns [lo(c), lo(c + 1)),
+    the last L CTAs D positions fewer; written from the rule, and cta(x) found
+    by search rather than by the closed form the library uses."""
+
+    def __init__(self, plan, C):
+        G, D = plan.grid, plan.late_tiles
+        L = min(G, max(0, G + plan.batch - plan.num_sms)) if D > 0 else 0
+        Cp = C + L * D
+        self.G = G
+        self.b = [k * Cp // G - D * max(0, k - (G - L)) for k in range(G + 1)]
+        assert self.b[0] == 0 and self.b[G] == C
+
+    def lo(self, c):
+        return self.b[c]
+
+    def cta(self, x):
+        c = max(k for k in range(self.G) if self.b[k] <= x)
+        assert x < self.b[c + 1]
+        return c
 
 
 def positions(plan, lens):
-    """Schedule 1 (mla_decode.h): tiles per sequence, first-tile positions, C."""
+    """Schedule 1 (mla_decode.h): tiles per sequence, first-tile positions, the partition."""
     R, U = plan.tile_tokens, plan.unit_cost
     w = [max(1, -(-L // R)) for L in lens]
     T = sum(w)
     assert plan.total_tiles == T
     X = [sum(w[:b]) + U * b for b in range(len(w))]
-    return w, X, T + U * max(0, len(w) - 1)
+    return w, X, Partition(plan, T + U * max(0, len(w) - 1))
 
 
 def contiguous_units(plan, lens):
     """Schedule 1 (mla_decode.h): per sequence its splits, each (start, end)."""
-    R, G = plan.tile_tokens, plan.grid
-    w, X, C = positions(plan, lens)
+    R = plan.tile_tokens
+    w, X, part = positions(plan, lens)
     out, start = [], 0
     for L, wb, x in zip(lens, w, X):
-        cf, cl = cta_of(x, C, G), cta_of(x + wb - 1, C, G)
+        cf, cl = part.cta(x), part.cta(x + wb - 1)
         for c in range(cf, cl + 1):
-            lo, hi = c * C // G, (c + 1) * C // G
+            lo, hi = part.lo(c), part.lo(c + 1)
             a, e = max(lo, x) - x, min(hi, x + wb) - x
             out.append((start + R * a, min(start + L, start + R * e)) if L > 0 else (start, start))
         start += max(L, 0)
@@ -62,18 +80,22 @@ def units_of(plan, lens):
 
 
 def check_contiguous(plan, lens):
-    """Schedule 1: every CTA's range is within one position of C / G, no CTA is
-    left without tiles, and the unit count per CTA matches the plan."""
-    G = plan.grid
-    w, X, C = positions(plan, lens)
+    """Schedule 1: every CTA's range is within one position of its share
+    (C' / G, less D for the late CTAs), no CTA is left without tiles, and the
+    unit count per CTA matches the plan."""
+    G, D = plan.grid, plan.late_tiles
+    w, X, part = positions(plan, lens)
+    L = min(G, max(0, G + plan.batch - plan.num_sms)) if D > 0 else 0
+    C = part.lo(G)
+    Cp = C + L * D
     for c in range(G):
-        n = (c + 1) * C // G - c * C // G
-        assert n in (C // G, -(-C // G))
+        n = part.lo(c + 1) - part.lo(c) + (D if c >= G - L else 0)
+        assert n in (Cp // G, -(-Cp // G)), (c, n)
     per_cta, tiles = [0] * G, [0] * G
     for wb, x in zip(w, X):
-        for c in range(cta_of(x, C, G), cta_of(x + wb - 1, C, G) + 1):
+        for c in range(part.cta(x), part.cta(x + wb - 1) + 1):
             per_cta[c] += 1
-            tiles[c] += min((c + 1) * C // G, x + wb) - max(c * C // G, x)
+            tiles[c] += min(part.lo(c + 1), x + wb) - max(part.lo(c), x)
     assert max(per_cta) == plan.units_per_cta
     assert min(tiles) >= 1, "a CTA without tiles"
     assert sum(tiles) == sum(w)
@@ -82,9 +104,8 @@ def check_contiguous(plan, lens):
 def n_splits_of(plan, lens):
     if plan.schedule == 0:
         return [n_splits(plan, L) for L in lens]
-    G = plan.grid
-    w, X, C = positions(plan, lens)
-    return [cta_of(x + wb - 1, C, G) - cta_of(x, C, G) + 1 for wb, x in zip(w, X)]
+    w, X, part = positions(plan, lens)
+    return [part.cta(x + wb - 1) - part.cta(x) + 1 for wb, x in zip(w, X)]
 
 
 def first_rows_of(plan, lens, ind):
@@ -93,10 +114,10 @@ def first_rows_of(plan, lens, ind):
     first = [-1] * 256
     us = units_of(plan, lens)
     if plan.schedule == 1:
-        w, X, C = positions(plan, lens)
+        w, X, part = positions(plan, lens)
         owner = []
         for wb, x in zip(w, X):
-            owner += list(range(cta_of(x, C, G), cta_of(x + wb - 1, C, G) + 1))
+            owner += list(range(part.cta(x), part.cta(x + wb - 1) + 1))
     else:
         owner = [u % G for u in range(len(us))]
     for (a, b), c in zip(us, owner):
@@ -340,3 +361,25 @@ def test_first_rows_follow_the_units():
     assert set(m.first_row) == {-1}
     pg = binding.mla_decode_plan_paged([0, 2, 5], [7, 3], 8, 8, "fp8", num_sms=152)
     assert set(pg.first_row) == {-1}
+
+
+@pytest.mark.parametrize("dtype,lens,late", [
+    ("fp8", [8192] * 64, True), ("mxfp4", [8192] * 32, True), ("bf16", [8192] * 64, False),
+    ("fp8", [1024] * 32, False),
+])
+def test_late_ctas_own_fewer_positions(dtype, lens, late):
+    """The CTAs that start behind the query-preparation grid (the last
+    G + batch - num_sms) own late_tiles positions fewer than the others; bf16
+    (no query preparation) and plans too small to share have none."""
+    ind = [0] + list(itertools.accumulate(lens))
+    plan = binding.mla_decode_plan(ind, dtype, num_sms=152)
+    assert (plan.late_tiles > 0) == late
+    if plan.schedule == 0:
+        return
+    w, X, part = positions(plan, lens)
+    sizes = [part.lo(c + 1) - part.lo(c) for c in range(plan.grid)]
+    if late:
+        L = plan.grid + plan.batch - plan.num_sms
+        early, tail = sizes[:plan.grid - L], sizes[plan.grid - L:]
+        assert min(early) - max(tail) >= plan.late_tiles - 1 and max(early) - min(tail) <= plan.late_tiles + 1
+    check_plan(lens, dtype)
