@@ -90,6 +90,8 @@ def parse(argv=None):
     ap.add_argument("--q-len", type=int, default=1,
                     help="query tokens per sequence (mla_decode_plan_multi; each token attends to the rows up "
                          "to its own entry)")
+    ap.add_argument("--mx-block-scaled", action="store_true",
+                    help="MXFP4 workload: scores by block-scaled MMAs on the e2m1 tile (plan.mx_scores = 1)")
     ap.add_argument("--page-size", type=int, default=0,
                     help="decode the workload's rows from a paged cache with pages of this many rows "
                          "(pages scattered at random; mla_decode_fwd_paged); 0 = contiguous cache")
@@ -146,7 +148,8 @@ def profiled_traffic(workload: str, kv_dtype: str):
 
 
 def workload_key(name: str, args) -> str:
-    return name + (f"_paged{args.page_size}" if args.page_size else "") + (f"_q{args.q_len}" if args.q_len > 1 else "")
+    return (name + (MX_BS_SUFFIX if getattr(args, "mx_block_scaled", False) else "") +
+            (f"_paged{args.page_size}" if args.page_size else "") + (f"_q{args.q_len}" if args.q_len > 1 else ""))
 
 
 def workload_kv_bytes(name: str) -> int:
@@ -336,6 +339,15 @@ def run_reference(args, inp, name, paged=None):
     print(json.dumps(line), flush=True)
 
 
+def check_device(w, where: str):
+    """The workload's device error word is clear; otherwise fail with the
+    detail words the kernels leave (CTA, thread, tag, detail; mla_decode.h)."""
+    err = w.dec.poll_error()
+    if err:
+        detail = w.dec.workspace[8:24].view(torch.int32).tolist()
+        raise RuntimeError(f"{w.name} ({where}): device error {err}, detail {detail}")
+
+
 class Workload:
     """One workload resident on the device, with its plan, workspace and the
     calls the bench times."""
@@ -428,16 +440,16 @@ def measure_per_config(args, rank, dev, stream, flush, peak, peak_kind, headline
     res = {}
     mx_name = next(n for n in synth.WORKLOAD_ORDER if synth.WORKLOADS[n][2] == "mxfp4")
     for name, mx_bs in [(n, False) for n in synth.WORKLOAD_ORDER] + [(mx_name, True)]:
-        if name == args.workload and not mx_bs:
-            res[name] = headline
+        if name == args.workload and mx_bs == args.mx_block_scaled:
+            res[name + (MX_BS_SUFFIX if mx_bs else "")] = headline
             continue
         w = Workload(name, args, rank, dev, mx_bs=mx_bs)
         for _ in range(max(3, args.warmup)):
             w.call(stream)
-        assert w.dec.poll_error() == 0, f"{name}: device error"
+        check_device(w, "warm-up")
         us = statistics.mean(time_calls(lambda: w.call(stream), args.steps, flush, stream))
         t_split, t_comb = w.time_stages(args.steps, flush, stream, us)
-        assert w.dec.poll_error() == 0, f"{name}: device error"
+        check_device(w, "timed calls")
         entry = {"value": round(us, 3), "unit": "us/call", "kv_bytes_per_call": w.inp.kv_bytes(),
                  "kv_gbs": round(w.inp.kv_bytes() / (us * 1e-6) / 1e9, 1),
                  "roofline": roofline_entry(w, args, t_split, t_comb, peak, peak_kind),
@@ -482,12 +494,12 @@ def main(argv=None):
             pg.barrier()
         torch.cuda.synchronize()
 
-    w = Workload(name, args, rank, dev)
+    w = Workload(name, args, rank, dev, mx_bs=args.mx_block_scaled)
     stream = torch.cuda.current_stream(dev)
     flush = L2Flush(dev)
     for _ in range(max(3, args.warmup)):
         w.call(stream)
-    assert w.dec.poll_error() == 0
+    check_device(w, "warm-up")
 
     # ---- headline: whole call, device time, L2 flushed before each call.  The
     # clock samples cover the timed steps and a soak of the same flushed calls
@@ -561,7 +573,7 @@ def main(argv=None):
         assert torch.equal(outs.host["out"], w.out.cpu()), f"end-to-end ({form}) output differs from the device call"
         e2e_forms[form] = statistics.mean(times)
     h2d, d2h = ins.nbytes, outs.nbytes
-    assert w.dec.poll_error() == 0
+    check_device(w, "timed calls and end-to-end forms")
     e2e_staged, e2e_host, t_split, t_comb = max_over_ranks(
         [e2e_forms["staged"], e2e_forms["host"], t_split, t_comb], pg, dev)
     roof = roofline_entry(w, args, t_split, t_comb, peak, peak_kind)

@@ -57,6 +57,26 @@ struct UnitDesc {
 constexpr int32_t kFinalFlag = (int32_t)0x80000000;
 constexpr int32_t kLastUnitBit = 1 << 30;
 
+// Error tags (word 4 of the workspace) naming where a device error was seen.
+enum : int32_t {
+  kTagWait = 1,         // a bounded mbarrier wait ran out (word 5: barrier address << 1 | parity)
+  kTagPage = 2,         // a page index outside [0, num_pages) (word 5: the index)
+  kTagScan = 3,         // the device kv_indptr / qo_indptr disagree with the plan (round-robin scan)
+  kTagScanContig = 4,   // the same, contiguous-range scan
+  kTagFirstTile = 5,    // the plan's first tile row is not the scan's (word 5: the row)
+};
+// Sets the workspace's error word to `code` unless an error is already there;
+// the first error also leaves where it was seen: words 2-5 = CTA, thread, tag,
+// detail.
+__device__ __forceinline__ void flag_error(int32_t* ws_err, int32_t code, int32_t tag, int32_t detail) {
+  if (atomicCAS(ws_err, 0, code) == 0) {
+    ws_err[2] = (int32_t)blockIdx.x;
+    ws_err[3] = (int32_t)threadIdx.x;
+    ws_err[4] = tag;
+    ws_err[5] = detail;
+  }
+}
+
 // Bounded mbarrier wait.  Returns false (after flagging the error) if the phase
 // did not complete within kWaitTimeoutNs, or immediately if another thread of
 // the CTA already gave up; the caller then carries on without the data so that
@@ -72,7 +92,7 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
     if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     if (global_timer_ns() - t0 > kWaitTimeoutNs) {
       *abort_flag = 1;
-      atomicCAS(ws_err, 0, kErrDeviceTimeout);
+      flag_error(ws_err, kErrDeviceTimeout, kTagWait, (int32_t)(smem_u32(bar) << 1 | (parity & 1)));
       return false;
     }
   }
@@ -142,7 +162,7 @@ __device__ __forceinline__ int cache_row(const Stage1Params& p, int v) {
   if (!p.paged) return v;
   int pg = __ldg(p.kv_indices + (v >> p.page_shift));
   if ((unsigned)pg >= (unsigned)p.num_pages) {
-    atomicCAS(p.ws_err, 0, kErrDeviceIndex);
+    flag_error(p.ws_err, kErrDeviceIndex, kTagPage, pg);
     pg = 0;
   }
   return (pg << p.page_shift) | (v & ((1 << p.page_shift) - 1));
@@ -297,7 +317,7 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
   if (tprefix != T || uprefix != nunits) bad = true;
   bad = __any_sync(0xffffffffu, bad);
   if (lane == 0) {
-    if (bad) atomicCAS(p.ws_err, 0, kErrDeviceIndex);
+    if (bad) flag_error(p.ws_err, kErrDeviceIndex, kTagScanContig, 0);
     *s_nunits = min(count, MAX_UNITS);
   }
 }
@@ -379,7 +399,7 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
   if (prefix != nunits) bad = true;
   bad = __any_sync(0xffffffffu, bad);
   if (lane == 0) {
-    if (bad) atomicCAS(p.ws_err, 0, kErrDeviceIndex);
+    if (bad) flag_error(p.ws_err, kErrDeviceIndex, kTagScan, 0);
     *s_nunits = min(count, MAX_UNITS);
   }
 }

@@ -291,7 +291,7 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
         if (have) nrows = tile_rows(p, nt0, nend);
         continue;
       }
-      atomicCAS(p.ws_err, 0, kErrDeviceIndex);
+      flag_error(p.ws_err, kErrDeviceIndex, kTagFirstTile, x.early_row);
       *x.abort_flag = 1;
       break;
     }
@@ -325,7 +325,7 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
   if (early_pending) {
     // the plan named a tile that this CTA's scan does not have: flag it, and
     // let the copy land before leaving
-    atomicCAS(p.ws_err, 0, kErrDeviceIndex);
+    flag_error(p.ws_err, kErrDeviceIndex, kTagFirstTile, x.early_row);
     *x.abort_flag = 1;
     for (int f = 0; f < 4; ++f) ++armed[f];
     ++armed[kPairSlots];
