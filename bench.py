@@ -447,15 +447,27 @@ def measure_per_config(args, rank, dev, stream, flush, peak, peak_kind, headline
         for _ in range(max(3, args.warmup)):
             w.call(stream)
         check_device(w, "warm-up")
-        us = statistics.mean(time_calls(lambda: w.call(stream), args.steps, flush, stream))
-        t_split, t_comb = w.time_stages(args.steps, flush, stream, us)
-        check_device(w, "timed calls")
+        # a device error in the timed calls voids them: they are taken once more
+        # and the error is reported in the entry (a second one fails the bench)
+        retried = None
+        for attempt in range(2):
+            us = statistics.mean(time_calls(lambda: w.call(stream), args.steps, flush, stream))
+            t_split, t_comb = w.time_stages(args.steps, flush, stream, us)
+            try:
+                check_device(w, "timed calls")
+                break
+            except RuntimeError as e:
+                if attempt == 1:
+                    raise
+                retried = str(e)
         entry = {"value": round(us, 3), "unit": "us/call", "kv_bytes_per_call": w.inp.kv_bytes(),
                  "kv_gbs": round(w.inp.kv_bytes() / (us * 1e-6) / 1e9, 1),
                  "roofline": roofline_entry(w, args, t_split, t_comb, peak, peak_kind),
                  "gpu_launches": args.steps * w.launches_per_call,
                  "plan": {k: w.plan.as_dict()[k] for k in ("num_work", "grid", "chunk_tokens", "splits_max",
                                                           "schedule")}}
+        if retried:
+            entry["device_error_then_retimed"] = retried
         if mx_bs:
             entry["form"] = "MXFP4 scores by block-scaled MMAs on the e2m1 tile (plan.mx_scores = 1)"
         if not args.no_cpu_baseline and not mx_bs:
