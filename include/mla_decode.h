@@ -217,12 +217,10 @@ MLA_API int mla_decode_combine(void* out, float* lse, const mla_plan* plan, void
  * the device disagreed with the plan -- the offending units are skipped;
  * MLA_ERR_DEVICE_TIMEOUT when a kernel stopped waiting for its own copies).
  * Returns MLA_OK when the word was clear.  For tests and debugging: the first
- * error also leaves int32 words 2-5 of the workspace = the CTA, the thread, a
- * tag (1: an mbarrier wait ran out, word 5 = the barrier's shared-memory
- * address << 1 | the parity waited for; 2: a page index outside the cache,
- * word 5 = the index; 3 / 4: kv_indptr or qo_indptr disagree with the plan in
- * the round-robin / contiguous unit scan; 5: the plan's first tile row is not
- * the scan's, word 5 = the row), which this call does not clear.
+ * error found by a unit scan also leaves int32 words 2-5 of the workspace =
+ * the CTA, the thread, a tag (3 / 4: kv_indptr or qo_indptr disagree with the
+ * plan in the round-robin / contiguous unit scan; 5: the plan's first tile row
+ * is not the scan's, word 5 = the row), which this call does not clear.
  */
 MLA_API int mla_decode_poll_error(void* workspace, void* stream);
 

@@ -57,10 +57,11 @@ struct UnitDesc {
 constexpr int32_t kFinalFlag = (int32_t)0x80000000;
 constexpr int32_t kLastUnitBit = 1 << 30;
 
-// Error tags (word 4 of the workspace) naming where a device error was seen.
+// Error tags (word 4 of the workspace) naming where an index error was seen
+// (the bounded waits and the page lookups only set the error word: the
+// recording below, inlined at their many call sites, cost the e4m3 split
+// kernel registers and about 2 us at bs64/kv8192).
 enum : int32_t {
-  kTagWait = 1,         // a bounded mbarrier wait ran out (word 5: barrier address << 1 | parity)
-  kTagPage = 2,         // a page index outside [0, num_pages) (word 5: the index)
   kTagScan = 3,         // the device kv_indptr / qo_indptr disagree with the plan (round-robin scan)
   kTagScanContig = 4,   // the same, contiguous-range scan
   kTagFirstTile = 5,    // the plan's first tile row is not the scan's (word 5: the row)
@@ -92,7 +93,7 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
     if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     if (global_timer_ns() - t0 > kWaitTimeoutNs) {
       *abort_flag = 1;
-      flag_error(ws_err, kErrDeviceTimeout, kTagWait, (int32_t)(smem_u32(bar) << 1 | (parity & 1)));
+      atomicCAS(ws_err, 0, kErrDeviceTimeout);
       return false;
     }
   }
@@ -162,7 +163,7 @@ __device__ __forceinline__ int cache_row(const Stage1Params& p, int v) {
   if (!p.paged) return v;
   int pg = __ldg(p.kv_indices + (v >> p.page_shift));
   if ((unsigned)pg >= (unsigned)p.num_pages) {
-    flag_error(p.ws_err, kErrDeviceIndex, kTagPage, pg);
+    atomicCAS(p.ws_err, 0, kErrDeviceIndex);
     pg = 0;
   }
   return (pg << p.page_shift) | (v & ((1 << p.page_shift) - 1));
