@@ -107,6 +107,9 @@ enum TraceSlot {
   kTrTileS = 16,       // [64] softmax: tile t's scores ready
   kTrTileData = 80,    // [32] QK issuer: tile t's data landed and its S buffer free
   kTrUnitLastPV = 112, // [8] unit k's last P.V complete (its epilogue starts)
+  kTrPrepEntry = 120,  // query-preparation CTA of the same index: entry,
+  kTrPrepWaited = 121, //   past its wait for earlier work,
+  kTrPrepDone = 122,   //   and its image written
   kTrSmid = 127,       // (a value) the SM the CTA ran on
 };
 

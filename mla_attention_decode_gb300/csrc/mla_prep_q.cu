@@ -28,8 +28,10 @@ namespace mla {
 // CTAs have finished (a per-CTA trace shows them entering about 3.3 us late).
 template <bool kMx>
 __global__ void __launch_bounds__(128, 9) mla_prep_q_kernel(const __grid_constant__ Stage1Params p) {
+  if (threadIdx.x == 0) trace_stamp(p, kTrPrepEntry);
   pdl_wait_primary();      // q and qo_indptr written by earlier work are visible
   pdl_launch_dependents();  // the split kernel may begin its set-up
+  if (threadIdx.x == 0) trace_stamp(p, kTrPrepWaited);
   const int b = blockIdx.x, j = threadIdx.x;
   const int qrow = query_row(p, b);
   // bring the sequence's kv_indptr entries into L2 for the split kernel's unit
@@ -75,6 +77,10 @@ __global__ void __launch_bounds__(128, 9) mla_prep_q_kernel(const __grid_constan
     *reinterpret_cast<uint2*>(dst + blk * 2048 + sw64_off(16 + h, col)) = make_uint2(lo0, lo1);
   }
   if (part == 0) reinterpret_cast<float*>(dst + kQImageBytes)[h] = p.sm_scale * kLog2e * kv_scale / sc;
+#if MLA_TRACE
+  __syncthreads();
+  if (threadIdx.x == 0) trace_stamp(p, kTrPrepDone);
+#endif
 }
 
 cudaError_t launch_prep_q(const Stage1Params& p, bool mx, cudaStream_t s) {

@@ -200,7 +200,8 @@ struct Ctx {
   uint64_t* bar;
   volatile int* abort_flag;
   uint32_t tmem;
-  int early_row;  // e4m3, one token: the row of the first tile, copied before the unit scan (-1: none)
+  int early_row;  // one token, contiguous cache: the first tile's row, its copy (e4m3: the tile; converted
+                  // MXFP4: its two staging halves) issued before the unit scan (-1: none)
 };
 
 __device__ __forceinline__ int tiles_of(const UnitDesc& d) { return (d.end - d.start + kTileRows - 1) / kTileRows; }
@@ -606,11 +607,25 @@ static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
   int nr0 = 0, nrows = 0;
   bool have = cur.next(x, nr0, nrows);
   int ncrow = (have && nrows > 0) ? cache_row(p, nr0) : 0;
+  const bool early = x.early_row >= 0;  // the prologue copied the first tile's two halves
   for (int hh = 0; have && !*x.abort_flag; ++hh) {
     const int rows = nrows, crow = ncrow;
     have = cur.next(x, nr0, nrows);
     if (have) ncrow = nrows > 0 ? cache_row(p, nr0) : 0;
     const int sl = hh % kStageSlots, use = hh / kStageSlots;
+    if (early && hh < 2) {
+      // the scan must agree with the plan's first row (it does unless the
+      // device kv_indptr differs from the plan's), else flag it and stop
+      if (hh == 0 && (rows <= 0 || crow != x.early_row)) {
+        flag_error(p.ws_err, kErrDeviceIndex, kTagFirstTile, x.early_row);
+        *x.abort_flag = 1;
+        uses[0] = uses[1] = 1;
+        break;
+      }
+      ++uses[sl];
+      advance_prefetch();
+      continue;
+    }
     if (use >= 1) wait_phase(&x.bar[kStageEmpty + sl], (use - 1) & 1, x.abort_flag, p.ws_err);
     if (*x.abort_flag) break;
     if (rows > 0) {
@@ -623,6 +638,13 @@ static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
     }
     ++uses[sl];
     advance_prefetch();
+  }
+  if (early && uses[0] == 0) {
+    // the plan named a tile that this CTA's scan does not have: flag it, and
+    // let the two copies land before leaving
+    flag_error(p.ws_err, kErrDeviceIndex, kTagFirstTile, x.early_row);
+    *x.abort_flag = 1;
+    uses[0] = uses[1] = 1;
   }
   if (*x.abort_flag) {
     // a wait gave up somewhere: never leave with copies in flight (bounded wait per slot)
@@ -1556,6 +1578,27 @@ __global__ void __launch_bounds__(Geo<kMx, kTok, kPath>::threads, 1)
         }
         mbar_arrive_expect_tx(&x.bar[kRopeFull], kChunkBytes);
         tma_load_2d(smem + L::rope, &p.tmap_kv64, 512, r0, &x.bar[kRopeFull], pol);
+        trace_stamp(p, kTrFirstLoad);
+        misc[3] = r0;
+      }
+    }
+    if constexpr (kMx && !kBs && kTok == 1 && !kSmallPages) {
+      // converted MXFP4: both staging halves of the first tile (64 packed rows
+      // each, fewer at the cache's end), before the unit scan, into staging
+      // slots 0 and 1 where the producer would put them
+      const int r0 = blockIdx.x < MLA_PLAN_FIRST_ROWS ? p.first_row[blockIdx.x] : -1;
+      if (r0 >= 0 && !p.paged) {
+        const uint64_t pol = policy_evict_first();
+        for (int hh = 0; hh < 2; ++hh) {
+          const int rr = r0 + hh * kHalfRows, n = max(0, min(kHalfRows, p.total_kv - rr));
+          if (n > 0) {
+            mbar_arrive_expect_tx(&x.bar[kStageFull + hh], (uint32_t)(n * kPackedRowBytes));
+            bulk_g2s(smem + L::stage + hh * kStageBytes, p.kv + (size_t)rr * kPackedRowBytes,
+                     (uint32_t)(n * kPackedRowBytes), &x.bar[kStageFull + hh], pol);
+          } else {
+            mbar_arrive(&x.bar[kStageFull + hh]);
+          }
+        }
         trace_stamp(p, kTrFirstLoad);
         misc[3] = r0;
       }

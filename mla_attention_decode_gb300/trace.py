@@ -26,6 +26,7 @@ from . import binding, build, synth
 SLOTS = 128
 ENTRY, SETUP, FIRST_LOAD, QUERY_READY, UNITS, TILES, EXIT, SCAN_DONE = 0, 1, 2, 3, 4, 5, 6, 7
 UNIT_DONE, TILE_S, TILE_DATA, UNIT_LAST_PV = 8, 16, 80, 112
+PREP_ENTRY, PREP_WAITED, PREP_DONE = 120, 121, 122  # rows < batch: the query-preparation CTAs
 N_TILE_S, N_TILE_DATA = 64, 32
 
 
@@ -119,12 +120,21 @@ def analyse(stamps: np.ndarray, event_us: float) -> dict:
         return {"min": round(float(v.min()), 2), "median": round(float(np.median(v)), 2),
                 "max": round(float(v.max()), 2)}
 
+    def prep(slot):
+        # the query-preparation grid (rows < batch; none for bf16 caches), relative to the
+        # first split CTA's entry: negative before it
+        v = stamps[:, slot]
+        return stats(us(v[v > 0]))
+
     exit_ = us(stamps[:, EXIT])
     slowest = int(np.argmax(exit_))
     sc = stamps[slowest]
     nt = int(min(sc[TILES], 64))
     return {
         "event_us_split_stage": round(event_us, 2),
+        "prep_entry_us": prep(PREP_ENTRY),
+        "prep_waited_us": prep(PREP_WAITED),
+        "prep_done_us": prep(PREP_DONE),
         "entry_us": stats(us(stamps[:, ENTRY])),
         "scan_done_us": stats(us(stamps[:, SCAN_DONE])),
         "setup_done_us": stats(us(stamps[:, SETUP])),
