@@ -1199,7 +1199,11 @@ __device__ __forceinline__ void write_unit(const Stage1Params& p, uint32_t tl_o,
 // Epilogue group (e4m3, one token per unit; warps 8-11, warp w reading TMEM
 // lanes [32 (w mod 4), +32)): for each unit with tiles, in order, takes the
 // softmax's l and m (kEpiReady), waits for the unit's last P.V, writes the
-// unit's output from its O^T buffer and frees the buffer.
+// unit's output from its O^T buffer and frees the buffer.  A CTA with two
+// units whose second has four tiles or more writes the first unit's output
+// after the second's: 32 KB of stores issued mid-stream delayed the copies of
+// the next tiles (a per-CTA trace at bs64/kv8192 showed the unit boundary
+// about 1.8 us longer with them), while at the end they follow the last P.V.
 template <bool kMx, int kTok>
 __device__ void epilogue_group(const Stage1Params& p, const Ctx& x, int ww, int lane) {
   using L = Layout<kMx, kTok>;
@@ -1208,27 +1212,39 @@ __device__ void epilogue_group(const Stage1Params& p, const Ctx& x, int ww, int 
   const uint32_t tl = x.tmem + ((uint32_t)(32 * ww) << 16);
   const float kv_scale = *static_cast<const float*>(p.kv_scale);
   const float* hand = reinterpret_cast<const float*>(x.smem + L::hand);
+  const bool defer = x.nunits == 2 && tiles_of(x.units[0]) > 0 && tiles_of(x.units[1]) >= 4;
   int ordinal = 0;
-  for (int k = 0; k < x.nunits; ++k) {
-    const UnitDesc d = x.units[k];
+  for (int k = 0; k < x.nunits + (defer ? 1 : 0); ++k) {
+    if (defer && k == 0) {
+      // the first unit's hand-over and last P.V; its buffer is not taken again
+      wait_phase(&x.bar[kEpiReady], 0, x.abort_flag, p.ws_err);
+      wait_phase(&x.bar[olast_bar(0)], 0, x.abort_flag, p.ws_err);
+      if (row == 0) trace_stamp(p, kTrUnitLastPV);
+      ++ordinal;
+      continue;
+    }
+    const bool late0 = defer && k == 2;  // the first unit's output, from buffer 0 (no waits left)
+    if (late0) ordinal = 0;
+    const int ku = late0 ? 0 : k;
+    const UnitDesc d = x.units[ku];
     if (tiles_of(d) == 0) continue;
     const int obuf = ordinal & 1, use = ordinal >> 1;
-    wait_phase(&x.bar[kEpiReady + obuf], use & 1, x.abort_flag, p.ws_err);
+    if (!late0) wait_phase(&x.bar[kEpiReady + obuf], use & 1, x.abort_flag, p.ws_err);
     float l[16], m[16];
 #pragma unroll
     for (int h = 0; h < 16; ++h) {
       l[h] = hand[32 * obuf + h];
       m[h] = hand[32 * obuf + 16 + h];
     }
-    wait_phase(&x.bar[olast_bar(obuf)], use & 1, x.abort_flag, p.ws_err);
-    if (row == 0 && k < 8) trace_stamp(p, kTrUnitLastPV + k);
+    if (!late0) wait_phase(&x.bar[olast_bar(obuf)], use & 1, x.abort_flag, p.ws_err);
+    if (row == 0 && k < 8 && !late0) trace_stamp(p, kTrUnitLastPV + k);
     tc::fence_after();
     write_unit(p, tl + TM::o + obuf * TM::obuf, TM::blk, row, (d.u & kFinalFlag) != 0, d.b, d.u & ~kFinalFlag, l, m,
                kv_scale);
-    if (row == 0 && k < 8) trace_stamp(p, kTrUnitDone + k);
+    if (row == 0 && ku < 8) trace_stamp(p, kTrUnitDone + ku);
     tc::fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&x.bar[ofree_bar(obuf)]);
+    if (lane == 0 && !late0) mbar_arrive(&x.bar[ofree_bar(obuf)]);
     ++ordinal;
   }
 }
