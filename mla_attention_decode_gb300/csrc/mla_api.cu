@@ -123,13 +123,21 @@ struct BalancedPlan {
 };
 
 // A unit boundary inside a CTA (the epilogue of one unit, the next unit's
-// query and the refill of the ring) costs about two tiles of pipeline time;
-// schedule 1 gives each boundary that weight when the CTAs have at least
-// four tiles each (below that the weight would leave CTAs without tiles).
+// query and the refill of the ring) costs about two e4m3 tiles of pipeline
+// time, and about one of MXFP4's longer tiles; schedule 1 gives each boundary
+// that weight when the CTAs have at least U + 2 tiles each (below that the
+// weight would leave CTAs without tiles).  Measured against weights one
+// higher and one lower: e4m3 bs64/kv8192 split stage 65.5 us against 66.6 (1)
+// and 66.1 (3); MXFP4 bs32/kv8192 51.6 us (1) against 53.6 (2) and 54.5 (3).
 #ifndef MLA_UNIT_COST
 #define MLA_UNIT_COST 2
 #endif
-constexpr int32_t kScheduleUnitCost = MLA_UNIT_COST;
+#ifndef MLA_UNIT_COST_MXFP4
+#define MLA_UNIT_COST_MXFP4 1
+#endif
+int32_t schedule_unit_cost(int kv_dtype) {
+  return kv_dtype == MLA_KV_MXFP4 ? MLA_UNIT_COST_MXFP4 : MLA_UNIT_COST;
+}
 
 // The busiest CTA's tiles plus kUnitCost per unit it owns, plus the combine
 // (same model as plan_cost).
@@ -142,7 +150,8 @@ BalancedPlan plan_balanced(const std::vector<int64_t>& lens, int num_sms, int kv
   if (bp.T == 0) return bp;
   bp.G = bp.T < num_sms ? bp.T : num_sms;
   const int64_t B = static_cast<int64_t>(lens.size());
-  bp.unit_cost = bp.T >= (kScheduleUnitCost + 2) * bp.G ? kScheduleUnitCost : 0;
+  const int32_t U = schedule_unit_cost(kv_dtype);
+  bp.unit_cost = bp.T >= (U + 2) * bp.G ? U : 0;
   bp.C = bp.T + bp.unit_cost * (B - 1);
   // the late CTAs' share, when every CTA keeps at least two positions
   bp.L = late_ctas(bp.G, prep_rows, num_sms);

@@ -105,7 +105,10 @@ def analyse(stamps: np.ndarray, event_us: float) -> dict:
         # a unit boundary: the gap between the unit's epilogue and the next tile's scores
         nu = int(min(n_units[c], 8))
         for k in range(nu):
-            if stamps[c, UNIT_DONE + k] > 0 and stamps[c, UNIT_LAST_PV + k] > 0:
+            # a unit written after the next unit's last P.V (the e4m3 epilogue defers the
+            # first of two) is left out: its span is the wait, not the write
+            deferred = k + 1 < nu and stamps[c, UNIT_DONE + k] > stamps[c, UNIT_LAST_PV + k + 1] > 0
+            if stamps[c, UNIT_DONE + k] > 0 and stamps[c, UNIT_LAST_PV + k] > 0 and not deferred:
                 epilogue.append(float(stamps[c, UNIT_DONE + k] - stamps[c, UNIT_LAST_PV + k]) / 1e3)
         for k in range(nu - 1):
             done = stamps[c, UNIT_DONE + k]
