@@ -571,7 +571,10 @@ static __device__ void producer_mx_bs(const Stage1Params& p, const Ctx& x) {
 // half's rows are contiguous in the cache: a unit's rows, or one page of at
 // least 64 rows); one lane issues them.  The rows' scale bytes are prefetched
 // into L2 for the converter warps.  A half with no rows (the second half of a
-// short tile) is signalled by a plain arrival.
+// short tile) is signalled by a plain arrival.  With one token and a
+// contiguous cache the kernel prologue has already copied the first tile's
+// two halves (the plan's first row); the producer checks that row against its
+// scan and goes on from the third half.
 static __device__ void producer_mx(const Stage1Params& p, const Ctx& x) {
   using L = Layout<true>;
   const uint64_t pol = policy_evict_first();  // KV rows are read once
