@@ -300,12 +300,15 @@ __device__ __forceinline__ void scan_units_contiguous(const Stage1Params& p, Uni
         p.ws_seq[2 * (TOK * b + i) + 1] = fits ? sb : 0;
       }
     }
-    const bool mine = sb > 0 && c >= cf && c < cf + sb;
+    // a unit past the plan's slots is not taken, and not counted (the list stays gap-free)
+    const bool over = sb > 0 && c >= cf && c < cf + sb && ub + (int)(c - cf) >= nunits;
+    if (over) bad = true;
+    const bool mine = sb > 0 && c >= cf && c < cf + sb && !over;
     const unsigned m = __ballot_sync(0xffffffffu, mine);
     if (mine) {
       const int pos = count + __popc(m & ((1u << lane) - 1));
       const int u = ub + (int)(c - cf);
-      if (pos >= MAX_UNITS || u >= nunits) {
+      if (pos >= MAX_UNITS) {
         bad = true;
       } else {
         const long long a = (lo > X ? lo : X) - X, e = (hi < X + w ? hi : X + w) - X;  // the sequence's tiles here
@@ -377,6 +380,12 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
       if (off < 0) off += p.grid;
       first = pb + off;
       if (first < pb + sb) n = (pb + sb - 1 - first) / p.grid + 1;
+      // units past the plan's slots (a device kv_indptr with more splits than
+      // the plan's) are not taken, and not counted: the list stays gap-free
+      if (n > 0 && first + (n - 1) * p.grid >= nunits) {
+        bad = true;
+        n = first < nunits ? (nunits - 1 - first) / p.grid + 1 : 0;
+      }
     }
     int nincl = n;
 #pragma unroll
@@ -389,7 +398,7 @@ __device__ __forceinline__ void scan_units(const Stage1Params& p, UnitDesc* unit
     for (int k = 0; k < n; ++k) {
       const int u = first + k * p.grid;
       const int s = u - pb;
-      if (pos + k >= MAX_UNITS || u >= nunits) {
+      if (pos + k >= MAX_UNITS) {
         bad = true;
         continue;
       }

@@ -347,11 +347,20 @@ def test_identical_rows_give_the_row(dtype):
     assert np.max(np.abs(got[0] - r[None, :])) <= 2e-3 * max(1.0, np.abs(r).max())
 
 
-def test_device_index_error_is_reported():
-    """kv_indptr on the device disagreeing with the plan: flagged, no fault."""
-    inp = synth.make_inputs([100, 100], "fp8", seed=59)
+@pytest.mark.parametrize("dtype", ["fp8", "mxfp4"])
+@pytest.mark.parametrize("case", ["past_end", "shifted"])
+def test_device_index_error_is_reported(dtype, case):
+    """kv_indptr on the device disagreeing with the plan: flagged, no fault.
+    past_end: an end beyond the plan's total_kv (the kernel treats the sequence
+    as empty); shifted: every row in bounds, but the second sequence starts
+    elsewhere than the plan's first-tile copy (issued before the unit scan)
+    assumed."""
+    inp = synth.make_inputs([100, 100], dtype, seed=59)
     bad = inp.kv_indptr.clone()
-    bad[2] = 100000  # beyond the plan's total_kv: the kernel treats it as empty
+    if case == "past_end":
+        bad[2] = 100000
+    else:
+        bad[1] = 50
     _, _, dec = gpu_decode(inp, kv_indptr_dev=bad.cuda())
     assert dec.poll_error() == binding.MLA_ERR_DEVICE_INDEX
     assert dec.poll_error() == 0  # cleared by the first poll
