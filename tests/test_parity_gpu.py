@@ -366,6 +366,23 @@ def test_device_index_error_is_reported(dtype, case):
     assert dec.poll_error() == 0  # cleared by the first poll
 
 
+@pytest.mark.parametrize("dtype", ["fp8", "mxfp4"])
+def test_device_index_error_contiguous_schedule(dtype):
+    """The contiguous-tile schedule with a device kv_indptr that swaps two
+    sequences' lengths (same total rows, every row in bounds): CTA ranges and
+    first tiles no longer match the plan's, which is flagged, with no fault
+    and no unit taken past the plan's partial slots."""
+    lens = [3000, 0, 5000, 1, 0, 0, 9000, 129, 4000, 0, 7777]
+    inp = synth.make_inputs(lens, dtype, seed=61)
+    swapped = [5000, 0, 3000, 1, 0, 0, 9000, 129, 4000, 0, 7777]
+    bad = torch.tensor([0] + list(np.cumsum(swapped)), dtype=torch.int32)
+    assert int(bad[-1]) == int(inp.kv_indptr[-1])
+    _, _, dec = gpu_decode(inp, kv_indptr_dev=bad.cuda(), num_sms=7)
+    assert dec.plan.schedule == 1
+    assert dec.poll_error() == binding.MLA_ERR_DEVICE_INDEX
+    assert dec.poll_error() == 0
+
+
 @pytest.mark.parametrize("name", synth.WORKLOAD_ORDER)
 def test_benchmark_workloads_full(orc, name):
     """Each of the five benchmark workloads at full size, in the benchmark's
