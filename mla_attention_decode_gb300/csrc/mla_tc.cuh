@@ -1156,29 +1156,39 @@ __device__ void pv_issuer(const Stage1Params& p, const Ctx& x) {
 // the query's two terms).  An unsplit sequence gets bf16 out and lse; a split
 // one an fp32 partial and lse in partial slot u.  l, m: the unit's softmax sum
 // and reference per head (log2 units); out_scale: the factor O^T carries.
+template <bool kTwo>
 __device__ __forceinline__ void write_unit(const Stage1Params& p, uint32_t tl_o, uint32_t blk, int row, bool final_out,
                                            int ob, int u, const float (&l)[16], const float (&m)[16],
                                            float out_scale) {
   float inv[16];
 #pragma unroll
   for (int h = 0; h < 16; ++h) inv[h] = l[h] > 0.f ? out_scale * __frcp_rn(l[h]) : 0.f;
+  // kTwo blocks of 128 features per TMEM round trip (MXFP4: 0.5 us off a
+  // bs32/kv8192 split stage; the e4m3 kernel, which needs four more registers
+  // for it, ran its short shapes 1.4 us slower and keeps one)
+  constexpr int kPer = kTwo ? 2 : 1;
 #pragma unroll 1
-  for (int fb = 0; fb < 4; ++fb) {
-    uint32_t o[32];
-    tc::ld32(tl_o + blk * fb, o);
+  for (int fp = 0; fp < 4; fp += kPer) {
+    uint32_t o[kPer][32];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) tc::ld32(tl_o + blk * (fp + j), o[j]);
     tc::wait_ld();
-    const int f = 128 * fb + row;
-    if (final_out) {
-      uint16_t* op = p.out + (size_t)ob * kHeads * kVDim + f;
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        const float v = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h])) * inv[h];
-        op[h * kVDim] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xffffu);
+    for (int j = 0; j < kPer; ++j) {
+      const int f = 128 * (fp + j) + row;
+      if (final_out) {
+        uint16_t* op = p.out + (size_t)ob * kHeads * kVDim + f;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const float v = (__uint_as_float(o[j][h]) + __uint_as_float(o[j][16 + h])) * inv[h];
+          op[h * kVDim] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xffffu);
+        }
+      } else {
+        float* op = p.ws_o + (size_t)u * kHeads * kVDim + f;
+#pragma unroll
+        for (int h = 0; h < 16; ++h)
+          op[h * kVDim] = (__uint_as_float(o[j][h]) + __uint_as_float(o[j][16 + h])) * inv[h];
       }
-    } else {
-      float* op = p.ws_o + (size_t)u * kHeads * kVDim + f;
-#pragma unroll
-      for (int h = 0; h < 16; ++h) op[h * kVDim] = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h])) * inv[h];
     }
   }
   // lse of head h is written by row h (every row holds all 16 values): pick
@@ -1242,7 +1252,7 @@ __device__ void epilogue_group(const Stage1Params& p, const Ctx& x, int ww, int 
     if (!late0) wait_phase(&x.bar[olast_bar(obuf)], use & 1, x.abort_flag, p.ws_err);
     if (row == 0 && k < 8 && !late0) trace_stamp(p, kTrUnitLastPV + k);
     tc::fence_after();
-    write_unit(p, tl + TM::o + obuf * TM::obuf, TM::blk, row, (d.u & kFinalFlag) != 0, d.b, d.u & ~kFinalFlag, l, m,
+    write_unit<false>(p, tl + TM::o + obuf * TM::obuf, TM::blk, row, (d.u & kFinalFlag) != 0, d.b, d.u & ~kFinalFlag, l, m,
                kv_scale);
     if (row == 0 && ku < 8) trace_stamp(p, kTrUnitDone + ku);
     tc::fence_before();
@@ -1529,7 +1539,7 @@ __device__ void softmax_epilogue(const Stage1Params& p, const Ctx& x, int ww, in
       ++ordinal;
       tc::fence_after();
       const float out_scale = kMx ? exp2_int(max(-126, min(127, gv))) : kv_scale;
-      write_unit(p, tl_o, TM::blk, row, final_out, ob, u, l_part, m_ref, out_scale);
+      write_unit<kMx>(p, tl_o, TM::blk, row, final_out, ob, u, l_part, m_ref, out_scale);
       if (row == 0 && ti == 0 && k < 8) trace_stamp(p, kTrUnitDone + k);
       tc::fence_before();
       __syncwarp();
