@@ -1163,9 +1163,10 @@ __device__ __forceinline__ void write_unit(const Stage1Params& p, uint32_t tl_o,
   float inv[16];
 #pragma unroll
   for (int h = 0; h < 16; ++h) inv[h] = l[h] > 0.f ? out_scale * __frcp_rn(l[h]) : 0.f;
-  // kTwo blocks of 128 features per TMEM round trip (MXFP4: 0.5 us off a
-  // bs32/kv8192 split stage; the e4m3 kernel, which needs four more registers
-  // for it, ran its short shapes 1.4 us slower and keeps one)
+  // kTwo: two blocks of 128 features per TMEM round trip (MXFP4: 0.1-0.5 us
+  // off a bs32/kv8192 split stage in two A/B runs; the e4m3 kernel, which
+  // needs four more registers for it, ran bs4/kv8192 1.4 us slower and keeps
+  // one block per round trip)
   constexpr int kPer = kTwo ? 2 : 1;
 #pragma unroll 1
   for (int fp = 0; fp < 4; fp += kPer) {
