@@ -122,9 +122,6 @@ struct Tmem {
   static constexpr uint32_t sfa = 256;
   static constexpr uint32_t sfb = 320;
 };
-#ifndef MLA_FIRST_TILE_WAIT
-#define MLA_FIRST_TILE_WAIT 0
-#endif
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kBarSoftmax = 1;  // named barrier of softmax group 0 (128 threads); group 1: 2
 constexpr uint32_t kIdescQK = tc::idesc_e4m3(128, 32, 0, 0);
@@ -295,11 +292,6 @@ __device__ void producer_e4m3(const Stage1Params& p, const Ctx& x) {
       flag_error(p.ws_err, kErrDeviceIndex, kTagFirstTile, x.early_row);
       *x.abort_flag = 1;
       break;
-    }
-    if (MLA_FIRST_TILE_WAIT && it == 1) {
-      // the first tile lands before the rest of the ring is requested
-      for (int f = 0; f < 4; ++f) wait_phase(&x.bar[kPairFull + f], 0, x.abort_flag, p.ws_err);
-      wait_phase(&x.bar[kRopeFull], 0, x.abort_flag, p.ws_err);
     }
     const TileRows rows = nrows;
     have = walk.next(x, nt0, nend);
